@@ -1,0 +1,250 @@
+"""Thin ctypes binding of libgge.so (include/gge.h).
+
+Argument marshalling only: torch tensors are turned into the C structs
+(device pointer, dtype code, extents, element strides) and handed to the C
+entry points of the same names; every step of the computation runs in the
+library's CUDA kernels.  PyTorch supplies device memory and the current
+stream.  There is no fallback: if the library cannot be loaded, ``load()``
+raises.
+"""
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from . import build as _build
+
+c_i32, c_i64, c_u32, c_u64 = ctypes.c_int32, ctypes.c_int64, ctypes.c_uint32, ctypes.c_uint64
+
+DTYPE = {torch.bfloat16: 0, torch.float16: 1, torch.float8_e4m3fn: 2, torch.float8_e5m2: 3,
+         torch.float32: 4}
+ACT = {"none": 0, None: 0, "relu": 1, "gelu_tanh": 2, "gelu_tanh_approx": 2, "silu": 3}
+STATUS = {0: "GGE_OK", 1: "GGE_ERR_INVALID_ARG", 2: "GGE_ERR_UNSUPPORTED",
+          3: "GGE_ERR_ALIGNMENT", 4: "GGE_ERR_WORKSPACE", 5: "GGE_ERR_CUDA",
+          6: "GGE_ERR_TIMEOUT", 7: "GGE_ERR_INDEX_RANGE"}
+
+
+class GgeTensor(ctypes.Structure):
+    _fields_ = [("ptr", ctypes.c_void_p), ("dtype", c_i32), ("reserved", c_i32),
+                ("rows", c_i64), ("cols", c_i64), ("batch", c_i64),
+                ("stride_row", c_i64), ("stride_col", c_i64), ("stride_batch", c_i64)]
+
+
+class GgeConfig(ctypes.Structure):
+    _fields_ = [("tile_n", c_i32), ("num_ctas", c_i32), ("raster_band", c_i32),
+                ("stages", c_i32), ("flags", c_i32), ("reserved", c_i32),
+                ("tile_counts", ctypes.c_void_p), ("timeout_ns", c_u64)]
+
+
+class GgeGemmArgs(ctypes.Structure):
+    _fields_ = [("A", GgeTensor), ("B", GgeTensor),
+                ("C", ctypes.POINTER(GgeTensor)), ("D", ctypes.POINTER(GgeTensor)),
+                ("PostAct", ctypes.POINTER(GgeTensor)),
+                ("alpha", ctypes.c_float), ("beta", ctypes.c_float),
+                ("alpha_dev", ctypes.c_void_p), ("beta_dev", ctypes.c_void_p),
+                ("act", c_i32), ("reserved", c_i32), ("config", ctypes.POINTER(GgeConfig))]
+
+
+class GgePlanInfo(ctypes.Structure):
+    _fields_ = [("tile_m", c_i32), ("tile_n", c_i32), ("tile_k", c_i32), ("stages", c_i32),
+                ("num_tiles", c_i32), ("grid", c_i32), ("threads", c_i32),
+                ("smem_bytes", c_i32), ("raster_band", c_i32), ("reserved", c_i32)]
+
+
+# every function include/gge.h declares, with its ctypes signature
+_SIGNATURES = {
+    "gge_workspace_size": (ctypes.c_size_t, [ctypes.POINTER(GgeGemmArgs), c_i32]),
+    "gge_gemm": (c_i32, [ctypes.POINTER(GgeGemmArgs), ctypes.c_void_p, ctypes.c_size_t,
+                         ctypes.c_void_p]),
+    "gge_gemm_act": (c_i32, [ctypes.POINTER(GgeGemmArgs), ctypes.c_void_p, ctypes.c_size_t,
+                             ctypes.c_void_p]),
+    "gge_gemm_varlen_m": (c_i32, [ctypes.POINTER(GgeGemmArgs), ctypes.c_void_p, c_i32,
+                                  ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
+    "gge_gemm_gather_a": (c_i32, [ctypes.POINTER(GgeGemmArgs), ctypes.c_void_p, ctypes.c_void_p,
+                                  c_i32, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
+    "gge_read_device_status": (c_i32, [ctypes.c_void_p, ctypes.c_void_p,
+                                       ctypes.POINTER(c_i32)]),
+    "gge_status_string": (ctypes.c_char_p, [c_i32]),
+    "gge_fastdivmod_params": (None, [c_i32, ctypes.POINTER(c_u32), ctypes.POINTER(c_u32)]),
+    "gge_fastdivmod_div": (c_i32, [c_i32, c_i32]),
+    "gge_schedule_map": (c_i32, [c_i32, c_i32, c_i32, c_i32, c_i32, ctypes.POINTER(c_i32)]),
+    "gge_plan": (c_i32, [ctypes.POINTER(GgeGemmArgs), c_i32, c_i32, ctypes.POINTER(GgePlanInfo)]),
+    "gge_version": (ctypes.c_char_p, []),
+}
+
+_lib = None
+_lock = threading.Lock()
+
+
+class GgeError(RuntimeError):
+    def __init__(self, code, where=""):
+        self.code = code
+        self.name = STATUS.get(code, str(code))
+        super().__init__(f"{where}: {self.name}")
+
+
+def load(path: str = None, build_if_missing: bool = True) -> ctypes.CDLL:
+    """Load libgge.so (building it in-tree first if it is missing)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = path or _build.LIB
+        if not os.path.exists(path):
+            if not build_if_missing:
+                raise FileNotFoundError(path)
+            _build.build()
+        lib = ctypes.CDLL(path)
+        for name, (res, args) in _SIGNATURES.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+        return lib
+
+
+# ---------------------------------------------------------------- marshalling
+
+def view(t: torch.Tensor, kind: str) -> GgeTensor:
+    """C view of a torch tensor.  kind: 'mk' (A), 'nk' (B) or 'mn' (C/D/PostAct);
+    2-D tensors are one batch, 3-D tensors are (batch, rows, cols)."""
+    if t.dim() == 2:
+        rows, cols = t.shape
+        batch, sr, sc, sb = 1, t.stride(0), t.stride(1), t.numel()
+    elif t.dim() == 3:
+        batch, rows, cols = t.shape
+        sb, sr, sc = t.stride()
+    else:
+        raise ValueError(f"{kind}: expected a 2-D or 3-D tensor")
+    if t.dtype not in DTYPE:
+        raise TypeError(f"{kind}: unsupported dtype {t.dtype}")
+    return GgeTensor(ctypes.c_void_p(t.data_ptr()), DTYPE[t.dtype], 0, rows, cols, batch,
+                     sr, sc, sb)
+
+
+_workspaces = {}
+
+
+def workspace(device=None) -> torch.Tensor:
+    """The per-device status workspace (zeroed once)."""
+    dev = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
+    if dev.index is None:
+        dev = torch.device("cuda", torch.cuda.current_device())
+    ws = _workspaces.get(dev.index)
+    if ws is None:
+        ws = torch.zeros(256, dtype=torch.uint8, device=dev)
+        _workspaces[dev.index] = ws
+    return ws
+
+
+def make_config(tile_n=0, num_ctas=0, raster_band=0, stages=0, flags=0, tile_counts=None,
+                timeout_ns=0):
+    return GgeConfig(tile_n, num_ctas, raster_band, stages, flags, 0,
+                     ctypes.c_void_p(tile_counts.data_ptr()) if tile_counts is not None else None,
+                     timeout_ns)
+
+
+def make_args(A, B, C=None, D=None, PostAct=None, alpha=1.0, beta=1.0, act="none",
+              alpha_dev=None, beta_dev=None, config=None, a_kind="mk"):
+    keep = []
+
+    def opt(t):
+        if t is None:
+            return None
+        v = view(t, "mn")
+        keep.append(v)
+        return ctypes.pointer(v)
+
+    args = GgeGemmArgs()
+    args.A = view(A, a_kind)
+    args.B = view(B, "nk")
+    args.C, args.D, args.PostAct = opt(C), opt(D), opt(PostAct)
+    args.alpha, args.beta = float(alpha), float(beta)
+    args.alpha_dev = ctypes.c_void_p(alpha_dev.data_ptr()) if alpha_dev is not None else None
+    args.beta_dev = ctypes.c_void_p(beta_dev.data_ptr()) if beta_dev is not None else None
+    args.act = ACT[act]
+    args.config = ctypes.pointer(config) if config is not None else None
+    args._keep = (keep, config)
+    return args
+
+
+def _stream(t: torch.Tensor):
+    return ctypes.c_void_p(torch.cuda.current_stream(t.device).cuda_stream)
+
+
+def _check(code, where):
+    if code != 0:
+        raise GgeError(code, where)
+
+
+# ------------------------------------------------------------- entry points
+
+def gge_gemm(A, B, D, C=None, alpha=1.0, beta=1.0, alpha_dev=None, beta_dev=None, config=None):
+    """D = alpha * A @ B^T + beta * C.  A (L,M,K)/(M,K), B (L,N,K)/(N,K), D (L,M,N)/(M,N)."""
+    lib = load()
+    args = make_args(A, B, C=C, D=D, alpha=alpha, beta=beta, alpha_dev=alpha_dev,
+                     beta_dev=beta_dev, config=config)
+    ws = workspace(D.device)
+    _check(lib.gge_gemm(ctypes.byref(args), ctypes.c_void_p(ws.data_ptr()), ws.numel(),
+                        _stream(D)), "gge_gemm")
+
+
+def gge_gemm_act(A, B, PostAct, act, D=None, C=None, alpha=1.0, beta=1.0, alpha_dev=None,
+                 beta_dev=None, config=None):
+    """D (optional) and PostAct = act(alpha * A @ B^T + beta * C)."""
+    lib = load()
+    args = make_args(A, B, C=C, D=D, PostAct=PostAct, alpha=alpha, beta=beta, act=act,
+                     alpha_dev=alpha_dev, beta_dev=beta_dev, config=config)
+    ws = workspace(PostAct.device)
+    _check(lib.gge_gemm_act(ctypes.byref(args), ctypes.c_void_p(ws.data_ptr()), ws.numel(),
+                            _stream(PostAct)), "gge_gemm_act")
+
+
+def gge_gemm_varlen_m(A, B, cu_seqlens_m, D=None, PostAct=None, act="none", C=None, alpha=1.0,
+                      beta=1.0, config=None):
+    """Varlen-M grouped GEMM: A (total_M, K), B (G, N, K), cu_seqlens_m int32 (G+1,) on device."""
+    lib = load()
+    out = D if D is not None else PostAct
+    args = make_args(A, B, C=C, D=D, PostAct=PostAct, alpha=alpha, beta=beta, act=act,
+                     config=config)
+    ws = workspace(out.device)
+    G = cu_seqlens_m.numel() - 1
+    _check(lib.gge_gemm_varlen_m(ctypes.byref(args), ctypes.c_void_p(cu_seqlens_m.data_ptr()), G,
+                                 ctypes.c_void_p(ws.data_ptr()), ws.numel(), _stream(out)),
+           "gge_gemm_varlen_m")
+
+
+def gge_gemm_gather_a(A_src, B, a_idx, cu_seqlens_m=None, D=None, PostAct=None, act="none",
+                      C=None, alpha=1.0, beta=1.0, config=None):
+    """Gather-A GEMM: effective A row r = A_src[a_idx[r]]; varlen-M when cu_seqlens_m is given."""
+    lib = load()
+    out = D if D is not None else PostAct
+    args = make_args(A_src, B, C=C, D=D, PostAct=PostAct, alpha=alpha, beta=beta, act=act,
+                     config=config)
+    ws = workspace(out.device)
+    G = cu_seqlens_m.numel() - 1 if cu_seqlens_m is not None else 0
+    cu = ctypes.c_void_p(cu_seqlens_m.data_ptr()) if cu_seqlens_m is not None else None
+    _check(lib.gge_gemm_gather_a(ctypes.byref(args), ctypes.c_void_p(a_idx.data_ptr()), cu, G,
+                                 ctypes.c_void_p(ws.data_ptr()), ws.numel(), _stream(out)),
+           "gge_gemm_gather_a")
+
+
+def gge_read_device_status(device=None):
+    """Synchronise the current stream and return (status_name, where, tile); clears it."""
+    lib = load()
+    ws = workspace(device)
+    detail = (c_i32 * 2)()
+    code = lib.gge_read_device_status(ctypes.c_void_p(ws.data_ptr()), _stream(ws), detail)
+    return STATUS.get(code, str(code)), detail[0], detail[1]
+
+
+def gge_plan(A, B, C=None, D=None, PostAct=None, act="none", num_groups=0, gather=False,
+             config=None):
+    lib = load()
+    args = make_args(A, B, C=C, D=D, PostAct=PostAct, act=act, config=config)
+    info = GgePlanInfo()
+    code = lib.gge_plan(ctypes.byref(args), num_groups, 1 if gather else 0, ctypes.byref(info))
+    _check(code, "gge_plan")
+    return {k: getattr(info, k) for k, _ in GgePlanInfo._fields_ if k != "reserved"}

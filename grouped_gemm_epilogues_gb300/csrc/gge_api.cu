@@ -1,0 +1,485 @@
+// Host side of libgge.so: argument validation, launch planning, TMA tensor
+// maps and the C ABI declared in include/gge.h.
+//
+// The checks follow the pages' rules (quack/dense_gemm_sm90.py,
+// GemmSm90.is_valid_dtypes and the wrapper's major / alignment handling):
+// 16-bit A and B of the same type, or two 8-bit types in K-major layout; the
+// contiguous dimension 16-byte aligned.  Everything here runs before the
+// launch; nothing allocates or synchronises.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/gge.h"
+#include "gge_launch.h"
+#include "gge_params.h"
+#include "gge_sched.cuh"
+
+namespace gge {
+namespace {
+
+constexpr int kTileM = 128;
+constexpr int kRowBytesHost = 128;
+constexpr int kMaxSmemOptin = 232448;  // 227 KiB per block on sm_100 / sm_103
+constexpr int kCtrlBytesHost = 256;
+constexpr int kMaxGroupsHost = 1024;
+constexpr size_t kWorkspaceBytes = 256;
+constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;
+constexpr int64_t kMaxExtent = (int64_t(1) << 31) - 1;
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+int sm_count() {
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+  if (dev >= 0 && dev < 64 && cache[dev] > 0) return cache[dev];
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
+  if (dev >= 0 && dev < 64) cache[dev] = n;
+  return n;
+}
+
+int elem_bytes(int32_t dt) {
+  switch (dt) {
+    case GGE_BF16: case GGE_F16: return 2;
+    case GGE_E4M3: case GGE_E5M2: return 1;
+    case GGE_F32: return 4;
+    default: return 0;
+  }
+}
+
+bool is16(int32_t dt) { return dt == GGE_BF16 || dt == GGE_F16; }
+bool is8(int32_t dt) { return dt == GGE_E4M3 || dt == GGE_E5M2; }
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+gge_status check_view(const gge_tensor& t) {
+  // an empty view (no elements) may carry a NULL pointer: it is never dereferenced
+  const bool empty = (t.rows == 0 || t.cols == 0);
+  if ((t.ptr == nullptr && !empty) || t.reserved != 0) return GGE_ERR_INVALID_ARG;
+  if (elem_bytes(t.dtype) == 0) return GGE_ERR_INVALID_ARG;
+  if (t.rows < 0 || t.cols < 0 || t.batch < 1) return GGE_ERR_INVALID_ARG;
+  if (t.rows > kMaxExtent || t.cols > kMaxExtent || t.batch > kMaxExtent) return GGE_ERR_UNSUPPORTED;
+  if (t.stride_row < 0 || t.stride_col < 0 || t.stride_batch < 0) return GGE_ERR_INVALID_ARG;
+  if (!aligned16(t.ptr)) return GGE_ERR_ALIGNMENT;
+  return GGE_OK;
+}
+
+// An output / C view: [M, N, L] N-major with 16-byte aligned rows and batches.
+gge_status check_mn(const gge_tensor* t, int64_t M, int64_t N, int64_t L, bool is_output) {
+  gge_status s = check_view(*t);
+  if (s != GGE_OK) return s;
+  if (t->dtype != GGE_BF16 && t->dtype != GGE_F16 && t->dtype != GGE_F32) return GGE_ERR_UNSUPPORTED;
+  if (t->rows != M || t->cols != N || t->batch != L) return GGE_ERR_INVALID_ARG;
+  if (N > 1 && t->stride_col != 1) return GGE_ERR_UNSUPPORTED;  // N-major only
+  const int es = elem_bytes(t->dtype);
+  if (M > 1 && t->stride_row < N) return GGE_ERR_INVALID_ARG;
+  if ((t->stride_row * es) % 16 != 0) return GGE_ERR_ALIGNMENT;
+  if (L > 1 && (t->stride_batch * es) % 16 != 0) return GGE_ERR_ALIGNMENT;
+  (void)is_output;
+  return GGE_OK;
+}
+
+enum class Form { Plain, Varlen, Gather, GatherVarlen };
+
+struct Plan {
+  Params p;
+  CUtensorMap tmA, tmB;
+  int bn;
+  bool gather;
+  LaunchShape shape;
+  int64_t M, N, K, L;
+  bool empty;  // nothing to compute
+  int band;
+};
+
+CUtensorMapDataType tmap_type(int es) {
+  return es == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_UINT16;
+}
+
+gge_status encode_3d(CUtensorMap* m, void* ptr, int es, uint64_t d0, uint64_t d1, uint64_t d2,
+                     uint64_t s1_bytes, uint64_t s2_bytes, uint32_t b0, uint32_t b1) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return GGE_ERR_CUDA;
+  const cuuint64_t dims[3] = {d0, d1, d2};
+  const cuuint64_t strides[2] = {s1_bytes, s2_bytes};
+  const cuuint32_t box[3] = {b0, b1, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(m, tmap_type(es), 3, ptr, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? GGE_OK : GGE_ERR_CUDA;
+}
+
+uint64_t batch_stride_bytes(const gge_tensor& t, int es) {
+  if (t.batch > 1) return static_cast<uint64_t>(t.stride_batch) * es;
+  // a single batch: any legal stride (never stepped over)
+  uint64_t s = static_cast<uint64_t>(std::max<int64_t>(t.rows, 1)) *
+               static_cast<uint64_t>(std::max<int64_t>(t.stride_row, 1)) * es;
+  return (s + 15) / 16 * 16;
+}
+
+// Validate and plan.  `encode` = build tensor maps (needs the CUDA driver).
+gge_status make_plan(const gge_gemm_args* a, Form form, const int32_t* a_idx,
+                     const int32_t* cu, int32_t G, bool want_act, bool act_entry, bool encode,
+                     Plan* out) {
+  if (a == nullptr || out == nullptr) return GGE_ERR_INVALID_ARG;
+  Plan& pl = *out;
+  std::memset(&pl, 0, sizeof(pl));
+  Params& p = pl.p;
+  const gge_config* cfg = a->config;
+  const bool varlen = (form == Form::Varlen || form == Form::GatherVarlen);
+  const bool gather = (form == Form::Gather || form == Form::GatherVarlen);
+  pl.gather = gather;
+
+  if (a->act < GGE_ACT_NONE || a->act > GGE_ACT_SILU) return GGE_ERR_INVALID_ARG;
+  if (act_entry) {
+    if (a->PostAct == nullptr) return GGE_ERR_INVALID_ARG;
+  } else if (!want_act) {
+    if (a->PostAct != nullptr || a->act != GGE_ACT_NONE) return GGE_ERR_INVALID_ARG;
+  }
+  if (a->PostAct == nullptr && a->act != GGE_ACT_NONE) return GGE_ERR_INVALID_ARG;
+  if (a->D == nullptr && a->PostAct == nullptr) return GGE_ERR_INVALID_ARG;
+
+  gge_status s = check_view(a->A);
+  if (s != GGE_OK) return s;
+  s = check_view(a->B);
+  if (s != GGE_OK) return s;
+  const int32_t adt = a->A.dtype, bdt = a->B.dtype;
+  const bool f8 = is8(adt);
+  if (!(is16(adt) || is8(adt))) return GGE_ERR_UNSUPPORTED;
+  if (is16(adt) && bdt != adt) return GGE_ERR_UNSUPPORTED;
+  if (f8 && !is8(bdt)) return GGE_ERR_UNSUPPORTED;
+  if (gather && f8) return GGE_ERR_UNSUPPORTED;
+  const int es = elem_bytes(adt);
+
+  // shapes from the output
+  const gge_tensor* o = a->D ? a->D : a->PostAct;
+  const int64_t M = o->rows, N = o->cols, L = o->batch;
+  const int64_t K = a->A.cols;
+  if (M < 0 || N < 0 || K < 0) return GGE_ERR_INVALID_ARG;
+  if (a->D) { s = check_mn(a->D, M, N, L, true); if (s != GGE_OK) return s; }
+  if (a->PostAct) { s = check_mn(a->PostAct, M, N, L, true); if (s != GGE_OK) return s; }
+  if (a->C) { s = check_mn(a->C, M, N, L, false); if (s != GGE_OK) return s; }
+  if (N % 8 != 0) return GGE_ERR_UNSUPPORTED;
+
+  // A: K-major; B: [N, K, Lb] K- or N-major.  With K == 0 neither is read.
+  bool b_mn = false;
+  if (a->B.rows != N || a->B.cols != K) return GGE_ERR_INVALID_ARG;
+  if (K > 0) {
+    if (K > 1 && a->A.stride_col != 1) return GGE_ERR_UNSUPPORTED;
+    if (a->A.rows > 1 && a->A.stride_row < K) return GGE_ERR_INVALID_ARG;
+    if ((a->A.stride_row * es) % 16 != 0) return GGE_ERR_ALIGNMENT;
+    if (a->A.batch > 1 && (a->A.stride_batch * es) % 16 != 0) return GGE_ERR_ALIGNMENT;
+    if (K == 1 || a->B.stride_col == 1) {
+      if (N > 1 && a->B.stride_row < K) return GGE_ERR_INVALID_ARG;
+      if ((a->B.stride_row * es) % 16 != 0) return GGE_ERR_ALIGNMENT;
+    } else if (a->B.stride_row == 1) {
+      b_mn = true;
+      if (f8) return GGE_ERR_UNSUPPORTED;  // 8-bit operands must be K-major
+      if (a->B.stride_col < N) return GGE_ERR_INVALID_ARG;
+      if ((a->B.stride_col * es) % 16 != 0) return GGE_ERR_ALIGNMENT;
+    } else {
+      return GGE_ERR_UNSUPPORTED;
+    }
+    if (a->B.batch > 1 && (a->B.stride_batch * es) % 16 != 0) return GGE_ERR_ALIGNMENT;
+  }
+
+  if (varlen) {
+    if (cu == nullptr) return GGE_ERR_INVALID_ARG;
+    if (G < 1 || G > kMaxGroupsHost) return GGE_ERR_UNSUPPORTED;
+    if (L != 1) return GGE_ERR_INVALID_ARG;
+    if (a->B.batch != G) return GGE_ERR_INVALID_ARG;
+    if (!gather && (a->A.rows != M || a->A.batch != 1)) return GGE_ERR_INVALID_ARG;
+  } else {
+    if (a->B.batch != L) return GGE_ERR_INVALID_ARG;
+    if (!gather && (a->A.rows != M || a->A.batch != L)) return GGE_ERR_INVALID_ARG;
+  }
+  if (gather) {
+    if (a_idx == nullptr) return GGE_ERR_INVALID_ARG;
+    if (a->A.batch != 1) return GGE_ERR_INVALID_ARG;
+    if ((K * es) % 16 != 0) return GGE_ERR_UNSUPPORTED;  // whole 16-byte chunks along K
+  }
+
+  // tile shape
+  int bn = cfg && cfg->tile_n ? cfg->tile_n : (N <= 128 ? 128 : 256);
+  if (bn != 128 && bn != 256) return GGE_ERR_UNSUPPORTED;
+  pl.bn = bn;
+  const int bk = kRowBytesHost / es;
+  const int stage_bytes = (kTileM + bn) * kRowBytesHost;
+  const int varlen_bytes = varlen ? 2 * 4 * (kMaxGroupsHost + 1) : 0;
+  const int fixed = 1024 + kCtrlBytesHost + varlen_bytes;
+  int stages = (kMaxSmemOptin - fixed) / stage_bytes;
+  stages = std::min(stages, 8);
+  if (cfg && cfg->stages > 0) stages = std::min(stages, cfg->stages);
+  if (stages < 2) return GGE_ERR_UNSUPPORTED;
+
+  pl.M = M; pl.N = N; pl.K = K; pl.L = L;
+  const int64_t tiles_n = (N + bn - 1) / bn;
+  const int64_t tiles_m = (M + kTileM - 1) / kTileM;
+  pl.empty = (M == 0 || N == 0 || L == 0);
+
+  p.M = static_cast<int32_t>(M);
+  p.N = static_cast<int32_t>(N);
+  p.K = static_cast<int32_t>(K);
+  p.L = static_cast<int32_t>(L);
+  p.bk = bk;
+  p.k_tiles = static_cast<int32_t>((K + bk - 1) / bk);
+  p.stages = stages;
+  p.tiles_n = static_cast<int32_t>(tiles_n);
+  p.tiles_n_div = FastDivmod::create(tiles_n > 0 ? static_cast<int32_t>(tiles_n) : 1);
+  int band = cfg && cfg->raster_band > 0 ? cfg->raster_band : 16;
+  int64_t num_tiles = 0;
+  if (!varlen) {
+    num_tiles = tiles_m * tiles_n * L;
+    if (num_tiles > kMaxExtent) return GGE_ERR_UNSUPPORTED;
+    p.sched = PlainSchedule::create(static_cast<int32_t>(tiles_m), static_cast<int32_t>(tiles_n),
+                                    static_cast<int32_t>(L), band);
+    band = p.sched.band;
+    p.num_tiles = static_cast<int32_t>(num_tiles);
+  } else {
+    p.num_groups = G;
+    p.cu_seqlens = cu;
+    // upper bound on the tile count (the exact count is formed on the device)
+    num_tiles = (M / kTileM + G) * tiles_n;
+    p.num_tiles = -1;
+  }
+  pl.band = band;
+  if (gather) {
+    p.a_idx = a_idx;
+    p.a_src = static_cast<const uint8_t*>(a->A.ptr);
+    p.a_src_ld = a->A.stride_row * es;
+    p.a_src_rows = static_cast<int32_t>(a->A.rows);
+    p.k_bytes = static_cast<int32_t>(K * es);
+  }
+  // epilogue
+  if (a->D) {
+    p.d = a->D->ptr; p.ldd = a->D->stride_row; p.sbd = a->D->stride_batch; p.d_dtype = a->D->dtype;
+  }
+  if (a->PostAct) {
+    p.post = a->PostAct->ptr; p.ldp = a->PostAct->stride_row; p.sbp = a->PostAct->stride_batch;
+    p.p_dtype = a->PostAct->dtype;
+  }
+  if (a->C) {
+    p.c = a->C->ptr; p.ldc = a->C->stride_row; p.sbc = a->C->stride_batch; p.c_dtype = a->C->dtype;
+  }
+  p.act = a->act;
+  p.alpha = a->alpha;
+  p.beta = a->beta;
+  p.alpha_dev = a->alpha_dev;
+  p.beta_dev = a->beta_dev;
+  // instruction descriptor: f32 accumulator, operand formats, B major, N >> 3, M >> 4
+  const uint32_t afmt = f8 ? (adt == GGE_E5M2 ? 1u : 0u) : (adt == GGE_BF16 ? 1u : 0u);
+  const uint32_t bfmt = f8 ? (bdt == GGE_E5M2 ? 1u : 0u) : (bdt == GGE_BF16 ? 1u : 0u);
+  p.idesc = (1u << 4) | (afmt << 7) | (bfmt << 10) | ((b_mn ? 1u : 0u) << 16) |
+            ((static_cast<uint32_t>(bn) >> 3) << 17) | ((static_cast<uint32_t>(kTileM) >> 4) << 24);
+  p.f8 = f8 ? 1 : 0;
+  p.b_mn_major = b_mn ? 1 : 0;
+  p.flags = cfg ? cfg->flags : 0;
+  p.tile_counts = cfg ? cfg->tile_counts : nullptr;
+  p.timeout_ns = (cfg && cfg->timeout_ns) ? cfg->timeout_ns : kDefaultTimeoutNs;
+
+  // launch shape
+  pl.shape.smem = static_cast<size_t>(fixed + stages * stage_bytes);
+  pl.shape.threads = gather ? (bn == 128 ? kernel_threads<128, true>() : kernel_threads<256, true>())
+                            : (bn == 128 ? kernel_threads<128, false>() : kernel_threads<256, false>());
+  int grid_cap = cfg && cfg->num_ctas > 0 ? cfg->num_ctas : -1;
+  if (grid_cap < 0 && encode) grid_cap = sm_count();
+  if (grid_cap <= 0 && encode) return GGE_ERR_CUDA;
+  pl.shape.grid = grid_cap > 0 ? static_cast<int>(std::min<int64_t>(num_tiles, grid_cap)) : -1;
+  if (pl.empty || !encode) return GGE_OK;
+  if (pl.shape.grid <= 0) pl.empty = true;  // e.g. varlen with no rows
+  if (pl.empty) return GGE_OK;
+
+  // tensor maps (never read when K == 0)
+  if (K > 0) {
+    if (!gather) {
+      s = encode_3d(&pl.tmA, a->A.ptr, es, K, a->A.rows, a->A.batch,
+                    static_cast<uint64_t>(a->A.stride_row) * es, batch_stride_bytes(a->A, es), bk,
+                    kTileM);
+      if (s != GGE_OK) return s;
+    }
+    if (!b_mn) {
+      s = encode_3d(&pl.tmB, a->B.ptr, es, K, N, a->B.batch,
+                    static_cast<uint64_t>(a->B.stride_row) * es, batch_stride_bytes(a->B, es), bk,
+                    bn);
+    } else {
+      gge_tensor t = a->B;
+      uint64_t sb = t.batch > 1 ? static_cast<uint64_t>(t.stride_batch) * es
+                                : (static_cast<uint64_t>(K) * t.stride_col * es + 15) / 16 * 16;
+      s = encode_3d(&pl.tmB, a->B.ptr, es, N, K, a->B.batch,
+                    static_cast<uint64_t>(a->B.stride_col) * es, sb, 64, bk);
+    }
+    if (s != GGE_OK) return s;
+  }
+  return GGE_OK;
+}
+
+gge_status check_workspace(void* ws, size_t bytes) {
+  if (ws == nullptr) return bytes == 0 ? GGE_OK : GGE_ERR_WORKSPACE;
+  if (bytes < kWorkspaceBytes) return GGE_ERR_WORKSPACE;
+  if (!aligned16(ws)) return GGE_ERR_ALIGNMENT;
+  return GGE_OK;
+}
+
+gge_status run(const gge_gemm_args* a, Form form, const int32_t* a_idx, const int32_t* cu,
+               int32_t G, bool want_act, bool act_entry, void* ws, size_t ws_bytes,
+               gge_stream_t stream) {
+  gge_status s = check_workspace(ws, ws_bytes);
+  if (s != GGE_OK) return s;
+  Plan pl;
+  s = make_plan(a, form, a_idx, cu, G, want_act, act_entry, true, &pl);
+  if (s != GGE_OK) return s;
+  if (pl.empty) return GGE_OK;
+  pl.p.status = static_cast<int32_t*>(ws);
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  if (pl.gather)
+    e = pl.bn == 128 ? launch_gemm<128, true>(pl.tmA, pl.tmB, pl.p, pl.shape, st)
+                     : launch_gemm<256, true>(pl.tmA, pl.tmB, pl.p, pl.shape, st);
+  else
+    e = pl.bn == 128 ? launch_gemm<128, false>(pl.tmA, pl.tmB, pl.p, pl.shape, st)
+                     : launch_gemm<256, false>(pl.tmA, pl.tmB, pl.p, pl.shape, st);
+  return e == cudaSuccess ? GGE_OK : GGE_ERR_CUDA;
+}
+
+}  // namespace
+}  // namespace gge
+
+using gge::Form;
+
+extern "C" {
+
+size_t gge_workspace_size(const gge_gemm_args* args, int32_t num_groups) {
+  (void)args;
+  (void)num_groups;
+  return gge::kWorkspaceBytes;
+}
+
+gge_status gge_gemm(const gge_gemm_args* args, void* ws, size_t ws_bytes, gge_stream_t stream) {
+  return gge::run(args, Form::Plain, nullptr, nullptr, 0, false, false, ws, ws_bytes, stream);
+}
+
+gge_status gge_gemm_act(const gge_gemm_args* args, void* ws, size_t ws_bytes,
+                        gge_stream_t stream) {
+  return gge::run(args, Form::Plain, nullptr, nullptr, 0, true, true, ws, ws_bytes, stream);
+}
+
+gge_status gge_gemm_varlen_m(const gge_gemm_args* args, const int32_t* cu_seqlens_m,
+                             int32_t num_groups, void* ws, size_t ws_bytes, gge_stream_t stream) {
+  return gge::run(args, Form::Varlen, nullptr, cu_seqlens_m, num_groups, true, false, ws, ws_bytes,
+                  stream);
+}
+
+gge_status gge_gemm_gather_a(const gge_gemm_args* args, const int32_t* a_idx,
+                             const int32_t* cu_seqlens_m, int32_t num_groups, void* ws,
+                             size_t ws_bytes, gge_stream_t stream) {
+  const Form f = cu_seqlens_m ? Form::GatherVarlen : Form::Gather;
+  return gge::run(args, f, a_idx, cu_seqlens_m, num_groups, true, false, ws, ws_bytes, stream);
+}
+
+gge_status gge_read_device_status(void* ws, gge_stream_t stream, int32_t* detail) {
+  if (ws == nullptr) return GGE_ERR_WORKSPACE;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(st) != cudaSuccess) return GGE_ERR_CUDA;
+  int32_t h[4] = {0, 0, 0, 0};
+  if (cudaMemcpy(h, ws, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess) return GGE_ERR_CUDA;
+  if (cudaMemset(ws, 0, sizeof(h)) != cudaSuccess) return GGE_ERR_CUDA;
+  if (detail) {
+    detail[0] = h[1];
+    detail[1] = h[2];
+  }
+  switch (h[0]) {
+    case 0: return GGE_OK;
+    case gge::DEV_TIMEOUT: return GGE_ERR_TIMEOUT;
+    case gge::DEV_INDEX_RANGE: return GGE_ERR_INDEX_RANGE;
+    default: return GGE_ERR_CUDA;
+  }
+}
+
+const char* gge_status_string(gge_status s) {
+  switch (s) {
+    case GGE_OK: return "ok";
+    case GGE_ERR_INVALID_ARG: return "invalid argument";
+    case GGE_ERR_UNSUPPORTED: return "unsupported configuration";
+    case GGE_ERR_ALIGNMENT: return "misaligned pointer or stride";
+    case GGE_ERR_WORKSPACE: return "workspace missing or too small";
+    case GGE_ERR_CUDA: return "CUDA error";
+    case GGE_ERR_TIMEOUT: return "device pipeline wait timed out";
+    case GGE_ERR_INDEX_RANGE: return "gather index or group offset out of range";
+    default: return "unknown status";
+  }
+}
+
+void gge_fastdivmod_params(int32_t divisor, uint32_t* multiplier, uint32_t* shift) {
+  const gge::FastDivmod f = gge::FastDivmod::create(divisor);
+  if (multiplier) *multiplier = f.multiplier;
+  if (shift) *shift = f.shift;
+}
+
+int32_t gge_fastdivmod_div(int32_t divisor, int32_t n) {
+  return gge::FastDivmod::create(divisor).div(n);
+}
+
+int32_t gge_schedule_map(int32_t tiles_m, int32_t tiles_n, int32_t batches, int32_t band,
+                         int32_t count, int32_t* out) {
+  const gge::PlainSchedule s = gge::PlainSchedule::create(tiles_m, tiles_n, batches, band);
+  for (int32_t t = 0; t < count && t < s.num_tiles; ++t) {
+    int32_t l, mb, nb;
+    s.map(t, l, mb, nb);
+    out[3 * t] = l;
+    out[3 * t + 1] = mb;
+    out[3 * t + 2] = nb;
+  }
+  return s.num_tiles;
+}
+
+gge_status gge_plan(const gge_gemm_args* args, int32_t num_groups, int32_t gather,
+                    gge_plan_info* out) {
+  if (out == nullptr) return GGE_ERR_INVALID_ARG;
+  gge::Plan pl;
+  const Form f = gather ? (num_groups > 0 ? Form::GatherVarlen : Form::Gather)
+                        : (num_groups > 0 ? Form::Varlen : Form::Plain);
+  // a dummy non-null index pointer lets the shape checks run
+  static const int32_t dummy = 0;
+  const gge_status s = gge::make_plan(args, f, gather ? &dummy : nullptr,
+                                      num_groups > 0 ? &dummy : nullptr, num_groups, true, false,
+                                      false, &pl);
+  if (s != GGE_OK) return s;
+  out->tile_m = gge::kTileM;
+  out->tile_n = pl.bn;
+  out->tile_k = pl.p.bk;
+  out->stages = pl.p.stages;
+  out->num_tiles = pl.p.num_groups > 0 ? -1 : pl.p.num_tiles;
+  out->grid = pl.shape.grid;
+  out->threads = pl.shape.threads;
+  out->smem_bytes = static_cast<int32_t>(pl.shape.smem);
+  out->raster_band = pl.band;
+  out->reserved = 0;
+  return GGE_OK;
+}
+
+const char* gge_version(void) { return "gge 0.1.0 (sm_103a, tcgen05)"; }
+
+}  // extern "C"

@@ -1,0 +1,6 @@
+// Kernel instantiation: 128-column tiles, tma A producer.
+#include "gge_inst.cuh"
+
+namespace gge {
+GGE_INSTANTIATE(128, false)
+}  // namespace gge

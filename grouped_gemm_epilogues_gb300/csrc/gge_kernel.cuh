@@ -1,0 +1,543 @@
+// Persistent, warp-specialised GEMM with a fused epilogue for sm_103a.
+//
+//   D       = alpha * A * B^T + beta * C          (rounded to D's dtype)
+//   PostAct = act(alpha * A * B^T + beta * C)     (act on the unrounded fp32 value)
+//
+// after quack/dense_gemm_sm90.py (GemmSm90) and quack/gemm_act_sm90.py
+// (GemmActSm90.epi_visit_acc_subtile), rebuilt for the 5th-generation
+// tensor core instead of Hopper warpgroup MMA:
+//
+//   warps 0-3  epilogue: TMEM -> registers (tcgen05.ld), alpha / beta / C /
+//              activation in fp32, round, store D and PostAct.  Warp w owns
+//              TMEM lanes 32w..32w+31, i.e. tile rows 32w..32w+31.
+//   warp  4    TMEM allocator and MMA issuer (one thread): tcgen05.mma
+//              128 x BN x 16 (x32 for 8-bit) from shared memory into a
+//              double-buffered fp32 TMEM accumulator, so the epilogue of
+//              tile i overlaps the main loop of tile i+1 (this replaces the
+//              pages' ping-pong warpgroups).
+//   warp  5    TMA producer: A and B k-tiles into an S-stage shared-memory
+//              ring (128-byte swizzle), one mbarrier pair per stage.
+//   warps 5-8  (gather-A form) row gather of A with 16-byte cp.async into the
+//              same swizzled layout, B still by TMA (GemmSm90.load_AB_gather_A).
+//
+// Every CTA walks the same static persistent schedule (tile t, t + grid, ...);
+// tile coordinates come from FastDivmod (plain) or from a per-group tile
+// prefix sum in shared memory (varlen-M, VarlenMTileScheduler's role).
+//
+// Every mbarrier wait is bounded by Params::timeout_ns of %globaltimer; on
+// expiry the kernel records DEV_TIMEOUT in the status words, raises a
+// shared abort flag so that every role leaves its loop, lets copies in flight
+// land, frees its TMEM and returns.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "gge_params.h"
+#include "gge_ptx.cuh"
+
+namespace gge {
+
+constexpr int kBM = 128;           // tile rows = TMEM lanes
+constexpr int kRowBytes = 128;     // bytes of K per stage row (one swizzle span)
+constexpr int kEpiWarps = 4;
+constexpr int kMmaWarp = 4;
+constexpr int kLoadWarp = 5;
+constexpr int kGatherWarps = 4;
+constexpr int kMaxGroups = 1024;   // varlen-M groups held in shared memory
+constexpr int kCtrlBytes = 256;    // barriers and flags
+
+template <int BN, bool GATHER>
+struct KernelCfg {
+  static constexpr int kABytes = kBM * kRowBytes;
+  static constexpr int kBBytes = BN * kRowBytes;
+  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kWarps = GATHER ? kLoadWarp + kGatherWarps : kLoadWarp + 1;
+  static constexpr int kThreads = kWarps * 32;
+  static constexpr int kTmemCols = 2 * BN;  // two accumulator buffers
+  static_assert(BN % 64 == 0 && BN <= 256, "BN must be 64, 128, 192 or 256");
+  static_assert(kTmemCols == 128 || kTmemCols == 256 || kTmemCols == 512,
+                "TMEM allocation must be a power of two");
+};
+
+// Shared-memory matrix descriptor for a K-major (or N-major) operand staged
+// with the 128-byte swizzle: start address, leading / stride byte offsets
+// (>> 4), descriptor version 1, swizzle mode 2 (128B).
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+  return static_cast<uint64_t>((addr >> 4) & 0x3FFFu) |
+         (static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16) |
+         (static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32) | (uint64_t(1) << 46) |
+         (uint64_t(2) << 61);
+}
+
+struct TileCoord {
+  int32_t m_row0;     // first output row of the tile (global row in varlen form)
+  int32_t row_limit;  // rows >= this are not written (batch end / group end)
+  int32_t n0;
+  int32_t batch;      // batch index (plain) or group index (varlen)
+  int32_t a_batch;    // third TMA coordinate of A
+};
+
+struct Shared {
+  uint32_t full, empty, tfull, tempty;  // barrier array bases (shared addresses)
+  volatile int32_t* abort;
+  const int32_t* prefix;  // varlen: tile prefix [G+1]
+  const int32_t* cu;      // varlen: cu_seqlens copy [G+1]
+};
+
+template <int BN>
+__device__ __forceinline__ TileCoord tile_coord(int32_t t, const Params& p, const Shared& sh) {
+  TileCoord tc;
+  if (p.num_groups > 0) {
+    int lo = 0, hi = p.num_groups;  // prefix[lo] <= t < prefix[hi]
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (sh.prefix[mid] <= t) lo = mid; else hi = mid;
+    }
+    int32_t mb, nb;
+    p.tiles_n_div.divmod(t - sh.prefix[lo], mb, nb);
+    tc.m_row0 = sh.cu[lo] + mb * kBM;
+    tc.row_limit = min(sh.cu[lo + 1], p.M);
+    tc.n0 = nb * BN;
+    tc.batch = lo;
+    tc.a_batch = 0;
+  } else {
+    int32_t l, mb, nb;
+    p.sched.map(t, l, mb, nb);
+    tc.m_row0 = mb * kBM;
+    tc.row_limit = p.M;
+    tc.n0 = nb * BN;
+    tc.batch = l;
+    tc.a_batch = l;
+  }
+  return tc;
+}
+
+__device__ __forceinline__ void record_status(const Params& p, int32_t code, int32_t where,
+                                              int32_t tile) {
+  if (p.status != nullptr) {
+    if (atomicCAS(p.status, 0, code) == 0) {
+      p.status[1] = where;
+      p.status[2] = tile;
+    }
+  }
+}
+
+// Slow path of a bounded mbarrier wait: poll until the phase completes, the
+// CTA aborts, or timeout_ns of %globaltimer pass (then record and abort).
+static __device__ __noinline__ bool wait_phase_slow(uint32_t bar, uint32_t parity, uint64_t timeout_ns,
+                                             int32_t* status, volatile int32_t* abort,
+                                             int32_t where, int32_t tile) {
+  const uint64_t t0 = ptx::globaltimer();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 32; ++i)
+      if (ptx::mbar_try_wait(bar, parity)) return true;
+    if (*abort) return false;
+    if (ptx::globaltimer() - t0 > timeout_ns) {
+      if (status != nullptr && atomicCAS(status, 0, DEV_TIMEOUT) == 0) {
+        status[1] = where;
+        status[2] = tile;
+      }
+      *abort = 1;
+      return false;
+    }
+  }
+}
+
+// Bounded wait on an mbarrier phase.  Returns false on abort or timeout.
+__device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, const Params& p,
+                                           const Shared& sh, int32_t where, int32_t tile) {
+  if (ptx::mbar_try_wait(bar, parity)) return true;
+  return wait_phase_slow(bar, parity, p.timeout_ns, p.status, sh.abort, where, tile);
+}
+
+// ------------------------------------------------------------- epilogue math
+
+__device__ __forceinline__ float act_apply(int act, float x) {
+  switch (act) {
+    case ACT_RELU:
+      return (x <= 0.f) ? 0.f : x;  // NaN propagates, -0 -> +0
+    case ACT_GELU_TANH: {
+      // 0.5 x (1 + tanh u) written as x / (1 + exp(-2u)): no cancellation in the tail
+      const float u = 0.7978845608028654f * fmaf(0.044715f * x, x * x, x);
+      return __fdividef(x, 1.f + __expf(-2.f * u));
+    }
+    case ACT_SILU:
+      return __fdividef(x, 1.f + __expf(-x));
+    default:
+      return x;
+  }
+}
+
+// Load 8 consecutive values of a 16-byte group as fp32.
+__device__ __forceinline__ void load8(const void* ptr, int dtype, float* out) {
+  if (dtype == DT_F32) {
+    const float4 a = __ldg(reinterpret_cast<const float4*>(ptr));
+    const float4 b = __ldg(reinterpret_cast<const float4*>(ptr) + 1);
+    out[0] = a.x; out[1] = a.y; out[2] = a.z; out[3] = a.w;
+    out[4] = b.x; out[5] = b.y; out[6] = b.z; out[7] = b.w;
+  } else {
+    const uint4 v = __ldg(reinterpret_cast<const uint4*>(ptr));
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      if (dtype == DT_BF16) {
+        const __nv_bfloat162 h = *reinterpret_cast<const __nv_bfloat162*>(&w[i]);
+        const float2 f = __bfloat1622float2(h);
+        out[2 * i] = f.x; out[2 * i + 1] = f.y;
+      } else {
+        const __half2 h = *reinterpret_cast<const __half2*>(&w[i]);
+        const float2 f = __half22float2(h);
+        out[2 * i] = f.x; out[2 * i + 1] = f.y;
+      }
+    }
+  }
+}
+
+// Round 8 fp32 values to the output dtype (RNE) and store them.
+__device__ __forceinline__ void store8(void* ptr, int dtype, const float* x) {
+  if (dtype == DT_F32) {
+    reinterpret_cast<float4*>(ptr)[0] = make_float4(x[0], x[1], x[2], x[3]);
+    reinterpret_cast<float4*>(ptr)[1] = make_float4(x[4], x[5], x[6], x[7]);
+  } else {
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      if (dtype == DT_BF16) {
+        const __nv_bfloat162 h = __floats2bfloat162_rn(x[2 * i], x[2 * i + 1]);
+        w[i] = *reinterpret_cast<const uint32_t*>(&h);
+      } else {
+        const __half2 h = __floats2half2_rn(x[2 * i], x[2 * i + 1]);
+        w[i] = *reinterpret_cast<const uint32_t*>(&h);
+      }
+    }
+    *reinterpret_cast<uint4*>(ptr) = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+}
+
+__device__ __forceinline__ int dtype_bytes(int dt) { return dt == DT_F32 ? 4 : 2; }
+
+// One thread, one output row, 32 consecutive columns starting at col0.
+__device__ __forceinline__ void epilogue_chunk(const Params& p, const uint32_t (&acc)[32],
+                                               int32_t row, int32_t col0, int32_t batch,
+                                               float alpha, float beta) {
+  float v[32];
+#pragma unroll
+  for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(acc[j]) * alpha;
+  const int64_t out_batch = (p.num_groups > 0) ? 0 : batch;
+  if (p.c != nullptr) {
+    const char* cbase = static_cast<const char*>(p.c) +
+                        (out_batch * p.sbc + static_cast<int64_t>(row) * p.ldc + col0) *
+                            dtype_bytes(p.c_dtype);
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+      if (col0 + 8 * g < p.N) {
+        float cv[8];
+        load8(cbase + 8 * g * dtype_bytes(p.c_dtype), p.c_dtype, cv);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) v[8 * g + j] = fmaf(beta, cv[j], v[8 * g + j]);
+      }
+    }
+  }
+  if (p.d != nullptr) {
+    char* dbase = static_cast<char*>(p.d) +
+                  (out_batch * p.sbd + static_cast<int64_t>(row) * p.ldd + col0) *
+                      dtype_bytes(p.d_dtype);
+#pragma unroll
+    for (int g = 0; g < 4; ++g)
+      if (col0 + 8 * g < p.N) store8(dbase + 8 * g * dtype_bytes(p.d_dtype), p.d_dtype, &v[8 * g]);
+  }
+  if (p.post != nullptr) {
+    char* pbase = static_cast<char*>(p.post) +
+                  (out_batch * p.sbp + static_cast<int64_t>(row) * p.ldp + col0) *
+                      dtype_bytes(p.p_dtype);
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+      if (col0 + 8 * g < p.N) {
+        float a[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) a[j] = act_apply(p.act, v[8 * g + j]);
+        store8(pbase + 8 * g * dtype_bytes(p.p_dtype), p.p_dtype, a);
+      }
+    }
+  }
+}
+
+// ------------------------------------------------------------------- roles
+
+template <int BN, bool GATHER>
+__device__ __forceinline__ void epilogue_role(const Params& p, const Shared& sh,
+                                              uint32_t tmem_base, int32_t num_tiles) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const float alpha = p.alpha_dev ? *p.alpha_dev : p.alpha;
+  const float beta = p.beta_dev ? *p.beta_dev : p.beta;
+  uint32_t acc = 0, acc_phase = 0;
+  for (int32_t t = blockIdx.x; t < num_tiles; t += gridDim.x) {
+    const TileCoord tc = tile_coord<BN>(t, p, sh);
+    // all lanes take the same branch: tcgen05.ld below is warp-collective
+    const bool ok = wait_phase(sh.tfull + 8 * acc, acc_phase, p, sh, 3, t);
+    if (!__all_sync(0xffffffffu, ok)) break;
+    ptx::tc_fence_after();
+    const int32_t row = tc.m_row0 + warp * 32 + lane;
+    const bool row_ok = row < tc.row_limit;
+    const uint32_t tbase = tmem_base + (static_cast<uint32_t>(warp * 32) << 16) + acc * BN;
+#pragma unroll 1
+    for (int c = 0; c < BN / 32; ++c) {
+      uint32_t v[32];
+      __syncwarp();  // tcgen05.ld / wait::ld are warp-collective
+      if (p.k_tiles > 0) {
+        ptx::tmem_ld_32x32b_x32(tbase + c * 32, v);
+        ptx::tmem_wait_ld(v);
+      } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] = 0u;
+      }
+      if (c == BN / 32 - 1) {  // accumulator fully read: hand the buffer back to the MMA warp
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(sh.tempty + 8 * acc);
+      }
+      const int32_t col0 = tc.n0 + c * 32;
+      if (row_ok && col0 < p.N) epilogue_chunk(p, v, row, col0, tc.batch, alpha, beta);
+    }
+    if ((p.flags & FLAG_TILE_COUNTS) && p.tile_counts != nullptr && warp == 0 && lane == 0)
+      atomicAdd(p.tile_counts + t, 1);
+    acc ^= 1u;
+    if (acc == 0) acc_phase ^= 1u;
+  }
+}
+
+template <int BN, bool GATHER>
+__device__ __forceinline__ void mma_role(const Params& p, const Shared& sh, uint32_t a0,
+                                         uint32_t b0, uint32_t tmem_base, int32_t num_tiles) {
+  using Cfg = KernelCfg<BN, GATHER>;
+  int stage = 0;
+  uint32_t phase = 0, acc = 0, acc_phase = 0;
+  // B descriptor strides: K-major rows are 128 B apart, 8-row swizzle atoms 1 KiB apart;
+  // N-major: 64-column chunks are (bk rows * 128 B) apart, 8-row K groups 1 KiB apart.
+  const uint32_t b_lbo = p.b_mn_major ? static_cast<uint32_t>(p.bk) * kRowBytes : 16u;
+  const uint32_t b_kstep = p.b_mn_major ? 16u * kRowBytes : 32u;
+  for (int32_t t = blockIdx.x; t < num_tiles; t += gridDim.x) {
+    if (!wait_phase(sh.tempty + 8 * acc, acc_phase ^ 1u, p, sh, 2, t)) return;
+    ptx::tc_fence_after();
+    const uint32_t d_tmem = tmem_base + acc * BN;
+    for (int kt = 0; kt < p.k_tiles; ++kt) {
+      if (!wait_phase(sh.full + 8 * stage, phase, p, sh, 1, t)) return;
+      ptx::tc_fence_after();
+      if (GATHER) ptx::fence_proxy_async_smem();  // cp.async (generic proxy) writes -> MMA reads
+      const uint32_t a_addr = a0 + stage * Cfg::kABytes;
+      const uint32_t b_addr = b0 + stage * Cfg::kBBytes;
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) {  // 4 MMAs of 32 bytes of K each
+        const uint64_t adesc = smem_desc(a_addr + kk * 32, 16u, 1024u);
+        const uint64_t bdesc = smem_desc(b_addr + kk * b_kstep, b_lbo, 1024u);
+        const uint32_t accumulate = (kt > 0 || kk > 0) ? 1u : 0u;
+        if (p.f8) ptx::mma_f8(d_tmem, adesc, bdesc, p.idesc, accumulate);
+        else ptx::mma_f16(d_tmem, adesc, bdesc, p.idesc, accumulate);
+      }
+      ptx::mma_commit(sh.empty + 8 * stage);  // frees the stage once these MMAs finish
+      if (++stage == p.stages) { stage = 0; phase ^= 1u; }
+    }
+    if (!(p.flags & FLAG_TEST_DROP_ACC_FULL)) ptx::mma_commit(sh.tfull + 8 * acc);
+    acc ^= 1u;
+    if (acc == 0) acc_phase ^= 1u;
+  }
+}
+
+template <int BN, bool GATHER>
+__device__ __forceinline__ void tma_producer_role(const Params& p, const Shared& sh,
+                                                  const CUtensorMap* tmA, const CUtensorMap* tmB,
+                                                  uint32_t a0, uint32_t b0, int32_t num_tiles) {
+  using Cfg = KernelCfg<BN, GATHER>;
+  int stage = 0;
+  uint32_t phase = 0;
+  for (int32_t t = blockIdx.x; t < num_tiles; t += gridDim.x) {
+    const TileCoord tc = tile_coord<BN>(t, p, sh);
+    for (int kt = 0; kt < p.k_tiles; ++kt) {
+      if (!wait_phase(sh.empty + 8 * stage, phase ^ 1u, p, sh, 0, t)) return;
+      const uint32_t full = sh.full + 8 * stage;
+      ptx::mbar_arrive_expect_tx(full, Cfg::kStageBytes);
+      const int32_t k0 = kt * p.bk;
+      ptx::tma_load_3d(a0 + stage * Cfg::kABytes, tmA, full, k0, tc.m_row0, tc.a_batch);
+      const uint32_t bdst = b0 + stage * Cfg::kBBytes;
+      if (!p.b_mn_major) {
+        ptx::tma_load_3d(bdst, tmB, full, k0, tc.n0, tc.batch);
+      } else {
+#pragma unroll
+        for (int j = 0; j < BN / 64; ++j)
+          ptx::tma_load_3d(bdst + j * (64 * kRowBytes), tmB, full, tc.n0 + 64 * j, k0, tc.batch);
+      }
+      if (++stage == p.stages) { stage = 0; phase ^= 1u; }
+    }
+  }
+}
+
+// Four warps: 8 threads per 128-byte A row, 16 rows per pass, 8 passes.
+template <int BN>
+__device__ __forceinline__ void gather_producer_role(const Params& p, const Shared& sh,
+                                                     const CUtensorMap* tmB, uint32_t a0,
+                                                     uint32_t b0, int32_t num_tiles) {
+  using Cfg = KernelCfg<BN, true>;
+  const int gt = threadIdx.x - kLoadWarp * 32;  // 0..127
+  const int chunk = gt & 7;
+  const int rsub = gt >> 3;
+  int stage = 0;
+  uint32_t phase = 0;
+  for (int32_t t = blockIdx.x; t < num_tiles; t += gridDim.x) {
+    const TileCoord tc = tile_coord<BN>(t, p, sh);
+    // index rows: plain gather reads a_idx[batch][row], varlen reads a_idx[global row]
+    const int64_t idx_base = (p.num_groups > 0) ? 0 : static_cast<int64_t>(tc.batch) * p.M;
+    int32_t src[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int32_t r = tc.m_row0 + rsub + 16 * i;
+      int32_t s = -1;
+      if (r < tc.row_limit) {
+        s = __ldg(p.a_idx + idx_base + r);
+        if (s < 0 || s >= p.a_src_rows) {
+          record_status(p, DEV_INDEX_RANGE, 4, t);
+          s = -1;  // the row is zero-filled instead of read
+        }
+      }
+      src[i] = s;
+    }
+    for (int kt = 0; kt < p.k_tiles; ++kt) {
+      if (!wait_phase(sh.empty + 8 * stage, phase ^ 1u, p, sh, 0, t)) return;
+      const uint32_t full = sh.full + 8 * stage;
+      if (gt == 0) {
+        ptx::mbar_arrive_expect_tx(full, Cfg::kBBytes);
+        ptx::tma_load_3d(b0 + stage * Cfg::kBBytes, tmB, full, kt * p.bk, tc.n0, tc.batch);
+      }
+      const int32_t kbyte = kt * kRowBytes + chunk * 16;
+      const uint32_t kvalid = (kbyte < p.k_bytes) ? 16u : 0u;
+      const uint32_t abase = a0 + stage * Cfg::kABytes;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int r = rsub + 16 * i;
+        const uint32_t dst = abase + r * kRowBytes + ((chunk ^ (r & 7)) << 4);
+        // a zero-byte copy still gets an in-bounds source address
+        const bool live = src[i] >= 0 && kvalid != 0u;
+        const uint8_t* s =
+            live ? p.a_src + static_cast<int64_t>(src[i]) * p.a_src_ld + kbyte : p.a_src;
+        ptx::cp_async_16(dst, s, live ? 16u : 0u);
+      }
+      ptx::cp_async_mbar_arrive_noinc(full);
+      if (++stage == p.stages) { stage = 0; phase ^= 1u; }
+    }
+  }
+}
+
+// ------------------------------------------------------------------ kernel
+
+template <int BN, bool GATHER>
+__global__ void __launch_bounds__(KernelCfg<BN, GATHER>::kThreads, 1)
+    gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                const __grid_constant__ Params p) {
+  using Cfg = KernelCfg<BN, GATHER>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = ptx::smem_addr(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;  // swizzle atoms need 1 KiB alignment
+  uint8_t* base_ptr = smem_raw + (base - raw);
+  const int S = p.stages;
+  const uint32_t a0 = base;
+  const uint32_t b0 = base + S * Cfg::kABytes;
+  uint8_t* ctrl = base_ptr + S * Cfg::kStageBytes;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ctrl + 8 * (2 * S + 4));
+  int32_t* abort_flag = reinterpret_cast<int32_t*>(tmem_slot + 1);
+  int32_t* prefix = reinterpret_cast<int32_t*>(ctrl + kCtrlBytes);
+  int32_t* cu_s = prefix + (kMaxGroups + 1);
+
+  Shared sh;
+  sh.full = ptx::smem_addr(ctrl);
+  sh.empty = sh.full + 8 * S;
+  sh.tfull = sh.empty + 8 * S;
+  sh.tempty = sh.tfull + 16;
+  sh.abort = abort_flag;
+  sh.prefix = prefix;
+  sh.cu = cu_s;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      ptx::mbar_init(sh.full + 8 * s, GATHER ? 1 + kGatherWarps * 32 : 1);
+      ptx::mbar_init(sh.empty + 8 * s, 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      ptx::mbar_init(sh.tfull + 8 * b, 1);
+      ptx::mbar_init(sh.tempty + 8 * b, kEpiWarps);
+    }
+    *abort_flag = 0;
+    ptx::fence_barrier_init();
+  }
+  if (warp == kLoadWarp && lane == 0) {
+    ptx::prefetch_tmap(&tmA);
+    ptx::prefetch_tmap(&tmB);
+  }
+  if (warp == kMmaWarp) {
+    ptx::tmem_alloc(ptx::smem_addr(tmem_slot), Cfg::kTmemCols);
+    ptx::tmem_relinquish();
+    ptx::tc_fence_before();
+  }
+  // varlen-M: copy cu_seqlens and build the per-group tile prefix (warp 0)
+  if (p.num_groups > 0 && warp == 0) {
+    const int G = p.num_groups;
+    const int per = (G + 31) / 32;
+    const int g0 = min(lane * per, G), g1 = min(g0 + per, G);
+    int32_t mine = 0;
+    for (int g = g0; g < g1; ++g) {
+      const int32_t lo = __ldg(p.cu_seqlens + g), hi = __ldg(p.cu_seqlens + g + 1);
+      if (lo < 0 || hi > p.M || hi < lo) record_status(p, DEV_INDEX_RANGE, 5, g);
+      const int32_t len = max(0, min(hi, p.M) - max(lo, 0));
+      mine += ((len + kBM - 1) / kBM) * p.tiles_n;
+    }
+    int32_t incl = mine;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    int32_t run = incl - mine;
+    for (int g = g0; g < g1; ++g) {
+      const int32_t lo = __ldg(p.cu_seqlens + g), hi = __ldg(p.cu_seqlens + g + 1);
+      const int32_t clo = max(lo, 0);
+      const int32_t len = max(0, min(hi, p.M) - clo);
+      prefix[g] = run;
+      cu_s[g] = clo;
+      run += ((len + kBM - 1) / kBM) * p.tiles_n;
+    }
+    if (lane == 31) {
+      prefix[G] = incl;
+      cu_s[G] = min(max(__ldg(p.cu_seqlens + G), 0), p.M);
+    }
+  }
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const int32_t num_tiles = (p.num_groups > 0) ? prefix[p.num_groups] : p.num_tiles;
+
+  if (warp < kEpiWarps) {
+    epilogue_role<BN, GATHER>(p, sh, tmem_base, num_tiles);
+  } else if (warp == kMmaWarp) {
+    if (lane == 0) mma_role<BN, GATHER>(p, sh, a0, b0, tmem_base, num_tiles);
+  } else if (GATHER) {
+    gather_producer_role<BN>(p, sh, &tmB, a0, b0, num_tiles);
+  } else if (lane == 0) {
+    tma_producer_role<BN, GATHER>(p, sh, &tmA, &tmB, a0, b0, num_tiles);
+  }
+
+  __syncthreads();
+  if (*abort_flag) {
+    // let copies and MMAs that were in flight land before the memory goes away
+    const uint64_t t0 = ptx::globaltimer();
+    while (ptx::globaltimer() - t0 < 200000ull) __nanosleep(1000);
+  }
+  if (warp == kMmaWarp) {
+    __syncwarp();  // lane 0 ran the MMA loop alone; dealloc is warp-collective
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem_base, Cfg::kTmemCols);
+  }
+}
+
+}  // namespace gge

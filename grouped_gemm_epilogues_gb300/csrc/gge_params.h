@@ -1,0 +1,76 @@
+// Kernel parameter block shared by the host launcher and the device kernel.
+#pragma once
+
+#include <cstdint>
+
+#include "gge_sched.cuh"
+
+namespace gge {
+
+enum : int32_t { DT_BF16 = 0, DT_F16 = 1, DT_E4M3 = 2, DT_E5M2 = 3, DT_F32 = 4 };
+enum : int32_t { ACT_NONE = 0, ACT_RELU = 1, ACT_GELU_TANH = 2, ACT_SILU = 3 };
+
+// Device status words (the first bytes of the caller's workspace).
+enum : int32_t {
+  DEV_OK = 0,
+  DEV_TIMEOUT = 6,      // an mbarrier wait ran past its time limit
+  DEV_INDEX_RANGE = 7,  // a gather index or a group offset was out of range
+};
+
+// Flags (debug / test switches carried in Params::flags).
+enum : int32_t {
+  FLAG_TILE_COUNTS = 1,        // epilogue counts visits per tile into tile_counts
+  FLAG_TEST_DROP_ACC_FULL = 2, // the MMA warp never signals "accumulator full" (timeout test)
+};
+
+struct Params {
+  // problem
+  int32_t M;        // rows per batch (plain) or total output rows (varlen)
+  int32_t N;
+  int32_t K;
+  int32_t L;        // batches (plain)
+  int32_t k_tiles;  // ceil(K / bk)
+  int32_t bk;       // K elements per stage row (128 bytes)
+  int32_t stages;
+  int32_t num_tiles;  // plain only
+  PlainSchedule sched;
+  FastDivmod tiles_n_div;  // varlen: local tile -> (m-tile, n-tile)
+  int32_t tiles_n;
+
+  // varlen-M
+  int32_t num_groups;  // 0: plain batched problem
+  const int32_t* cu_seqlens;
+
+  // gather-A
+  const int32_t* a_idx;   // [L][M] (plain) or [total_M] (varlen)
+  const uint8_t* a_src;   // source matrix base
+  int64_t a_src_ld;       // bytes between source rows
+  int32_t a_src_rows;
+  int32_t k_bytes;        // K * element size (gather K-tail predicate)
+
+  // epilogue
+  void* d;
+  int64_t ldd, sbd;       // elements
+  void* post;
+  int64_t ldp, sbp;
+  const void* c;
+  int64_t ldc, sbc;
+  int32_t d_dtype, p_dtype, c_dtype;
+  int32_t act;
+  float alpha, beta;
+  const float* alpha_dev;
+  const float* beta_dev;
+
+  // MMA
+  uint32_t idesc;
+  int32_t f8;          // operands are 8-bit (kind::f8f6f4)
+  int32_t b_mn_major;  // B staged N-major (16-bit operands only)
+
+  // control
+  int32_t* status;       // workspace: [0] code, [1] where, [2] tile, [3] detail
+  int32_t* tile_counts;  // debug visit counters
+  int32_t flags;
+  uint64_t timeout_ns;
+};
+
+}  // namespace gge

@@ -1,0 +1,104 @@
+// FastDivmod and the persistent tile schedule (host + device).
+//
+// FastDivmod follows quack/fast_math.py (quack-kernels 0.2.0): for a divisor
+// d, p = 31 + ceil(log2 d), multiplier = ceil(2^p / d), shift = p - 32, and
+// n / d = umulhi(n, multiplier) >> shift for 0 <= n < 2^31 (d == 1 is passed
+// through, since its shift would be -1).  It is exact on that domain
+// (Granlund & Montgomery 1994: m*d - 2^p lies in [0, d), so the error term
+// n*(m*d - 2^p) < 2^31 * 2^ceil(log2 d) = 2^p never reaches the next integer).
+//
+// The plain schedule maps a linear tile index to (batch, m-tile, n-tile):
+// batches outermost, then bands of `band` m-tiles; inside a band the m-tile
+// varies fastest, so CTAs that run at the same time share B tiles and a
+// band's A rows, which keeps the working set of one wave inside L2.
+// This plays the role of the pages' raster order / max_swizzle_size
+// (quack/dense_gemm_sm90.py, GemmSm90 tile scheduler arguments).
+#pragma once
+
+#include <cstdint>
+
+#if defined(__CUDACC__)
+#define GGE_HD __host__ __device__ __forceinline__
+#else
+#define GGE_HD inline
+#endif
+
+namespace gge {
+
+struct FastDivmod {
+  int32_t divisor;
+  uint32_t multiplier;
+  uint32_t shift;
+
+  static inline FastDivmod create(int32_t d) {
+    FastDivmod f;
+    f.divisor = d;
+    // ceil(log2 d): floor(log2 d) plus one unless d is a power of two
+    int lg = 0;
+    while ((1u << lg) < static_cast<uint32_t>(d) && lg < 31) ++lg;
+    const uint32_t p = 31u + static_cast<uint32_t>(lg);
+    const uint64_t num = (uint64_t(1) << p) + static_cast<uint64_t>(d) - 1u;
+    f.multiplier = static_cast<uint32_t>(num / static_cast<uint64_t>(d));
+    f.shift = p - 32u;  // wraps to 0xffffffff for d == 1, never used then
+    return f;
+  }
+
+  GGE_HD int32_t div(int32_t n) const {
+    if (divisor == 1) return n;
+#if defined(__CUDA_ARCH__)
+    uint32_t hi;
+    asm("mul.hi.u32 %0, %1, %2;" : "=r"(hi) : "r"(static_cast<uint32_t>(n)), "r"(multiplier));
+#else
+    const uint32_t hi = static_cast<uint32_t>(
+        (static_cast<uint64_t>(static_cast<uint32_t>(n)) * multiplier) >> 32);
+#endif
+    return static_cast<int32_t>(hi >> shift);
+  }
+
+  GGE_HD void divmod(int32_t n, int32_t& q, int32_t& r) const {
+    q = div(n);
+    r = n - q * divisor;
+  }
+};
+
+struct PlainSchedule {
+  int32_t tiles_m, tiles_n, batches;
+  int32_t band;          // m-tiles per raster band
+  int32_t full_bands;    // tiles_m / band
+  int32_t num_tiles;     // tiles_m * tiles_n * batches
+  FastDivmod per_batch;  // tiles_m * tiles_n
+  FastDivmod band_tiles; // band * tiles_n
+  FastDivmod band_rows;  // band
+  FastDivmod tail_rows;  // tiles_m % band (1 when the bands divide evenly)
+
+  static inline PlainSchedule create(int32_t tiles_m, int32_t tiles_n, int32_t batches,
+                                     int32_t band) {
+    PlainSchedule s;
+    if (band < 1) band = 1;
+    if (band > tiles_m) band = tiles_m > 0 ? tiles_m : 1;
+    s.tiles_m = tiles_m;
+    s.tiles_n = tiles_n;
+    s.batches = batches;
+    s.band = band;
+    s.full_bands = tiles_m / band;
+    s.num_tiles = tiles_m * tiles_n * batches;
+    s.per_batch = FastDivmod::create(tiles_m * tiles_n > 0 ? tiles_m * tiles_n : 1);
+    s.band_tiles = FastDivmod::create(band * (tiles_n > 0 ? tiles_n : 1));
+    s.band_rows = FastDivmod::create(band);
+    const int32_t tail = tiles_m % band;
+    s.tail_rows = FastDivmod::create(tail > 0 ? tail : 1);
+    return s;
+  }
+
+  // t in [0, num_tiles)  ->  (batch, m-tile, n-tile)
+  GGE_HD void map(int32_t t, int32_t& l, int32_t& mb, int32_t& nb) const {
+    int32_t r, b, w, i;
+    per_batch.divmod(t, l, r);
+    band_tiles.divmod(r, b, w);
+    const FastDivmod& rows = (b < full_bands) ? band_rows : tail_rows;
+    rows.divmod(w, nb, i);
+    mb = b * band + i;
+  }
+};
+
+}  // namespace gge

@@ -1,0 +1,211 @@
+/*
+ * gge.h -- C ABI of libgge.so: fused persistent GEMM epilogues on one GB300
+ * (sm_103a).
+ *
+ * The operation is the one the QuACK pages implement for Hopper
+ * (quack-kernels 0.2.0: quack/dense_gemm_sm90.py ``GemmSm90``,
+ * quack/gemm_act_sm90.py ``GemmActSm90`` / ``gemm_act_sm90``):
+ *
+ *   D[m,n,l]       = alpha * sum_k A[m,k,l] * B[n,k,l] + beta * C[m,n,l]
+ *   PostAct[m,n,l] = act( same value, before rounding )
+ *
+ * with fp32 accumulation; each output is rounded once (round to nearest even)
+ * to its own dtype.  Without C there is no beta term (the pages' epilogue
+ * visit adds ``beta * C`` only when C is given).
+ *
+ * Conventions for every entry point:
+ *   - All tensor pointers are DEVICE pointers owned by the caller.  Nothing is
+ *     allocated, freed or synchronised by the library (except
+ *     gge_read_device_status, which synchronises the given stream).
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default).
+ *   - Validation happens on the host before any launch; a rejected call
+ *     launches nothing and returns GGE_ERR_INVALID_ARG / GGE_ERR_UNSUPPORTED /
+ *     GGE_ERR_ALIGNMENT / GGE_ERR_WORKSPACE.  A failed launch returns
+ *     GGE_ERR_CUDA.  Faults found on the device (a wait that ran out of time,
+ *     a gather index or group offset out of range) are written to the
+ *     workspace and read back with gge_read_device_status.
+ *   - Strides are in ELEMENTS.  The contiguous dimension of every tensor must
+ *     have stride 1, every other stride and every base pointer must be 16-byte
+ *     aligned (the pages' rule: the contiguous dimension 16-byte aligned).
+ *   - Sizes are int64 in the structs but every extent must be < 2^31.
+ */
+#ifndef GGE_H_
+#define GGE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* gge_stream_t; /* same type as cudaStream_t */
+
+typedef enum gge_status {
+  GGE_OK = 0,
+  GGE_ERR_INVALID_ARG = 1, /* NULL where a pointer is required, inconsistent shapes */
+  GGE_ERR_UNSUPPORTED = 2, /* valid request outside what the kernels implement      */
+  GGE_ERR_ALIGNMENT = 3,   /* base pointer or stride not 16-byte aligned             */
+  GGE_ERR_WORKSPACE = 4,   /* workspace NULL or smaller than gge_workspace_size      */
+  GGE_ERR_CUDA = 5,        /* a CUDA runtime / driver call failed                    */
+  GGE_ERR_TIMEOUT = 6,     /* device: a pipeline wait ran past its time limit        */
+  GGE_ERR_INDEX_RANGE = 7  /* device: gather index / group offset out of range       */
+} gge_status;
+
+typedef enum gge_dtype {
+  GGE_BF16 = 0,
+  GGE_F16 = 1,
+  GGE_E4M3 = 2, /* float8_e4m3fn */
+  GGE_E5M2 = 3, /* float8_e5m2   */
+  GGE_F32 = 4
+} gge_dtype;
+
+/* Activations of the fused epilogue.  The pages list relu and
+ * gelu_tanh_approx (quack/gemm_act_sm90.py ``act_fn_map``); SiLU is the
+ * textbook x / (1 + exp(-x)). */
+typedef enum gge_act {
+  GGE_ACT_NONE = 0,
+  GGE_ACT_RELU = 1,      /* x > 0 ? x : 0                                        */
+  GGE_ACT_GELU_TANH = 2, /* 0.5 x (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3)))      */
+  GGE_ACT_SILU = 3       /* x / (1 + exp(-x))                                    */
+} gge_act;
+
+/* A strided 3-D view [rows, cols, batch]. */
+typedef struct gge_tensor {
+  void* ptr;            /* device pointer to element [0,0,0]                    */
+  int32_t dtype;        /* gge_dtype                                            */
+  int32_t reserved;     /* must be 0                                            */
+  int64_t rows, cols, batch;
+  int64_t stride_row, stride_col, stride_batch; /* in elements                  */
+} gge_tensor;
+
+/* Optional tuning / debug knobs; pass NULL for the defaults. */
+typedef struct gge_config {
+  int32_t tile_n;         /* 0 = auto; else 64, 128 or 256 output columns per tile */
+  int32_t num_ctas;       /* 0 = one persistent CTA per SM                         */
+  int32_t raster_band;    /* 0 = auto; m-tiles per raster band (plain problems)    */
+  int32_t stages;         /* 0 = as many as shared memory holds                    */
+  int32_t flags;          /* bit 0: count tile visits into tile_counts            */
+  int32_t reserved;
+  int32_t* tile_counts;   /* device int32 per tile (debug coverage), or NULL       */
+  uint64_t timeout_ns;    /* 0 = default (2 s) limit for each pipeline wait        */
+} gge_config;
+
+/*
+ * Arguments of one GEMM.
+ *   A : [M, K, L]  rows = M, cols = K.  K-major (stride_col == 1).  In the
+ *       gather form A is the SOURCE matrix [rows_src, K, 1].
+ *   B : [N, K, L]  rows = N, cols = K.  K-major (stride_col == 1) or, for
+ *       16-bit operands, N-major (stride_row == 1).  8-bit operands must be
+ *       K-major (as on the pages).
+ *   C : optional [M, N, L] input, N-major.  NULL: no beta term.
+ *   D : optional [M, N, L] output, N-major.
+ *   PostAct : optional [M, N, L] output of act(...), N-major.  Required when
+ *       act != GGE_ACT_NONE.
+ *   Dtypes: A and B both 16-bit and equal (bf16 or f16), or both 8-bit
+ *       (e4m3 / e5m2 in any combination).  C, D, PostAct: bf16, f16 or f32.
+ *   N must be a multiple of 8.
+ *   alpha_dev / beta_dev: optional device float scalars that override alpha /
+ *       beta (read once per CTA).
+ */
+typedef struct gge_gemm_args {
+  gge_tensor A;
+  gge_tensor B;
+  const gge_tensor* C;
+  const gge_tensor* D;
+  const gge_tensor* PostAct;
+  float alpha;
+  float beta;
+  const float* alpha_dev;
+  const float* beta_dev;
+  int32_t act;               /* gge_act */
+  int32_t reserved;
+  const gge_config* config;  /* NULL = defaults */
+} gge_gemm_args;
+
+/* Bytes of device workspace a call needs (status words); the workspace is
+ * caller-owned, at least 16-byte aligned, and must be zeroed once before first
+ * use.  It is reusable across calls on the same stream. */
+size_t gge_workspace_size(const gge_gemm_args* args, int32_t num_groups);
+
+/* D = alpha A B^T + beta C (PostAct must be NULL and act NONE).
+ * Page: quack/dense_gemm_sm90.py, gemm_sm90 / GemmSm90.epi_visit_acc_subtile. */
+gge_status gge_gemm(const gge_gemm_args* args, void* workspace, size_t workspace_bytes,
+                    gge_stream_t stream);
+
+/* D (optional) and PostAct = act(alpha A B^T + beta C), act applied to the
+ * unrounded fp32 value.  Page: quack/gemm_act_sm90.py, gemm_act_sm90 /
+ * GemmActSm90.epi_visit_acc_subtile. */
+gge_status gge_gemm_act(const gge_gemm_args* args, void* workspace, size_t workspace_bytes,
+                        gge_stream_t stream);
+
+/* Varlen-M grouped GEMM: A is [total_M, K, 1], B is [N, K, G] (batch = G
+ * groups), C / D / PostAct are [total_M, N, 1].  Group g owns rows
+ * cu_seqlens_m[g] .. cu_seqlens_m[g+1]-1 and multiplies them by B[:,:,g];
+ * rows outside every group are not written.  cu_seqlens_m: DEVICE int32
+ * [G+1], non-decreasing, cu[0] >= 0, cu[G] <= total_M (violations are
+ * clamped and reported as GGE_ERR_INDEX_RANGE by gge_read_device_status).
+ * 1 <= G <= 1024.  act as in gge_gemm_act.
+ * Page: quack/dense_gemm_sm90.py, GemmSm90 with VarlenArguments(mCuSeqlensM). */
+gge_status gge_gemm_varlen_m(const gge_gemm_args* args, const int32_t* cu_seqlens_m,
+                             int32_t num_groups, void* workspace, size_t workspace_bytes,
+                             gge_stream_t stream);
+
+/* Gather-A GEMM: row r of the effective A is row a_idx[r] of the source
+ * matrix args->A ([rows_src, K, 1], K-major, 16-bit).  With cu_seqlens_m
+ * (DEVICE int32 [G+1]) it is the varlen-M problem above, a_idx being
+ * [total_M] with total_M = rows of D / PostAct; with cu_seqlens_m == NULL it
+ * is a plain batched problem of M = rows of D per batch and a_idx [L][M].
+ * An index outside [0, rows_src) reads zeros and is reported as
+ * GGE_ERR_INDEX_RANGE.  Page: quack/dense_gemm_sm90.py,
+ * GemmSm90.load_AB_gather_A (mAIdx). */
+gge_status gge_gemm_gather_a(const gge_gemm_args* args, const int32_t* a_idx,
+                             const int32_t* cu_seqlens_m, int32_t num_groups, void* workspace,
+                             size_t workspace_bytes, gge_stream_t stream);
+
+/* Synchronises `stream`, returns the device status recorded in `workspace`
+ * since it was last cleared (GGE_OK, GGE_ERR_TIMEOUT or GGE_ERR_INDEX_RANGE)
+ * and clears it.  `detail` (may be NULL) receives [where, tile]. */
+gge_status gge_read_device_status(void* workspace, gge_stream_t stream, int32_t* detail);
+
+const char* gge_status_string(gge_status status);
+
+/* ---- host-side helpers (no GPU needed) -------------------------------- */
+
+/* FastDivmod parameters as quack/fast_math.py FastDivmod.create builds them:
+ * p = 31 + ceil(log2 d), multiplier = ceil(2^p / d), shift = p - 32. */
+void gge_fastdivmod_params(int32_t divisor, uint32_t* multiplier, uint32_t* shift);
+
+/* q = n / d by the FastDivmod formula (host build of the device code),
+ * for 0 <= n < 2^31. */
+int32_t gge_fastdivmod_div(int32_t divisor, int32_t n);
+
+/* The plain persistent schedule: tile index t -> (batch, m-tile, n-tile) for a
+ * grid of tiles_m x tiles_n tiles per batch and `batches` batches, with
+ * `band` m-tiles per raster band.  Writes `count` triples into out[3*count]
+ * for t = 0 .. count-1.  Returns the number of tiles of the problem. */
+int32_t gge_schedule_map(int32_t tiles_m, int32_t tiles_n, int32_t batches, int32_t band,
+                         int32_t count, int32_t* out);
+
+/* The launch plan the library would use for `args` (tile and pipeline
+ * shape).  Returns GGE_OK or the validation error of the call. */
+typedef struct gge_plan_info {
+  int32_t tile_m, tile_n, tile_k, stages;
+  int32_t num_tiles;  /* plain problems; -1 for varlen (known on the device only) */
+  int32_t grid;
+  int32_t threads;
+  int32_t smem_bytes;
+  int32_t raster_band;
+  int32_t reserved;
+} gge_plan_info;
+gge_status gge_plan(const gge_gemm_args* args, int32_t num_groups, int32_t gather,
+                    gge_plan_info* out);
+
+/* Library version string. */
+const char* gge_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GGE_H_ */

@@ -1,0 +1,149 @@
+"""The C-ABI library loads, exports every declared symbol, and its host-side
+logic (validation, FastDivmod, schedule, plan) is right -- no GPU needed."""
+
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+import torch
+
+from grouped_gemm_epilogues_gb300 import binding
+from oracle import fastdivmod as fdm
+from oracle import tiles as ot
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+GOLDEN = os.path.join(ROOT, "tests", "golden")
+
+
+@pytest.fixture(scope="module")
+def L():
+    return binding.load()
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "gge.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(gge_[a-z_0-9]+)\s*\(", src)))
+
+
+def test_exports_every_declared_symbol(L):
+    names = declared_functions()
+    assert "gge_gemm" in names and "gge_gemm_gather_a" in names
+    for n in names:
+        assert hasattr(L, n), n
+    assert set(names) == set(binding._SIGNATURES), "binding signatures out of sync with gge.h"
+
+
+def test_version_and_status_strings(L):
+    assert b"sm_103a" in L.gge_version()
+    for code in range(8):
+        assert L.gge_status_string(code)
+
+
+def test_fastdivmod_params_match_oracle_golden(L):
+    rows = [ln.split() for ln in open(os.path.join(GOLDEN, "fastdivmod_params.txt"))
+            if not ln.startswith("#")]
+    for d, m, s in rows:
+        mm, ss = ctypes.c_uint32(), ctypes.c_uint32()
+        L.gge_fastdivmod_params(int(d), ctypes.byref(mm), ctypes.byref(ss))
+        assert (mm.value, ss.value) == (int(m), int(s)), d
+        assert fdm.create(int(d))[1:] == (int(m), int(s))
+
+
+def test_fastdivmod_host_division(L):
+    rng = np.random.default_rng(0)
+    for d in [1, 2, 3, 7, 12, 32, 1000, 65537, 2 ** 31 - 1] + list(rng.integers(1, 2 ** 31, 8)):
+        for n in list(rng.integers(0, 2 ** 31, 300)) + [0, d - 1, d, 2 ** 31 - 1]:
+            if 0 <= n < 2 ** 31:
+                assert L.gge_fastdivmod_div(int(d), int(n)) == int(n) // int(d)
+
+
+@pytest.mark.parametrize("tm,tn,lb,band", [(64, 32, 1, 16), (16, 16, 16, 16), (3, 5, 2, 2),
+                                            (7, 3, 1, 4), (2, 1, 1, 16), (256, 6, 1, 8),
+                                            (1, 1, 1, 1), (33, 7, 3, 5)])
+def test_schedule_covers_every_tile_once(L, tm, tn, lb, band):
+    n = tm * tn * lb
+    out = (ctypes.c_int32 * (3 * n))()
+    assert L.gge_schedule_map(tm, tn, lb, band, n, out) == n
+    got = [tuple(out[3 * i:3 * i + 3]) for i in range(n)]
+    assert len(set(got)) == n
+    assert set(got) == ot.plain_tiles(tm * 128, tn * 256, lb, 128, 256)
+
+
+def _args(M=256, N=256, K=256, dt=torch.bfloat16, out=torch.bfloat16, **kw):
+    A = torch.zeros(M, K, dtype=dt)
+    B = torch.zeros(N, K, dtype=dt)
+    D = torch.zeros(M, N, dtype=out)
+    return binding.make_args(A, B, D=D, **kw), (A, B, D)
+
+
+def _call(L, args, ws=None, nbytes=0):
+    return L.gge_gemm(ctypes.byref(args), ws, nbytes, None)
+
+
+def test_validation_rejects_before_any_launch(L):
+    args, keep = _args()
+    bad = binding.make_args(*keep[:2], D=keep[2])
+    bad.A.ptr = None
+    assert _call(L, bad) == 1                                   # NULL pointer
+    bad = binding.make_args(*keep[:2], D=keep[2])
+    bad.A.ptr = ctypes.c_void_p(keep[0].data_ptr() + 2)
+    assert _call(L, bad) == 3                                   # misaligned base
+    bad = binding.make_args(*keep[:2], D=keep[2])
+    bad.B.rows = 128
+    assert _call(L, bad) == 1                                   # shape mismatch
+    A8 = torch.zeros(256, 256, dtype=torch.float8_e4m3fn)
+    B16 = torch.zeros(256, 256, dtype=torch.bfloat16)
+    bad = binding.make_args(A8, B16, D=keep[2])
+    assert _call(L, bad) == 2                                   # mixed 8/16-bit operands
+    Bn = torch.zeros(256, 256, dtype=torch.float8_e5m2).t()
+    bad = binding.make_args(A8, Bn, D=keep[2])
+    assert _call(L, bad) == 2                                   # 8-bit N-major B
+    bad = binding.make_args(keep[0], keep[1], D=torch.zeros(256, 256, dtype=torch.bfloat16).t())
+    assert _call(L, bad) == 2                                   # M-major output
+    P = torch.zeros(256, 256, dtype=torch.bfloat16)
+    bad = binding.make_args(keep[0], keep[1], D=keep[2], PostAct=P, act="relu")
+    assert _call(L, bad) == 1                                   # gge_gemm takes no PostAct
+    good, _ = _args()
+    assert _call(L, good, ctypes.c_void_p(16), 8) == 4          # workspace too small
+    bad = binding.make_args(torch.zeros(256, 250, dtype=torch.bfloat16),
+                            torch.zeros(256, 250, dtype=torch.bfloat16), D=keep[2])
+    assert _call(L, bad) == 3                                   # row stride not 16-byte aligned
+    bad = binding.make_args(torch.zeros(256, 256, dtype=torch.bfloat16),
+                            torch.zeros(252, 256, dtype=torch.bfloat16),
+                            D=torch.zeros(256, 252, dtype=torch.bfloat16))
+    assert _call(L, bad) in (2, 3)                              # N not a multiple of 8
+
+
+def test_act_entry_requires_postact(L):
+    args, keep = _args()
+    assert L.gge_gemm_act(ctypes.byref(args), None, 0, None) == 1
+
+
+def test_varlen_argument_checks(L):
+    A = torch.zeros(1000, 128, dtype=torch.bfloat16)
+    B = torch.zeros(4, 256, 128, dtype=torch.bfloat16)
+    D = torch.zeros(1000, 256, dtype=torch.bfloat16)
+    cu = torch.zeros(5, dtype=torch.int32)
+    args = binding.make_args(A, B, D=D)
+    assert L.gge_gemm_varlen_m(ctypes.byref(args), None, 4, None, 0, None) == 1
+    assert L.gge_gemm_varlen_m(ctypes.byref(args), ctypes.c_void_p(cu.data_ptr()), 0, None, 0,
+                               None) == 2
+    assert L.gge_gemm_varlen_m(ctypes.byref(args), ctypes.c_void_p(cu.data_ptr()), 3, None, 0,
+                               None) == 1  # B has 4 groups
+
+
+def test_plan_without_gpu(L):
+    A = torch.zeros(8192, 8192, dtype=torch.bfloat16)
+    D = torch.zeros(8192, 8192, dtype=torch.bfloat16)
+    cfg = binding.make_config(num_ctas=152)
+    info = binding.gge_plan(A, A, D=D, config=cfg)
+    assert info["tile_m"] == 128 and info["tile_n"] == 256 and info["tile_k"] == 64
+    assert info["num_tiles"] == 64 * 32 and info["grid"] == 152
+    assert 2 <= info["stages"] <= 8 and info["smem_bytes"] <= 232448
+    A8 = torch.zeros(512, 512, dtype=torch.float8_e4m3fn)
+    D8 = torch.zeros(512, 512, dtype=torch.bfloat16)
+    info = binding.gge_plan(A8, A8.to(torch.float8_e5m2), D=D8, config=cfg)
+    assert info["tile_k"] == 128

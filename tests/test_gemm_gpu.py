@@ -1,0 +1,174 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle.
+
+Small cases span several tiles in M and N plus ragged tails in M, N and K;
+the named workloads run at full size with the oracle evaluated on sampled
+rows (every batch, rows from the first, last and a middle tile)."""
+
+import numpy as np
+import pytest
+import torch
+
+from grouped_gemm_epilogues_gb300 import binding, workloads as wl
+from oracle import activations, formats
+from oracle import gemm as og
+
+from helpers import FMT, FMT_NAME, check, dec, oracle_plain
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def _outputs(w, M, N, L, device=DEV, pad=0, fill=float("nan")):
+    """D / PostAct buffers; pad > 0 adds guard columns that must stay untouched."""
+    out = {}
+    for key, dt in (("D", w.d_dtype), ("P", w.p_dtype)):
+        if dt is None:
+            continue
+        full = torch.full((L, M, N + pad), fill, dtype=wl.DT[dt], device=device)
+        out[key] = full[:, :, :N] if pad else full
+        out[key + "_full"] = full
+    return out
+
+
+def _run_plain(w, t, out, config=None):
+    A, B = t["A"].to(DEV), t["B"].to(DEV)
+    C = t["C"].to(DEV) if "C" in t else None
+    if w.act == "none" and "P" not in out:
+        binding.gge_gemm(A, B, out["D"], C=C, alpha=w.alpha, beta=w.beta, config=config)
+    else:
+        binding.gge_gemm_act(A, B, out["P"], w.act, D=out.get("D"), C=C, alpha=w.alpha,
+                             beta=w.beta, config=config)
+    torch.cuda.synchronize()
+    assert binding.gge_read_device_status()[0] == "GGE_OK"
+
+
+def _check_plain(w, t, out, rows=None):
+    ref = oracle_plain(t, w, rows)
+    worst = []
+    if "D" in out:
+        got = out["D"].cpu()
+        if rows is not None:
+            got = got[:, rows]
+        worst.append(check(got, ref["D"], ref["bound"], FMT_NAME[w.d_dtype], "none", "D"))
+    if "P" in out:
+        got = out["P"].cpu()
+        if rows is not None:
+            got = got[:, rows]
+        worst.append(check(got, ref["P"], ref["bound"], FMT_NAME[w.p_dtype], w.act, "PostAct"))
+    return worst
+
+
+SMALL = [
+    # (base workload, M, N, K, L, overrides)
+    ("gemm_256_bf16", 256, 256, 256, 1, {}),
+    ("gemm_256_bf16", 200, 136, 72, 1, {}),
+    ("gemm_256_bf16", 300, 520, 200, 1, {}),
+    ("gemm_256_bf16", 129, 264, 8, 2, {}),
+    ("gemm_256_bf16", 1, 8, 64, 1, {}),
+    ("gemm_act_4096_bf16_gelu", 384, 512, 256, 1, {}),
+    ("gemm_act_4096_bf16_gelu", 333, 392, 136, 2, {}),
+    ("gemm_act_4096_bf16_gelu", 256, 256, 512, 1, {"act": "silu"}),
+    ("gemm_act_4096_bf16_gelu", 256, 256, 512, 1, {"act": "relu", "d_dtype": "f32",
+                                                   "p_dtype": "f16"}),
+    ("gemm_act_4096_bf16_gelu", 256, 256, 128, 1, {"alpha": 0.0, "beta": -1.5}),
+    ("gemm_8192_f16_relu", 296, 384, 320, 3, {}),
+    ("gemm_8192_f16_relu", 128, 640, 136, 1, {"b_major": "k"}),
+    ("gemm_8192_f16_relu", 260, 256, 200, 2, {"d_dtype": "f16", "act": "gelu_tanh"}),
+    ("gemm_8192_fp8", 384, 512, 512, 1, {}),
+    ("gemm_8192_fp8", 200, 264, 256, 2, {"ab_dtype": "e5m2", "b_dtype": "e4m3"}),
+    ("gemm_8192_fp8", 256, 256, 1024, 1, {"ab_dtype": "e4m3", "b_dtype": "e4m3",
+                                         "act": "silu", "p_dtype": "bf16"}),
+]
+
+
+@pytest.mark.parametrize("case", SMALL, ids=lambda c: f"{c[0]}-{c[1]}x{c[2]}x{c[3]}x{c[4]}-{c[5]}")
+def test_small_parity(case):
+    name, M, N, K, L, kw = case
+    w = wl.small(name, M, N, K, L, **kw)
+    t = wl.make(w)
+    out = _outputs(w, M, N, L)
+    _run_plain(w, t, out)
+    _check_plain(w, t, out)
+
+
+@pytest.mark.parametrize("tile_n", [128, 256])
+def test_tile_shapes_and_guard_columns(tile_n):
+    w = wl.small("gemm_act_4096_bf16_gelu", 392, 264, 320, 2)
+    t = wl.make(w)
+    out = _outputs(w, 392, 264, 2, pad=24, fill=7.0)
+    _run_plain(w, t, out, config=binding.make_config(tile_n=tile_n))
+    _check_plain(w, t, out)
+    for k in ("D_full", "P_full"):
+        assert (out[k][:, :, 264:].float() == 7.0).all()
+
+
+def test_k_zero_gives_beta_c():
+    w = wl.small("gemm_act_4096_bf16_gelu", 128, 256, 0, 1)
+    t = wl.make(w)
+    out = _outputs(w, 128, 256, 1)
+    _run_plain(w, t, out)
+    _check_plain(w, t, out)
+
+
+def test_device_scalars_override():
+    w = wl.small("gemm_act_4096_bf16_gelu", 256, 256, 128, 1, alpha=0.75, beta=-0.25)
+    t = wl.make(w)
+    out = _outputs(w, 256, 256, 1)
+    a = torch.tensor([0.75], device=DEV)
+    b = torch.tensor([-0.25], device=DEV)
+    binding.gge_gemm_act(t["A"].to(DEV), t["B"].to(DEV), out["P"], w.act, D=out["D"],
+                         C=t["C"].to(DEV), alpha=99.0, beta=99.0, alpha_dev=a, beta_dev=b)
+    torch.cuda.synchronize()
+    _check_plain(w, t, out)
+
+
+def test_deterministic():
+    w = wl.small("gemm_act_4096_bf16_gelu", 512, 512, 1024, 1)
+    t = wl.make(w)
+    o1 = _outputs(w, 512, 512, 1)
+    o2 = _outputs(w, 512, 512, 1)
+    _run_plain(w, t, o1)
+    _run_plain(w, t, o2)
+    assert torch.equal(o1["D"].view(torch.int16), o2["D"].view(torch.int16))
+    assert torch.equal(o1["P"].view(torch.int16), o2["P"].view(torch.int16))
+
+
+def test_schedule_covers_each_tile_once():
+    w = wl.small("gemm_256_bf16", 1000, 776, 64, 3)
+    t = wl.make(w)
+    out = _outputs(w, 1000, 776, 3)
+    tiles = 8 * 4 * 3
+    counts = torch.zeros(tiles, dtype=torch.int32, device=DEV)
+    cfg = binding.make_config(flags=1, tile_counts=counts, num_ctas=7, raster_band=3)
+    _run_plain(w, t, out, config=cfg)
+    assert (counts.cpu() == 1).all()
+    _check_plain(w, t, out)
+
+
+def _sample_rows(M, BM=128, n=96, seed=0):
+    rng = np.random.default_rng(seed)
+    rows = set(range(0, min(M, BM)))               # the first tile
+    rows |= set(range(max(0, M - 40), M))          # the tail
+    rows |= set(int(x) for x in rng.integers(0, M, n))
+    return np.array(sorted(rows))
+
+
+FULL = ["gemm_256_bf16", "gemm_act_4096_bf16_gelu", "gemm_8192_f16_relu",
+        "bgemm_2048x2048x4096x16_f16_relu", "gemm_8192_fp8", "gemm_act_8192_bf16_gelu"]
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name", FULL)
+def test_full_size_sampled(name):
+    w = wl.WORKLOADS[name]
+    t = wl.make(w)
+    out = _outputs(w, w.M, w.N, w.L)
+    _run_plain(w, t, out)
+    rows = None if w.M * w.N * w.K * w.L <= 2 ** 27 else _sample_rows(w.M)
+    _check_plain(w, t, out, rows)
+    # properties over every element: finite, and PostAct consistent with its activation
+    for k in ("D", "P"):
+        if k in out:
+            assert torch.isfinite(out[k].float()).all()
+    if "P" in out and w.act == "relu":
+        assert (out["P"].float() >= 0).all()
