@@ -1,0 +1,458 @@
+"""Throughput of the fused GEMM hot path on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+One step is one call of the hot path (one persistent-kernel launch through
+the C ABI) over one batch of seeded synthetic input of the named workload
+(default: 4096^3 bf16 GEMM + C (beta 0.5) + gelu_tanh writing D and PostAct).
+Inputs are resident in HBM; consecutive steps rotate over input sets whose
+total size exceeds the 129 MB L2, so no step reads warm operands.  Device
+time comes from CUDA events on the launching stream around exactly K steps,
+bracketed by a barrier and a synchronize; rank 0 prints one JSON line.
+
+Under torchrun (N > 1) each rank runs the same problem on its own GPU (the
+problems are independent: weak scaling, no collective on the data path) and
+the max time over ranks is used.
+
+``--impl reference`` times the CPU oracle on the host cores on a bounded
+sample of the same workload (the reference arm of this build).
+"""
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from grouped_gemm_epilogues_gb300 import workloads as wl  # noqa: E402
+
+METRIC = "TFLOP/s per GEMM shape and % of GB300 dense bf16/fp8 tensor peak (1 GPU)"
+DEFAULT_WORKLOAD = "gemm_act_4096_bf16_gelu"
+L2_BYTES = 129 * 1024 * 1024
+NOMINAL_PEAK = {"bf16": 2250.0, "f16": 2250.0, "e4m3": 4500.0, "e5m2": 4500.0}
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# ------------------------------------------------------------------ helpers
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "grouped_gemm_epilogues_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel sources."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+    except (OSError, ValueError):
+        return None
+    e = d.get(workload)
+    if not e or e.get("kernel_hash") != kernel_source_hash():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+        self.t = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.t.join(timeout=2)
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax = float(parts[1])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------- our arm (GPU)
+
+def _device_sets(w, dev, n_sets):
+    sets = []
+    base = wl.make(w)
+    for i in range(n_sets):
+        s = {}
+        for k, v in base.items():
+            if isinstance(v, torch.Tensor):
+                s[k] = v.to(dev) if i == 0 else v.to(dev).clone()
+        if i > 0:  # distinct values per set (same distribution): permute A rows
+            s["A"] = torch.roll(s["A"], shifts=i, dims=-2).contiguous()
+        L = 1 if w.groups else w.L
+        shape = (w.M, w.N) if w.groups else (L, w.M, w.N)
+        if w.d_dtype:
+            s["D"] = torch.empty(shape, dtype=wl.DT[w.d_dtype], device=dev)
+        if w.p_dtype:
+            s["P"] = torch.empty(shape, dtype=wl.DT[w.p_dtype], device=dev)
+        sets.append(s)
+    return base, sets
+
+
+def _set_bytes(s):
+    return sum(v.numel() * v.element_size() for v in s.values() if isinstance(v, torch.Tensor))
+
+
+def _step_fn(w, binding):
+    def step(s):
+        if w.groups:
+            if w.gather_rows:
+                binding.gge_gemm_gather_a(s["A"], s["B"], s["a_idx"], s["cu_seqlens_m"],
+                                          D=s.get("D"), PostAct=s.get("P"), act=w.act,
+                                          C=s.get("C"), alpha=w.alpha, beta=w.beta)
+            else:
+                binding.gge_gemm_varlen_m(s["A"], s["B"], s["cu_seqlens_m"], D=s.get("D"),
+                                          PostAct=s.get("P"), act=w.act, C=s.get("C"),
+                                          alpha=w.alpha, beta=w.beta)
+        elif w.act == "none" and "P" not in s:
+            binding.gge_gemm(s["A"], s["B"], s["D"], C=s.get("C"), alpha=w.alpha, beta=w.beta)
+        else:
+            binding.gge_gemm_act(s["A"], s["B"], s["P"], w.act, D=s.get("D"), C=s.get("C"),
+                                 alpha=w.alpha, beta=w.beta)
+    return step
+
+
+def run_ours(args, w):
+    from grouped_gemm_epilogues_gb300 import binding
+
+    ws_n, rank, local = dist_env()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    if ws_n > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    binding.load()
+
+    base, probe = _device_sets(w, dev, 1)
+    per_set = _set_bytes(probe[0])
+    n_sets = max(2, int(np.ceil(2.5 * L2_BYTES / per_set)) + 1)
+    n_sets = min(n_sets, 8)
+    del probe
+    _, sets = _device_sets(w, dev, n_sets)
+    step = _step_fn(w, binding)
+    stream = torch.cuda.current_stream(dev)
+
+    def barrier():
+        if ws_n > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    sampler = ClockSampler(local)
+    for i in range(args.warmup):
+        step(sets[i % n_sets])
+    torch.cuda.synchronize()
+    status = binding.gge_read_device_status(dev)
+    if status[0] != "GGE_OK":
+        raise RuntimeError(f"device status after warm-up: {status}")
+
+    sampler.start()
+    # settle clocks under load before the timed region (extra warm-up work)
+    t_end = time.time() + 0.5
+    i = 0
+    while time.time() < t_end:
+        for _ in range(20):
+            step(sets[i % n_sets])
+            i += 1
+        torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for i in range(args.steps):
+        step(sets[i % n_sets])
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    clocks = sampler.stop()
+    ms = e0.elapsed_time(e1)
+    status = binding.gge_read_device_status(dev)
+    if status[0] != "GGE_OK":
+        raise RuntimeError(f"device status after the timed region: {status}")
+    ms_per_step = ms / args.steps
+    if ws_n > 1:
+        import torch.distributed as dist
+        t = torch.tensor([ms_per_step], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_per_step = float(t.item())
+
+    flops = w.flops
+    value = ws_n * flops / (ms_per_step * 1e-3) / 1e12
+
+    # end-to-end through the public API with host buffers
+    e2e = run_e2e(args, w, base, dev, step)
+
+    peaks, src = measured_peaks()
+    bf16 = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
+    is8 = w.ab_dtype in ("e4m3", "e5m2")
+    peak = bf16 * (2.0 if is8 else 1.0)
+    achieved = flops / (ms_per_step * 1e-3) / 1e12
+    roofline = {
+        "bound": "tensor", "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
+        "frac": round(achieved / peak, 4), "traffic": profiled_traffic(w.name),
+        "peak_source": f"{src} cuBLAS bf16 burst" + (" x2 (fp8/bf16 nominal ratio)" if is8 else ""),
+        "frac_of_nominal_dense_peak": round(achieved / NOMINAL_PEAK[w.ab_dtype], 4),
+    }
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": "TFLOP/s", "n_gpus": ws_n,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": w.ab_dtype if w.bdt == w.ab_dtype else f"{w.ab_dtype}x{w.bdt}",
+        "data": "synthetic",
+        "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "L": w.L,
+                   "groups": w.groups, "gather_rows": w.gather_rows, "act": w.act,
+                   "with_c": w.with_c, "alpha": w.alpha, "beta": w.beta,
+                   "accumulate": "f32", "out": w.p_dtype or w.d_dtype,
+                   "l2": f"{n_sets} rotating input sets of {per_set / 2**20:.0f} MiB (> L2)",
+                   "parallelism": f"replicas{ws_n}" if ws_n > 1 else "single"},
+        "roofline": roofline,
+        "e2e": e2e,
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+    }
+    if rank == 0 and ws_n == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, base, budget_s=args.cpu_seconds)
+    if ws_n > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return line, rank
+
+
+def run_e2e(args, w, base, dev, step):
+    """Same metric through the public API with host (pinned) buffers: every
+    step copies its inputs host->device and its outputs device->host."""
+    host_in = {k: v.pin_memory() for k, v in base.items() if isinstance(v, torch.Tensor)}
+    dsets = {k: torch.empty_like(v, device=dev) for k, v in host_in.items()}
+    L = 1 if w.groups else w.L
+    shape = (w.M, w.N) if w.groups else (L, w.M, w.N)
+    outs = {}
+    if w.d_dtype:
+        outs["D"] = torch.empty(shape, dtype=wl.DT[w.d_dtype], device=dev)
+    if w.p_dtype:
+        outs["P"] = torch.empty(shape, dtype=wl.DT[w.p_dtype], device=dev)
+    host_out = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in outs.items()}
+    s = dict(dsets)
+    s.update(outs)
+    h2d = sum(v.numel() * v.element_size() for v in host_in.values())
+    d2h = sum(v.numel() * v.element_size() for v in host_out.values())
+
+    def one():
+        for k, v in host_in.items():
+            dsets[k].copy_(v, non_blocking=True)
+        step(s)
+        for k, v in outs.items():
+            host_out[k].copy_(v, non_blocking=True)
+
+    n = max(3, min(args.steps, 50))
+    for _ in range(3):
+        one()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream(dev)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(n):
+        one()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / n
+    return {"value": round(w.flops / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+            "ms_per_step": round(ms, 4), "steps": n}
+
+
+# ------------------------------------------------------ the oracle (CPU)
+
+def _oracle_rows(w, base, rows):
+    """The oracle on a subset of output rows of the workload; returns the
+    FLOPs that the sample covers."""
+    from oracle import activations, formats, gemm as og
+
+    def dec(t):
+        t = t.contiguous()
+        fmt = {torch.bfloat16: formats.BF16, torch.float16: formats.F16,
+               torch.float8_e4m3fn: formats.E4M3, torch.float8_e5m2: formats.E5M2,
+               torch.float32: formats.F32}[t.dtype]
+        ity = {1: torch.uint8, 2: torch.int16, 4: torch.int32}[fmt.nbytes]
+        return formats.decode(t.view(ity).numpy(), fmt)
+
+    fm = {"bf16": formats.BF16, "f16": formats.F16, "f32": formats.F32, None: None}
+    kw = dict(alpha=w.alpha, beta=w.beta, act=w.act, d_fmt=fm[w.d_dtype], p_fmt=fm[w.p_dtype])
+    if w.groups:
+        cu = base["cu_seqlens_m"].numpy()
+        A = base["A"][base["a_idx"][rows].long()] if w.gather_rows else base["A"][rows]
+        out_rows = 0
+        B = base["B"]
+        # rows of the sample grouped by their group
+        g_of = np.searchsorted(cu, rows, side="right") - 1
+        for g in np.unique(g_of):
+            sel = np.nonzero(g_of == g)[0]
+            og.gemm(dec(A[sel])[None], dec(B[g])[None], None, **kw)
+            out_rows += len(sel)
+        return 2.0 * out_rows * w.N * w.K
+    A = base["A"][:, rows]
+    C = base["C"][:, rows] if "C" in base else None
+    og.gemm(dec(A), dec(base["B"]), None if C is None else dec(C), **kw)
+    return 2.0 * len(rows) * w.N * w.K * w.L
+
+
+def cpu_baseline(w, base, budget_s=15.0):
+    """Time the oracle as it stands on the host cores over a bounded sample
+    of the workload's output rows (about budget_s seconds of work)."""
+    M = w.M
+    rows = np.arange(0, min(M, 16))
+    t0 = time.perf_counter()
+    f = _oracle_rows(w, base, rows)
+    dt = time.perf_counter() - t0
+    rate = f / max(dt, 1e-6)
+    per_row = f / len(rows)
+    n = int(min(M, max(16, budget_s * rate / per_row)))
+    rng = np.random.default_rng(0)
+    rows = np.sort(rng.choice(M, size=n, replace=False))
+    t0 = time.perf_counter()
+    f = _oracle_rows(w, base, rows)
+    dt = time.perf_counter() - t0
+    return {"value": round(f / dt / 1e12, 6), "unit": "TFLOP/s", "cores": os.cpu_count(),
+            "kind": "oracle",
+            "sample": f"{n} of {M} output rows (all N, K{', batches' if w.L > 1 else ''}), "
+                      f"{f / 1e9:.1f} GFLOP in {dt:.1f} s, float64 numpy/BLAS"}
+
+
+def run_reference(args, w):
+    ws_n, rank, _ = dist_env()
+    if rank != 0:
+        return None, rank
+    base = wl.make(w)
+    total_budget = 150.0
+    per_step = total_budget / max(1, args.steps + args.warmup)
+    # calibrate the rows per step to the budget
+    probe_rows = np.arange(min(w.M, 8))
+    t0 = time.perf_counter()
+    f = _oracle_rows(w, base, probe_rows)
+    dt = max(time.perf_counter() - t0, 1e-6)
+    per_row_s = dt / len(probe_rows)
+    n = int(min(w.M, max(1, per_step / per_row_s)))
+    rng = np.random.default_rng(0)
+    samples = [np.sort(rng.choice(w.M, size=n, replace=False))
+               for _ in range(args.steps + args.warmup)]
+    for i in range(args.warmup):
+        _oracle_rows(w, base, samples[i])
+    t0 = time.perf_counter()
+    flops = 0.0
+    for i in range(args.steps):
+        flops += _oracle_rows(w, base, samples[args.warmup + i])
+    dt = time.perf_counter() - t0
+    value = flops / dt / 1e12
+    ms_per_step = dt * 1e3 / args.steps
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s",
+        "n_gpus": ws_n, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "L": w.L},
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": os.cpu_count(),
+                         "kind": "oracle",
+                         "sample": f"{n} of {w.M} output rows per step, float64 numpy/BLAS"},
+        "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    return line, rank
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(wl.WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    w = wl.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        line, rank = run_reference(args, w)
+    else:
+        line, rank = run_ours(args, w)
+    if rank == 0 and line is not None:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()
