@@ -151,8 +151,9 @@ def _device_sets(w, dev, n_sets):
         for k, v in base.items():
             if isinstance(v, torch.Tensor):
                 s[k] = v.to(dev) if i == 0 else v.to(dev).clone()
-        if i > 0:  # distinct values per set (same distribution): permute A rows
-            s["A"] = torch.roll(s["A"], shifts=i, dims=-2).contiguous()
+        if i > 0:  # distinct values per set (same distribution): rotate A's rows
+            a = s["A"]
+            s["A"] = torch.roll(a.view(torch.uint8), shifts=i, dims=-2).view(a.dtype).contiguous()
         L = 1 if w.groups else w.L
         shape = (w.M, w.N) if w.groups else (L, w.M, w.N)
         if w.d_dtype:

@@ -34,7 +34,7 @@ class GgeTensor(ctypes.Structure):
 
 class GgeConfig(ctypes.Structure):
     _fields_ = [("tile_n", c_i32), ("num_ctas", c_i32), ("raster_band", c_i32),
-                ("stages", c_i32), ("flags", c_i32), ("reserved", c_i32),
+                ("stages", c_i32), ("flags", c_i32), ("cta_group", c_i32),
                 ("tile_counts", ctypes.c_void_p), ("timeout_ns", c_u64)]
 
 
@@ -50,7 +50,7 @@ class GgeGemmArgs(ctypes.Structure):
 class GgePlanInfo(ctypes.Structure):
     _fields_ = [("tile_m", c_i32), ("tile_n", c_i32), ("tile_k", c_i32), ("stages", c_i32),
                 ("num_tiles", c_i32), ("grid", c_i32), ("threads", c_i32),
-                ("smem_bytes", c_i32), ("raster_band", c_i32), ("reserved", c_i32)]
+                ("smem_bytes", c_i32), ("raster_band", c_i32), ("cta_group", c_i32)]
 
 
 # every function include/gge.h declares, with its ctypes signature
@@ -140,8 +140,8 @@ def workspace(device=None) -> torch.Tensor:
 
 
 def make_config(tile_n=0, num_ctas=0, raster_band=0, stages=0, flags=0, tile_counts=None,
-                timeout_ns=0):
-    return GgeConfig(tile_n, num_ctas, raster_band, stages, flags, 0,
+                timeout_ns=0, cta_group=0):
+    return GgeConfig(tile_n, num_ctas, raster_band, stages, flags, cta_group,
                      ctypes.c_void_p(tile_counts.data_ptr()) if tile_counts is not None else None,
                      timeout_ns)
 
@@ -247,4 +247,4 @@ def gge_plan(A, B, C=None, D=None, PostAct=None, act="none", num_groups=0, gathe
     info = GgePlanInfo()
     code = lib.gge_plan(ctypes.byref(args), num_groups, 1 if gather else 0, ctypes.byref(info))
     _check(code, "gge_plan")
-    return {k: getattr(info, k) for k, _ in GgePlanInfo._fields_ if k != "reserved"}
+    return {k: getattr(info, k) for k, _ in GgePlanInfo._fields_}

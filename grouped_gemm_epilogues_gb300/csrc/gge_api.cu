@@ -107,6 +107,7 @@ struct Plan {
   Params p;
   CUtensorMap tmA, tmB;
   int bn;
+  int cg;  // CTAs per tile: 1, or 2 for a CTA pair (cta_group::2)
   bool gather;
   LaunchShape shape;
   int64_t M, N, K, L;
@@ -138,6 +139,20 @@ uint64_t batch_stride_bytes(const gge_tensor& t, int es) {
   uint64_t s = static_cast<uint64_t>(std::max<int64_t>(t.rows, 1)) *
                static_cast<uint64_t>(std::max<int64_t>(t.stride_row, 1)) * es;
   return (s + 15) / 16 * 16;
+}
+
+// ---- the kernel variants: (BN, gather, CTAs per tile)
+
+int variant_threads(int bn, bool gather, int cg) {
+  if (gather) return bn == 128 ? kernel_threads<128, true, 1>() : kernel_threads<256, true, 1>();
+  if (cg == 2) return kernel_threads<256, false, 2>();
+  return bn == 128 ? kernel_threads<128, false, 1>() : kernel_threads<256, false, 1>();
+}
+
+int variant_units(int bn, bool gather, int cg, size_t smem) {
+  if (gather) return bn == 128 ? max_active_units<128, true, 1>(smem) : max_active_units<256, true, 1>(smem);
+  if (cg == 2) return max_active_units<256, false, 2>(smem);
+  return bn == 128 ? max_active_units<128, false, 1>(smem) : max_active_units<256, false, 1>(smem);
 }
 
 // Validate and plan.  `encode` = build tensor maps (needs the CUDA driver).
@@ -222,12 +237,17 @@ gge_status make_plan(const gge_gemm_args* a, Form form, const int32_t* a_idx,
     if ((K * es) % 16 != 0) return GGE_ERR_UNSUPPORTED;  // whole 16-byte chunks along K
   }
 
-  // tile shape
+  // tile shape: 128 x BN on one CTA, or 256 x 256 on a CTA pair
   int bn = cfg && cfg->tile_n ? cfg->tile_n : (N <= 128 ? 128 : 256);
   if (bn != 128 && bn != 256) return GGE_ERR_UNSUPPORTED;
+  int cg = cfg && cfg->cta_group ? cfg->cta_group : ((!gather && bn == 256 && M >= 256) ? 2 : 1);
+  if (cg != 1 && cg != 2) return GGE_ERR_UNSUPPORTED;
+  if (cg == 2 && (gather || bn != 256)) return GGE_ERR_UNSUPPORTED;
   pl.bn = bn;
+  pl.cg = cg;
+  const int tile_m = kTileM * cg;
   const int bk = kRowBytesHost / es;
-  const int stage_bytes = (kTileM + bn) * kRowBytesHost;
+  const int stage_bytes = (kTileM + bn / cg) * kRowBytesHost;
   const int varlen_bytes = varlen ? 2 * 4 * (kMaxGroupsHost + 1) : 0;
   const int fixed = 1024 + kCtrlBytesHost + varlen_bytes;
   int stages = (kMaxSmemOptin - fixed) / stage_bytes;
@@ -237,7 +257,7 @@ gge_status make_plan(const gge_gemm_args* a, Form form, const int32_t* a_idx,
 
   pl.M = M; pl.N = N; pl.K = K; pl.L = L;
   const int64_t tiles_n = (N + bn - 1) / bn;
-  const int64_t tiles_m = (M + kTileM - 1) / kTileM;
+  const int64_t tiles_m = (M + tile_m - 1) / tile_m;
   pl.empty = (M == 0 || N == 0 || L == 0);
 
   p.M = static_cast<int32_t>(M);
@@ -262,7 +282,7 @@ gge_status make_plan(const gge_gemm_args* a, Form form, const int32_t* a_idx,
     p.num_groups = G;
     p.cu_seqlens = cu;
     // upper bound on the tile count (the exact count is formed on the device)
-    num_tiles = (M / kTileM + G) * tiles_n;
+    num_tiles = (M / tile_m + G) * tiles_n;
     p.num_tiles = -1;
   }
   pl.band = band;
@@ -293,21 +313,23 @@ gge_status make_plan(const gge_gemm_args* a, Form form, const int32_t* a_idx,
   const uint32_t afmt = f8 ? (adt == GGE_E5M2 ? 1u : 0u) : (adt == GGE_BF16 ? 1u : 0u);
   const uint32_t bfmt = f8 ? (bdt == GGE_E5M2 ? 1u : 0u) : (bdt == GGE_BF16 ? 1u : 0u);
   p.idesc = (1u << 4) | (afmt << 7) | (bfmt << 10) | ((b_mn ? 1u : 0u) << 16) |
-            ((static_cast<uint32_t>(bn) >> 3) << 17) | ((static_cast<uint32_t>(kTileM) >> 4) << 24);
+            ((static_cast<uint32_t>(bn) >> 3) << 17) | ((static_cast<uint32_t>(tile_m) >> 4) << 24);
   p.f8 = f8 ? 1 : 0;
   p.b_mn_major = b_mn ? 1 : 0;
   p.flags = cfg ? cfg->flags : 0;
   p.tile_counts = cfg ? cfg->tile_counts : nullptr;
   p.timeout_ns = (cfg && cfg->timeout_ns) ? cfg->timeout_ns : kDefaultTimeoutNs;
 
-  // launch shape
+  // launch shape: a persistent grid of at most one CTA (pair) per resident slot
   pl.shape.smem = static_cast<size_t>(fixed + stages * stage_bytes);
-  pl.shape.threads = gather ? (bn == 128 ? kernel_threads<128, true>() : kernel_threads<256, true>())
-                            : (bn == 128 ? kernel_threads<128, false>() : kernel_threads<256, false>());
-  int grid_cap = cfg && cfg->num_ctas > 0 ? cfg->num_ctas : -1;
-  if (grid_cap < 0 && encode) grid_cap = sm_count();
-  if (grid_cap <= 0 && encode) return GGE_ERR_CUDA;
-  pl.shape.grid = grid_cap > 0 ? static_cast<int>(std::min<int64_t>(num_tiles, grid_cap)) : -1;
+  pl.shape.threads = variant_threads(bn, gather, cg);
+  int units_cap = cfg && cfg->num_ctas > 0 ? std::max(1, cfg->num_ctas / cg) : -1;
+  if (encode) {
+    const int resident = variant_units(bn, gather, cg, pl.shape.smem);
+    if (resident <= 0) return GGE_ERR_CUDA;
+    units_cap = units_cap > 0 ? std::min(units_cap, resident) : resident;
+  }
+  pl.shape.grid = units_cap > 0 ? cg * static_cast<int>(std::min<int64_t>(num_tiles, units_cap)) : -1;
   if (pl.empty || !encode) return GGE_OK;
   if (pl.shape.grid <= 0) pl.empty = true;  // e.g. varlen with no rows
   if (pl.empty) return GGE_OK;
@@ -323,7 +345,7 @@ gge_status make_plan(const gge_gemm_args* a, Form form, const int32_t* a_idx,
     if (!b_mn) {
       s = encode_3d(&pl.tmB, a->B.ptr, es, K, N, a->B.batch,
                     static_cast<uint64_t>(a->B.stride_row) * es, batch_stride_bytes(a->B, es), bk,
-                    bn);
+                    bn / cg);
     } else {
       gge_tensor t = a->B;
       uint64_t sb = t.batch > 1 ? static_cast<uint64_t>(t.stride_batch) * es
@@ -356,11 +378,13 @@ gge_status run(const gge_gemm_args* a, Form form, const int32_t* a_idx, const in
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e;
   if (pl.gather)
-    e = pl.bn == 128 ? launch_gemm<128, true>(pl.tmA, pl.tmB, pl.p, pl.shape, st)
-                     : launch_gemm<256, true>(pl.tmA, pl.tmB, pl.p, pl.shape, st);
+    e = pl.bn == 128 ? launch_gemm<128, true, 1>(pl.tmA, pl.tmB, pl.p, pl.shape, st)
+                     : launch_gemm<256, true, 1>(pl.tmA, pl.tmB, pl.p, pl.shape, st);
+  else if (pl.cg == 2)
+    e = launch_gemm<256, false, 2>(pl.tmA, pl.tmB, pl.p, pl.shape, st);
   else
-    e = pl.bn == 128 ? launch_gemm<128, false>(pl.tmA, pl.tmB, pl.p, pl.shape, st)
-                     : launch_gemm<256, false>(pl.tmA, pl.tmB, pl.p, pl.shape, st);
+    e = pl.bn == 128 ? launch_gemm<128, false, 1>(pl.tmA, pl.tmB, pl.p, pl.shape, st)
+                     : launch_gemm<256, false, 1>(pl.tmA, pl.tmB, pl.p, pl.shape, st);
   return e == cudaSuccess ? GGE_OK : GGE_ERR_CUDA;
 }
 
@@ -467,7 +491,7 @@ gge_status gge_plan(const gge_gemm_args* args, int32_t num_groups, int32_t gathe
                                       num_groups > 0 ? &dummy : nullptr, num_groups, true, false,
                                       false, &pl);
   if (s != GGE_OK) return s;
-  out->tile_m = gge::kTileM;
+  out->tile_m = gge::kTileM * pl.cg;
   out->tile_n = pl.bn;
   out->tile_k = pl.p.bk;
   out->stages = pl.p.stages;
@@ -476,7 +500,7 @@ gge_status gge_plan(const gge_gemm_args* args, int32_t num_groups, int32_t gathe
   out->threads = pl.shape.threads;
   out->smem_bytes = static_cast<int32_t>(pl.shape.smem);
   out->raster_band = pl.band;
-  out->reserved = 0;
+  out->cta_group = pl.cg;
   return GGE_OK;
 }
 

@@ -8,21 +8,30 @@
 
 namespace gge {
 
-template <int BN, bool GATHER>
-cudaError_t launch_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const Params& p,
-                        const LaunchShape& shape, cudaStream_t stream) {
-  auto kern = gemm_kernel<BN, GATHER>;
+template <int BN, bool GATHER, int CG>
+cudaError_t set_smem_limit(size_t smem) {
+  auto kern = gemm_kernel<BN, GATHER, CG>;
   // the dynamic shared-memory limit is a per-device function attribute
   static std::atomic<size_t> smem_set[64];
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= 64 || smem_set[dev].load() < shape.smem) {
+  if (dev < 0 || dev >= 64 || smem_set[dev].load() < smem) {
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(shape.smem));
+                             static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    if (dev >= 0 && dev < 64) smem_set[dev].store(shape.smem);
+    if (dev >= 0 && dev < 64) smem_set[dev].store(smem);
   }
+  return cudaSuccess;
+}
+
+template <int BN, bool GATHER, int CG>
+cudaError_t launch_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const Params& p,
+                        const LaunchShape& shape, cudaStream_t stream) {
+  auto kern = gemm_kernel<BN, GATHER, CG>;
+  cudaError_t e = set_smem_limit<BN, GATHER, CG>(shape.smem);
+  if (e != cudaSuccess) return e;
+  cudaLaunchAttribute attr[1];
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(shape.grid, 1, 1);
   cfg.blockDim = dim3(shape.threads, 1, 1);
@@ -30,18 +39,56 @@ cudaError_t launch_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const Pa
   cfg.stream = stream;
   cfg.attrs = nullptr;
   cfg.numAttrs = 0;
+  if (CG > 1) {
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = CG;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
   return cudaLaunchKernelEx(&cfg, kern, tmA, tmB, p);
 }
 
-template <int BN, bool GATHER>
+template <int BN, bool GATHER, int CG>
 int kernel_threads() {
-  return KernelCfg<BN, GATHER>::kThreads;
+  return KernelCfg<BN, GATHER, CG>::kThreads;
 }
 
-#define GGE_INSTANTIATE(BN, GATHER)                                                          \
-  template cudaError_t launch_gemm<BN, GATHER>(const CUtensorMap&, const CUtensorMap&,     \
-                                               const Params&, const LaunchShape&,          \
-                                               cudaStream_t);                              \
-  template int kernel_threads<BN, GATHER>();
+template <int BN, bool GATHER, int CG>
+int max_active_units(size_t smem) {
+  auto kern = gemm_kernel<BN, GATHER, CG>;
+  if (set_smem_limit<BN, GATHER, CG>(smem) != cudaSuccess) return -1;
+  if (CG == 1) {
+    int per_sm = 0, dev = 0, sms = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, KernelCfg<BN, GATHER, CG>::kThreads,
+                                                      smem) != cudaSuccess)
+      return -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
+    return per_sm * sms;
+  }
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = CG;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(CG * 256, 1, 1);
+  cfg.blockDim = dim3(KernelCfg<BN, GATHER, CG>::kThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) return -1;
+  return n;
+}
+
+#define GGE_INSTANTIATE(BN, GATHER, CG)                                                      \
+  template cudaError_t launch_gemm<BN, GATHER, CG>(const CUtensorMap&, const CUtensorMap&, \
+                                                   const Params&, const LaunchShape&,      \
+                                                   cudaStream_t);                          \
+  template int kernel_threads<BN, GATHER, CG>();                                           \
+  template int max_active_units<BN, GATHER, CG>(size_t);
 
 }  // namespace gge

@@ -2,5 +2,5 @@
 #include "gge_inst.cuh"
 
 namespace gge {
-GGE_INSTANTIATE(128, false)
+GGE_INSTANTIATE(128, false, 1)
 }  // namespace gge

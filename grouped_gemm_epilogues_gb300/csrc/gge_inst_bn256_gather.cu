@@ -2,5 +2,5 @@
 #include "gge_inst.cuh"
 
 namespace gge {
-GGE_INSTANTIATE(256, true)
+GGE_INSTANTIATE(256, true, 1)
 }  // namespace gge

@@ -2,5 +2,5 @@
 #include "gge_inst.cuh"
 
 namespace gge {
-GGE_INSTANTIATE(256, false)
+GGE_INSTANTIATE(256, false, 1)
 }  // namespace gge

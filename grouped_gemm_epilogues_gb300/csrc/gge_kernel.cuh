@@ -20,7 +20,15 @@
 //   warps 5-8  (gather-A form) row gather of A with 16-byte cp.async into the
 //              same swizzled layout, B still by TMA (GemmSm90.load_AB_gather_A).
 //
-// Every CTA walks the same static persistent schedule (tile t, t + grid, ...);
+// With CG = 2 a cluster of two CTAs (a CTA pair) computes a 256 x BN tile:
+// each CTA stages its own 128 rows of A and half of the BN columns of B, the
+// leader CTA issues tcgen05.mma.cta_group::2 over both CTAs' shared memory,
+// and each CTA's TMEM receives its own 128 accumulator rows.  The pair halves
+// the B bytes each SM stages per FLOP, so a stage is 32 KiB instead of 48 KiB
+// and seven stages fit; this is the Blackwell counterpart of the pages'
+// Hopper clusters with TMA multicast.
+//
+// Every CTA (pair) walks the same static persistent schedule (tile t, t + grid, ...);
 // tile coordinates come from FastDivmod (plain) or from a per-group tile
 // prefix sum in shared memory (varlen-M, VarlenMTileScheduler's role).
 //
@@ -47,10 +55,12 @@ constexpr int kGatherWarps = 4;
 constexpr int kMaxGroups = 1024;   // varlen-M groups held in shared memory
 constexpr int kCtrlBytes = 256;    // barriers and flags
 
-template <int BN, bool GATHER>
+template <int BN, bool GATHER, int CG>
 struct KernelCfg {
+  static constexpr int kTileM = kBM * CG;        // rows of one (pair) tile
+  static constexpr int kBRows = BN / CG;         // B rows staged by each CTA
   static constexpr int kABytes = kBM * kRowBytes;
-  static constexpr int kBBytes = BN * kRowBytes;
+  static constexpr int kBBytes = kBRows * kRowBytes;
   static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr int kWarps = GATHER ? kLoadWarp + kGatherWarps : kLoadWarp + 1;
   static constexpr int kThreads = kWarps * 32;
@@ -58,6 +68,8 @@ struct KernelCfg {
   static_assert(BN % 64 == 0 && BN <= 256, "BN must be 64, 128, 192 or 256");
   static_assert(kTmemCols == 128 || kTmemCols == 256 || kTmemCols == 512,
                 "TMEM allocation must be a power of two");
+  static_assert(CG == 1 || CG == 2, "one CTA or a CTA pair");
+  static_assert(!(GATHER && CG == 2), "the row gather runs on single-CTA tiles");
 };
 
 // Shared-memory matrix descriptor for a K-major (or N-major) operand staged
@@ -85,7 +97,7 @@ struct Shared {
   const int32_t* cu;      // varlen: cu_seqlens copy [G+1]
 };
 
-template <int BN>
+template <int BN, int TILE_M>
 __device__ __forceinline__ TileCoord tile_coord(int32_t t, const Params& p, const Shared& sh) {
   TileCoord tc;
   if (p.num_groups > 0) {
@@ -96,7 +108,7 @@ __device__ __forceinline__ TileCoord tile_coord(int32_t t, const Params& p, cons
     }
     int32_t mb, nb;
     p.tiles_n_div.divmod(t - sh.prefix[lo], mb, nb);
-    tc.m_row0 = sh.cu[lo] + mb * kBM;
+    tc.m_row0 = sh.cu[lo] + mb * TILE_M;
     tc.row_limit = min(sh.cu[lo + 1], p.M);
     tc.n0 = nb * BN;
     tc.batch = lo;
@@ -104,7 +116,7 @@ __device__ __forceinline__ TileCoord tile_coord(int32_t t, const Params& p, cons
   } else {
     int32_t l, mb, nb;
     p.sched.map(t, l, mb, nb);
-    tc.m_row0 = mb * kBM;
+    tc.m_row0 = mb * TILE_M;
     tc.row_limit = p.M;
     tc.n0 = nb * BN;
     tc.batch = l;
@@ -127,12 +139,13 @@ __device__ __forceinline__ void record_status(const Params& p, int32_t code, int
 // CTA aborts, or timeout_ns of %globaltimer pass (then record and abort).
 static __device__ __noinline__ bool wait_phase_slow(uint32_t bar, uint32_t parity, uint64_t timeout_ns,
                                              int32_t* status, volatile int32_t* abort,
-                                             int32_t where, int32_t tile) {
+                                             int32_t where, int32_t tile, bool cluster_scope) {
   const uint64_t t0 = ptx::globaltimer();
   while (true) {
 #pragma unroll 1
     for (int i = 0; i < 32; ++i)
-      if (ptx::mbar_try_wait(bar, parity)) return true;
+      if (cluster_scope ? ptx::mbar_try_wait_cluster(bar, parity) : ptx::mbar_try_wait(bar, parity))
+        return true;
     if (*abort) return false;
     if (ptx::globaltimer() - t0 > timeout_ns) {
       if (status != nullptr && atomicCAS(status, 0, DEV_TIMEOUT) == 0) {
@@ -146,10 +159,13 @@ static __device__ __noinline__ bool wait_phase_slow(uint32_t bar, uint32_t parit
 }
 
 // Bounded wait on an mbarrier phase.  Returns false on abort or timeout.
+// CLUSTER: acquire at cluster scope (barriers that the peer CTA signals).
+template <bool CLUSTER = false>
 __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, const Params& p,
                                            const Shared& sh, int32_t where, int32_t tile) {
-  if (ptx::mbar_try_wait(bar, parity)) return true;
-  return wait_phase_slow(bar, parity, p.timeout_ns, p.status, sh.abort, where, tile);
+  if (CLUSTER ? ptx::mbar_try_wait_cluster(bar, parity) : ptx::mbar_try_wait(bar, parity))
+    return true;
+  return wait_phase_slow(bar, parity, p.timeout_ns, p.status, sh.abort, where, tile, CLUSTER);
 }
 
 // ------------------------------------------------------------- epilogue math
@@ -265,21 +281,24 @@ __device__ __forceinline__ void epilogue_chunk(const Params& p, const uint32_t (
 }
 
 // ------------------------------------------------------------------- roles
+// `unit` / `units`: this CTA's (pair's) index and the number of CTAs (pairs).
 
-template <int BN, bool GATHER>
+template <int BN, bool GATHER, int CG>
 __device__ __forceinline__ void epilogue_role(const Params& p, const Shared& sh,
-                                              uint32_t tmem_base, int32_t num_tiles) {
+                                              uint32_t tmem_base, int32_t num_tiles,
+                                              uint32_t rank, int32_t unit, int32_t units) {
+  using Cfg = KernelCfg<BN, GATHER, CG>;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const float alpha = p.alpha_dev ? *p.alpha_dev : p.alpha;
   const float beta = p.beta_dev ? *p.beta_dev : p.beta;
   uint32_t acc = 0, acc_phase = 0;
-  for (int32_t t = blockIdx.x; t < num_tiles; t += gridDim.x) {
-    const TileCoord tc = tile_coord<BN>(t, p, sh);
+  for (int32_t t = unit; t < num_tiles; t += units) {
+    const TileCoord tc = tile_coord<BN, Cfg::kTileM>(t, p, sh);
     // all lanes take the same branch: tcgen05.ld below is warp-collective
-    const bool ok = wait_phase(sh.tfull + 8 * acc, acc_phase, p, sh, 3, t);
+    const bool ok = wait_phase<CG == 2>(sh.tfull + 8 * acc, acc_phase, p, sh, 3, t);
     if (!__all_sync(0xffffffffu, ok)) break;
     ptx::tc_fence_after();
-    const int32_t row = tc.m_row0 + warp * 32 + lane;
+    const int32_t row = tc.m_row0 + static_cast<int32_t>(rank) * kBM + warp * 32 + lane;
     const bool row_ok = row < tc.row_limit;
     const uint32_t tbase = tmem_base + (static_cast<uint32_t>(warp * 32) << 16) + acc * BN;
 #pragma unroll 1
@@ -296,78 +315,125 @@ __device__ __forceinline__ void epilogue_role(const Params& p, const Shared& sh,
       if (c == BN / 32 - 1) {  // accumulator fully read: hand the buffer back to the MMA warp
         ptx::tc_fence_before();
         __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(sh.tempty + 8 * acc);
+        if (lane == 0) {
+          if (CG == 1) ptx::mbar_arrive(sh.tempty + 8 * acc);
+          else ptx::mbar_arrive_cluster(ptx::mapa(sh.tempty + 8 * acc, 0));
+        }
       }
       const int32_t col0 = tc.n0 + c * 32;
       if (row_ok && col0 < p.N) epilogue_chunk(p, v, row, col0, tc.batch, alpha, beta);
     }
-    if ((p.flags & FLAG_TILE_COUNTS) && p.tile_counts != nullptr && warp == 0 && lane == 0)
+    if ((p.flags & FLAG_TILE_COUNTS) && p.tile_counts != nullptr && rank == 0 && warp == 0 &&
+        lane == 0)
       atomicAdd(p.tile_counts + t, 1);
     acc ^= 1u;
     if (acc == 0) acc_phase ^= 1u;
   }
 }
 
-template <int BN, bool GATHER>
+// The whole MMA warp walks the loop (so descriptors stay warp-uniform); one
+// elected lane issues the MMAs and commits.
+template <int BN, bool GATHER, int CG>
 __device__ __forceinline__ void mma_role(const Params& p, const Shared& sh, uint32_t a0,
-                                         uint32_t b0, uint32_t tmem_base, int32_t num_tiles) {
-  using Cfg = KernelCfg<BN, GATHER>;
+                                         uint32_t b0, uint32_t tmem_base, int32_t num_tiles,
+                                         int32_t unit, int32_t units) {
+  using Cfg = KernelCfg<BN, GATHER, CG>;
   int stage = 0;
   uint32_t phase = 0, acc = 0, acc_phase = 0;
   // B descriptor strides: K-major rows are 128 B apart, 8-row swizzle atoms 1 KiB apart;
   // N-major: 64-column chunks are (bk rows * 128 B) apart, 8-row K groups 1 KiB apart.
   const uint32_t b_lbo = p.b_mn_major ? static_cast<uint32_t>(p.bk) * kRowBytes : 16u;
   const uint32_t b_kstep = p.b_mn_major ? 16u * kRowBytes : 32u;
-  for (int32_t t = blockIdx.x; t < num_tiles; t += gridDim.x) {
-    if (!wait_phase(sh.tempty + 8 * acc, acc_phase ^ 1u, p, sh, 2, t)) return;
+  for (int32_t t = unit; t < num_tiles; t += units) {
+    bool ok = wait_phase<CG == 2>(sh.tempty + 8 * acc, acc_phase ^ 1u, p, sh, 2, t);
+    if (!__all_sync(0xffffffffu, ok)) return;
     ptx::tc_fence_after();
     const uint32_t d_tmem = tmem_base + acc * BN;
     for (int kt = 0; kt < p.k_tiles; ++kt) {
-      if (!wait_phase(sh.full + 8 * stage, phase, p, sh, 1, t)) return;
+      ok = wait_phase<CG == 2>(sh.full + 8 * stage, phase, p, sh, 1, t);
+      if (!__all_sync(0xffffffffu, ok)) return;
       ptx::tc_fence_after();
       if (GATHER) ptx::fence_proxy_async_smem();  // cp.async (generic proxy) writes -> MMA reads
       const uint32_t a_addr = a0 + stage * Cfg::kABytes;
       const uint32_t b_addr = b0 + stage * Cfg::kBBytes;
+      if (ptx::elect_one()) {
 #pragma unroll
-      for (int kk = 0; kk < 4; ++kk) {  // 4 MMAs of 32 bytes of K each
-        const uint64_t adesc = smem_desc(a_addr + kk * 32, 16u, 1024u);
-        const uint64_t bdesc = smem_desc(b_addr + kk * b_kstep, b_lbo, 1024u);
-        const uint32_t accumulate = (kt > 0 || kk > 0) ? 1u : 0u;
-        if (p.f8) ptx::mma_f8(d_tmem, adesc, bdesc, p.idesc, accumulate);
-        else ptx::mma_f16(d_tmem, adesc, bdesc, p.idesc, accumulate);
+        for (int kk = 0; kk < 4; ++kk) {  // 4 MMAs of 32 bytes of K each
+          const uint64_t adesc = smem_desc(a_addr + kk * 32, 16u, 1024u);
+          const uint64_t bdesc = smem_desc(b_addr + kk * b_kstep, b_lbo, 1024u);
+          const uint32_t accumulate = (kt > 0 || kk > 0) ? 1u : 0u;
+          if (CG == 1) {
+            if (p.f8) ptx::mma_f8(d_tmem, adesc, bdesc, p.idesc, accumulate);
+            else ptx::mma_f16(d_tmem, adesc, bdesc, p.idesc, accumulate);
+          } else {
+            if (p.f8) ptx::mma_f8_pair(d_tmem, adesc, bdesc, p.idesc, accumulate);
+            else ptx::mma_f16_pair(d_tmem, adesc, bdesc, p.idesc, accumulate);
+          }
+        }
+        // frees the stage (in both CTAs of a pair) once these MMAs finish
+        if (CG == 1) ptx::mma_commit(sh.empty + 8 * stage);
+        else ptx::mma_commit_pair(sh.empty + 8 * stage, 0x3);
       }
-      ptx::mma_commit(sh.empty + 8 * stage);  // frees the stage once these MMAs finish
+      __syncwarp();
       if (++stage == p.stages) { stage = 0; phase ^= 1u; }
     }
-    if (!(p.flags & FLAG_TEST_DROP_ACC_FULL)) ptx::mma_commit(sh.tfull + 8 * acc);
+    if (!(p.flags & FLAG_TEST_DROP_ACC_FULL) && ptx::elect_one()) {
+      if (CG == 1) ptx::mma_commit(sh.tfull + 8 * acc);
+      else ptx::mma_commit_pair(sh.tfull + 8 * acc, 0x3);
+    }
+    __syncwarp();
     acc ^= 1u;
     if (acc == 0) acc_phase ^= 1u;
   }
 }
 
-template <int BN, bool GATHER>
+// The whole producer warp walks the loop; one elected lane issues the copies.
+template <int BN, bool GATHER, int CG>
 __device__ __forceinline__ void tma_producer_role(const Params& p, const Shared& sh,
                                                   const CUtensorMap* tmA, const CUtensorMap* tmB,
-                                                  uint32_t a0, uint32_t b0, int32_t num_tiles) {
-  using Cfg = KernelCfg<BN, GATHER>;
+                                                  uint32_t a0, uint32_t b0, int32_t num_tiles,
+                                                  uint32_t rank, int32_t unit, int32_t units) {
+  using Cfg = KernelCfg<BN, GATHER, CG>;
   int stage = 0;
   uint32_t phase = 0;
-  for (int32_t t = blockIdx.x; t < num_tiles; t += gridDim.x) {
-    const TileCoord tc = tile_coord<BN>(t, p, sh);
+  for (int32_t t = unit; t < num_tiles; t += units) {
+    const TileCoord tc = tile_coord<BN, Cfg::kTileM>(t, p, sh);
+    const int32_t row0 = tc.m_row0 + static_cast<int32_t>(rank) * kBM;
+    const int32_t bn0 = tc.n0 + static_cast<int32_t>(rank) * Cfg::kBRows;
     for (int kt = 0; kt < p.k_tiles; ++kt) {
-      if (!wait_phase(sh.empty + 8 * stage, phase ^ 1u, p, sh, 0, t)) return;
+      const bool ok = wait_phase<CG == 2>(sh.empty + 8 * stage, phase ^ 1u, p, sh, 0, t);
+      if (!__all_sync(0xffffffffu, ok)) return;
       const uint32_t full = sh.full + 8 * stage;
-      ptx::mbar_arrive_expect_tx(full, Cfg::kStageBytes);
       const int32_t k0 = kt * p.bk;
-      ptx::tma_load_3d(a0 + stage * Cfg::kABytes, tmA, full, k0, tc.m_row0, tc.a_batch);
+      const uint32_t adst = a0 + stage * Cfg::kABytes;
       const uint32_t bdst = b0 + stage * Cfg::kBBytes;
-      if (!p.b_mn_major) {
-        ptx::tma_load_3d(bdst, tmB, full, k0, tc.n0, tc.batch);
-      } else {
+      if (ptx::elect_one()) {
+        if (CG == 1) {
+          ptx::mbar_arrive_expect_tx(full, Cfg::kStageBytes);
+          ptx::tma_load_3d(adst, tmA, full, k0, row0, tc.a_batch);
+          if (!p.b_mn_major) {
+            ptx::tma_load_3d(bdst, tmB, full, k0, bn0, tc.batch);
+          } else {
 #pragma unroll
-        for (int j = 0; j < BN / 64; ++j)
-          ptx::tma_load_3d(bdst + j * (64 * kRowBytes), tmB, full, tc.n0 + 64 * j, k0, tc.batch);
+            for (int j = 0; j < Cfg::kBRows / 64; ++j)
+              ptx::tma_load_3d(bdst + j * (64 * kRowBytes), tmB, full, bn0 + 64 * j, k0, tc.batch);
+          }
+        } else {
+          // both CTAs' bytes complete on the leader's barrier, which the leader arms
+          if (rank == 0) ptx::mbar_arrive_expect_tx(full, 2 * Cfg::kStageBytes);
+          const uint32_t lead = ptx::mapa(full, 0);
+          ptx::tma_load_3d_pair(adst, tmA, lead, k0, row0, tc.a_batch);
+          if (!p.b_mn_major) {
+            ptx::tma_load_3d_pair(bdst, tmB, lead, k0, bn0, tc.batch);
+          } else {
+#pragma unroll
+            for (int j = 0; j < Cfg::kBRows / 64; ++j)
+              ptx::tma_load_3d_pair(bdst + j * (64 * kRowBytes), tmB, lead, bn0 + 64 * j, k0,
+                                    tc.batch);
+          }
+        }
       }
+      __syncwarp();
       if (++stage == p.stages) { stage = 0; phase ^= 1u; }
     }
   }
@@ -378,14 +444,14 @@ template <int BN>
 __device__ __forceinline__ void gather_producer_role(const Params& p, const Shared& sh,
                                                      const CUtensorMap* tmB, uint32_t a0,
                                                      uint32_t b0, int32_t num_tiles) {
-  using Cfg = KernelCfg<BN, true>;
+  using Cfg = KernelCfg<BN, true, 1>;
   const int gt = threadIdx.x - kLoadWarp * 32;  // 0..127
   const int chunk = gt & 7;
   const int rsub = gt >> 3;
   int stage = 0;
   uint32_t phase = 0;
   for (int32_t t = blockIdx.x; t < num_tiles; t += gridDim.x) {
-    const TileCoord tc = tile_coord<BN>(t, p, sh);
+    const TileCoord tc = tile_coord<BN, kBM>(t, p, sh);
     // index rows: plain gather reads a_idx[batch][row], varlen reads a_idx[global row]
     const int64_t idx_base = (p.num_groups > 0) ? 0 : static_cast<int64_t>(tc.batch) * p.M;
     int32_t src[8];
@@ -405,7 +471,7 @@ __device__ __forceinline__ void gather_producer_role(const Params& p, const Shar
     for (int kt = 0; kt < p.k_tiles; ++kt) {
       if (!wait_phase(sh.empty + 8 * stage, phase ^ 1u, p, sh, 0, t)) return;
       const uint32_t full = sh.full + 8 * stage;
-      if (gt == 0) {
+      if (gt < 32 && ptx::elect_one()) {  // one lane of the first gather warp: B by TMA
         ptx::mbar_arrive_expect_tx(full, Cfg::kBBytes);
         ptx::tma_load_3d(b0 + stage * Cfg::kBBytes, tmB, full, kt * p.bk, tc.n0, tc.batch);
       }
@@ -430,11 +496,11 @@ __device__ __forceinline__ void gather_producer_role(const Params& p, const Shar
 
 // ------------------------------------------------------------------ kernel
 
-template <int BN, bool GATHER>
-__global__ void __launch_bounds__(KernelCfg<BN, GATHER>::kThreads, 1)
+template <int BN, bool GATHER, int CG>
+__global__ void __launch_bounds__(KernelCfg<BN, GATHER, CG>::kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ Params p) {
-  using Cfg = KernelCfg<BN, GATHER>;
+  using Cfg = KernelCfg<BN, GATHER, CG>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = ptx::smem_addr(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;  // swizzle atoms need 1 KiB alignment
@@ -458,6 +524,9 @@ __global__ void __launch_bounds__(KernelCfg<BN, GATHER>::kThreads, 1)
   sh.cu = cu_s;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = (CG == 2) ? ptx::cluster_ctarank() : 0u;
+  const int32_t unit = static_cast<int32_t>(blockIdx.x) / CG;
+  const int32_t units = static_cast<int32_t>(gridDim.x) / CG;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -466,18 +535,23 @@ __global__ void __launch_bounds__(KernelCfg<BN, GATHER>::kThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       ptx::mbar_init(sh.tfull + 8 * b, 1);
-      ptx::mbar_init(sh.tempty + 8 * b, kEpiWarps);
+      ptx::mbar_init(sh.tempty + 8 * b, kEpiWarps * CG);
     }
     *abort_flag = 0;
     ptx::fence_barrier_init();
   }
-  if (warp == kLoadWarp && lane == 0) {
+  if (warp == kLoadWarp && lane == 0 && p.k_tiles > 0) {
     ptx::prefetch_tmap(&tmA);
     ptx::prefetch_tmap(&tmB);
   }
   if (warp == kMmaWarp) {
-    ptx::tmem_alloc(ptx::smem_addr(tmem_slot), Cfg::kTmemCols);
-    ptx::tmem_relinquish();
+    if (CG == 1) {
+      ptx::tmem_alloc(ptx::smem_addr(tmem_slot), Cfg::kTmemCols);
+      ptx::tmem_relinquish();
+    } else {
+      ptx::tmem_alloc_pair(ptx::smem_addr(tmem_slot), Cfg::kTmemCols);
+      ptx::tmem_relinquish_pair();
+    }
     ptx::tc_fence_before();
   }
   // varlen-M: copy cu_seqlens and build the per-group tile prefix (warp 0)
@@ -490,7 +564,7 @@ __global__ void __launch_bounds__(KernelCfg<BN, GATHER>::kThreads, 1)
       const int32_t lo = __ldg(p.cu_seqlens + g), hi = __ldg(p.cu_seqlens + g + 1);
       if (lo < 0 || hi > p.M || hi < lo) record_status(p, DEV_INDEX_RANGE, 5, g);
       const int32_t len = max(0, min(hi, p.M) - max(lo, 0));
-      mine += ((len + kBM - 1) / kBM) * p.tiles_n;
+      mine += ((len + Cfg::kTileM - 1) / Cfg::kTileM) * p.tiles_n;
     }
     int32_t incl = mine;
 #pragma unroll
@@ -505,7 +579,7 @@ __global__ void __launch_bounds__(KernelCfg<BN, GATHER>::kThreads, 1)
       const int32_t len = max(0, min(hi, p.M) - clo);
       prefix[g] = run;
       cu_s[g] = clo;
-      run += ((len + kBM - 1) / kBM) * p.tiles_n;
+      run += ((len + Cfg::kTileM - 1) / Cfg::kTileM) * p.tiles_n;
     }
     if (lane == 31) {
       prefix[G] = incl;
@@ -513,30 +587,34 @@ __global__ void __launch_bounds__(KernelCfg<BN, GATHER>::kThreads, 1)
     }
   }
   __syncthreads();
+  if (CG == 2) ptx::cluster_sync();  // the peer's barriers exist before anyone signals them
   ptx::tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const int32_t num_tiles = (p.num_groups > 0) ? prefix[p.num_groups] : p.num_tiles;
 
   if (warp < kEpiWarps) {
-    epilogue_role<BN, GATHER>(p, sh, tmem_base, num_tiles);
+    epilogue_role<BN, GATHER, CG>(p, sh, tmem_base, num_tiles, rank, unit, units);
   } else if (warp == kMmaWarp) {
-    if (lane == 0) mma_role<BN, GATHER>(p, sh, a0, b0, tmem_base, num_tiles);
+    if (rank == 0) mma_role<BN, GATHER, CG>(p, sh, a0, b0, tmem_base, num_tiles, unit, units);
   } else if (GATHER) {
     gather_producer_role<BN>(p, sh, &tmB, a0, b0, num_tiles);
-  } else if (lane == 0) {
-    tma_producer_role<BN, GATHER>(p, sh, &tmA, &tmB, a0, b0, num_tiles);
+  } else {
+    tma_producer_role<BN, GATHER, CG>(p, sh, &tmA, &tmB, a0, b0, num_tiles, rank, unit, units);
   }
 
   __syncthreads();
+  // no CTA of a pair leaves (or frees TMEM) while its peer may still signal it
+  if (CG == 2) ptx::cluster_sync();
   if (*abort_flag) {
     // let copies and MMAs that were in flight land before the memory goes away
     const uint64_t t0 = ptx::globaltimer();
     while (ptx::globaltimer() - t0 < 200000ull) __nanosleep(1000);
   }
   if (warp == kMmaWarp) {
-    __syncwarp();  // lane 0 ran the MMA loop alone; dealloc is warp-collective
+    __syncwarp();  // dealloc is warp-collective
     ptx::tc_fence_after();
-    ptx::tmem_dealloc(tmem_base, Cfg::kTmemCols);
+    if (CG == 1) ptx::tmem_dealloc(tmem_base, Cfg::kTmemCols);
+    else ptx::tmem_dealloc_pair(tmem_base, Cfg::kTmemCols);
   }
 }
 

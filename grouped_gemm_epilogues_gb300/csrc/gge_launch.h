@@ -14,11 +14,15 @@ struct LaunchShape {
   size_t smem;
 };
 
-template <int BN, bool GATHER>
+template <int BN, bool GATHER, int CG>
 cudaError_t launch_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const Params& p,
                         const LaunchShape& shape, cudaStream_t stream);
 
-template <int BN, bool GATHER>
+template <int BN, bool GATHER, int CG>
 int kernel_threads();
+
+// Clusters of CG CTAs (with `smem` bytes each) that can be resident at once.
+template <int BN, bool GATHER, int CG>
+int max_active_units(size_t smem);
 
 }  // namespace gge

@@ -86,7 +86,9 @@ typedef struct gge_config {
   int32_t raster_band;    /* 0 = auto; m-tiles per raster band (plain problems)    */
   int32_t stages;         /* 0 = as many as shared memory holds                    */
   int32_t flags;          /* bit 0: count tile visits into tile_counts            */
-  int32_t reserved;
+  int32_t cta_group;      /* 0 = auto; 1 = one CTA per 128-row tile; 2 = a CTA pair
+                             per 256-row tile (tcgen05 cta_group::2, 256-column
+                             tiles, not with gather-A)                             */
   int32_t* tile_counts;   /* device int32 per tile (debug coverage), or NULL       */
   uint64_t timeout_ns;    /* 0 = default (2 s) limit for each pipeline wait        */
 } gge_config;
@@ -190,13 +192,13 @@ int32_t gge_schedule_map(int32_t tiles_m, int32_t tiles_n, int32_t batches, int3
 /* The launch plan the library would use for `args` (tile and pipeline
  * shape).  Returns GGE_OK or the validation error of the call. */
 typedef struct gge_plan_info {
-  int32_t tile_m, tile_n, tile_k, stages;
+  int32_t tile_m, tile_n, tile_k, stages;  /* tile_m: rows per (pair) tile */
   int32_t num_tiles;  /* plain problems; -1 for varlen (known on the device only) */
   int32_t grid;
   int32_t threads;
   int32_t smem_bytes;
   int32_t raster_band;
-  int32_t reserved;
+  int32_t cta_group;  /* 1 or 2 CTAs per tile */
 } gge_plan_info;
 gge_status gge_plan(const gge_gemm_args* args, int32_t num_groups, int32_t gather,
                     gge_plan_info* out);

@@ -140,8 +140,14 @@ def test_plan_without_gpu(L):
     D = torch.zeros(8192, 8192, dtype=torch.bfloat16)
     cfg = binding.make_config(num_ctas=152)
     info = binding.gge_plan(A, A, D=D, config=cfg)
-    assert info["tile_m"] == 128 and info["tile_n"] == 256 and info["tile_k"] == 64
-    assert info["num_tiles"] == 64 * 32 and info["grid"] == 152
+    # a CTA pair per 256 x 256 tile by default
+    assert info["cta_group"] == 2 and info["tile_m"] == 256 and info["tile_n"] == 256
+    assert info["tile_k"] == 64
+    assert info["num_tiles"] == 32 * 32 and info["grid"] == 152
+    assert info["stages"] == 7
+    cfg1 = binding.make_config(num_ctas=152, cta_group=1)
+    info = binding.gge_plan(A, A, D=D, config=cfg1)
+    assert info["tile_m"] == 128 and info["num_tiles"] == 64 * 32 and info["stages"] == 4
     assert 2 <= info["stages"] <= 8 and info["smem_bytes"] <= 232448
     A8 = torch.zeros(512, 512, dtype=torch.float8_e4m3fn)
     D8 = torch.zeros(512, 512, dtype=torch.bfloat16)

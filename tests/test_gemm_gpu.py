@@ -91,12 +91,12 @@ def test_small_parity(case):
     _check_plain(w, t, out)
 
 
-@pytest.mark.parametrize("tile_n", [128, 256])
-def test_tile_shapes_and_guard_columns(tile_n):
+@pytest.mark.parametrize("tile_n,cta_group", [(128, 1), (256, 1), (256, 2)])
+def test_tile_shapes_and_guard_columns(tile_n, cta_group):
     w = wl.small("gemm_act_4096_bf16_gelu", 392, 264, 320, 2)
     t = wl.make(w)
     out = _outputs(w, 392, 264, 2, pad=24, fill=7.0)
-    _run_plain(w, t, out, config=binding.make_config(tile_n=tile_n))
+    _run_plain(w, t, out, config=binding.make_config(tile_n=tile_n, cta_group=cta_group))
     _check_plain(w, t, out)
     for k in ("D_full", "P_full"):
         assert (out[k][:, :, 264:].float() == 7.0).all()
@@ -133,15 +133,32 @@ def test_deterministic():
     assert torch.equal(o1["P"].view(torch.int16), o2["P"].view(torch.int16))
 
 
-def test_schedule_covers_each_tile_once():
+@pytest.mark.parametrize("cta_group", [1, 2])
+def test_schedule_covers_each_tile_once(cta_group):
     w = wl.small("gemm_256_bf16", 1000, 776, 64, 3)
     t = wl.make(w)
     out = _outputs(w, 1000, 776, 3)
-    tiles = 8 * 4 * 3
-    counts = torch.zeros(tiles, dtype=torch.int32, device=DEV)
-    cfg = binding.make_config(flags=1, tile_counts=counts, num_ctas=7, raster_band=3)
+    tiles = (8 // cta_group) * 4 * 3 if cta_group == 1 else 4 * 4 * 3
+    counts = torch.zeros(tiles + 8, dtype=torch.int32, device=DEV)
+    cfg = binding.make_config(flags=1, tile_counts=counts, num_ctas=7 * cta_group, raster_band=3,
+                              cta_group=cta_group)
     _run_plain(w, t, out, config=cfg)
-    assert (counts.cpu() == 1).all()
+    c = counts.cpu()
+    assert (c[:tiles] == 1).all() and (c[tiles:] == 0).all()
+    _check_plain(w, t, out)
+
+
+@pytest.mark.parametrize("cta_group", [1, 2])
+@pytest.mark.parametrize("case", [("gemm_8192_f16_relu", 520, 512, 264, 2, {}),
+                                  ("gemm_8192_fp8", 640, 768, 384, 1, {}),
+                                  ("gemm_act_4096_bf16_gelu", 256, 256, 64, 1, {})],
+                         ids=lambda c: c[0] if isinstance(c, tuple) else str(c))
+def test_cta_group_variants(case, cta_group):
+    name, M, N, K, L, kw = case
+    w = wl.small(name, M, N, K, L, **kw)
+    t = wl.make(w)
+    out = _outputs(w, M, N, L)
+    _run_plain(w, t, out, config=binding.make_config(tile_n=256, cta_group=cta_group))
     _check_plain(w, t, out)
 
 

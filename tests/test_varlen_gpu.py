@@ -107,14 +107,16 @@ def test_varlen_rows_outside_groups_untouched():
     _check(w, t, out, _oracle(w, t, False))
 
 
-def test_varlen_tile_coverage():
+@pytest.mark.parametrize("cta_group", [1, 2])
+def test_varlen_tile_coverage(cta_group):
     w = wl.small("varlen_gather_g64_m32768_silu", 1500, 520, 64, groups=9, empty_groups=3,
                  gather_rows=0)
     t = wl.make(w)
     cu = t["cu_seqlens_m"].numpy()
-    expect = ot.varlen_tiles(cu, w.N, 128, 256)
+    expect = ot.varlen_tiles(cu, w.N, 128 * cta_group, 256)
     counts = torch.zeros(len(expect) + 16, dtype=torch.int32, device=DEV)
-    cfg = binding.make_config(flags=1, tile_counts=counts, num_ctas=5)
+    cfg = binding.make_config(flags=1, tile_counts=counts, num_ctas=5 * cta_group,
+                              cta_group=cta_group)
     out = _run(w, t, False, config=cfg)
     c = counts.cpu().numpy()
     assert (c[:len(expect)] == 1).all() and (c[len(expect):] == 0).all()
