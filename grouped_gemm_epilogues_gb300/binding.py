@@ -64,6 +64,7 @@ _SIGNATURES = {
                                   ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
     "gge_gemm_gather_a": (c_i32, [ctypes.POINTER(GgeGemmArgs), ctypes.c_void_p, ctypes.c_void_p,
                                   c_i32, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
+    "gge_gemm_act_static_scratch": (c_i32, [ctypes.POINTER(GgeGemmArgs), ctypes.c_void_p]),
     "gge_read_device_status": (c_i32, [ctypes.c_void_p, ctypes.c_void_p,
                                        ctypes.POINTER(c_i32)]),
     "gge_status_string": (ctypes.c_char_p, [c_i32]),
@@ -200,6 +201,17 @@ def gge_gemm_act(A, B, PostAct, act, D=None, C=None, alpha=1.0, beta=1.0, alpha_
     ws = workspace(PostAct.device)
     _check(lib.gge_gemm_act(ctypes.byref(args), ctypes.c_void_p(ws.data_ptr()), ws.numel(),
                             _stream(PostAct)), "gge_gemm_act")
+
+
+def gge_gemm_act_static_scratch(A, B, PostAct, act, D=None, C=None, alpha=1.0, beta=1.0,
+                                config=None):
+    """gge_gemm_act for callers that cannot allocate: no workspace argument, the
+    library's own fixed scratch area is used (see include/gge.h)."""
+    lib = load()
+    args = make_args(A, B, C=C, D=D, PostAct=PostAct, alpha=alpha, beta=beta, act=act,
+                     config=config)
+    _check(lib.gge_gemm_act_static_scratch(ctypes.byref(args), _stream(PostAct)),
+           "gge_gemm_act_static_scratch")
 
 
 def gge_gemm_varlen_m(A, B, cu_seqlens_m, D=None, PostAct=None, act="none", C=None, alpha=1.0,

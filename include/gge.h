@@ -165,6 +165,23 @@ gge_status gge_gemm_gather_a(const gge_gemm_args* args, const int32_t* a_idx,
                              const int32_t* cu_seqlens_m, int32_t num_groups, void* workspace,
                              size_t workspace_bytes, gge_stream_t stream);
 
+/* gge_gemm_act without a caller workspace, for callers that cannot allocate
+ * device memory where they run the GEMM (a host framework that owns all device
+ * memory through its own arena or caching allocator, or a latency-critical path
+ * that must not call the allocator).  The pages have no counterpart: it is an
+ * addition of this library.
+ *   - The scratch (the status words) lives in a fixed 1024-byte __device__ area
+ *     inside the library, held on every GPU that loads it until process exit.
+ *     A call whose gge_workspace_size exceeds 1024 bytes returns
+ *     GGE_ERR_WORKSPACE.
+ *   - The first call on a device looks up that area's device address (on the
+ *     current device); make that first call before any stream capture.
+ *   - Each call clears the status words (an async memset on `stream`), then
+ *     launches the same kernel as gge_gemm_act.  Nothing is allocated.
+ *   - All calls on a device share the one area: calls that overlap on the GPU
+ *     (different streams without ordering) race on it. */
+gge_status gge_gemm_act_static_scratch(const gge_gemm_args* args, gge_stream_t stream);
+
 /* Synchronises `stream`, returns the device status recorded in `workspace`
  * since it was last cleared (GGE_OK, GGE_ERR_TIMEOUT or GGE_ERR_INDEX_RANGE)
  * and clears it.  `detail` (may be NULL) receives [where, tile]. */
