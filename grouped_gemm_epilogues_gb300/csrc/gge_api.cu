@@ -145,14 +145,65 @@ uint64_t batch_stride_bytes(const gge_tensor& t, int es) {
 
 int variant_threads(int bn, bool gather, int cg) {
   if (gather) return bn == 128 ? kernel_threads<128, true, 1>() : kernel_threads<256, true, 1>();
-  if (cg == 2) return kernel_threads<256, false, 2>();
+  if (cg == 2) {
+    switch (bn) {
+      case 224: return kernel_threads<224, false, 2>();
+      case 192: return kernel_threads<192, false, 2>();
+      case 160: return kernel_threads<160, false, 2>();
+      default: return kernel_threads<256, false, 2>();
+    }
+  }
   return bn == 128 ? kernel_threads<128, false, 1>() : kernel_threads<256, false, 1>();
 }
 
 int variant_units(int bn, bool gather, int cg, size_t smem) {
   if (gather) return bn == 128 ? max_active_units<128, true, 1>(smem) : max_active_units<256, true, 1>(smem);
-  if (cg == 2) return max_active_units<256, false, 2>(smem);
+  if (cg == 2) {
+    switch (bn) {
+      case 224: return max_active_units<224, false, 2>(smem);
+      case 192: return max_active_units<192, false, 2>(smem);
+      case 160: return max_active_units<160, false, 2>(smem);
+      default: return max_active_units<256, false, 2>(smem);
+    }
+  }
   return bn == 128 ? max_active_units<128, false, 1>(smem) : max_active_units<256, false, 1>(smem);
+}
+
+cudaError_t variant_launch(const Plan& pl, cudaStream_t st) {
+  if (pl.gather)
+    return pl.bn == 128 ? launch_gemm<128, true, 1>(pl.tmA, pl.tmB, pl.p, pl.shape, st)
+                        : launch_gemm<256, true, 1>(pl.tmA, pl.tmB, pl.p, pl.shape, st);
+  if (pl.cg == 2) {
+    switch (pl.bn) {
+      case 224: return launch_gemm<224, false, 2>(pl.tmA, pl.tmB, pl.p, pl.shape, st);
+      case 192: return launch_gemm<192, false, 2>(pl.tmA, pl.tmB, pl.p, pl.shape, st);
+      case 160: return launch_gemm<160, false, 2>(pl.tmA, pl.tmB, pl.p, pl.shape, st);
+      default: return launch_gemm<256, false, 2>(pl.tmA, pl.tmB, pl.p, pl.shape, st);
+    }
+  }
+  return pl.bn == 128 ? launch_gemm<128, false, 1>(pl.tmA, pl.tmB, pl.p, pl.shape, st)
+                      : launch_gemm<256, false, 1>(pl.tmA, pl.tmB, pl.p, pl.shape, st);
+}
+
+// Relative time of a pair tile of width bn: tensor-core time per 16-deep MMA
+// step (math bn/2 cycles per SM) plus the operand bytes it fetches (measured
+// ~6.5 cycles per KiB: A 4 KiB + B 16*bn bytes per SM).
+double pair_tile_cost(int bn) { return 0.6 * bn + 26.0; }
+
+// Pair tile width with the least (rounds x tile cost) for `units` resident pairs.
+int choose_pair_bn(int64_t tiles_m, int64_t N, int64_t L, int64_t units) {
+  static const int kWidths[] = {256, 224, 192, 160};
+  int best = 256;
+  double best_cost = 0.0;
+  for (int bn : kWidths) {
+    const int64_t tiles = tiles_m * ((N + bn - 1) / bn) * L;
+    const int64_t rounds = (tiles + units - 1) / units;
+    const double cost = static_cast<double>(rounds) * pair_tile_cost(bn);
+    if (bn == 256 || cost < best_cost * 0.97) {  // prefer the widest tile unless clearly better
+      if (bn == 256 || cost < best_cost) { best = bn; best_cost = cost; }
+    }
+  }
+  return best;
 }
 
 // Validate and plan.  `encode` = build tensor maps (needs the CUDA driver).
@@ -237,12 +288,31 @@ gge_status make_plan(const gge_gemm_args* a, Form form, const int32_t* a_idx,
     if ((K * es) % 16 != 0) return GGE_ERR_UNSUPPORTED;  // whole 16-byte chunks along K
   }
 
-  // tile shape: 128 x BN on one CTA, or 256 x 256 on a CTA pair
-  int bn = cfg && cfg->tile_n ? cfg->tile_n : (N <= 128 ? 128 : 256);
-  if (bn != 128 && bn != 256) return GGE_ERR_UNSUPPORTED;
-  int cg = cfg && cfg->cta_group ? cfg->cta_group : ((!gather && bn == 256 && M >= 256) ? 2 : 1);
+  // tile shape: 128 x BN on one CTA, or 256 x BN on a CTA pair
+  int cg = cfg && cfg->cta_group ? cfg->cta_group : ((!gather && N > 128 && M >= 256) ? 2 : 1);
   if (cg != 1 && cg != 2) return GGE_ERR_UNSUPPORTED;
-  if (cg == 2 && (gather || bn != 256)) return GGE_ERR_UNSUPPORTED;
+  if (cg == 2 && gather) return GGE_ERR_UNSUPPORTED;
+  int bn = cfg && cfg->tile_n ? cfg->tile_n : 0;
+  if (cg == 1) {
+    if (bn == 0) bn = N <= 128 ? 128 : 256;
+    if (bn != 128 && bn != 256) return GGE_ERR_UNSUPPORTED;
+  } else {
+    if (bn == 0) {
+      bn = 256;
+      // narrower tiles even out the last wave; N-major B stages 64-column chunks
+      if (!b_mn && !varlen) {
+        int64_t units = cfg && cfg->num_ctas > 0 ? cfg->num_ctas / 2 : 0;
+        if (units <= 0 && encode) {
+          const size_t smem256 = 1024 + kCtrlBytesHost +
+                                 7 * (kTileM + 128) * kRowBytesHost;  // the 256-wide plan
+          units = variant_units(256, false, 2, smem256);
+        }
+        if (units > 0) bn = choose_pair_bn((M + 2 * kTileM - 1) / (2 * kTileM), N, L, units);
+      }
+    }
+    if (bn != 256 && bn != 224 && bn != 192 && bn != 160) return GGE_ERR_UNSUPPORTED;
+    if (b_mn && bn != 256) return GGE_ERR_UNSUPPORTED;
+  }
   pl.bn = bn;
   pl.cg = cg;
   const int tile_m = kTileM * cg;
@@ -376,15 +446,7 @@ gge_status run(const gge_gemm_args* a, Form form, const int32_t* a_idx, const in
   if (pl.empty) return GGE_OK;
   pl.p.status = static_cast<int32_t*>(ws);
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  cudaError_t e;
-  if (pl.gather)
-    e = pl.bn == 128 ? launch_gemm<128, true, 1>(pl.tmA, pl.tmB, pl.p, pl.shape, st)
-                     : launch_gemm<256, true, 1>(pl.tmA, pl.tmB, pl.p, pl.shape, st);
-  else if (pl.cg == 2)
-    e = launch_gemm<256, false, 2>(pl.tmA, pl.tmB, pl.p, pl.shape, st);
-  else
-    e = pl.bn == 128 ? launch_gemm<128, false, 1>(pl.tmA, pl.tmB, pl.p, pl.shape, st)
-                     : launch_gemm<256, false, 1>(pl.tmA, pl.tmB, pl.p, pl.shape, st);
+  const cudaError_t e = variant_launch(pl, st);
   return e == cudaSuccess ? GGE_OK : GGE_ERR_CUDA;
 }
 

@@ -1,0 +1,6 @@
+// Kernel instantiation: 256 x 160 tiles on a CTA pair (tcgen05 cta_group::2), TMA A producer.
+#include "gge_inst.cuh"
+
+namespace gge {
+GGE_INSTANTIATE(160, false, 2)
+}  // namespace gge

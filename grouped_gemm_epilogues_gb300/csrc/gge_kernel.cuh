@@ -20,7 +20,8 @@
 //   warps 5-8  (gather-A form) row gather of A with 16-byte cp.async into the
 //              same swizzled layout, B still by TMA (GemmSm90.load_AB_gather_A).
 //
-// With CG = 2 a cluster of two CTAs (a CTA pair) computes a 256 x BN tile:
+// With CG = 2 a cluster of two CTAs (a CTA pair) computes a 256 x BN tile
+// (BN = 256, 224, 192 or 160; narrower tiles even out the last wave):
 // each CTA stages its own 128 rows of A and half of the BN columns of B, the
 // leader CTA issues tcgen05.mma.cta_group::2 over both CTAs' shared memory,
 // and each CTA's TMEM receives its own 128 accumulator rows.  The pair halves
@@ -64,10 +65,10 @@ struct KernelCfg {
   static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr int kWarps = GATHER ? kLoadWarp + kGatherWarps : kLoadWarp + 1;
   static constexpr int kThreads = kWarps * 32;
-  static constexpr int kTmemCols = 2 * BN;  // two accumulator buffers
-  static_assert(BN % 64 == 0 && BN <= 256, "BN must be 64, 128, 192 or 256");
-  static_assert(kTmemCols == 128 || kTmemCols == 256 || kTmemCols == 512,
-                "TMEM allocation must be a power of two");
+  // two accumulator buffers of BN columns; the allocation is the next power of two
+  static constexpr int kTmemCols = (2 * BN <= 128) ? 128 : (2 * BN <= 256) ? 256 : 512;
+  static_assert(BN % 32 == 0 && BN >= 64 && BN <= 256, "BN: a multiple of 32 in [64, 256]");
+  static_assert(kBRows % 8 == 0, "B rows per CTA must fill 8-row swizzle atoms");
   static_assert(CG == 1 || CG == 2, "one CTA or a CTA pair");
   static_assert(!(GATHER && CG == 2), "the row gather runs on single-CTA tiles");
 };

@@ -81,7 +81,9 @@ typedef struct gge_tensor {
 
 /* Optional tuning / debug knobs; pass NULL for the defaults. */
 typedef struct gge_config {
-  int32_t tile_n;         /* 0 = auto; else 64, 128 or 256 output columns per tile */
+  int32_t tile_n;         /* 0 = auto; else output columns per tile: 128 or 256 on
+                             one CTA, 256, 224, 192 or 160 on a CTA pair (the
+                             narrower pair tiles need a K-major B)                 */
   int32_t num_ctas;       /* 0 = one persistent CTA per SM                         */
   int32_t raster_band;    /* 0 = auto; m-tiles per raster band (plain problems)    */
   int32_t stages;         /* 0 = as many as shared memory holds                    */

@@ -149,6 +149,12 @@ def test_plan_without_gpu(L):
     info = binding.gge_plan(A, A, D=D, config=cfg1)
     assert info["tile_m"] == 128 and info["num_tiles"] == 64 * 32 and info["stages"] == 4
     assert 2 <= info["stages"] <= 8 and info["smem_bytes"] <= 232448
+    # 4096^2 on 76 pairs: 256-wide tiles need 3.37 rounds, 224-wide exactly 4 shorter ones
+    A4 = torch.zeros(4096, 4096, dtype=torch.bfloat16)
+    info = binding.gge_plan(A4, A4, D=A4, config=cfg)
+    assert info["cta_group"] == 2 and info["tile_n"] == 224 and info["num_tiles"] == 16 * 19
+    Bn = torch.zeros(4096, 4096, dtype=torch.bfloat16).t()  # N-major B keeps 256-wide tiles
+    assert binding.gge_plan(A4, Bn, D=A4, config=cfg)["tile_n"] == 256
     A8 = torch.zeros(512, 512, dtype=torch.float8_e4m3fn)
     D8 = torch.zeros(512, 512, dtype=torch.bfloat16)
     info = binding.gge_plan(A8, A8.to(torch.float8_e5m2), D=D8, config=cfg)

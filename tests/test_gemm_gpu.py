@@ -148,6 +148,23 @@ def test_schedule_covers_each_tile_once(cta_group):
     _check_plain(w, t, out)
 
 
+@pytest.mark.parametrize("tile_n", [224, 192, 160])
+@pytest.mark.parametrize("case", [("gemm_act_4096_bf16_gelu", 520, 712, 264, 2, {}),
+                                  ("gemm_8192_fp8", 512, 680, 384, 1, {}),
+                                  ("gemm_8192_f16_relu", 300, 456, 200, 1, {"b_major": "k"})],
+                         ids=lambda c: c[0] if isinstance(c, tuple) else str(c))
+def test_narrow_pair_tiles(case, tile_n):
+    name, M, N, K, L, kw = case
+    w = wl.small(name, M, N, K, L, **kw)
+    t = wl.make(w)
+    out = _outputs(w, M, N, L, pad=16, fill=5.0)
+    _run_plain(w, t, out, config=binding.make_config(tile_n=tile_n, cta_group=2))
+    _check_plain(w, t, out)
+    for k in ("D_full", "P_full"):
+        if k in out:
+            assert (out[k][:, :, N:].float() == 5.0).all()
+
+
 @pytest.mark.parametrize("cta_group", [1, 2])
 @pytest.mark.parametrize("case", [("gemm_8192_f16_relu", 520, 512, 264, 2, {}),
                                   ("gemm_8192_fp8", 640, 768, 384, 1, {}),
