@@ -510,7 +510,7 @@ __global__ void __launch_bounds__(KernelCfg<BN, GATHER, CG>::kThreads, 1)
   const uint32_t a0 = base;
   const uint32_t b0 = base + S * Cfg::kABytes;
   uint8_t* ctrl = base_ptr + S * Cfg::kStageBytes;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ctrl + 8 * (2 * S + 4));
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ctrl + 8 * (2 * S + 5));
   int32_t* abort_flag = reinterpret_cast<int32_t*>(tmem_slot + 1);
   int32_t* prefix = reinterpret_cast<int32_t*>(ctrl + kCtrlBytes);
   int32_t* cu_s = prefix + (kMaxGroups + 1);
@@ -520,6 +520,7 @@ __global__ void __launch_bounds__(KernelCfg<BN, GATHER, CG>::kThreads, 1)
   sh.empty = sh.full + 8 * S;
   sh.tfull = sh.empty + 8 * S;
   sh.tempty = sh.tfull + 16;
+  const uint32_t drain_bar = sh.tempty + 16;  // MMAs in flight have finished
   sh.abort = abort_flag;
   sh.prefix = prefix;
   sh.cu = cu_s;
@@ -538,6 +539,7 @@ __global__ void __launch_bounds__(KernelCfg<BN, GATHER, CG>::kThreads, 1)
       ptx::mbar_init(sh.tfull + 8 * b, 1);
       ptx::mbar_init(sh.tempty + 8 * b, kEpiWarps * CG);
     }
+    ptx::mbar_init(drain_bar, 1);
     *abort_flag = 0;
     ptx::fence_barrier_init();
   }
@@ -603,6 +605,17 @@ __global__ void __launch_bounds__(KernelCfg<BN, GATHER, CG>::kThreads, 1)
     tma_producer_role<BN, GATHER, CG>(p, sh, &tmA, &tmB, a0, b0, num_tiles, rank, unit, units);
   }
 
+  __syncthreads();
+  // Every MMA this CTA issued has finished before TMEM is freed (after an abort
+  // nobody else has waited for them); the wait is bounded like all others.
+  if (warp == kMmaWarp && rank == 0) {
+    if (ptx::elect_one()) {
+      if (CG == 1) ptx::mma_commit(drain_bar);
+      else ptx::mma_commit_pair(drain_bar, 0x1);
+    }
+    __syncwarp();
+    wait_phase<CG == 2>(drain_bar, 0, p, sh, 6, -1);
+  }
   __syncthreads();
   // no CTA of a pair leaves (or frees TMEM) while its peer may still signal it
   if (CG == 2) ptx::cluster_sync();

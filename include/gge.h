@@ -87,7 +87,10 @@ typedef struct gge_config {
   int32_t num_ctas;       /* 0 = one persistent CTA per SM                         */
   int32_t raster_band;    /* 0 = auto; m-tiles per raster band (plain problems)    */
   int32_t stages;         /* 0 = as many as shared memory holds                    */
-  int32_t flags;          /* bit 0: count tile visits into tile_counts            */
+  int32_t flags;          /* bit 0: count tile visits into tile_counts;
+                             bit 1: test hook -- the MMA warp never signals a
+                             finished accumulator, so the epilogue's bounded wait
+                             runs out and the call reports GGE_ERR_TIMEOUT        */
   int32_t cta_group;      /* 0 = auto; 1 = one CTA per 128-row tile; 2 = a CTA pair
                              per 256-row tile (tcgen05 cta_group::2, 256-column
                              tiles, not with gather-A)                             */
