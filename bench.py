@@ -371,17 +371,24 @@ def _oracle_rows(w, base, rows):
     return 2.0 * len(rows) * w.N * w.K * w.L
 
 
+def _rows_for_budget(w, base, budget_s):
+    """Rows whose oracle run takes about budget_s: two probes separate the fixed
+    cost (decoding B) from the per-row cost."""
+    t0 = time.perf_counter()
+    _oracle_rows(w, base, np.arange(min(w.M, 8)))
+    t1 = time.perf_counter()
+    _oracle_rows(w, base, np.arange(min(w.M, 72)))
+    t2 = time.perf_counter()
+    per_row = max((t2 - t1) - (t1 - t0), 1e-6) / max(1, min(w.M, 72) - min(w.M, 8))
+    fixed = max((t1 - t0) - 8 * per_row, 0.0)
+    return int(min(w.M, max(16, (budget_s - fixed) / per_row)))
+
+
 def cpu_baseline(w, base, budget_s=15.0):
     """Time the oracle as it stands on the host cores over a bounded sample
     of the workload's output rows (about budget_s seconds of work)."""
     M = w.M
-    rows = np.arange(0, min(M, 16))
-    t0 = time.perf_counter()
-    f = _oracle_rows(w, base, rows)
-    dt = time.perf_counter() - t0
-    rate = f / max(dt, 1e-6)
-    per_row = f / len(rows)
-    n = int(min(M, max(16, budget_s * rate / per_row)))
+    n = _rows_for_budget(w, base, budget_s)
     rng = np.random.default_rng(0)
     rows = np.sort(rng.choice(M, size=n, replace=False))
     t0 = time.perf_counter()
@@ -400,13 +407,7 @@ def run_reference(args, w):
     base = wl.make(w)
     total_budget = 150.0
     per_step = total_budget / max(1, args.steps + args.warmup)
-    # calibrate the rows per step to the budget
-    probe_rows = np.arange(min(w.M, 8))
-    t0 = time.perf_counter()
-    f = _oracle_rows(w, base, probe_rows)
-    dt = max(time.perf_counter() - t0, 1e-6)
-    per_row_s = dt / len(probe_rows)
-    n = int(min(w.M, max(1, per_step / per_row_s)))
+    n = _rows_for_budget(w, base, per_step)
     rng = np.random.default_rng(0)
     samples = [np.sort(rng.choice(w.M, size=n, replace=False))
                for _ in range(args.steps + args.warmup)]
