@@ -20,7 +20,8 @@ c_i32, c_i64, c_u32, c_u64 = ctypes.c_int32, ctypes.c_int64, ctypes.c_uint32, ct
 
 DTYPE = {torch.bfloat16: 0, torch.float16: 1, torch.float8_e4m3fn: 2, torch.float8_e5m2: 3,
          torch.float32: 4}
-ACT = {"none": 0, None: 0, "relu": 1, "gelu_tanh": 2, "gelu_tanh_approx": 2, "silu": 3}
+ACT = {"none": 0, None: 0, "relu": 1, "gelu_tanh": 2, "gelu_tanh_approx": 2, "silu": 3,
+       "relu_sq": 4}
 STATUS = {0: "GGE_OK", 1: "GGE_ERR_INVALID_ARG", 2: "GGE_ERR_UNSUPPORTED",
           3: "GGE_ERR_ALIGNMENT", 4: "GGE_ERR_WORKSPACE", 5: "GGE_ERR_CUDA",
           6: "GGE_ERR_TIMEOUT", 7: "GGE_ERR_INDEX_RANGE"}
@@ -64,6 +65,8 @@ _SIGNATURES = {
                                   ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
     "gge_gemm_gather_a": (c_i32, [ctypes.POINTER(GgeGemmArgs), ctypes.c_void_p, ctypes.c_void_p,
                                   c_i32, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
+    "gge_gemm_dact": (c_i32, [ctypes.POINTER(GgeGemmArgs), ctypes.c_void_p, ctypes.c_size_t,
+                              ctypes.c_void_p]),
     "gge_gemm_act_static_scratch": (c_i32, [ctypes.POINTER(GgeGemmArgs), ctypes.c_void_p]),
     "gge_read_device_status": (c_i32, [ctypes.c_void_p, ctypes.c_void_p,
                                        ctypes.POINTER(c_i32)]),
@@ -201,6 +204,15 @@ def gge_gemm_act(A, B, PostAct, act, D=None, C=None, alpha=1.0, beta=1.0, alpha_
     ws = workspace(PostAct.device)
     _check(lib.gge_gemm_act(ctypes.byref(args), ctypes.c_void_p(ws.data_ptr()), ws.numel(),
                             _stream(PostAct)), "gge_gemm_act")
+
+
+def gge_gemm_dact(A, B, PreAct, D, act, PostAct=None, config=None):
+    """Backward activation epilogue: D = act'(PreAct) * (A @ B^T), PostAct = act(PreAct)."""
+    lib = load()
+    args = make_args(A, B, C=PreAct, D=D, PostAct=PostAct, act=act, config=config)
+    ws = workspace(D.device)
+    _check(lib.gge_gemm_dact(ctypes.byref(args), ctypes.c_void_p(ws.data_ptr()), ws.numel(),
+                             _stream(D)), "gge_gemm_dact")
 
 
 def gge_gemm_act_static_scratch(A, B, PostAct, act, D=None, C=None, alpha=1.0, beta=1.0,

@@ -209,7 +209,7 @@ int choose_pair_bn(int64_t tiles_m, int64_t N, int64_t L, int64_t units) {
 // Validate and plan.  `encode` = build tensor maps (needs the CUDA driver).
 gge_status make_plan(const gge_gemm_args* a, Form form, const int32_t* a_idx,
                      const int32_t* cu, int32_t G, bool want_act, bool act_entry, bool encode,
-                     Plan* out) {
+                     Plan* out, bool dact = false) {
   if (a == nullptr || out == nullptr) return GGE_ERR_INVALID_ARG;
   Plan& pl = *out;
   std::memset(&pl, 0, sizeof(pl));
@@ -219,13 +219,16 @@ gge_status make_plan(const gge_gemm_args* a, Form form, const int32_t* a_idx,
   const bool gather = (form == Form::Gather || form == Form::GatherVarlen);
   pl.gather = gather;
 
-  if (a->act < GGE_ACT_NONE || a->act > GGE_ACT_SILU) return GGE_ERR_INVALID_ARG;
-  if (act_entry) {
+  if (a->act < GGE_ACT_NONE || a->act > GGE_ACT_RELU_SQ) return GGE_ERR_INVALID_ARG;
+  if (dact) {
+    // backward epilogue: C = pre-activation and D = dx are required, PostAct optional
+    if (a->C == nullptr || a->D == nullptr || a->act == GGE_ACT_NONE) return GGE_ERR_INVALID_ARG;
+  } else if (act_entry) {
     if (a->PostAct == nullptr) return GGE_ERR_INVALID_ARG;
   } else if (!want_act) {
     if (a->PostAct != nullptr || a->act != GGE_ACT_NONE) return GGE_ERR_INVALID_ARG;
   }
-  if (a->PostAct == nullptr && a->act != GGE_ACT_NONE) return GGE_ERR_INVALID_ARG;
+  if (!dact && a->PostAct == nullptr && a->act != GGE_ACT_NONE) return GGE_ERR_INVALID_ARG;
   if (a->D == nullptr && a->PostAct == nullptr) return GGE_ERR_INVALID_ARG;
 
   gge_status s = check_view(a->A);
@@ -375,6 +378,7 @@ gge_status make_plan(const gge_gemm_args* a, Form form, const int32_t* a_idx,
     p.c = a->C->ptr; p.ldc = a->C->stride_row; p.sbc = a->C->stride_batch; p.c_dtype = a->C->dtype;
   }
   p.act = a->act;
+  p.dact = dact ? 1 : 0;
   p.alpha = a->alpha;
   p.beta = a->beta;
   p.alpha_dev = a->alpha_dev;
@@ -437,11 +441,11 @@ gge_status check_workspace(void* ws, size_t bytes) {
 
 gge_status run(const gge_gemm_args* a, Form form, const int32_t* a_idx, const int32_t* cu,
                int32_t G, bool want_act, bool act_entry, void* ws, size_t ws_bytes,
-               gge_stream_t stream) {
+               gge_stream_t stream, bool dact = false) {
   gge_status s = check_workspace(ws, ws_bytes);
   if (s != GGE_OK) return s;
   Plan pl;
-  s = make_plan(a, form, a_idx, cu, G, want_act, act_entry, true, &pl);
+  s = make_plan(a, form, a_idx, cu, G, want_act, act_entry, true, &pl, dact);
   if (s != GGE_OK) return s;
   if (pl.empty) return GGE_OK;
   pl.p.status = static_cast<int32_t*>(ws);
@@ -470,6 +474,11 @@ gge_status gge_gemm(const gge_gemm_args* args, void* ws, size_t ws_bytes, gge_st
 gge_status gge_gemm_act(const gge_gemm_args* args, void* ws, size_t ws_bytes,
                         gge_stream_t stream) {
   return gge::run(args, Form::Plain, nullptr, nullptr, 0, true, true, ws, ws_bytes, stream);
+}
+
+gge_status gge_gemm_dact(const gge_gemm_args* args, void* ws, size_t ws_bytes,
+                         gge_stream_t stream) {
+  return gge::run(args, Form::Plain, nullptr, nullptr, 0, true, false, ws, ws_bytes, stream, true);
 }
 
 gge_status gge_gemm_varlen_m(const gge_gemm_args* args, const int32_t* cu_seqlens_m,

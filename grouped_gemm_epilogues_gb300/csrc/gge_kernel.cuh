@@ -182,8 +182,33 @@ __device__ __forceinline__ float act_apply(int act, float x) {
     }
     case ACT_SILU:
       return __fdividef(x, 1.f + __expf(-x));
+    case ACT_RELU_SQ:
+      return (x <= 0.f) ? 0.f : x * x;
     default:
       return x;
+  }
+}
+
+// act'(x) for the backward epilogue.
+__device__ __forceinline__ float dact_apply(int act, float x) {
+  switch (act) {
+    case ACT_RELU:
+      return (x > 0.f) ? 1.f : 0.f;
+    case ACT_RELU_SQ:
+      return (x <= 0.f) ? 0.f : 2.f * x;
+    case ACT_GELU_TANH: {
+      // s = sigmoid(2u) = (1 + tanh u) / 2 and 1 - tanh^2 u = 4 s (1 - s)
+      const float u = 0.7978845608028654f * fmaf(0.044715f * x, x * x, x);
+      const float s = __fdividef(1.f, 1.f + __expf(-2.f * u));
+      const float du = 0.7978845608028654f * fmaf(3.f * 0.044715f * x, x, 1.f);
+      return fmaf(2.f * x * s * (1.f - s), du, s);
+    }
+    case ACT_SILU: {
+      const float s = __fdividef(1.f, 1.f + __expf(-x));
+      return s * fmaf(x, 1.f - s, 1.f);
+    }
+    default:
+      return 1.f;
   }
 }
 
@@ -235,10 +260,45 @@ __device__ __forceinline__ void store8(void* ptr, int dtype, const float* x) {
 
 __device__ __forceinline__ int dtype_bytes(int dt) { return dt == DT_F32 ? 4 : 2; }
 
+// Backward epilogue for one thread's 32 columns: x (the pre-activation) comes
+// from C, dout is the accumulator; D = act'(x) * dout, PostAct = act(x).
+__device__ __forceinline__ void epilogue_chunk_dact(const Params& p, const uint32_t (&acc)[32],
+                                                 int32_t row, int32_t col0, int32_t batch) {
+  const int64_t out_batch = (p.num_groups > 0) ? 0 : batch;
+  const char* cbase = static_cast<const char*>(p.c) +
+                      (out_batch * p.sbc + static_cast<int64_t>(row) * p.ldc + col0) *
+                          dtype_bytes(p.c_dtype);
+  char* dbase = static_cast<char*>(p.d) +
+                (out_batch * p.sbd + static_cast<int64_t>(row) * p.ldd + col0) *
+                    dtype_bytes(p.d_dtype);
+  char* pbase = p.post == nullptr ? nullptr
+                                  : static_cast<char*>(p.post) +
+                                        (out_batch * p.sbp + static_cast<int64_t>(row) * p.ldp +
+                                         col0) * dtype_bytes(p.p_dtype);
+#pragma unroll
+  for (int g = 0; g < 4; ++g) {  // unrolled: acc stays in registers
+    if (col0 + 8 * g >= p.N) continue;
+    float x[8], dx[8];
+    load8(cbase + 8 * g * dtype_bytes(p.c_dtype), p.c_dtype, x);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) dx[j] = dact_apply(p.act, x[j]) * __uint_as_float(acc[8 * g + j]);
+    store8(dbase + 8 * g * dtype_bytes(p.d_dtype), p.d_dtype, dx);
+    if (pbase != nullptr) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) x[j] = act_apply(p.act, x[j]);
+      store8(pbase + 8 * g * dtype_bytes(p.p_dtype), p.p_dtype, x);
+    }
+  }
+}
+
 // One thread, one output row, 32 consecutive columns starting at col0.
 __device__ __forceinline__ void epilogue_chunk(const Params& p, const uint32_t (&acc)[32],
                                                int32_t row, int32_t col0, int32_t batch,
                                                float alpha, float beta) {
+  if (p.dact) {
+    epilogue_chunk_dact(p, acc, row, col0, batch);
+    return;
+  }
   float v[32];
 #pragma unroll
   for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(acc[j]) * alpha;

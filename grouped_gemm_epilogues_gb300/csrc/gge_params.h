@@ -8,7 +8,7 @@
 namespace gge {
 
 enum : int32_t { DT_BF16 = 0, DT_F16 = 1, DT_E4M3 = 2, DT_E5M2 = 3, DT_F32 = 4 };
-enum : int32_t { ACT_NONE = 0, ACT_RELU = 1, ACT_GELU_TANH = 2, ACT_SILU = 3 };
+enum : int32_t { ACT_NONE = 0, ACT_RELU = 1, ACT_GELU_TANH = 2, ACT_SILU = 3, ACT_RELU_SQ = 4 };
 
 // Device status words (the first bytes of the caller's workspace).
 enum : int32_t {
@@ -57,6 +57,7 @@ struct Params {
   int64_t ldc, sbc;
   int32_t d_dtype, p_dtype, c_dtype;
   int32_t act;
+  int32_t dact;  // backward epilogue: C is the pre-activation x, D = act'(x) * acc, PostAct = act(x)
   float alpha, beta;
   const float* alpha_dev;
   const float* beta_dev;

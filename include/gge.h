@@ -67,7 +67,8 @@ typedef enum gge_act {
   GGE_ACT_NONE = 0,
   GGE_ACT_RELU = 1,      /* x > 0 ? x : 0                                        */
   GGE_ACT_GELU_TANH = 2, /* 0.5 x (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3)))      */
-  GGE_ACT_SILU = 3       /* x / (1 + exp(-x))                                    */
+  GGE_ACT_SILU = 3,      /* x / (1 + exp(-x))                                    */
+  GGE_ACT_RELU_SQ = 4    /* relu(x)^2 (act_fn_map's relu_sq)                     */
 } gge_act;
 
 /* A strided 3-D view [rows, cols, batch]. */
@@ -145,6 +146,15 @@ gge_status gge_gemm(const gge_gemm_args* args, void* workspace, size_t workspace
  * GemmActSm90.epi_visit_acc_subtile. */
 gge_status gge_gemm_act(const gge_gemm_args* args, void* workspace, size_t workspace_bytes,
                         gge_stream_t stream);
+
+/* Backward activation epilogue: the accumulator S = A B^T is the incoming
+ * gradient dout, C (required) holds the pre-activation x, and
+ *   D = act'(x) * S      (required)        PostAct = act(x)   (optional)
+ * with act in {relu, relu_sq, gelu_tanh, silu}; alpha and beta are not used.
+ * Page: quack-kernels 0.2.0 diff, quack/gemm_dact_sm90.py, gemm_dact_sm90 /
+ * GemmDActSm90.epi_visit_acc_subtile (act_bwd(x, dout) -> (dx, out)). */
+gge_status gge_gemm_dact(const gge_gemm_args* args, void* workspace, size_t workspace_bytes,
+                         gge_stream_t stream);
 
 /* Varlen-M grouped GEMM: A is [total_M, K, 1], B is [N, K, G] (batch = G
  * groups), C / D / PostAct are [total_M, N, 1].  Group g owns rows

@@ -33,6 +33,7 @@ from . import activations
 from .formats import Fmt, round_to, quantum
 
 ACC_REL_TOL = 1e-5  # |err| <= 1e-5 * sum_k |a_k b_k| (+ one output ulp)
+DACT_SLACK = {activations.GELU_TANH: 1e-6, activations.SILU: 1e-6}
 
 
 def _epilogue(S, absS, C, alpha, beta, act):
@@ -111,6 +112,29 @@ def gemm_gather_a(A_src, a_idx, B, cu_seqlens_m=None, C=None, **kw):
         r = gemm(A_eff[None], np.asarray(B, np.float64).reshape(1, *np.shape(B)[-2:]), Cb, **kw)
         return {k: v[0] for k, v in r.items()}
     return gemm_varlen_m(A_eff, B, cu_seqlens_m, C, **kw)
+
+
+def gemm_dact(A, B, PreAct, *, act, d_fmt: Fmt = None, p_fmt: Fmt = None):
+    """Backward activation epilogue (quack/gemm_dact_sm90.py, GemmDActSm90):
+    the accumulator S = A B^T is dout; C carries the pre-activation x;
+    D = act'(x) * S (dx) and PostAct = act(x).  The pages' dact visit applies
+    neither alpha nor beta.  A [L,M,K], B [L,N,K], PreAct [L,M,N]."""
+    A = np.asarray(A, dtype=np.float64)
+    B = np.asarray(B, dtype=np.float64)
+    x = np.asarray(PreAct, dtype=np.float64)
+    S = np.matmul(A, np.swapaxes(B, -1, -2))
+    absS = np.matmul(np.abs(A), np.swapaxes(np.abs(B), -1, -2))
+    dx = activations.DFN[act](x) * S
+    post = activations.apply(act, x)
+    # the device evaluates act'(x) in fp32 (error <= 1e-6 for gelu_tanh and silu, exact
+    # for relu and relu_sq): DACT_SLACK / ACC_REL_TOL adds that term to the bound
+    slack = DACT_SLACK.get(act, 0.0) / ACC_REL_TOL
+    out = {"v": dx, "S": S, "bound": (np.abs(activations.DFN[act](x)) + slack) * absS}
+    if d_fmt is not None:
+        out["D"] = round_to(dx, d_fmt)
+    if p_fmt is not None:
+        out["P"] = round_to(post, p_fmt)
+    return out
 
 
 def tolerance(bound, ref_rounded, fmt: Fmt, lipschitz=1.0):

@@ -36,8 +36,10 @@ def oracle_plain(t, w, rows=None):
 FMT_NAME = {"bf16": formats.BF16, "f16": formats.F16, "f32": formats.F32, None: None}
 
 
-def check(got: torch.Tensor, ref, bound, fmt, act="none", what=""):
+def check(got: torch.Tensor, ref, bound, fmt, act="none", what="", x=None):
+    """x: the unrounded pre-activation values (needed for relu_sq's pointwise bound)."""
+    lip = activations.lipschitz(act, x) if act != "none" else 1.0
     ok, worst, idx = og.compare(dec(got) if isinstance(got, torch.Tensor) else got, ref, bound,
-                                fmt, activations.LIPSCHITZ.get(act, 1.0))
+                                fmt, lip)
     assert ok, f"{what}: worst error {worst:.3g} x tolerance at {idx}"
     return worst

@@ -54,7 +54,8 @@ def _check_plain(w, t, out, rows=None):
         got = out["P"].cpu()
         if rows is not None:
             got = got[:, rows]
-        worst.append(check(got, ref["P"], ref["bound"], FMT_NAME[w.p_dtype], w.act, "PostAct"))
+        worst.append(check(got, ref["P"], ref["bound"], FMT_NAME[w.p_dtype], w.act, "PostAct",
+                           x=ref["v"]))
     return worst
 
 
@@ -71,6 +72,7 @@ SMALL = [
     ("gemm_act_4096_bf16_gelu", 256, 256, 512, 1, {"act": "relu", "d_dtype": "f32",
                                                    "p_dtype": "f16"}),
     ("gemm_act_4096_bf16_gelu", 256, 256, 128, 1, {"alpha": 0.0, "beta": -1.5}),
+    ("gemm_act_4096_bf16_gelu", 264, 264, 200, 1, {"act": "relu_sq"}),
     ("gemm_8192_f16_relu", 296, 384, 320, 3, {}),
     ("gemm_8192_f16_relu", 128, 640, 136, 1, {"b_major": "k"}),
     ("gemm_8192_f16_relu", 260, 256, 200, 2, {"d_dtype": "f16", "act": "gelu_tanh"}),

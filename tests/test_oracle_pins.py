@@ -472,3 +472,47 @@ def test_planted_fastdivmod_mistake_is_caught():
     for bad in (OffByOneShift, FloorMultiplier):
         with pytest.raises(AssertionError):
             check_fastdivmod(bad)
+
+
+# ------------------------------------------------- backward epilogue (dact)
+
+@pytest.mark.parametrize("name,fn", [
+    (act.RELU, torch.relu),
+    (act.RELU_SQ, lambda t: torch.relu(t) ** 2),
+    (act.GELU_TANH, lambda t: torch.nn.functional.gelu(t, approximate="tanh")),
+    (act.SILU, torch.nn.functional.silu),
+])
+def test_derivatives_match_torch_autograd(name, fn):
+    x = torch.linspace(-15, 15, 30001, dtype=torch.float64, requires_grad=True)
+    g, = torch.autograd.grad(fn(x).sum(), x)
+    d = act.DFN[name](x.detach().numpy())
+    ok = np.abs(x.detach().numpy()) > 1e-9          # relu' at 0 is a convention
+    assert np.allclose(d[ok], g.numpy()[ok], rtol=1e-12, atol=1e-14)
+    assert np.array_equal(act.relu_sq(x.detach().numpy()), (torch.relu(x) ** 2).detach().numpy())
+
+
+@pytest.mark.parametrize("name", [act.GELU_TANH, act.SILU, act.RELU_SQ])
+def test_derivatives_match_finite_differences(name):
+    x = np.linspace(-8, 8, 1601) + 1e-3
+    h = 1e-6
+    fd = (act.apply(name, x + h) - act.apply(name, x - h)) / (2 * h)
+    assert np.allclose(act.DFN[name](x), fd, rtol=1e-6, atol=1e-8)
+
+
+def test_gemm_dact_pins():
+    rng = np.random.default_rng(8)
+    M, N, K = 6, 5, 6
+    B = rng.integers(-4, 5, size=(1, N, K)).astype(float)
+    x = rng.integers(-3, 4, size=(1, M, N)).astype(float) / 2
+    # identity A: dout = B^T, so dx = act'(x) * B^T exactly
+    r = og.gemm_dact(np.eye(M)[None], B, x, act=act.RELU, d_fmt=fm.F32, p_fmt=fm.F32)
+    assert np.array_equal(r["D"][0], np.where(x[0] > 0, 1.0, 0.0) * B[0].T)
+    assert np.array_equal(r["P"][0], np.maximum(x[0], 0.0))
+    # brute force, relu_sq: dx = 2 relu(x) * sum_k a b
+    A = rng.integers(-4, 5, size=(1, M, K)).astype(float)
+    r = og.gemm_dact(A, B, x, act=act.RELU_SQ, d_fmt=fm.F32, p_fmt=fm.F32)
+    for m in range(M):
+        for n in range(N):
+            s = sum(A[0, m, k] * B[0, n, k] for k in range(K))
+            assert r["D"][0, m, n] == 2 * max(x[0, m, n], 0.0) * s
+            assert r["P"][0, m, n] == max(x[0, m, n], 0.0) ** 2
