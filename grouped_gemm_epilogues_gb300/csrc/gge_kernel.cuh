@@ -7,17 +7,17 @@
 // (GemmActSm90.epi_visit_acc_subtile), rebuilt for the 5th-generation
 // tensor core instead of Hopper warpgroup MMA:
 //
-//   warps 0-3  epilogue: TMEM -> registers (tcgen05.ld), alpha / beta / C /
+//   warps 0-7  epilogue: TMEM -> registers (tcgen05.ld), alpha / beta / C /
 //              activation in fp32, round, store D and PostAct.  Warp w owns
-//              TMEM lanes 32w..32w+31, i.e. tile rows 32w..32w+31.
-//   warp  4    TMEM allocator and MMA issuer (one thread): tcgen05.mma
+//              TMEM lanes 32(w%4)..+31 (tile rows) and every other 32-column chunk.
+//   warp  8    TMEM allocator and MMA issuer (one elected lane): tcgen05.mma
 //              128 x BN x 16 (x32 for 8-bit) from shared memory into a
 //              double-buffered fp32 TMEM accumulator, so the epilogue of
 //              tile i overlaps the main loop of tile i+1 (this replaces the
 //              pages' ping-pong warpgroups).
-//   warp  5    TMA producer: A and B k-tiles into an S-stage shared-memory
+//   warp  9    TMA producer: A and B k-tiles into an S-stage shared-memory
 //              ring (128-byte swizzle), one mbarrier pair per stage.
-//   warps 5-8  (gather-A form) row gather of A with 16-byte cp.async into the
+//   warps 9-12 (gather-A form) row gather of A with 16-byte cp.async into the
 //              same swizzled layout, B still by TMA (GemmSm90.load_AB_gather_A).
 //
 // With CG = 2 a cluster of two CTAs (a CTA pair) computes a 256 x BN tile
@@ -49,9 +49,7 @@ namespace gge {
 
 constexpr int kBM = 128;           // tile rows = TMEM lanes
 constexpr int kRowBytes = 128;     // bytes of K per stage row (one swizzle span)
-constexpr int kEpiWarps = 4;
-constexpr int kMmaWarp = 4;
-constexpr int kLoadWarp = 5;
+
 constexpr int kGatherWarps = 4;
 constexpr int kMaxGroups = 1024;   // varlen-M groups held in shared memory
 constexpr int kCtrlBytes = 256;    // barriers and flags
@@ -63,6 +61,11 @@ struct KernelCfg {
   static constexpr int kABytes = kBM * kRowBytes;
   static constexpr int kBBytes = kBRows * kRowBytes;
   static constexpr int kStageBytes = kABytes + kBBytes;
+  // epilogue warps: two per TMEM lane quadrant (four with the gather producers,
+  // which need the registers), then the MMA warp, then the producer warp(s)
+  static constexpr int kEpiWarps = GATHER ? 4 : 8;
+  static constexpr int kMmaWarp = kEpiWarps;
+  static constexpr int kLoadWarp = kEpiWarps + 1;
   static constexpr int kWarps = GATHER ? kLoadWarp + kGatherWarps : kLoadWarp + 1;
   static constexpr int kThreads = kWarps * 32;
   // two accumulator buffers of BN columns; the allocation is the next power of two
@@ -260,14 +263,54 @@ __device__ __forceinline__ void store8(void* ptr, int dtype, const float* x) {
 
 __device__ __forceinline__ int dtype_bytes(int dt) { return dt == DT_F32 ? 4 : 2; }
 
+// Raw bits of one thread's 32 columns of C (16-bit C uses w[0..3], fp32 C all 8).
+struct CRegs {
+  uint4 w[8];
+};
+
+// Issue the loads of C[row, col0 .. col0+32) (no arithmetic: the values are
+// used one chunk later, so the load latency hides behind that chunk's work).
+__device__ __forceinline__ void load_c_chunk(const Params& p, int32_t row, int32_t col0,
+                                             int32_t batch, CRegs& c) {
+  const int64_t out_batch = (p.num_groups > 0) ? 0 : batch;
+  const int es = dtype_bytes(p.c_dtype);
+  const uint4* base = reinterpret_cast<const uint4*>(
+      static_cast<const char*>(p.c) +
+      (out_batch * p.sbc + static_cast<int64_t>(row) * p.ldc + col0) * es);
+  const int per = 8 / (4 / es);  // 16-byte words of 32 columns: 4 (16-bit) or 8 (fp32)
+  const int cols = 16 / es;      // columns per 16-byte word
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+    if (i < per && col0 + cols * i < p.N) c.w[i] = __ldg(base + i);
+}
+
+// Eight values of the prefetched C chunk (group g of 8 columns) as fp32.
+__device__ __forceinline__ void c_values8(const CRegs& c, int dtype, int g, float* out) {
+  if (dtype == DT_F32) {
+    const uint4 a = c.w[2 * g], b = c.w[2 * g + 1];
+    out[0] = __uint_as_float(a.x); out[1] = __uint_as_float(a.y);
+    out[2] = __uint_as_float(a.z); out[3] = __uint_as_float(a.w);
+    out[4] = __uint_as_float(b.x); out[5] = __uint_as_float(b.y);
+    out[6] = __uint_as_float(b.z); out[7] = __uint_as_float(b.w);
+  } else {
+    const uint32_t w[4] = {c.w[g].x, c.w[g].y, c.w[g].z, c.w[g].w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      float2 f;
+      if (dtype == DT_BF16) f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[i]));
+      else f = __half22float2(*reinterpret_cast<const __half2*>(&w[i]));
+      out[2 * i] = f.x;
+      out[2 * i + 1] = f.y;
+    }
+  }
+}
+
 // Backward epilogue for one thread's 32 columns: x (the pre-activation) comes
 // from C, dout is the accumulator; D = act'(x) * dout, PostAct = act(x).
 __device__ __forceinline__ void epilogue_chunk_dact(const Params& p, const uint32_t (&acc)[32],
-                                                 int32_t row, int32_t col0, int32_t batch) {
+                                                 int32_t row, int32_t col0, int32_t batch,
+                                                 const CRegs& creg) {
   const int64_t out_batch = (p.num_groups > 0) ? 0 : batch;
-  const char* cbase = static_cast<const char*>(p.c) +
-                      (out_batch * p.sbc + static_cast<int64_t>(row) * p.ldc + col0) *
-                          dtype_bytes(p.c_dtype);
   char* dbase = static_cast<char*>(p.d) +
                 (out_batch * p.sbd + static_cast<int64_t>(row) * p.ldd + col0) *
                     dtype_bytes(p.d_dtype);
@@ -279,7 +322,7 @@ __device__ __forceinline__ void epilogue_chunk_dact(const Params& p, const uint3
   for (int g = 0; g < 4; ++g) {  // unrolled: acc stays in registers
     if (col0 + 8 * g >= p.N) continue;
     float x[8], dx[8];
-    load8(cbase + 8 * g * dtype_bytes(p.c_dtype), p.c_dtype, x);
+    c_values8(creg, p.c_dtype, g, x);
 #pragma unroll
     for (int j = 0; j < 8; ++j) dx[j] = dact_apply(p.act, x[j]) * __uint_as_float(acc[8 * g + j]);
     store8(dbase + 8 * g * dtype_bytes(p.d_dtype), p.d_dtype, dx);
@@ -294,9 +337,9 @@ __device__ __forceinline__ void epilogue_chunk_dact(const Params& p, const uint3
 // One thread, one output row, 32 consecutive columns starting at col0.
 __device__ __forceinline__ void epilogue_chunk(const Params& p, const uint32_t (&acc)[32],
                                                int32_t row, int32_t col0, int32_t batch,
-                                               float alpha, float beta) {
+                                               float alpha, float beta, const CRegs& creg) {
   if (p.dact) {
-    epilogue_chunk_dact(p, acc, row, col0, batch);
+    epilogue_chunk_dact(p, acc, row, col0, batch, creg);
     return;
   }
   float v[32];
@@ -304,14 +347,11 @@ __device__ __forceinline__ void epilogue_chunk(const Params& p, const uint32_t (
   for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(acc[j]) * alpha;
   const int64_t out_batch = (p.num_groups > 0) ? 0 : batch;
   if (p.c != nullptr) {
-    const char* cbase = static_cast<const char*>(p.c) +
-                        (out_batch * p.sbc + static_cast<int64_t>(row) * p.ldc + col0) *
-                            dtype_bytes(p.c_dtype);
 #pragma unroll
     for (int g = 0; g < 4; ++g) {
       if (col0 + 8 * g < p.N) {
         float cv[8];
-        load8(cbase + 8 * g * dtype_bytes(p.c_dtype), p.c_dtype, cv);
+        c_values8(creg, p.c_dtype, g, cv);
 #pragma unroll
         for (int j = 0; j < 8; ++j) v[8 * g + j] = fmaf(beta, cv[j], v[8 * g + j]);
       }
@@ -344,26 +384,40 @@ __device__ __forceinline__ void epilogue_chunk(const Params& p, const uint32_t (
 // ------------------------------------------------------------------- roles
 // `unit` / `units`: this CTA's (pair's) index and the number of CTAs (pairs).
 
+// Eight epilogue warps (four in the gather form), two per TMEM lane quadrant
+// (warp w reads lanes 32*(w%4) .. +31); warp w takes the 32-column chunks c
+// with c % 2 == w / 4, so two independent dependency chains per quadrant hide
+// the TMEM-load and memory latencies.  C for the next chunk is loaded one chunk ahead (the
+// first before the accumulator is ready).
 template <int BN, bool GATHER, int CG>
 __device__ __forceinline__ void epilogue_role(const Params& p, const Shared& sh,
                                               uint32_t tmem_base, int32_t num_tiles,
                                               uint32_t rank, int32_t unit, int32_t units) {
   using Cfg = KernelCfg<BN, GATHER, CG>;
+  constexpr int kChunks = BN / 32;
+  constexpr int kStride = Cfg::kEpiWarps / 4;  // warps per TMEM lane quadrant
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int quad = warp & 3, half = warp >> 2;
   const float alpha = p.alpha_dev ? *p.alpha_dev : p.alpha;
   const float beta = p.beta_dev ? *p.beta_dev : p.beta;
   uint32_t acc = 0, acc_phase = 0;
   for (int32_t t = unit; t < num_tiles; t += units) {
     const TileCoord tc = tile_coord<BN, Cfg::kTileM>(t, p, sh);
+    const int32_t row = tc.m_row0 + static_cast<int32_t>(rank) * kBM + quad * 32 + lane;
+    const bool row_ok = row < tc.row_limit;
+    const bool has_c = p.c != nullptr && row_ok;
+    CRegs cnext;
+    if (has_c && tc.n0 + half * 32 < p.N) load_c_chunk(p, row, tc.n0 + half * 32, tc.batch, cnext);
     // all lanes take the same branch: tcgen05.ld below is warp-collective
     const bool ok = wait_phase<CG == 2>(sh.tfull + 8 * acc, acc_phase, p, sh, 3, t);
     if (!__all_sync(0xffffffffu, ok)) break;
     ptx::tc_fence_after();
-    const int32_t row = tc.m_row0 + static_cast<int32_t>(rank) * kBM + warp * 32 + lane;
-    const bool row_ok = row < tc.row_limit;
-    const uint32_t tbase = tmem_base + (static_cast<uint32_t>(warp * 32) << 16) + acc * BN;
+    const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + acc * BN;
 #pragma unroll 1
-    for (int c = 0; c < BN / 32; ++c) {
+    for (int c = half; c < kChunks; c += kStride) {
+      const CRegs ccur = cnext;
+      if (has_c && c + kStride < kChunks && tc.n0 + (c + kStride) * 32 < p.N)
+        load_c_chunk(p, row, tc.n0 + (c + kStride) * 32, tc.batch, cnext);
       uint32_t v[32];
       __syncwarp();  // tcgen05.ld / wait::ld are warp-collective
       if (p.k_tiles > 0) {
@@ -373,7 +427,7 @@ __device__ __forceinline__ void epilogue_role(const Params& p, const Shared& sh,
 #pragma unroll
         for (int j = 0; j < 32; ++j) v[j] = 0u;
       }
-      if (c == BN / 32 - 1) {  // accumulator fully read: hand the buffer back to the MMA warp
+      if (c + kStride >= kChunks) {  // this warp's last chunk: hand its share of the buffer back
         ptx::tc_fence_before();
         __syncwarp();
         if (lane == 0) {
@@ -382,7 +436,7 @@ __device__ __forceinline__ void epilogue_role(const Params& p, const Shared& sh,
         }
       }
       const int32_t col0 = tc.n0 + c * 32;
-      if (row_ok && col0 < p.N) epilogue_chunk(p, v, row, col0, tc.batch, alpha, beta);
+      if (row_ok && col0 < p.N) epilogue_chunk(p, v, row, col0, tc.batch, alpha, beta, ccur);
     }
     if ((p.flags & FLAG_TILE_COUNTS) && p.tile_counts != nullptr && rank == 0 && warp == 0 &&
         lane == 0)
@@ -506,7 +560,7 @@ __device__ __forceinline__ void gather_producer_role(const Params& p, const Shar
                                                      const CUtensorMap* tmB, uint32_t a0,
                                                      uint32_t b0, int32_t num_tiles) {
   using Cfg = KernelCfg<BN, true, 1>;
-  const int gt = threadIdx.x - kLoadWarp * 32;  // 0..127
+  const int gt = threadIdx.x - Cfg::kLoadWarp * 32;  // 0..127
   const int chunk = gt & 7;
   const int rsub = gt >> 3;
   int stage = 0;
@@ -597,17 +651,17 @@ __global__ void __launch_bounds__(KernelCfg<BN, GATHER, CG>::kThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       ptx::mbar_init(sh.tfull + 8 * b, 1);
-      ptx::mbar_init(sh.tempty + 8 * b, kEpiWarps * CG);
+      ptx::mbar_init(sh.tempty + 8 * b, Cfg::kEpiWarps * CG);
     }
     ptx::mbar_init(drain_bar, 1);
     *abort_flag = 0;
     ptx::fence_barrier_init();
   }
-  if (warp == kLoadWarp && lane == 0 && p.k_tiles > 0) {
+  if (warp == Cfg::kLoadWarp && lane == 0 && p.k_tiles > 0) {
     ptx::prefetch_tmap(&tmA);
     ptx::prefetch_tmap(&tmB);
   }
-  if (warp == kMmaWarp) {
+  if (warp == Cfg::kMmaWarp) {
     if (CG == 1) {
       ptx::tmem_alloc(ptx::smem_addr(tmem_slot), Cfg::kTmemCols);
       ptx::tmem_relinquish();
@@ -655,9 +709,9 @@ __global__ void __launch_bounds__(KernelCfg<BN, GATHER, CG>::kThreads, 1)
   const uint32_t tmem_base = *tmem_slot;
   const int32_t num_tiles = (p.num_groups > 0) ? prefix[p.num_groups] : p.num_tiles;
 
-  if (warp < kEpiWarps) {
+  if (warp < Cfg::kEpiWarps) {
     epilogue_role<BN, GATHER, CG>(p, sh, tmem_base, num_tiles, rank, unit, units);
-  } else if (warp == kMmaWarp) {
+  } else if (warp == Cfg::kMmaWarp) {
     if (rank == 0) mma_role<BN, GATHER, CG>(p, sh, a0, b0, tmem_base, num_tiles, unit, units);
   } else if (GATHER) {
     gather_producer_role<BN>(p, sh, &tmB, a0, b0, num_tiles);
@@ -668,7 +722,7 @@ __global__ void __launch_bounds__(KernelCfg<BN, GATHER, CG>::kThreads, 1)
   __syncthreads();
   // Every MMA this CTA issued has finished before TMEM is freed (after an abort
   // nobody else has waited for them); the wait is bounded like all others.
-  if (warp == kMmaWarp && rank == 0) {
+  if (warp == Cfg::kMmaWarp && rank == 0) {
     if (ptx::elect_one()) {
       if (CG == 1) ptx::mma_commit(drain_bar);
       else ptx::mma_commit_pair(drain_bar, 0x1);
@@ -684,7 +738,7 @@ __global__ void __launch_bounds__(KernelCfg<BN, GATHER, CG>::kThreads, 1)
     const uint64_t t0 = ptx::globaltimer();
     while (ptx::globaltimer() - t0 < 200000ull) __nanosleep(1000);
   }
-  if (warp == kMmaWarp) {
+  if (warp == Cfg::kMmaWarp) {
     __syncwarp();  // dealloc is warp-collective
     ptx::tc_fence_after();
     if (CG == 1) ptx::tmem_dealloc(tmem_base, Cfg::kTmemCols);
