@@ -119,8 +119,47 @@ CUtensorMapDataType tmap_type(int es) {
   return es == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_UINT16;
 }
 
+// Encoded tensor maps are cached (keyed by everything that goes into them), so
+// repeated calls on the same buffers skip the driver call.
+struct TmapKey {
+  void* ptr;
+  uint64_t d0, d1, d2, s1, s2;
+  uint32_t b0, b1;
+  int es;
+  bool operator==(const TmapKey& o) const {
+    return ptr == o.ptr && d0 == o.d0 && d1 == o.d1 && d2 == o.d2 && s1 == o.s1 && s2 == o.s2 &&
+           b0 == o.b0 && b1 == o.b1 && es == o.es;
+  }
+};
+
+struct TmapCache {
+  static constexpr int kEntries = 64;
+  std::mutex mu;
+  TmapKey key[kEntries];
+  CUtensorMap map[kEntries];
+  uint64_t used[kEntries] = {};  // 0: empty; else last-use tick
+  uint64_t tick = 0;
+};
+
+TmapCache& tmap_cache() {
+  static TmapCache c;
+  return c;
+}
+
 gge_status encode_3d(CUtensorMap* m, void* ptr, int es, uint64_t d0, uint64_t d1, uint64_t d2,
                      uint64_t s1_bytes, uint64_t s2_bytes, uint32_t b0, uint32_t b1) {
+  const TmapKey k{ptr, d0, d1, d2, s1_bytes, s2_bytes, b0, b1, es};
+  TmapCache& c = tmap_cache();
+  {
+    std::lock_guard<std::mutex> g(c.mu);
+    for (int i = 0; i < TmapCache::kEntries; ++i) {
+      if (c.used[i] != 0 && c.key[i] == k) {
+        c.used[i] = ++c.tick;
+        *m = c.map[i];
+        return GGE_OK;
+      }
+    }
+  }
   EncodeTiledFn fn = encode_fn();
   if (fn == nullptr) return GGE_ERR_CUDA;
   const cuuint64_t dims[3] = {d0, d1, d2};
@@ -130,7 +169,15 @@ gge_status encode_3d(CUtensorMap* m, void* ptr, int es, uint64_t d0, uint64_t d1
   CUresult r = fn(m, tmap_type(es), 3, ptr, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? GGE_OK : GGE_ERR_CUDA;
+  if (r != CUDA_SUCCESS) return GGE_ERR_CUDA;
+  std::lock_guard<std::mutex> g(c.mu);
+  int victim = 0;
+  for (int i = 0; i < TmapCache::kEntries; ++i)
+    if (c.used[i] < c.used[victim]) victim = i;  // an empty slot (0) or the least recent
+  c.key[victim] = k;
+  c.map[victim] = *m;
+  c.used[victim] = ++c.tick;
+  return GGE_OK;
 }
 
 uint64_t batch_stride_bytes(const gge_tensor& t, int es) {
@@ -156,7 +203,33 @@ int variant_threads(int bn, bool gather, int cg) {
   return bn == 128 ? kernel_threads<128, false, 1>() : kernel_threads<256, false, 1>();
 }
 
+int variant_units_uncached(int bn, bool gather, int cg, size_t smem);
+
+// Resident CTAs (pairs) per device for a variant and shared-memory size, cached.
 int variant_units(int bn, bool gather, int cg, size_t smem) {
+  struct Entry { int dev, bn, cg; bool gather; size_t smem; int units; };
+  static std::mutex mu;
+  static Entry cache[64];
+  static int n = 0;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+  {
+    std::lock_guard<std::mutex> g(mu);
+    for (int i = 0; i < n; ++i) {
+      const Entry& e = cache[i];
+      if (e.dev == dev && e.bn == bn && e.cg == cg && e.gather == gather && e.smem == smem)
+        return e.units;
+    }
+  }
+  const int units = variant_units_uncached(bn, gather, cg, smem);
+  if (units > 0) {
+    std::lock_guard<std::mutex> g(mu);
+    if (n < 64) cache[n++] = Entry{dev, bn, cg, gather, smem, units};
+  }
+  return units;
+}
+
+int variant_units_uncached(int bn, bool gather, int cg, size_t smem) {
   if (gather) return bn == 128 ? max_active_units<128, true, 1>(smem) : max_active_units<256, true, 1>(smem);
   if (cg == 2) {
     switch (bn) {
