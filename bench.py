@@ -51,6 +51,24 @@ def dist_env():
     return ws, rank, local
 
 
+def max_over_ranks(value, world_size, device=None):
+    """The slowest rank's value (every rank gets it); no-op for one rank.
+    Works on any process-group backend (a CUDA tensor for NCCL, CPU for gloo)."""
+    if world_size <= 1:
+        return float(value)
+    import torch.distributed as dist
+    t = torch.tensor([float(value)], dtype=torch.float64,
+                     device=device if device is not None else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(flops_per_step, world_size, ms_per_step):
+    """Whole-job TFLOP/s: every rank runs its own problem per step (replicas,
+    weak scaling), timed by the slowest rank."""
+    return world_size * flops_per_step / (ms_per_step * 1e-3) / 1e12
+
+
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -272,15 +290,9 @@ def run_ours(args, w):
     status = binding.gge_read_device_status(dev)
     if status[0] != "GGE_OK":
         raise RuntimeError(f"device status after the timed region: {status}")
-    ms_per_step = ms / args.steps
-    if ws_n > 1:
-        import torch.distributed as dist
-        t = torch.tensor([ms_per_step], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_per_step = float(t.item())
-
+    ms_per_step = max_over_ranks(ms / args.steps, ws_n, dev)
     flops = w.flops
-    value = ws_n * flops / (ms_per_step * 1e-3) / 1e12
+    value = job_throughput(flops, ws_n, ms_per_step)
 
     # end-to-end through the public API with host buffers
     e2e = run_e2e(args, w, base, dev, step)
