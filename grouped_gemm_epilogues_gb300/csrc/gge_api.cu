@@ -25,7 +25,7 @@ namespace {
 constexpr int kTileM = 128;
 constexpr int kRowBytesHost = 128;
 constexpr int kMaxSmemOptin = 232448;  // 227 KiB per block on sm_100 / sm_103
-constexpr int kCtrlBytesHost = 256;
+constexpr int kCtrlBytesHost = 512;
 constexpr int kMaxGroupsHost = 1024;
 constexpr size_t kWorkspaceBytes = 256;
 constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;
@@ -517,6 +517,10 @@ gge_status run(const gge_gemm_args* a, Form form, const int32_t* a_idx, const in
                gge_stream_t stream, bool dact = false) {
   gge_status s = check_workspace(ws, ws_bytes);
   if (s != GGE_OK) return s;
+  // the dynamic tile scheduler keeps its claim counter in the workspace
+  if (a != nullptr && a->config != nullptr && (a->config->flags & FLAG_DYNAMIC_SCHED) &&
+      ws == nullptr)
+    return GGE_ERR_WORKSPACE;
   Plan pl;
   s = make_plan(a, form, a_idx, cu, G, want_act, act_entry, true, &pl, dact);
   if (s != GGE_OK) return s;

@@ -52,7 +52,8 @@ constexpr int kRowBytes = 128;     // bytes of K per stage row (one swizzle span
 
 constexpr int kGatherWarps = 4;
 constexpr int kMaxGroups = 1024;   // varlen-M groups held in shared memory
-constexpr int kCtrlBytes = 256;    // barriers and flags
+constexpr int kCtrlBytes = 512;    // barriers, flags and the tile ring
+constexpr int kSchedDepth = 4;     // tile indices in flight between the fetching warp and the rest
 
 template <int BN, bool GATHER, int CG>
 struct KernelCfg {
@@ -170,6 +171,58 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, const 
   if (CLUSTER ? ptx::mbar_try_wait_cluster(bar, parity) : ptx::mbar_try_wait(bar, parity))
     return true;
   return wait_phase_slow(bar, parity, p.timeout_ns, p.status, sh.abort, where, tile, CLUSTER);
+}
+
+// ------------------------------------------------------------- tile stream
+// Every role walks the same tile sequence.  Static: unit, unit + units, ...
+// Dynamic (quack/dense_gemm_sm90.py's tile_count_semaphore): after its first
+// tile, the fetching warp (the producer; the leader's producer for a pair)
+// claims tiles from an atomic counter in the workspace and hands each index to
+// the other warps (and the peer CTA) through a small shared-memory ring.  An
+// index >= num_tiles ends every role's loop.
+struct TileSched {
+  int32_t unit, units;
+  int32_t* counter;      // workspace claim counter (dynamic)
+  uint32_t full, empty;  // ring barriers (kSchedDepth each)
+  uint32_t ring;         // int32 ring[kSchedDepth]
+  bool dyn;
+};
+
+template <int CG>
+__device__ __forceinline__ int32_t sched_fetch(const TileSched& ts, int i, const Params& p,
+                                               const Shared& sh) {
+  if (!ts.dyn) return ts.unit + i * ts.units;
+  const int slot = i % kSchedDepth;
+  const uint32_t ph = static_cast<uint32_t>(i / kSchedDepth) & 1u;
+  const bool ok = wait_phase<CG == 2>(ts.empty + 8 * slot, ph ^ 1u, p, sh, 7, i);
+  if (!__all_sync(0xffffffffu, ok)) return 0x7fffffff;
+  int32_t t = 0;
+  if ((threadIdx.x & 31) == 0) {
+    t = (i == 0) ? ts.unit : ts.units + atomicAdd(ts.counter, 1);
+    const uint32_t slot_addr = ts.ring + 4 * slot;
+    ptx::st_shared_u32(slot_addr, static_cast<uint32_t>(t));
+    if (CG == 2) ptx::st_shared_cluster_u32(ptx::mapa(slot_addr, 1), static_cast<uint32_t>(t));
+    ptx::mbar_arrive(ts.full + 8 * slot);
+    if (CG == 2) ptx::mbar_arrive_cluster(ptx::mapa(ts.full + 8 * slot, 1));
+  }
+  return __shfl_sync(0xffffffffu, t, 0);
+}
+
+template <int CG>
+__device__ __forceinline__ int32_t sched_next(const TileSched& ts, int i, const Params& p,
+                                              const Shared& sh) {
+  if (!ts.dyn) return ts.unit + i * ts.units;
+  const int slot = i % kSchedDepth;
+  const uint32_t ph = static_cast<uint32_t>(i / kSchedDepth) & 1u;
+  const bool ok = wait_phase<CG == 2>(ts.full + 8 * slot, ph, p, sh, 7, i);
+  if (!__all_sync(0xffffffffu, ok)) return 0x7fffffff;
+  const int32_t t = static_cast<int32_t>(ptx::ld_shared_u32(ts.ring + 4 * slot));
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) {  // this warp is done with the slot (the leader's ring owns it)
+    if (CG == 1) ptx::mbar_arrive(ts.empty + 8 * slot);
+    else ptx::mbar_arrive_cluster(ptx::mapa(ts.empty + 8 * slot, 0));
+  }
+  return t;
 }
 
 // ------------------------------------------------------------- epilogue math
@@ -392,7 +445,7 @@ __device__ __forceinline__ void epilogue_chunk(const Params& p, const uint32_t (
 template <int BN, bool GATHER, int CG>
 __device__ __forceinline__ void epilogue_role(const Params& p, const Shared& sh,
                                               uint32_t tmem_base, int32_t num_tiles,
-                                              uint32_t rank, int32_t unit, int32_t units) {
+                                              uint32_t rank, const TileSched& ts) {
   using Cfg = KernelCfg<BN, GATHER, CG>;
   constexpr int kChunks = BN / 32;
   constexpr int kStride = Cfg::kEpiWarps / 4;  // warps per TMEM lane quadrant
@@ -401,7 +454,9 @@ __device__ __forceinline__ void epilogue_role(const Params& p, const Shared& sh,
   const float alpha = p.alpha_dev ? *p.alpha_dev : p.alpha;
   const float beta = p.beta_dev ? *p.beta_dev : p.beta;
   uint32_t acc = 0, acc_phase = 0;
-  for (int32_t t = unit; t < num_tiles; t += units) {
+  for (int i = 0;; ++i) {
+    const int32_t t = sched_next<CG>(ts, i, p, sh);
+    if (t >= num_tiles) break;
     const TileCoord tc = tile_coord<BN, Cfg::kTileM>(t, p, sh);
     const int32_t row = tc.m_row0 + static_cast<int32_t>(rank) * kBM + quad * 32 + lane;
     const bool row_ok = row < tc.row_limit;
@@ -451,7 +506,7 @@ __device__ __forceinline__ void epilogue_role(const Params& p, const Shared& sh,
 template <int BN, bool GATHER, int CG>
 __device__ __forceinline__ void mma_role(const Params& p, const Shared& sh, uint32_t a0,
                                          uint32_t b0, uint32_t tmem_base, int32_t num_tiles,
-                                         int32_t unit, int32_t units) {
+                                         const TileSched& ts) {
   using Cfg = KernelCfg<BN, GATHER, CG>;
   int stage = 0;
   uint32_t phase = 0, acc = 0, acc_phase = 0;
@@ -459,7 +514,9 @@ __device__ __forceinline__ void mma_role(const Params& p, const Shared& sh, uint
   // N-major: 64-column chunks are (bk rows * 128 B) apart, 8-row K groups 1 KiB apart.
   const uint32_t b_lbo = p.b_mn_major ? static_cast<uint32_t>(p.bk) * kRowBytes : 16u;
   const uint32_t b_kstep = p.b_mn_major ? 16u * kRowBytes : 32u;
-  for (int32_t t = unit; t < num_tiles; t += units) {
+  for (int i = 0;; ++i) {
+    const int32_t t = sched_next<CG>(ts, i, p, sh);
+    if (t >= num_tiles) break;
     bool ok = wait_phase<CG == 2>(sh.tempty + 8 * acc, acc_phase ^ 1u, p, sh, 2, t);
     if (!__all_sync(0xffffffffu, ok)) return;
     ptx::tc_fence_after();
@@ -507,11 +564,14 @@ template <int BN, bool GATHER, int CG>
 __device__ __forceinline__ void tma_producer_role(const Params& p, const Shared& sh,
                                                   const CUtensorMap* tmA, const CUtensorMap* tmB,
                                                   uint32_t a0, uint32_t b0, int32_t num_tiles,
-                                                  uint32_t rank, int32_t unit, int32_t units) {
+                                                  uint32_t rank, const TileSched& ts) {
   using Cfg = KernelCfg<BN, GATHER, CG>;
   int stage = 0;
   uint32_t phase = 0;
-  for (int32_t t = unit; t < num_tiles; t += units) {
+  for (int i = 0;; ++i) {
+    // the producer fetches the tile stream (the peer CTA of a pair reads it)
+    const int32_t t = (rank == 0) ? sched_fetch<CG>(ts, i, p, sh) : sched_next<CG>(ts, i, p, sh);
+    if (t >= num_tiles) break;
     const TileCoord tc = tile_coord<BN, Cfg::kTileM>(t, p, sh);
     const int32_t row0 = tc.m_row0 + static_cast<int32_t>(rank) * kBM;
     const int32_t bn0 = tc.n0 + static_cast<int32_t>(rank) * Cfg::kBRows;
@@ -558,14 +618,18 @@ __device__ __forceinline__ void tma_producer_role(const Params& p, const Shared&
 template <int BN>
 __device__ __forceinline__ void gather_producer_role(const Params& p, const Shared& sh,
                                                      const CUtensorMap* tmB, uint32_t a0,
-                                                     uint32_t b0, int32_t num_tiles) {
+                                                     uint32_t b0, int32_t num_tiles,
+                                                     const TileSched& ts) {
   using Cfg = KernelCfg<BN, true, 1>;
   const int gt = threadIdx.x - Cfg::kLoadWarp * 32;  // 0..127
   const int chunk = gt & 7;
   const int rsub = gt >> 3;
   int stage = 0;
   uint32_t phase = 0;
-  for (int32_t t = blockIdx.x; t < num_tiles; t += gridDim.x) {
+  for (int i = 0;; ++i) {
+    // the first gather warp fetches the tile stream, the other three read it
+    const int32_t t = (gt < 32) ? sched_fetch<1>(ts, i, p, sh) : sched_next<1>(ts, i, p, sh);
+    if (t >= num_tiles) break;
     const TileCoord tc = tile_coord<BN, kBM>(t, p, sh);
     // index rows: plain gather reads a_idx[batch][row], varlen reads a_idx[global row]
     const int64_t idx_base = (p.num_groups > 0) ? 0 : static_cast<int64_t>(tc.batch) * p.M;
@@ -624,7 +688,7 @@ __global__ void __launch_bounds__(KernelCfg<BN, GATHER, CG>::kThreads, 1)
   const uint32_t a0 = base;
   const uint32_t b0 = base + S * Cfg::kABytes;
   uint8_t* ctrl = base_ptr + S * Cfg::kStageBytes;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ctrl + 8 * (2 * S + 5));
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ctrl + 8 * (2 * S + 5 + 2 * kSchedDepth));
   int32_t* abort_flag = reinterpret_cast<int32_t*>(tmem_slot + 1);
   int32_t* prefix = reinterpret_cast<int32_t*>(ctrl + kCtrlBytes);
   int32_t* cu_s = prefix + (kMaxGroups + 1);
@@ -635,14 +699,20 @@ __global__ void __launch_bounds__(KernelCfg<BN, GATHER, CG>::kThreads, 1)
   sh.tfull = sh.empty + 8 * S;
   sh.tempty = sh.tfull + 16;
   const uint32_t drain_bar = sh.tempty + 16;  // MMAs in flight have finished
+  TileSched ts;
+  ts.unit = static_cast<int32_t>(blockIdx.x) / CG;
+  ts.units = static_cast<int32_t>(gridDim.x) / CG;
+  ts.dyn = (p.flags & FLAG_DYNAMIC_SCHED) != 0 && p.status != nullptr;
+  ts.counter = p.status + 4;
+  ts.full = drain_bar + 8;
+  ts.empty = ts.full + 8 * kSchedDepth;
+  ts.ring = ptx::smem_addr(tmem_slot + 2);
   sh.abort = abort_flag;
   sh.prefix = prefix;
   sh.cu = cu_s;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = (CG == 2) ? ptx::cluster_ctarank() : 0u;
-  const int32_t unit = static_cast<int32_t>(blockIdx.x) / CG;
-  const int32_t units = static_cast<int32_t>(gridDim.x) / CG;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -654,6 +724,14 @@ __global__ void __launch_bounds__(KernelCfg<BN, GATHER, CG>::kThreads, 1)
       ptx::mbar_init(sh.tempty + 8 * b, Cfg::kEpiWarps * CG);
     }
     ptx::mbar_init(drain_bar, 1);
+    // ring slot consumers: the MMA warp, every epilogue warp (both CTAs of a pair),
+    // the peer's producer (pair) or the other gather warps
+    const uint32_t consumers = (CG == 2) ? 2 * Cfg::kEpiWarps + 2
+                                         : Cfg::kEpiWarps + 1 + (GATHER ? kGatherWarps - 1 : 0);
+    for (int i = 0; i < kSchedDepth; ++i) {
+      ptx::mbar_init(ts.full + 8 * i, 1);
+      ptx::mbar_init(ts.empty + 8 * i, consumers);
+    }
     *abort_flag = 0;
     ptx::fence_barrier_init();
   }
@@ -710,13 +788,13 @@ __global__ void __launch_bounds__(KernelCfg<BN, GATHER, CG>::kThreads, 1)
   const int32_t num_tiles = (p.num_groups > 0) ? prefix[p.num_groups] : p.num_tiles;
 
   if (warp < Cfg::kEpiWarps) {
-    epilogue_role<BN, GATHER, CG>(p, sh, tmem_base, num_tiles, rank, unit, units);
+    epilogue_role<BN, GATHER, CG>(p, sh, tmem_base, num_tiles, rank, ts);
   } else if (warp == Cfg::kMmaWarp) {
-    if (rank == 0) mma_role<BN, GATHER, CG>(p, sh, a0, b0, tmem_base, num_tiles, unit, units);
+    if (rank == 0) mma_role<BN, GATHER, CG>(p, sh, a0, b0, tmem_base, num_tiles, ts);
   } else if (GATHER) {
-    gather_producer_role<BN>(p, sh, &tmB, a0, b0, num_tiles);
+    gather_producer_role<BN>(p, sh, &tmB, a0, b0, num_tiles, ts);
   } else {
-    tma_producer_role<BN, GATHER, CG>(p, sh, &tmA, &tmB, a0, b0, num_tiles, rank, unit, units);
+    tma_producer_role<BN, GATHER, CG>(p, sh, &tmA, &tmB, a0, b0, num_tiles, rank, ts);
   }
 
   __syncthreads();
@@ -737,6 +815,14 @@ __global__ void __launch_bounds__(KernelCfg<BN, GATHER, CG>::kThreads, 1)
     // let copies and MMAs that were in flight land before the memory goes away
     const uint64_t t0 = ptx::globaltimer();
     while (ptx::globaltimer() - t0 < 200000ull) __nanosleep(1000);
+  }
+  // the last CTA (pair) to finish clears the claim counter for the next call
+  if (ts.dyn && rank == 0 && threadIdx.x == 0) {
+    __threadfence();
+    if (atomicAdd(p.status + 5, 1) == ts.units - 1) {
+      atomicExch(p.status + 4, 0);
+      atomicExch(p.status + 5, 0);
+    }
   }
   if (warp == Cfg::kMmaWarp) {
     __syncwarp();  // dealloc is warp-collective

@@ -21,6 +21,7 @@ enum : int32_t {
 enum : int32_t {
   FLAG_TILE_COUNTS = 1,        // epilogue counts visits per tile into tile_counts
   FLAG_TEST_DROP_ACC_FULL = 2, // the MMA warp never signals "accumulator full" (timeout test)
+  FLAG_DYNAMIC_SCHED = 4,      // tiles claimed from an atomic counter instead of a fixed stride
 };
 
 struct Params {
@@ -68,7 +69,8 @@ struct Params {
   int32_t b_mn_major;  // B staged N-major (16-bit operands only)
 
   // control
-  int32_t* status;       // workspace: [0] code, [1] where, [2] tile, [3] detail
+  int32_t* status;       // workspace: [0] code, [1] where, [2] tile, [3] detail,
+                         //            [4] tile claim counter, [5] finished CTAs (pairs)
   int32_t* tile_counts;  // debug visit counters
   int32_t flags;
   uint64_t timeout_ns;

@@ -91,7 +91,10 @@ typedef struct gge_config {
   int32_t flags;          /* bit 0: count tile visits into tile_counts;
                              bit 1: test hook -- the MMA warp never signals a
                              finished accumulator, so the epilogue's bounded wait
-                             runs out and the call reports GGE_ERR_TIMEOUT        */
+                             runs out and the call reports GGE_ERR_TIMEOUT;
+                             bit 2: dynamic tile scheduler -- after its first
+                             tile each CTA (pair) claims the next one from a
+                             counter in the workspace (needs a workspace)        */
   int32_t cta_group;      /* 0 = auto; 1 = one CTA per 128-row tile; 2 = a CTA pair
                              per 256-row tile (tcgen05 cta_group::2, 256-column
                              tiles, not with gather-A)                             */
@@ -131,7 +134,8 @@ typedef struct gge_gemm_args {
   const gge_config* config;  /* NULL = defaults */
 } gge_gemm_args;
 
-/* Bytes of device workspace a call needs (status words); the workspace is
+/* Bytes of device workspace a call needs (status words and the dynamic
+ * scheduler's counters); the workspace is
  * caller-owned, at least 16-byte aligned, and must be zeroed once before first
  * use.  It is reusable across calls on the same stream. */
 size_t gge_workspace_size(const gge_gemm_args* args, int32_t num_groups);
