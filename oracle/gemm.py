@@ -160,3 +160,42 @@ def compare(got, ref_rounded, bound, fmt: Fmt, lipschitz=1.0):
     worst = float(ratio.max()) if ratio.size else 0.0
     idx = np.unravel_index(int(np.argmax(ratio)), ratio.shape) if ratio.size else None
     return bool(nan_ok and inf_ok and worst <= 1.0), worst, idx
+
+
+def gemm_varlen_k(A, B, cu_seqlens_k, C=None, *, alpha=1.0, beta=1.0,
+                  act=activations.NONE, d_fmt: Fmt = None, p_fmt: Fmt = None):
+    """Varlen-K grouped GEMM (the ``varlen_k`` paths of ``GemmSm90.kernel``:
+    B is offset by ``cu_seqlens_k[batch_idx]`` along K, ``len_k`` is
+    ``cu_seqlens_k[batch_idx + 1] - cu_seqlens_k[batch_idx]``, and a group
+    with ``k_tile_cnt == 0`` keeps a zero accumulator).
+
+    A [M, total_K]; B [N, total_K]; cu_seqlens_k [G+1] non-decreasing with
+    cu[0] >= 0 and cu[G] <= total_K; C [G, M, N] or None.  Group g contracts
+    the K columns cu[g] .. cu[g+1]-1 of A and B:
+    ``v[g] = alpha * A[:, K_g] @ B[:, K_g]^T + beta * C[g]``.  Columns outside
+    every group take part in no product.  Returns arrays shaped [G, M, N].
+    """
+    A = np.asarray(A, dtype=np.float64)
+    B = np.asarray(B, dtype=np.float64)
+    cu = np.asarray(cu_seqlens_k, dtype=np.int64)
+    G = len(cu) - 1
+    M, N = A.shape[0], B.shape[0]
+    parts = []
+    for g in range(G):
+        lo, hi = int(cu[g]), int(cu[g + 1])
+        Cg = None if C is None else np.asarray(C, np.float64)[g:g + 1]
+        # an empty range gives the zero accumulator (matmul over no terms)
+        parts.append(gemm(A[None, :, lo:hi], B[None, :, lo:hi], Cg, alpha=alpha, beta=beta,
+                          act=act, d_fmt=d_fmt, p_fmt=p_fmt))
+    if not parts:
+        return {"v": np.zeros((0, M, N)), "bound": np.zeros((0, M, N))}
+    return {k: np.concatenate([r[k] for r in parts]) for k in parts[0]}
+
+
+def gemm_gather_k(A_src, a_idx, B, cu_seqlens_k, C=None, **kw):
+    """Varlen-K GEMM whose A is gathered along K (``gather_A`` with
+    ``varlen_k`` in ``GemmSm90.kernel``: the index tensor is offset by
+    ``cu_seqlens_k[batch_idx]``): column k of the effective A is column
+    ``a_idx[k]`` of ``A_src`` [M, K_src]; B is read at the position k itself."""
+    A_eff = np.asarray(A_src, dtype=np.float64)[:, np.asarray(a_idx, dtype=np.int64)]
+    return gemm_varlen_k(A_eff, B, cu_seqlens_k, C, **kw)

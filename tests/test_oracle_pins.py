@@ -516,3 +516,140 @@ def test_gemm_dact_pins():
             s = sum(A[0, m, k] * B[0, n, k] for k in range(K))
             assert r["D"][0, m, n] == 2 * max(x[0, m, n], 0.0) * s
             assert r["P"][0, m, n] == max(x[0, m, n], 0.0) ** 2
+
+
+# ------------------------------------------------------- varlen-K, gather-K
+# Each check takes the varlen-K oracle (and the gather-K one) so that the
+# planted-mistake test below can run the same checks on a broken copy.
+
+def check_varlen_k_brute_force(vk):
+    rng = random.Random(9)
+    M, N, total = 3, 4, 14
+    cu = [0, 3, 3, 9, 12, 12]            # groups 1 and 4 empty, columns 12, 13 unused
+    G = len(cu) - 1
+    A = [[rng.randint(-3, 3) for _ in range(total)] for _ in range(M)]
+    B = [[rng.randint(-3, 3) for _ in range(total)] for _ in range(N)]
+    Cm = [[[rng.randint(-5, 5) for _ in range(N)] for _ in range(M)] for _ in range(G)]
+    r = vk(np.array(A, float), np.array(B, float), cu, np.array(Cm, float), alpha=2.0,
+           beta=0.5, act=act.RELU, d_fmt=fm.F32, p_fmt=fm.F32)
+    assert r["D"].shape == (G, M, N)
+    for g in range(G):
+        for m in range(M):
+            for n in range(N):
+                s = 0
+                sa = 0
+                for k in range(cu[g], cu[g + 1]):
+                    s += A[m][k] * B[n][k]
+                    sa += abs(A[m][k] * B[n][k])
+                v = 2.0 * s + 0.5 * Cm[g][m][n]
+                assert r["D"][g, m, n] == v
+                assert r["P"][g, m, n] == max(v, 0.0)
+                assert r["bound"][g, m, n] == 2.0 * sa
+
+
+def check_varlen_k_partition_sum(vk):
+    # groups that tile [0, total_K) add up to the full product (alpha 1, no C)
+    rng = np.random.default_rng(10)
+    A = rng.integers(-4, 5, size=(5, 40)).astype(float)
+    B = rng.integers(-4, 5, size=(6, 40)).astype(float)
+    cu = [0, 7, 7, 8, 25, 40]
+    r = vk(A, B, cu, d_fmt=fm.F32)
+    assert np.array_equal(r["D"].sum(axis=0), A @ B.T)
+
+
+def check_varlen_k_empty_group(vk):
+    # an empty group keeps the zero accumulator: D = beta * C, PostAct = act(beta * C)
+    rng = np.random.default_rng(11)
+    C = rng.integers(-4, 5, size=(3, 2, 3)).astype(float)
+    A = rng.integers(-4, 5, size=(2, 8)).astype(float)
+    B = rng.integers(-4, 5, size=(3, 8)).astype(float)
+    r = vk(A, B, [0, 4, 4, 8], C, alpha=3.0, beta=-0.5, act=act.RELU, d_fmt=fm.F32, p_fmt=fm.F32)
+    assert np.array_equal(r["D"][1], -0.5 * C[1])
+    assert np.array_equal(r["P"][1], np.maximum(-0.5 * C[1], 0.0))
+    assert np.array_equal(r["bound"][1], np.zeros((2, 3)))
+
+
+def check_varlen_k_equal_groups_are_batched(vk):
+    # equal group lengths: the batched GEMM of the K-blocks, each with its own C
+    rng = np.random.default_rng(12)
+    G, M, N, k = 4, 3, 5, 6
+    A = rng.standard_normal((M, G * k))
+    B = rng.standard_normal((N, G * k))
+    C = rng.standard_normal((G, M, N))
+    r = vk(A, B, np.arange(G + 1) * k, C, alpha=0.75, beta=1.5, d_fmt=fm.F32)
+    Ab = np.stack([A[:, g * k:(g + 1) * k] for g in range(G)])
+    Bb = np.stack([B[:, g * k:(g + 1) * k] for g in range(G)])
+    rb = og.gemm(Ab, Bb, C, alpha=0.75, beta=1.5, d_fmt=fm.F32)
+    assert np.array_equal(r["v"], rb["v"])
+
+
+VARLEN_K_PINS = [check_varlen_k_brute_force, check_varlen_k_partition_sum,
+                 check_varlen_k_empty_group, check_varlen_k_equal_groups_are_batched]
+
+
+@pytest.mark.parametrize("pin", VARLEN_K_PINS, ids=lambda f: f.__name__)
+def test_varlen_k_pins(pin):
+    pin(og.gemm_varlen_k)
+
+
+def check_gather_k(gk):
+    rng = np.random.default_rng(13)
+    M, N, Ksrc = 3, 4, 20
+    src = rng.integers(-5, 6, size=(M, Ksrc)).astype(float)
+    cu = [0, 5, 5, 11]
+    total = 11
+    B = rng.integers(-5, 6, size=(N, total)).astype(float)
+    # identity indices: the plain varlen-K GEMM over the first columns
+    r_id = gk(src, np.arange(total), B, cu, d_fmt=fm.F32)
+    assert np.array_equal(r_id["D"], og.gemm_varlen_k(src[:, :total], B, cu, d_fmt=fm.F32)["D"])
+    # brute force with a random index (repeats allowed)
+    idx = rng.integers(0, Ksrc, size=total)
+    r = gk(src, idx, B, cu, d_fmt=fm.F32)
+    for g in range(3):
+        for m in range(M):
+            for n in range(N):
+                s = sum(src[m, idx[k]] * B[n, k] for k in range(cu[g], cu[g + 1]))
+                assert r["D"][g, m, n] == s
+
+
+def test_gather_k_pins():
+    check_gather_k(og.gemm_gather_k)
+
+
+def test_planted_varlen_k_mistakes_are_caught():
+    def range_one_past(A, B, cu, C=None, **kw):        # contracts one column too many
+        cu = np.asarray(cu).copy()
+        hi = np.minimum(cu[1:] + 1, np.asarray(A).shape[1])
+        out = [og.gemm_varlen_k(A, B, [cu[g], hi[g]], None if C is None else C[g:g + 1], **kw)
+               for g in range(len(cu) - 1)]
+        return {k: np.concatenate([o[k] for o in out]) for k in out[0]}
+
+    def from_zero(A, B, cu, C=None, **kw):              # every group starts at column 0
+        out = [og.gemm_varlen_k(A, B, [0, cu[g + 1]], None if C is None else C[g:g + 1], **kw)
+               for g in range(len(cu) - 1)]
+        return {k: np.concatenate([o[k] for o in out]) for k in out[0]}
+
+    def first_c(A, B, cu, C=None, **kw):                # C of group 0 for every group
+        if C is not None:
+            C = np.broadcast_to(np.asarray(C)[:1], np.shape(C))
+        return og.gemm_varlen_k(A, B, cu, C, **kw)
+
+    def b_storage_transposed(A, B, cu, C=None, **kw):   # reads B's [N, K] storage as [K, N]
+        B = np.asarray(B, float)
+        return og.gemm_varlen_k(A, B.reshape(B.shape[1], B.shape[0]).T, cu, C, **kw)
+
+    for bad in (range_one_past, from_zero, first_c, b_storage_transposed):
+        failures = 0
+        for pin in VARLEN_K_PINS:
+            try:
+                pin(bad)
+            except (AssertionError, ValueError, IndexError):
+                failures += 1
+        assert failures > 0, bad.__name__
+
+    def gathers_b_too(A_src, a_idx, B, cu, C=None, **kw):
+        return og.gemm_varlen_k(np.asarray(A_src)[:, a_idx], np.asarray(B)[:, np.minimum(
+            a_idx, np.shape(B)[1] - 1)], cu, C, **kw)
+
+    with pytest.raises(AssertionError):
+        check_gather_k(gathers_b_too)
