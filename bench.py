@@ -161,6 +161,27 @@ class ClockSampler:
 
 # ---------------------------------------------------------- our arm (GPU)
 
+def _out_shape(w):
+    if w.k_groups:
+        return (w.k_groups, w.M, w.N)
+    return (w.M, w.N) if w.groups else (w.L, w.M, w.N)
+
+
+def _to_device(v, dev):
+    """A device copy with the same strides (a transposed view stays transposed)."""
+    d = torch.empty_strided(v.shape, v.stride(), dtype=v.dtype, device=dev)
+    d.copy_(v)
+    return d
+
+
+def _rotate_rows(a, i):
+    """Distinct values of the same distribution: roll the storage rows of A
+    (the rows of its contiguous form; a transposed view is rolled underneath)."""
+    t = a if a.is_contiguous() else a.transpose(-1, -2)
+    r = torch.roll(t.view(torch.uint8), shifts=i, dims=-2).view(t.dtype).contiguous()
+    return r if a.is_contiguous() else r.transpose(-1, -2)
+
+
 def _device_sets(w, dev, n_sets):
     sets = []
     base = wl.make(w)
@@ -168,12 +189,10 @@ def _device_sets(w, dev, n_sets):
         s = {}
         for k, v in base.items():
             if isinstance(v, torch.Tensor):
-                s[k] = v.to(dev) if i == 0 else v.to(dev).clone()
-        if i > 0:  # distinct values per set (same distribution): rotate A's rows
-            a = s["A"]
-            s["A"] = torch.roll(a.view(torch.uint8), shifts=i, dims=-2).view(a.dtype).contiguous()
-        L = 1 if w.groups else w.L
-        shape = (w.M, w.N) if w.groups else (L, w.M, w.N)
+                s[k] = _to_device(v, dev)
+        if i > 0:
+            s["A"] = _rotate_rows(s["A"], i)
+        shape = _out_shape(w)
         if w.d_dtype:
             s["D"] = torch.empty(shape, dtype=wl.DT[w.d_dtype], device=dev)
         if w.p_dtype:
@@ -188,7 +207,11 @@ def _set_bytes(s):
 
 def _step_fn(w, binding):
     def step(s):
-        if w.groups:
+        if w.k_groups:
+            binding.gge_gemm_varlen_k(s["A"], s["B"], s["cu_seqlens_k"], D=s.get("D"),
+                                      PostAct=s.get("P"), act=w.act, C=s.get("C"),
+                                      alpha=w.alpha, beta=w.beta)
+        elif w.groups:
             if w.gather_rows:
                 binding.gge_gemm_gather_a(s["A"], s["B"], s["a_idx"], s["cu_seqlens_m"],
                                           D=s.get("D"), PostAct=s.get("P"), act=w.act,
@@ -316,6 +339,8 @@ def run_ours(args, w):
         "data": "synthetic",
         "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "L": w.L,
                    "groups": w.groups, "gather_rows": w.gather_rows, "act": w.act,
+                   **({"k_groups": w.k_groups, "a_major": w.a_major, "b_major": w.b_major}
+                      if w.k_groups else {}),
                    "with_c": w.with_c, "alpha": w.alpha, "beta": w.beta,
                    "accumulate": "f32", "out": w.p_dtype or w.d_dtype,
                    "l2": (f"{n_sets} rotating input sets of {per_set / 2**20:.0f} MiB (> L2)"
@@ -340,10 +365,14 @@ def run_ours(args, w):
 def run_e2e(args, w, base, dev, step):
     """Same metric through the public API with host (pinned) buffers: every
     step copies its inputs host->device and its outputs device->host."""
-    host_in = {k: v.pin_memory() for k, v in base.items() if isinstance(v, torch.Tensor)}
-    dsets = {k: torch.empty_like(v, device=dev) for k, v in host_in.items()}
-    L = 1 if w.groups else w.L
-    shape = (w.M, w.N) if w.groups else (L, w.M, w.N)
+    host_in = {}
+    for k, v in base.items():
+        if isinstance(v, torch.Tensor):   # pinned, in the same layout as the device copy
+            h = torch.empty_strided(v.shape, v.stride(), dtype=v.dtype, pin_memory=True)
+            host_in[k] = h.copy_(v)
+    dsets = {k: torch.empty_strided(v.shape, v.stride(), dtype=v.dtype, device=dev)
+             for k, v in host_in.items()}
+    shape = _out_shape(w)
     outs = {}
     if w.d_dtype:
         outs["D"] = torch.empty(shape, dtype=wl.DT[w.d_dtype], device=dev)
@@ -397,6 +426,13 @@ def _oracle_rows(w, base, rows):
 
     fm = {"bf16": formats.BF16, "f16": formats.F16, "f32": formats.F32, None: None}
     kw = dict(alpha=w.alpha, beta=w.beta, act=w.act, d_fmt=fm[w.d_dtype], p_fmt=fm[w.p_dtype])
+    if w.k_groups:
+        # output rows m of every group: A's rows against all of B
+        C = base["C"][:, rows] if "C" in base else None
+        og.gemm_varlen_k(dec(base["A"][rows]), dec(base["B"]), base["cu_seqlens_k"].numpy(),
+                         None if C is None else dec(C), **kw)
+        cu = base["cu_seqlens_k"].numpy()
+        return 2.0 * len(rows) * w.N * float(cu[-1] - cu[0])
     if w.groups:
         cu = base["cu_seqlens_m"].numpy()
         A = base["A"][base["a_idx"][rows].long()] if w.gather_rows else base["A"][rows]

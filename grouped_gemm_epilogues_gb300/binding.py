@@ -57,11 +57,14 @@ class GgePlanInfo(ctypes.Structure):
 # every function include/gge.h declares, with its ctypes signature
 _SIGNATURES = {
     "gge_workspace_size": (ctypes.c_size_t, [ctypes.POINTER(GgeGemmArgs), c_i32]),
+    "gge_workspace_size_varlen_k": (ctypes.c_size_t, [ctypes.POINTER(GgeGemmArgs), c_i32]),
     "gge_gemm": (c_i32, [ctypes.POINTER(GgeGemmArgs), ctypes.c_void_p, ctypes.c_size_t,
                          ctypes.c_void_p]),
     "gge_gemm_act": (c_i32, [ctypes.POINTER(GgeGemmArgs), ctypes.c_void_p, ctypes.c_size_t,
                              ctypes.c_void_p]),
     "gge_gemm_varlen_m": (c_i32, [ctypes.POINTER(GgeGemmArgs), ctypes.c_void_p, c_i32,
+                                  ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
+    "gge_gemm_varlen_k": (c_i32, [ctypes.POINTER(GgeGemmArgs), ctypes.c_void_p, c_i32,
                                   ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
     "gge_gemm_gather_a": (c_i32, [ctypes.POINTER(GgeGemmArgs), ctypes.c_void_p, ctypes.c_void_p,
                                   c_i32, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
@@ -131,14 +134,18 @@ def view(t: torch.Tensor, kind: str) -> GgeTensor:
 _workspaces = {}
 
 
-def workspace(device=None) -> torch.Tensor:
-    """The per-device status workspace (zeroed once)."""
+def workspace(device=None, nbytes: int = 256) -> torch.Tensor:
+    """The per-device workspace (zeroed when made), at least ``nbytes`` long.
+    Growing it keeps the status words (the first 256 bytes) of the old one."""
     dev = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
     if dev.index is None:
         dev = torch.device("cuda", torch.cuda.current_device())
     ws = _workspaces.get(dev.index)
-    if ws is None:
-        ws = torch.zeros(256, dtype=torch.uint8, device=dev)
+    if ws is None or ws.numel() < nbytes:
+        new = torch.zeros(max(nbytes, 256), dtype=torch.uint8, device=dev)
+        if ws is not None:
+            new[:256].copy_(ws[:256])
+        ws = new
         _workspaces[dev.index] = ws
     return ws
 
@@ -240,6 +247,22 @@ def gge_gemm_varlen_m(A, B, cu_seqlens_m, D=None, PostAct=None, act="none", C=No
            "gge_gemm_varlen_m")
 
 
+def gge_gemm_varlen_k(A, B, cu_seqlens_k, D=None, PostAct=None, act="none", C=None, alpha=1.0,
+                      beta=1.0, config=None):
+    """Varlen-K grouped GEMM: A (M, total_K), B (N, total_K), cu_seqlens_k int32 (G+1,) on
+    device; C / D / PostAct (G, M, N).  Group g contracts K columns cu[g] .. cu[g+1]-1."""
+    lib = load()
+    out = D if D is not None else PostAct
+    args = make_args(A, B, C=C, D=D, PostAct=PostAct, alpha=alpha, beta=beta, act=act,
+                     config=config)
+    G = cu_seqlens_k.numel() - 1
+    need = lib.gge_workspace_size_varlen_k(ctypes.byref(args), G)
+    ws = workspace(out.device, need)
+    _check(lib.gge_gemm_varlen_k(ctypes.byref(args), ctypes.c_void_p(cu_seqlens_k.data_ptr()), G,
+                                 ctypes.c_void_p(ws.data_ptr()), ws.numel(), _stream(out)),
+           "gge_gemm_varlen_k")
+
+
 def gge_gemm_gather_a(A_src, B, a_idx, cu_seqlens_m=None, D=None, PostAct=None, act="none",
                       C=None, alpha=1.0, beta=1.0, config=None):
     """Gather-A GEMM: effective A row r = A_src[a_idx[r]]; varlen-M when cu_seqlens_m is given."""
@@ -264,11 +287,16 @@ def gge_read_device_status(device=None):
     return STATUS.get(code, str(code)), detail[0], detail[1]
 
 
+FORM = {"default": 0, "gather_a": 1, "varlen_k": 2}
+
+
 def gge_plan(A, B, C=None, D=None, PostAct=None, act="none", num_groups=0, gather=False,
-             config=None):
+             config=None, form=None):
+    """The launch plan; form: 'default' (plain / varlen-M), 'gather_a' or 'varlen_k'."""
     lib = load()
     args = make_args(A, B, C=C, D=D, PostAct=PostAct, act=act, config=config)
     info = GgePlanInfo()
-    code = lib.gge_plan(ctypes.byref(args), num_groups, 1 if gather else 0, ctypes.byref(info))
+    f = FORM[form] if form is not None else (1 if gather else 0)
+    code = lib.gge_plan(ctypes.byref(args), num_groups, f, ctypes.byref(info))
     _check(code, "gge_plan")
     return {k: getattr(info, k) for k, _ in GgePlanInfo._fields_}

@@ -28,6 +28,9 @@ constexpr int kMaxSmemOptin = 232448;  // 227 KiB per block on sm_100 / sm_103
 constexpr int kCtrlBytesHost = 512;
 constexpr int kMaxGroupsHost = 1024;
 constexpr size_t kWorkspaceBytes = 256;
+constexpr size_t kMapSlotsHost = 8;      // varlen-K tensor-map slots per CTA (kernel kMapSlots)
+constexpr size_t kMapSlotBytesHost = 256;
+constexpr int kMaxStages = 8;            // never more stages than map slots
 constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;
 constexpr int64_t kMaxExtent = (int64_t(1) << 31) - 1;
 
@@ -101,7 +104,7 @@ gge_status check_mn(const gge_tensor* t, int64_t M, int64_t N, int64_t L, bool i
   return GGE_OK;
 }
 
-enum class Form { Plain, Varlen, Gather, GatherVarlen };
+enum class Form { Plain, Varlen, Gather, GatherVarlen, VarlenK };
 
 struct Plan {
   Params p;
@@ -185,6 +188,14 @@ uint64_t batch_stride_bytes(const gge_tensor& t, int es) {
   // a single batch: any legal stride (never stepped over)
   uint64_t s = static_cast<uint64_t>(std::max<int64_t>(t.rows, 1)) *
                static_cast<uint64_t>(std::max<int64_t>(t.stride_row, 1)) * es;
+  return (s + 15) / 16 * 16;
+}
+
+// The same for an M- / N-major view, whose K columns are stride_col apart.
+uint64_t mn_batch_stride_bytes(const gge_tensor& t, int es) {
+  if (t.batch > 1) return static_cast<uint64_t>(t.stride_batch) * es;
+  uint64_t s = static_cast<uint64_t>(std::max<int64_t>(t.cols, 1)) *
+               static_cast<uint64_t>(std::max<int64_t>(t.stride_col, 1)) * es;
   return (s + 15) / 16 * 16;
 }
 
@@ -290,6 +301,7 @@ gge_status make_plan(const gge_gemm_args* a, Form form, const int32_t* a_idx,
   const gge_config* cfg = a->config;
   const bool varlen = (form == Form::Varlen || form == Form::GatherVarlen);
   const bool gather = (form == Form::Gather || form == Form::GatherVarlen);
+  const bool vk = (form == Form::VarlenK);
   pl.gather = gather;
 
   if (a->act < GGE_ACT_NONE || a->act > GGE_ACT_RELU_SQ) return GGE_ERR_INVALID_ARG;
@@ -326,13 +338,22 @@ gge_status make_plan(const gge_gemm_args* a, Form form, const int32_t* a_idx,
   if (a->C) { s = check_mn(a->C, M, N, L, false); if (s != GGE_OK) return s; }
   if (N % 8 != 0) return GGE_ERR_UNSUPPORTED;
 
-  // A: K-major; B: [N, K, Lb] K- or N-major.  With K == 0 neither is read.
-  bool b_mn = false;
+  // A: [M, K, La] K-major, or M-major (16-bit, TMA-loaded A only); B: [N, K, Lb]
+  // K- or N-major (16-bit).  With K == 0 neither is read.
+  bool a_mn = false, b_mn = false;
   if (a->B.rows != N || a->B.cols != K) return GGE_ERR_INVALID_ARG;
   if (K > 0) {
-    if (K > 1 && a->A.stride_col != 1) return GGE_ERR_UNSUPPORTED;
-    if (a->A.rows > 1 && a->A.stride_row < K) return GGE_ERR_INVALID_ARG;
-    if ((a->A.stride_row * es) % 16 != 0) return GGE_ERR_ALIGNMENT;
+    if (K == 1 || a->A.stride_col == 1) {
+      if (a->A.rows > 1 && a->A.stride_row < K) return GGE_ERR_INVALID_ARG;
+      if ((a->A.stride_row * es) % 16 != 0) return GGE_ERR_ALIGNMENT;
+    } else if (a->A.stride_row == 1 && !gather) {
+      a_mn = true;
+      if (f8) return GGE_ERR_UNSUPPORTED;  // 8-bit operands must be K-major
+      if (a->A.stride_col < a->A.rows) return GGE_ERR_INVALID_ARG;
+      if ((a->A.stride_col * es) % 16 != 0) return GGE_ERR_ALIGNMENT;
+    } else {
+      return GGE_ERR_UNSUPPORTED;
+    }
     if (a->A.batch > 1 && (a->A.stride_batch * es) % 16 != 0) return GGE_ERR_ALIGNMENT;
     if (K == 1 || a->B.stride_col == 1) {
       if (N > 1 && a->B.stride_row < K) return GGE_ERR_INVALID_ARG;
@@ -348,7 +369,13 @@ gge_status make_plan(const gge_gemm_args* a, Form form, const int32_t* a_idx,
     if (a->B.batch > 1 && (a->B.stride_batch * es) % 16 != 0) return GGE_ERR_ALIGNMENT;
   }
 
-  if (varlen) {
+  if (vk) {
+    // A [M, total_K], B [N, total_K], outputs [G, M, N]
+    if (cu == nullptr) return GGE_ERR_INVALID_ARG;
+    if (G < 1 || G > kMaxGroupsHost) return GGE_ERR_UNSUPPORTED;
+    if (L != G) return GGE_ERR_INVALID_ARG;
+    if (a->A.rows != M || a->A.batch != 1 || a->B.batch != 1) return GGE_ERR_INVALID_ARG;
+  } else if (varlen) {
     if (cu == nullptr) return GGE_ERR_INVALID_ARG;
     if (G < 1 || G > kMaxGroupsHost) return GGE_ERR_UNSUPPORTED;
     if (L != 1) return GGE_ERR_INVALID_ARG;
@@ -376,7 +403,7 @@ gge_status make_plan(const gge_gemm_args* a, Form form, const int32_t* a_idx,
     if (bn == 0) {
       bn = 256;
       // narrower tiles even out the last wave; N-major B stages 64-column chunks
-      if (!b_mn && !varlen) {
+      if (!b_mn && !varlen && !vk) {
         int64_t units = cfg && cfg->num_ctas > 0 ? cfg->num_ctas / 2 : 0;
         if (units <= 0 && encode) {
           const size_t smem256 = 1024 + kCtrlBytesHost +
@@ -394,10 +421,10 @@ gge_status make_plan(const gge_gemm_args* a, Form form, const int32_t* a_idx,
   const int tile_m = kTileM * cg;
   const int bk = kRowBytesHost / es;
   const int stage_bytes = (kTileM + bn / cg) * kRowBytesHost;
-  const int varlen_bytes = varlen ? 2 * 4 * (kMaxGroupsHost + 1) : 0;
+  const int varlen_bytes = (varlen || vk) ? 2 * 4 * (kMaxGroupsHost + 1) : 0;
   const int fixed = 1024 + kCtrlBytesHost + varlen_bytes;
   int stages = (kMaxSmemOptin - fixed) / stage_bytes;
-  stages = std::min(stages, 8);
+  stages = std::min(stages, kMaxStages);
   if (cfg && cfg->stages > 0) stages = std::min(stages, cfg->stages);
   if (stages < 2) return GGE_ERR_UNSUPPORTED;
 
@@ -424,6 +451,12 @@ gge_status make_plan(const gge_gemm_args* a, Form form, const int32_t* a_idx,
                                     static_cast<int32_t>(L), band);
     band = p.sched.band;
     p.num_tiles = static_cast<int32_t>(num_tiles);
+    if (vk) {
+      p.k_groups = G;
+      p.cu_seqlens_k = cu;
+      // a K-major operand's TMA boxes start on 16-byte boundaries of its rows
+      p.k_align = (a_mn && b_mn) ? 1 : 16 / es;
+    }
   } else {
     p.num_groups = G;
     p.cu_seqlens = cu;
@@ -456,12 +489,14 @@ gge_status make_plan(const gge_gemm_args* a, Form form, const int32_t* a_idx,
   p.beta = a->beta;
   p.alpha_dev = a->alpha_dev;
   p.beta_dev = a->beta_dev;
-  // instruction descriptor: f32 accumulator, operand formats, B major, N >> 3, M >> 4
+  // instruction descriptor: f32 accumulator, operand formats, A / B major, N >> 3, M >> 4
   const uint32_t afmt = f8 ? (adt == GGE_E5M2 ? 1u : 0u) : (adt == GGE_BF16 ? 1u : 0u);
   const uint32_t bfmt = f8 ? (bdt == GGE_E5M2 ? 1u : 0u) : (bdt == GGE_BF16 ? 1u : 0u);
-  p.idesc = (1u << 4) | (afmt << 7) | (bfmt << 10) | ((b_mn ? 1u : 0u) << 16) |
+  p.idesc = (1u << 4) | (afmt << 7) | (bfmt << 10) | ((a_mn ? 1u : 0u) << 15) |
+            ((b_mn ? 1u : 0u) << 16) |
             ((static_cast<uint32_t>(bn) >> 3) << 17) | ((static_cast<uint32_t>(tile_m) >> 4) << 24);
   p.f8 = f8 ? 1 : 0;
+  p.a_mn_major = a_mn ? 1 : 0;
   p.b_mn_major = b_mn ? 1 : 0;
   p.flags = cfg ? cfg->flags : 0;
   p.tile_counts = cfg ? cfg->tile_counts : nullptr;
@@ -483,10 +518,15 @@ gge_status make_plan(const gge_gemm_args* a, Form form, const int32_t* a_idx,
 
   // tensor maps (never read when K == 0)
   if (K > 0) {
-    if (!gather) {
+    if (!gather && !a_mn) {
       s = encode_3d(&pl.tmA, a->A.ptr, es, K, a->A.rows, a->A.batch,
                     static_cast<uint64_t>(a->A.stride_row) * es, batch_stride_bytes(a->A, es), bk,
                     kTileM);
+      if (s != GGE_OK) return s;
+    } else if (!gather) {
+      s = encode_3d(&pl.tmA, a->A.ptr, es, a->A.rows, K, a->A.batch,
+                    static_cast<uint64_t>(a->A.stride_col) * es, mn_batch_stride_bytes(a->A, es),
+                    64, bk);
       if (s != GGE_OK) return s;
     }
     if (!b_mn) {
@@ -494,15 +534,18 @@ gge_status make_plan(const gge_gemm_args* a, Form form, const int32_t* a_idx,
                     static_cast<uint64_t>(a->B.stride_row) * es, batch_stride_bytes(a->B, es), bk,
                     bn / cg);
     } else {
-      gge_tensor t = a->B;
-      uint64_t sb = t.batch > 1 ? static_cast<uint64_t>(t.stride_batch) * es
-                                : (static_cast<uint64_t>(K) * t.stride_col * es + 15) / 16 * 16;
       s = encode_3d(&pl.tmB, a->B.ptr, es, N, K, a->B.batch,
-                    static_cast<uint64_t>(a->B.stride_col) * es, sb, 64, bk);
+                    static_cast<uint64_t>(a->B.stride_col) * es, mn_batch_stride_bytes(a->B, es),
+                    64, bk);
     }
     if (s != GGE_OK) return s;
   }
   return GGE_OK;
+}
+
+size_t varlen_k_workspace(const Plan& pl) {
+  return kWorkspaceBytes + static_cast<size_t>(std::max(pl.shape.grid, 0)) * kMapSlotsHost *
+                               kMapSlotBytesHost;
 }
 
 gge_status check_workspace(void* ws, size_t bytes) {
@@ -525,6 +568,12 @@ gge_status run(const gge_gemm_args* a, Form form, const int32_t* a_idx, const in
   s = make_plan(a, form, a_idx, cu, G, want_act, act_entry, true, &pl, dact);
   if (s != GGE_OK) return s;
   if (pl.empty) return GGE_OK;
+  if (form == Form::VarlenK) {
+    // per-CTA tensor-map slots follow the status words
+    if (ws == nullptr || ws_bytes < varlen_k_workspace(pl)) return GGE_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return GGE_ERR_ALIGNMENT;
+    pl.p.kmaps = static_cast<uint8_t*>(ws) + kWorkspaceBytes;
+  }
   pl.p.status = static_cast<int32_t*>(ws);
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   const cudaError_t e = variant_launch(pl, st);
@@ -569,6 +618,21 @@ gge_status gge_gemm_gather_a(const gge_gemm_args* args, const int32_t* a_idx,
                              size_t ws_bytes, gge_stream_t stream) {
   const Form f = cu_seqlens_m ? Form::GatherVarlen : Form::Gather;
   return gge::run(args, f, a_idx, cu_seqlens_m, num_groups, true, false, ws, ws_bytes, stream);
+}
+
+size_t gge_workspace_size_varlen_k(const gge_gemm_args* args, int32_t num_groups) {
+  static const int32_t dummy = 0;
+  gge::Plan pl;
+  if (gge::make_plan(args, Form::VarlenK, nullptr, &dummy, num_groups, true, false, true, &pl) !=
+      GGE_OK)
+    return 0;
+  return gge::varlen_k_workspace(pl);
+}
+
+gge_status gge_gemm_varlen_k(const gge_gemm_args* args, const int32_t* cu_seqlens_k,
+                             int32_t num_groups, void* ws, size_t ws_bytes, gge_stream_t stream) {
+  return gge::run(args, Form::VarlenK, nullptr, cu_seqlens_k, num_groups, true, false, ws,
+                  ws_bytes, stream);
 }
 
 gge_status gge_read_device_status(void* ws, gge_stream_t stream, int32_t* detail) {
@@ -627,12 +691,17 @@ int32_t gge_schedule_map(int32_t tiles_m, int32_t tiles_n, int32_t batches, int3
   return s.num_tiles;
 }
 
-gge_status gge_plan(const gge_gemm_args* args, int32_t num_groups, int32_t gather,
+gge_status gge_plan(const gge_gemm_args* args, int32_t num_groups, int32_t form,
                     gge_plan_info* out) {
   if (out == nullptr) return GGE_ERR_INVALID_ARG;
+  if (form != GGE_FORM_DEFAULT && form != GGE_FORM_GATHER_A && form != GGE_FORM_VARLEN_K)
+    return GGE_ERR_INVALID_ARG;
   gge::Plan pl;
-  const Form f = gather ? (num_groups > 0 ? Form::GatherVarlen : Form::Gather)
-                        : (num_groups > 0 ? Form::Varlen : Form::Plain);
+  const bool gather = form == GGE_FORM_GATHER_A;
+  const Form f = form == GGE_FORM_VARLEN_K
+                     ? Form::VarlenK
+                     : gather ? (num_groups > 0 ? Form::GatherVarlen : Form::Gather)
+                              : (num_groups > 0 ? Form::Varlen : Form::Plain);
   // a dummy non-null index pointer lets the shape checks run
   static const int32_t dummy = 0;
   const gge_status s = gge::make_plan(args, f, gather ? &dummy : nullptr,
@@ -643,7 +712,7 @@ gge_status gge_plan(const gge_gemm_args* args, int32_t num_groups, int32_t gathe
   out->tile_n = pl.bn;
   out->tile_k = pl.p.bk;
   out->stages = pl.p.stages;
-  out->num_tiles = pl.p.num_groups > 0 ? -1 : pl.p.num_tiles;
+  out->num_tiles = pl.p.num_groups > 0 ? -1 : pl.p.num_tiles;  // varlen-M: formed on the device
   out->grid = pl.shape.grid;
   out->threads = pl.shape.threads;
   out->smem_bytes = static_cast<int32_t>(pl.shape.smem);

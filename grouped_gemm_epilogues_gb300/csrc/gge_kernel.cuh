@@ -51,9 +51,16 @@ constexpr int kBM = 128;           // tile rows = TMEM lanes
 constexpr int kRowBytes = 128;     // bytes of K per stage row (one swizzle span)
 
 constexpr int kGatherWarps = 4;
-constexpr int kMaxGroups = 1024;   // varlen-M groups held in shared memory
-constexpr int kCtrlBytes = 512;    // barriers, flags and the tile ring
+constexpr int kMaxGroups = 1024;   // varlen groups held in shared memory
+constexpr int kCtrlBytes = 512;    // barriers, flags and the tile ring (bytes 0..255),
+                                   // the varlen-K tensor-map scratch (256..511)
+constexpr int kMapScratch = 256;
 constexpr int kSchedDepth = 4;     // tile indices in flight between the fetching warp and the rest
+constexpr int kMapSlots = 8;       // varlen-K: tensor-map copies per CTA (>= pipeline stages)
+constexpr int kMapSlotBytes = 256; // one A and one B tensor map
+// barriers for up to 8 stages, the TMEM slot, the abort flag and the tile ring
+static_assert(8 * (2 * 8 + 5 + 2 * kSchedDepth) + 8 + 4 * kSchedDepth <= kMapScratch,
+              "control block overlaps the tensor-map scratch");
 
 template <int BN, bool GATHER, int CG>
 struct KernelCfg {
@@ -93,13 +100,14 @@ struct TileCoord {
   int32_t n0;
   int32_t batch;      // batch index (plain) or group index (varlen)
   int32_t a_batch;    // third TMA coordinate of A
+  int32_t b_batch;    // third TMA coordinate of B
 };
 
 struct Shared {
   uint32_t full, empty, tfull, tempty;  // barrier array bases (shared addresses)
   volatile int32_t* abort;
-  const int32_t* prefix;  // varlen: tile prefix [G+1]
-  const int32_t* cu;      // varlen: cu_seqlens copy [G+1]
+  const int32_t* prefix;  // varlen-M: tile prefix [G+1]; varlen-K: group K ends [G]
+  const int32_t* cu;      // varlen-M: cu_seqlens copy [G+1]; varlen-K: group K starts [G]
 };
 
 template <int BN, int TILE_M>
@@ -118,6 +126,7 @@ __device__ __forceinline__ TileCoord tile_coord(int32_t t, const Params& p, cons
     tc.n0 = nb * BN;
     tc.batch = lo;
     tc.a_batch = 0;
+    tc.b_batch = lo;
   } else {
     int32_t l, mb, nb;
     p.sched.map(t, l, mb, nb);
@@ -125,9 +134,22 @@ __device__ __forceinline__ TileCoord tile_coord(int32_t t, const Params& p, cons
     tc.row_limit = p.M;
     tc.n0 = nb * BN;
     tc.batch = l;
-    tc.a_batch = l;
+    // varlen-K operands are single [rows, total_K] matrices
+    tc.a_batch = p.k_groups > 0 ? 0 : l;
+    tc.b_batch = tc.a_batch;
   }
   return tc;
+}
+
+// The K columns a tile contracts: [k0, k_end) in k-tiles of bk.
+struct KRange {
+  int32_t k0, k_end, tiles;
+};
+
+__device__ __forceinline__ KRange k_range(const Params& p, const Shared& sh, int32_t batch) {
+  if (p.k_groups == 0) return KRange{0, p.K, p.k_tiles};
+  const int32_t lo = sh.cu[batch], hi = sh.prefix[batch];
+  return KRange{lo, hi, (hi - lo + p.bk - 1) / p.bk};
 }
 
 __device__ __forceinline__ void record_status(const Params& p, int32_t code, int32_t where,
@@ -458,6 +480,8 @@ __device__ __forceinline__ void epilogue_role(const Params& p, const Shared& sh,
     const int32_t t = sched_next<CG>(ts, i, p, sh);
     if (t >= num_tiles) break;
     const TileCoord tc = tile_coord<BN, Cfg::kTileM>(t, p, sh);
+    // a tile with no k-tiles (K == 0, or an empty varlen-K group) keeps a zero accumulator
+    const bool has_acc = k_range(p, sh, tc.batch).tiles > 0;
     const int32_t row = tc.m_row0 + static_cast<int32_t>(rank) * kBM + quad * 32 + lane;
     const bool row_ok = row < tc.row_limit;
     const bool has_c = p.c != nullptr && row_ok;
@@ -475,7 +499,7 @@ __device__ __forceinline__ void epilogue_role(const Params& p, const Shared& sh,
         load_c_chunk(p, row, tc.n0 + (c + kStride) * 32, tc.batch, cnext);
       uint32_t v[32];
       __syncwarp();  // tcgen05.ld / wait::ld are warp-collective
-      if (p.k_tiles > 0) {
+      if (has_acc) {
         ptx::tmem_ld_32x32b_x32(tbase + c * 32, v);
         ptx::tmem_wait_ld(v);
       } else {
@@ -510,8 +534,11 @@ __device__ __forceinline__ void mma_role(const Params& p, const Shared& sh, uint
   using Cfg = KernelCfg<BN, GATHER, CG>;
   int stage = 0;
   uint32_t phase = 0, acc = 0, acc_phase = 0;
-  // B descriptor strides: K-major rows are 128 B apart, 8-row swizzle atoms 1 KiB apart;
-  // N-major: 64-column chunks are (bk rows * 128 B) apart, 8-row K groups 1 KiB apart.
+  // Descriptor strides: K-major rows are 128 B apart, 8-row swizzle atoms 1 KiB apart;
+  // M- / N-major: 64-element chunks are (bk rows * 128 B) apart, 8-row K groups 1 KiB
+  // apart, and one MMA's 16 K rows span 2 KiB.
+  const uint32_t a_lbo = p.a_mn_major ? static_cast<uint32_t>(p.bk) * kRowBytes : 16u;
+  const uint32_t a_kstep = p.a_mn_major ? 16u * kRowBytes : 32u;
   const uint32_t b_lbo = p.b_mn_major ? static_cast<uint32_t>(p.bk) * kRowBytes : 16u;
   const uint32_t b_kstep = p.b_mn_major ? 16u * kRowBytes : 32u;
   for (int i = 0;; ++i) {
@@ -521,7 +548,10 @@ __device__ __forceinline__ void mma_role(const Params& p, const Shared& sh, uint
     if (!__all_sync(0xffffffffu, ok)) return;
     ptx::tc_fence_after();
     const uint32_t d_tmem = tmem_base + acc * BN;
-    for (int kt = 0; kt < p.k_tiles; ++kt) {
+    const int32_t k_tiles =
+        p.k_groups > 0 ? k_range(p, sh, tile_coord<BN, Cfg::kTileM>(t, p, sh).batch).tiles
+                       : p.k_tiles;
+    for (int kt = 0; kt < k_tiles; ++kt) {
       ok = wait_phase<CG == 2>(sh.full + 8 * stage, phase, p, sh, 1, t);
       if (!__all_sync(0xffffffffu, ok)) return;
       ptx::tc_fence_after();
@@ -531,7 +561,7 @@ __device__ __forceinline__ void mma_role(const Params& p, const Shared& sh, uint
       if (ptx::elect_one()) {
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {  // 4 MMAs of 32 bytes of K each
-          const uint64_t adesc = smem_desc(a_addr + kk * 32, 16u, 1024u);
+          const uint64_t adesc = smem_desc(a_addr + kk * a_kstep, a_lbo, 1024u);
           const uint64_t bdesc = smem_desc(b_addr + kk * b_kstep, b_lbo, 1024u);
           const uint32_t accumulate = (kt > 0 || kk > 0) ? 1u : 0u;
           if (CG == 1) {
@@ -559,53 +589,100 @@ __device__ __forceinline__ void mma_role(const Params& p, const Shared& sh, uint
   }
 }
 
+// One TMA box into this CTA's shared memory; a pair's copies signal the leader's barrier.
+template <int CG>
+__device__ __forceinline__ void tma_load(uint32_t dst, const CUtensorMap* m, uint32_t bar,
+                                         int32_t x, int32_t y, int32_t z) {
+  if (CG == 1) ptx::tma_load_3d(dst, m, bar, x, y, z);
+  else ptx::tma_load_3d_pair(dst, m, bar, x, y, z);
+}
+
+// Varlen-K: write a copy of the A and B tensor maps whose K extent ends at the
+// group's last column into this CTA's map slot `slot` (the pages'
+// update_tensormap_shape), so that the group's last k-tile reads zeros past
+// its end instead of the next group's columns.  Warp-collective.
+__device__ __forceinline__ const uint8_t* publish_kmaps(const Params& p, const CUtensorMap* tmA,
+                                                        const CUtensorMap* tmB, uint32_t scratch,
+                                                        int slot, int32_t k_end) {
+  const int lane = threadIdx.x & 31;
+  uint8_t* dst = p.kmaps + (static_cast<int64_t>(blockIdx.x) * kMapSlots + slot) * kMapSlotBytes;
+  ptx::st_shared_u32(scratch + 4 * lane, reinterpret_cast<const uint32_t*>(tmA)[lane]);
+  ptx::st_shared_u32(scratch + 128 + 4 * lane, reinterpret_cast<const uint32_t*>(tmB)[lane]);
+  __syncwarp();
+  if (lane == 0) {
+    // K is dimension 0 of a K-major map and dimension 1 of an M- / N-major one
+    if (p.a_mn_major) ptx::tmap_set_global_dim<1>(scratch, k_end);
+    else ptx::tmap_set_global_dim<0>(scratch, k_end);
+    if (p.b_mn_major) ptx::tmap_set_global_dim<1>(scratch + 128, k_end);
+    else ptx::tmap_set_global_dim<0>(scratch + 128, k_end);
+  }
+  __syncwarp();
+  ptx::tmap_publish(dst, scratch);
+  ptx::tmap_publish(dst + 128, scratch + 128);
+  ptx::tmap_acquire(dst);
+  ptx::tmap_acquire(dst + 128);
+  return dst;
+}
+
 // The whole producer warp walks the loop; one elected lane issues the copies.
 template <int BN, bool GATHER, int CG>
 __device__ __forceinline__ void tma_producer_role(const Params& p, const Shared& sh,
                                                   const CUtensorMap* tmA, const CUtensorMap* tmB,
-                                                  uint32_t a0, uint32_t b0, int32_t num_tiles,
-                                                  uint32_t rank, const TileSched& ts) {
+                                                  uint32_t a0, uint32_t b0, uint32_t map_scratch,
+                                                  int32_t num_tiles, uint32_t rank,
+                                                  const TileSched& ts) {
   using Cfg = KernelCfg<BN, GATHER, CG>;
   int stage = 0;
   uint32_t phase = 0;
+  // varlen-K: the group whose maps are in use, and the slot they occupy
+  int32_t map_group = -1;
+  int map_slot = kMapSlots - 1;
+  const CUtensorMap* mA = tmA;
+  const CUtensorMap* mB = tmB;
   for (int i = 0;; ++i) {
     // the producer fetches the tile stream (the peer CTA of a pair reads it)
     const int32_t t = (rank == 0) ? sched_fetch<CG>(ts, i, p, sh) : sched_next<CG>(ts, i, p, sh);
     if (t >= num_tiles) break;
     const TileCoord tc = tile_coord<BN, Cfg::kTileM>(t, p, sh);
+    const KRange kr = k_range(p, sh, tc.batch);
     const int32_t row0 = tc.m_row0 + static_cast<int32_t>(rank) * kBM;
     const int32_t bn0 = tc.n0 + static_cast<int32_t>(rank) * Cfg::kBRows;
-    for (int kt = 0; kt < p.k_tiles; ++kt) {
+    for (int kt = 0; kt < kr.tiles; ++kt) {
       const bool ok = wait_phase<CG == 2>(sh.empty + 8 * stage, phase ^ 1u, p, sh, 0, t);
       if (!__all_sync(0xffffffffu, ok)) return;
+      if (p.k_groups > 0 && kt == 0 && tc.batch != map_group) {
+        // A slot is rewritten kMapSlots (>= stages) group changes after its last
+        // use; every group issues at least one k-tile, and the wait above has
+        // seen the k-tile `stages` back consumed, so no copy still reads it.
+        map_slot = (map_slot + 1 == kMapSlots) ? 0 : map_slot + 1;
+        const uint8_t* m = publish_kmaps(p, tmA, tmB, map_scratch, map_slot, kr.k_end);
+        mA = reinterpret_cast<const CUtensorMap*>(m);
+        mB = reinterpret_cast<const CUtensorMap*>(m + 128);
+        map_group = tc.batch;
+      }
       const uint32_t full = sh.full + 8 * stage;
-      const int32_t k0 = kt * p.bk;
+      const int32_t k0 = kr.k0 + kt * p.bk;
       const uint32_t adst = a0 + stage * Cfg::kABytes;
       const uint32_t bdst = b0 + stage * Cfg::kBBytes;
       if (ptx::elect_one()) {
-        if (CG == 1) {
-          ptx::mbar_arrive_expect_tx(full, Cfg::kStageBytes);
-          ptx::tma_load_3d(adst, tmA, full, k0, row0, tc.a_batch);
-          if (!p.b_mn_major) {
-            ptx::tma_load_3d(bdst, tmB, full, k0, bn0, tc.batch);
-          } else {
-#pragma unroll
-            for (int j = 0; j < Cfg::kBRows / 64; ++j)
-              ptx::tma_load_3d(bdst + j * (64 * kRowBytes), tmB, full, bn0 + 64 * j, k0, tc.batch);
-          }
+        // both CTAs' bytes of a pair complete on the leader's barrier, which the leader arms
+        if (CG == 1) ptx::mbar_arrive_expect_tx(full, Cfg::kStageBytes);
+        else if (rank == 0) ptx::mbar_arrive_expect_tx(full, 2 * Cfg::kStageBytes);
+        const uint32_t bar = (CG == 1) ? full : ptx::mapa(full, 0);
+        // K-major operands: one box of (bk columns, rows); M- / N-major: 64-wide boxes of bk rows
+        if (!p.a_mn_major) {
+          tma_load<CG>(adst, mA, bar, k0, row0, tc.a_batch);
         } else {
-          // both CTAs' bytes complete on the leader's barrier, which the leader arms
-          if (rank == 0) ptx::mbar_arrive_expect_tx(full, 2 * Cfg::kStageBytes);
-          const uint32_t lead = ptx::mapa(full, 0);
-          ptx::tma_load_3d_pair(adst, tmA, lead, k0, row0, tc.a_batch);
-          if (!p.b_mn_major) {
-            ptx::tma_load_3d_pair(bdst, tmB, lead, k0, bn0, tc.batch);
-          } else {
 #pragma unroll
-            for (int j = 0; j < Cfg::kBRows / 64; ++j)
-              ptx::tma_load_3d_pair(bdst + j * (64 * kRowBytes), tmB, lead, bn0 + 64 * j, k0,
-                                    tc.batch);
-          }
+          for (int j = 0; j < kBM / 64; ++j)
+            tma_load<CG>(adst + j * (64 * kRowBytes), mA, bar, row0 + 64 * j, k0, tc.a_batch);
+        }
+        if (!p.b_mn_major) {
+          tma_load<CG>(bdst, mB, bar, k0, bn0, tc.b_batch);
+        } else {
+#pragma unroll
+          for (int j = 0; j < Cfg::kBRows / 64; ++j)
+            tma_load<CG>(bdst + j * (64 * kRowBytes), mB, bar, bn0 + 64 * j, k0, tc.b_batch);
         }
       }
       __syncwarp();
@@ -652,7 +729,7 @@ __device__ __forceinline__ void gather_producer_role(const Params& p, const Shar
       const uint32_t full = sh.full + 8 * stage;
       if (gt < 32 && ptx::elect_one()) {  // one lane of the first gather warp: B by TMA
         ptx::mbar_arrive_expect_tx(full, Cfg::kBBytes);
-        ptx::tma_load_3d(b0 + stage * Cfg::kBBytes, tmB, full, kt * p.bk, tc.n0, tc.batch);
+        ptx::tma_load_3d(b0 + stage * Cfg::kBBytes, tmB, full, kt * p.bk, tc.n0, tc.b_batch);
       }
       const int32_t kbyte = kt * kRowBytes + chunk * 16;
       const uint32_t kvalid = (kbyte < p.k_bytes) ? 16u : 0u;
@@ -781,6 +858,21 @@ __global__ void __launch_bounds__(KernelCfg<BN, GATHER, CG>::kThreads, 1)
       cu_s[G] = min(max(__ldg(p.cu_seqlens + G), 0), p.M);
     }
   }
+  // varlen-K: each group's K columns [start, end).  A group that breaks the
+  // rules (out of [0, total_K], decreasing, or a start that is not a whole
+  // 16 bytes into a K-major row) is recorded and contracts nothing.
+  if (p.k_groups > 0 && warp == 0) {
+    for (int g = lane; g < p.k_groups; g += 32) {
+      int32_t lo = __ldg(p.cu_seqlens_k + g), hi = __ldg(p.cu_seqlens_k + g + 1);
+      const bool bad = lo < 0 || hi < lo || hi > p.K || (hi > lo && lo % p.k_align != 0);
+      if (bad) {
+        record_status(p, DEV_INDEX_RANGE, 8, g);
+        lo = hi = 0;
+      }
+      cu_s[g] = lo;
+      prefix[g] = hi;
+    }
+  }
   __syncthreads();
   if (CG == 2) ptx::cluster_sync();  // the peer's barriers exist before anyone signals them
   ptx::tc_fence_after();
@@ -794,7 +886,8 @@ __global__ void __launch_bounds__(KernelCfg<BN, GATHER, CG>::kThreads, 1)
   } else if (GATHER) {
     gather_producer_role<BN>(p, sh, &tmB, a0, b0, num_tiles, ts);
   } else {
-    tma_producer_role<BN, GATHER, CG>(p, sh, &tmA, &tmB, a0, b0, num_tiles, rank, ts);
+    tma_producer_role<BN, GATHER, CG>(p, sh, &tmA, &tmB, a0, b0,
+                                      ptx::smem_addr(ctrl + kMapScratch), num_tiles, rank, ts);
   }
 
   __syncthreads();

@@ -42,6 +42,13 @@ struct Params {
   int32_t num_groups;  // 0: plain batched problem
   const int32_t* cu_seqlens;
 
+  // varlen-K: batch l of the schedule is group l, which contracts the K
+  // columns cu_seqlens_k[l] .. cu_seqlens_k[l+1]-1 of A [M, total_K] and B [N, total_K]
+  int32_t k_groups;            // 0: every batch contracts all K columns
+  const int32_t* cu_seqlens_k;
+  int32_t k_align;             // group starts must be multiples of this (K-major operands)
+  uint8_t* kmaps;              // workspace: per CTA, kMapSlots pairs of 128-byte A / B tensor maps
+
   // gather-A
   const int32_t* a_idx;   // [L][M] (plain) or [total_M] (varlen)
   const uint8_t* a_src;   // source matrix base
@@ -66,6 +73,7 @@ struct Params {
   // MMA
   uint32_t idesc;
   int32_t f8;          // operands are 8-bit (kind::f8f6f4)
+  int32_t a_mn_major;  // A staged M-major (16-bit operands only)
   int32_t b_mn_major;  // B staged N-major (16-bit operands only)
 
   // control

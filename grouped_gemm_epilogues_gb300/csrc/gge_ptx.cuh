@@ -309,5 +309,28 @@ __device__ __forceinline__ void mma_commit_pair(uint32_t bar, uint16_t cta_mask)
       : "memory");
 }
 
+// ---- tensor-map edits (per-group K extents)
+
+// Set the global extent of dimension ORD of a tensor map held in shared memory.
+template <int ORD>
+__device__ __forceinline__ void tmap_set_global_dim(uint32_t smem_map, int32_t extent) {
+  asm volatile("tensormap.replace.tile.global_dim.shared::cta.b1024.b32 [%0], %1, %2;"
+               :: "r"(smem_map), "n"(ORD), "r"(extent) : "memory");
+}
+
+// Warp-collective: copy a 128-byte tensor map from shared to global memory and
+// make it visible to the tensor-map proxy (release at GPU scope).
+__device__ __forceinline__ void tmap_publish(void* gmem_map, uint32_t smem_map) {
+  asm volatile(
+      "tensormap.cp_fenceproxy.global.shared::cta.tensormap::generic.release.gpu.sync.aligned "
+      "[%0], [%1], 128;" :: "l"(gmem_map), "r"(smem_map) : "memory");
+}
+
+// Acquire a tensor map published above before a TMA copy uses it.
+__device__ __forceinline__ void tmap_acquire(const void* gmem_map) {
+  asm volatile("fence.proxy.tensormap::generic.acquire.gpu [%0], 128;" :: "l"(gmem_map)
+               : "memory");
+}
+
 }  // namespace ptx
 }  // namespace gge

@@ -15,7 +15,10 @@ Recipe (fixed here so that every run sees the same bytes):
     (Exponential(1) draws), with 4 groups given weight 0 so that some groups
     are empty;
   * gather indices: ``floor(torch.rand * rows_src)`` as int32 (with
-    replacement, duplicates allowed).
+    replacement, duplicates allowed);
+  * varlen-K group lengths: the same split of total_K columns (tokens) over
+    the groups as the varlen-M rows, optionally rounded to a multiple of
+    ``k_multiple`` (the remainder goes to the last non-empty group).
 
 Storage layouts (torch shapes; the GEMM's logical operands are A[m,k,l],
 B[n,k,l], C/D/PostAct[m,n,l]):
@@ -23,6 +26,12 @@ B[n,k,l], C/D/PostAct[m,n,l]):
   B kmajor (L, N, K) contiguous                -> K-major
   B nmajor (L, K, N) contiguous, used as .transpose(1, 2) -> N-major
   C/D/P    (L, M, N) contiguous                -> N-major
+  varlen-K (weight-gradient form, per group g: D[g] = A[:, K_g] B[:, K_g]^T):
+  A mmajor (total_K, M) contiguous, used as .t() -> [M, total_K] M-major
+  A kmajor (M, total_K) contiguous                -> K-major
+  B nmajor (total_K, N) contiguous, used as .t() -> [N, total_K] N-major
+  B kmajor (N, total_K) contiguous                -> K-major
+  C/D/P    (G, M, N) contiguous
 """
 
 from dataclasses import dataclass, field
@@ -56,6 +65,9 @@ class Workload:
     groups: int = 0                    # varlen-M groups (0: plain)
     empty_groups: int = 0
     gather_rows: int = 0               # gather-A source rows (0: no gather)
+    k_groups: int = 0                  # varlen-K groups (K = total_K); 0: not varlen-K
+    a_major: str = "k"                 # varlen-K: "k" or "m"
+    k_multiple: int = 1                # varlen-K: group lengths rounded to this
     seed: int = 0
     description: str = field(default="", compare=False)
 
@@ -89,6 +101,11 @@ WORKLOADS = {
     "gemm_8192_fp8": Workload(
         "gemm_8192_fp8", 8192, 8192, 8192, ab_dtype="e4m3", b_dtype="e5m2", dist="normal",
         alpha=1.0 / 64, d_dtype="bf16", description="8192^3 e4m3 x e5m2, alpha 1/64, bf16 D"),
+    "varlen_k_g64_k32768_wgrad": Workload(
+        "varlen_k_g64_k32768_wgrad", 1536, 4096, 32768, k_groups=64, empty_groups=4,
+        a_major="m", b_major="n", d_dtype="bf16",
+        description="varlen-K weight gradient of the varlen-M layer: 64 groups over 32768 "
+                    "tokens, D[g] = dY_g^T X_g (1536 x 4096), A M-major, B N-major, bf16"),
     "gemm_act_8192_bf16_gelu": Workload(
         "gemm_act_8192_bf16_gelu", 8192, 8192, 8192, act="gelu_tanh", d_dtype="bf16",
         p_dtype="bf16", description="8192^3 bf16 GEMM + gelu_tanh, writes D and PostAct"),
@@ -120,11 +137,36 @@ def group_sizes(total_m: int, groups: int, empty: int, seed: int) -> np.ndarray:
     return np.bincount(g, minlength=groups).astype(np.int64)
 
 
+def k_group_offsets(w: Workload) -> np.ndarray:
+    """cu_seqlens_k of a varlen-K workload (int64, G+1 entries)."""
+    sizes = group_sizes(w.K, w.k_groups, w.empty_groups, w.seed)
+    if w.k_multiple > 1:
+        rounded = sizes // w.k_multiple * w.k_multiple
+        last = int(np.nonzero(sizes)[0][-1])
+        rounded[last] += w.K - rounded.sum() - (w.K % w.k_multiple)
+        sizes = rounded
+    cu = np.zeros(w.k_groups + 1, dtype=np.int64)
+    cu[1:] = np.cumsum(sizes)
+    return cu
+
+
 def make(w: Workload, device="cpu"):
     """Return a dict of tensors (on ``device``) for workload ``w``."""
     gen = torch.Generator().manual_seed(w.seed)
     out = {"workload": w}
-    if w.groups:
+    if w.k_groups:
+        if w.a_major == "m":
+            out["A"] = _draw(gen, (w.K, w.M), w.dist, 1.0, w.ab_dtype).t()
+        else:
+            out["A"] = _draw(gen, (w.M, w.K), w.dist, 1.0, w.ab_dtype)
+        if w.b_major == "n":
+            out["B"] = _draw(gen, (w.K, w.N), w.dist, w.b_scale, w.bdt).t()
+        else:
+            out["B"] = _draw(gen, (w.N, w.K), w.dist, w.b_scale, w.bdt)
+        out["cu_seqlens_k"] = torch.from_numpy(k_group_offsets(w).astype(np.int32))
+        if w.with_c:
+            out["C"] = _draw(gen, (w.k_groups, w.M, w.N), "uniform", 1.0, w.d_dtype or w.p_dtype)
+    elif w.groups:
         rows_src = w.gather_rows if w.gather_rows else w.M
         out["A"] = _draw(gen, (rows_src, w.K), w.dist, 1.0, w.ab_dtype)
         out["B"] = _draw(gen, (w.groups, w.N, w.K), w.dist, w.b_scale, w.bdt)

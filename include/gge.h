@@ -104,8 +104,10 @@ typedef struct gge_config {
 
 /*
  * Arguments of one GEMM.
- *   A : [M, K, L]  rows = M, cols = K.  K-major (stride_col == 1).  In the
- *       gather form A is the SOURCE matrix [rows_src, K, 1].
+ *   A : [M, K, L]  rows = M, cols = K.  K-major (stride_col == 1) or, for
+ *       16-bit operands loaded by TMA (every form but gather-A), M-major
+ *       (stride_row == 1).  In the gather form A is the SOURCE matrix
+ *       [rows_src, K, 1], K-major.
  *   B : [N, K, L]  rows = N, cols = K.  K-major (stride_col == 1) or, for
  *       16-bit operands, N-major (stride_row == 1).  8-bit operands must be
  *       K-major (as on the pages).
@@ -135,10 +137,16 @@ typedef struct gge_gemm_args {
 } gge_gemm_args;
 
 /* Bytes of device workspace a call needs (status words and the dynamic
- * scheduler's counters); the workspace is
- * caller-owned, at least 16-byte aligned, and must be zeroed once before first
- * use.  It is reusable across calls on the same stream. */
+ * scheduler's counters), for every entry point except gge_gemm_varlen_k; the
+ * workspace is caller-owned, at least 16-byte aligned, and must be zeroed once
+ * before first use.  It is reusable across calls on the same stream. */
 size_t gge_workspace_size(const gge_gemm_args* args, int32_t num_groups);
+
+/* Workspace bytes gge_gemm_varlen_k needs for these arguments on the current
+ * device: the status words plus 2 KiB of tensor-map copies per CTA of the
+ * launch (one CTA per SM at most: about 0.3 MiB on a 152-SM GPU).  Returns 0
+ * if the arguments are invalid for gge_gemm_varlen_k. */
+size_t gge_workspace_size_varlen_k(const gge_gemm_args* args, int32_t num_groups);
 
 /* D = alpha A B^T + beta C (PostAct must be NULL and act NONE).
  * Page: quack/dense_gemm_sm90.py, gemm_sm90 / GemmSm90.epi_visit_acc_subtile. */
@@ -169,6 +177,28 @@ gge_status gge_gemm_dact(const gge_gemm_args* args, void* workspace, size_t work
  * 1 <= G <= 1024.  act as in gge_gemm_act.
  * Page: quack/dense_gemm_sm90.py, GemmSm90 with VarlenArguments(mCuSeqlensM). */
 gge_status gge_gemm_varlen_m(const gge_gemm_args* args, const int32_t* cu_seqlens_m,
+                             int32_t num_groups, void* workspace, size_t workspace_bytes,
+                             gge_stream_t stream);
+
+/* Varlen-K grouped GEMM (the weight-gradient shape of grouped experts):
+ * A is [M, total_K, 1], B is [N, total_K, 1], C / D / PostAct are [M, N, G]
+ * (batch = G groups).  Group g contracts the K columns
+ * cu_seqlens_k[g] .. cu_seqlens_k[g+1]-1:
+ *   D[:,:,g] = alpha * A[:, K_g] B[:, K_g]^T + beta * C[:,:,g]
+ * and an empty group gives alpha * 0 + beta * C.  Columns outside every group
+ * take part in no product.  cu_seqlens_k: DEVICE int32 [G+1], non-decreasing,
+ * cu[0] >= 0, cu[G] <= total_K.  When A or B is K-major, every non-empty
+ * group must start on a 16-byte boundary of the K-major rows (a multiple of 8
+ * for 16-bit, 16 for 8-bit operands); with A M-major and B N-major any
+ * offsets are allowed.  A group that breaks these rules contracts nothing and
+ * is reported as GGE_ERR_INDEX_RANGE by gge_read_device_status.
+ * 1 <= G <= 1024.  act as in gge_gemm_act.  The workspace (256-byte aligned,
+ * zeroed once) must hold gge_workspace_size_varlen_k bytes: the kernel keeps
+ * per-CTA copies of the A / B tensor maps there, rewritten with each group's
+ * K extent.  Page: quack/dense_gemm_sm90.py, GemmSm90 with
+ * VarlenArguments(mCuSeqlensK) (update_tensormap_shape per group; a group
+ * with k_tile_cnt == 0 keeps a zero accumulator). */
+gge_status gge_gemm_varlen_k(const gge_gemm_args* args, const int32_t* cu_seqlens_k,
                              int32_t num_groups, void* workspace, size_t workspace_bytes,
                              gge_stream_t stream);
 
@@ -226,17 +256,21 @@ int32_t gge_schedule_map(int32_t tiles_m, int32_t tiles_n, int32_t batches, int3
                          int32_t count, int32_t* out);
 
 /* The launch plan the library would use for `args` (tile and pipeline
- * shape).  Returns GGE_OK or the validation error of the call. */
+ * shape).  form: GGE_FORM_DEFAULT (plain, or varlen-M when num_groups > 0),
+ * GGE_FORM_GATHER_A or GGE_FORM_VARLEN_K.  Returns GGE_OK or the validation
+ * error of the call. */
+enum { GGE_FORM_DEFAULT = 0, GGE_FORM_GATHER_A = 1, GGE_FORM_VARLEN_K = 2 };
 typedef struct gge_plan_info {
   int32_t tile_m, tile_n, tile_k, stages;  /* tile_m: rows per (pair) tile */
-  int32_t num_tiles;  /* plain problems; -1 for varlen (known on the device only) */
+  int32_t num_tiles;  /* plain and varlen-K problems; -1 for varlen-M (known on
+                         the device only) */
   int32_t grid;
   int32_t threads;
   int32_t smem_bytes;
   int32_t raster_band;
   int32_t cta_group;  /* 1 or 2 CTAs per tile */
 } gge_plan_info;
-gge_status gge_plan(const gge_gemm_args* args, int32_t num_groups, int32_t gather,
+gge_status gge_plan(const gge_gemm_args* args, int32_t num_groups, int32_t form,
                     gge_plan_info* out);
 
 /* Library version string. */

@@ -159,3 +159,40 @@ def test_plan_without_gpu(L):
     D8 = torch.zeros(512, 512, dtype=torch.bfloat16)
     info = binding.gge_plan(A8, A8.to(torch.float8_e5m2), D=D8, config=cfg)
     assert info["tile_k"] == 128
+
+
+def test_varlen_k_argument_checks_and_plan(L):
+    M, N, total, G = 512, 384, 1000, 4
+    A = torch.zeros(total, M, dtype=torch.bfloat16).t()       # M-major A [M, total_K]
+    B = torch.zeros(total, N, dtype=torch.bfloat16).t()       # N-major B [N, total_K]
+    D = torch.zeros(G, M, N, dtype=torch.bfloat16)
+    cu = torch.zeros(G + 1, dtype=torch.int32)
+    cup = ctypes.c_void_p(cu.data_ptr())
+    args = binding.make_args(A, B, D=D)
+    assert L.gge_gemm_varlen_k(ctypes.byref(args), None, G, None, 0, None) == 1   # no offsets
+    assert L.gge_gemm_varlen_k(ctypes.byref(args), cup, 0, None, 0, None) == 2    # G = 0
+    assert L.gge_gemm_varlen_k(ctypes.byref(args), cup, 3, None, 0, None) == 1    # D has 4 groups
+    bad = binding.make_args(A, B, D=torch.zeros(G, M, N, dtype=torch.bfloat16)[:, :256])
+    assert L.gge_gemm_varlen_k(ctypes.byref(bad), cup, G, None, 0, None) == 1     # M mismatch
+    A8 = torch.zeros(total, M, dtype=torch.float8_e4m3fn).t()
+    B8 = torch.zeros(N, total, dtype=torch.float8_e4m3fn)
+    bad = binding.make_args(A8, B8, D=D)
+    assert L.gge_gemm_varlen_k(ctypes.byref(bad), cup, G, None, 0, None) == 2     # 8-bit M-major A
+    cfg = binding.make_config(num_ctas=152)
+    info = binding.gge_plan(A, B, D=D, num_groups=G, form="varlen_k", config=cfg)
+    assert info["cta_group"] == 2 and info["tile_n"] == 256
+    assert info["num_tiles"] == G * 2 * 2 and info["grid"] == 2 * 16
+    # the tensor-map workspace: 256 status bytes + 8 slots of 256 bytes per CTA
+    # (gge_workspace_size_varlen_k itself asks the device for its occupancy)
+    with pytest.raises(binding.GgeError):
+        binding.gge_plan(A, B, D=D, num_groups=G, form="gather_a", config=cfg)
+
+
+def test_m_major_a_plans_for_tma_forms_only(L):
+    A = torch.zeros(512, 256, dtype=torch.bfloat16).t()       # [256, 512] M-major
+    B = torch.zeros(384, 512, dtype=torch.bfloat16)
+    D = torch.zeros(256, 384, dtype=torch.bfloat16)
+    cfg = binding.make_config(num_ctas=152)
+    assert binding.gge_plan(A, B, D=D, config=cfg)["tile_m"] == 256
+    with pytest.raises(binding.GgeError):                     # the row gather reads K-major rows
+        binding.gge_plan(A, B, D=D, gather=True, config=cfg)

@@ -208,3 +208,20 @@ def test_full_size_sampled(name):
             assert torch.isfinite(out[k].float()).all()
     if "P" in out and w.act == "relu":
         assert (out["P"].float() >= 0).all()
+
+
+@pytest.mark.parametrize("M,N,K,L,b_major,cg", [
+    (384, 264, 200, 1, "k", 2),
+    (328, 512, 136, 2, "n", 2),
+    (200, 256, 72, 3, "k", 1),
+    (256, 128, 512, 1, "n", 1),
+])
+def test_m_major_a(M, N, K, L, b_major, cg):
+    # A stored (L, K, M) and used as its (M, K) transpose: M-major A through TMA
+    w = wl.small("gemm_act_4096_bf16_gelu", M, N, K, L, b_major=b_major)
+    t = wl.make(w)
+    t["A"] = t["A"].transpose(1, 2).contiguous().transpose(1, 2)
+    assert t["A"].stride(1) == 1
+    out = _outputs(w, M, N, L)
+    _run_plain(w, t, out, config=binding.make_config(cta_group=cg))
+    _check_plain(w, t, out)
