@@ -26,6 +26,7 @@ constexpr int kTileM = 128;
 constexpr int kRowBytesHost = 128;
 constexpr int kMaxSmemOptin = 232448;  // 227 KiB per block on sm_100 / sm_103
 constexpr int kCtrlBytesHost = 512;
+constexpr int kOutStageBytesHost = 4096;  // epilogue staging per epilogue warp (kOutStageBytes)
 constexpr int kMaxGroupsHost = 1024;
 constexpr size_t kWorkspaceBytes = 256;
 constexpr size_t kMapSlotsHost = 8;      // varlen-K tensor-map slots per CTA (kernel kMapSlots)
@@ -406,8 +407,11 @@ gge_status make_plan(const gge_gemm_args* a, Form form, const int32_t* a_idx,
       if (!b_mn && !varlen && !vk) {
         int64_t units = cfg && cfg->num_ctas > 0 ? cfg->num_ctas / 2 : 0;
         if (units <= 0 && encode) {
-          const size_t smem256 = 1024 + kCtrlBytesHost +
-                                 7 * (kTileM + 128) * kRowBytesHost;  // the 256-wide plan
+          // the 256-wide plan: as many stages of (128 + 128) rows as fit, at most kMaxStages
+          const int fixed256 = 1024 + kCtrlBytesHost + 8 * kOutStageBytesHost;
+          const int st256 = (kTileM + 128) * kRowBytesHost;
+          const size_t smem256 =
+              fixed256 + std::min(kMaxStages, (kMaxSmemOptin - fixed256) / st256) * st256;
           units = variant_units(256, false, 2, smem256);
         }
         if (units > 0) bn = choose_pair_bn((M + 2 * kTileM - 1) / (2 * kTileM), N, L, units);
@@ -422,7 +426,8 @@ gge_status make_plan(const gge_gemm_args* a, Form form, const int32_t* a_idx,
   const int bk = kRowBytesHost / es;
   const int stage_bytes = (kTileM + bn / cg) * kRowBytesHost;
   const int varlen_bytes = (varlen || vk) ? 2 * 4 * (kMaxGroupsHost + 1) : 0;
-  const int fixed = 1024 + kCtrlBytesHost + varlen_bytes;
+  const int epi_warps = gather ? 4 : 8;
+  const int fixed = 1024 + kCtrlBytesHost + varlen_bytes + epi_warps * kOutStageBytesHost;
   int stages = (kMaxSmemOptin - fixed) / stage_bytes;
   stages = std::min(stages, kMaxStages);
   if (cfg && cfg->stages > 0) stages = std::min(stages, cfg->stages);

@@ -55,6 +55,7 @@ constexpr int kMaxGroups = 1024;   // varlen groups held in shared memory
 constexpr int kCtrlBytes = 512;    // barriers, flags and the tile ring (bytes 0..255),
                                    // the varlen-K tensor-map scratch (256..511)
 constexpr int kMapScratch = 256;
+constexpr int kOutStageBytes = 4096;  // epilogue staging per epilogue warp: 32 rows x 128 B
 constexpr int kSchedDepth = 4;     // tile indices in flight between the fetching warp and the rest
 constexpr int kMapSlots = 8;       // varlen-K: tensor-map copies per CTA (>= pipeline stages)
 constexpr int kMapSlotBytes = 256; // one A and one B tensor map
@@ -141,15 +142,28 @@ __device__ __forceinline__ TileCoord tile_coord(int32_t t, const Params& p, cons
   return tc;
 }
 
-// The K columns a tile contracts: [k0, k_end) in k-tiles of bk.
+// The K columns a tile contracts: [k0, k_end) in k-tiles of bk.  `ragged`: a
+// varlen-K group whose length is not a whole number of MMA K-steps, so its
+// last step must read zeros past k_end (through a tensor map clipped at k_end);
+// every other range is cut exactly by issuing only the K-steps it covers.
 struct KRange {
   int32_t k0, k_end, tiles;
+  bool ragged;
 };
 
+__device__ __forceinline__ int32_t mma_kstep(const Params& p) { return p.f8 ? 32 : 16; }
+
 __device__ __forceinline__ KRange k_range(const Params& p, const Shared& sh, int32_t batch) {
-  if (p.k_groups == 0) return KRange{0, p.K, p.k_tiles};
+  if (p.k_groups == 0) return KRange{0, p.K, p.k_tiles, false};
   const int32_t lo = sh.cu[batch], hi = sh.prefix[batch];
-  return KRange{lo, hi, (hi - lo + p.bk - 1) / p.bk};
+  return KRange{lo, hi, (hi - lo + p.bk - 1) / p.bk, ((hi - lo) & (mma_kstep(p) - 1)) != 0};
+}
+
+// MMA K-steps of k-tile kt (4 per full k-tile; the last one stops at k_end).
+__device__ __forceinline__ int32_t ksteps_of(const Params& p, const KRange& kr, int32_t kt) {
+  const int32_t left = kr.k_end - (kr.k0 + kt * p.bk);
+  const int32_t step = mma_kstep(p);
+  return min(4, (left + step - 1) / step);
 }
 
 __device__ __forceinline__ void record_status(const Params& p, int32_t code, int32_t where,
@@ -242,7 +256,7 @@ __device__ __forceinline__ int32_t sched_next(const TileSched& ts, int i, const 
   __syncwarp();
   if ((threadIdx.x & 31) == 0) {  // this warp is done with the slot (the leader's ring owns it)
     if (CG == 1) ptx::mbar_arrive(ts.empty + 8 * slot);
-    else ptx::mbar_arrive_cluster(ptx::mapa(ts.empty + 8 * slot, 0));
+    else ptx::mbar_arrive_remote(ptx::mapa(ts.empty + 8 * slot, 0));
   }
   return t;
 }
@@ -290,169 +304,192 @@ __device__ __forceinline__ float dact_apply(int act, float x) {
   }
 }
 
-// Load 8 consecutive values of a 16-byte group as fp32.
-__device__ __forceinline__ void load8(const void* ptr, int dtype, float* out) {
-  if (dtype == DT_F32) {
-    const float4 a = __ldg(reinterpret_cast<const float4*>(ptr));
-    const float4 b = __ldg(reinterpret_cast<const float4*>(ptr) + 1);
-    out[0] = a.x; out[1] = a.y; out[2] = a.z; out[3] = a.w;
-    out[4] = b.x; out[5] = b.y; out[6] = b.z; out[7] = b.w;
-  } else {
-    const uint4 v = __ldg(reinterpret_cast<const uint4*>(ptr));
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      if (dtype == DT_BF16) {
-        const __nv_bfloat162 h = *reinterpret_cast<const __nv_bfloat162*>(&w[i]);
-        const float2 f = __bfloat1622float2(h);
-        out[2 * i] = f.x; out[2 * i + 1] = f.y;
-      } else {
-        const __half2 h = *reinterpret_cast<const __half2*>(&w[i]);
-        const float2 f = __half22float2(h);
-        out[2 * i] = f.x; out[2 * i + 1] = f.y;
-      }
-    }
-  }
-}
-
-// Round 8 fp32 values to the output dtype (RNE) and store them.
-__device__ __forceinline__ void store8(void* ptr, int dtype, const float* x) {
-  if (dtype == DT_F32) {
-    reinterpret_cast<float4*>(ptr)[0] = make_float4(x[0], x[1], x[2], x[3]);
-    reinterpret_cast<float4*>(ptr)[1] = make_float4(x[4], x[5], x[6], x[7]);
-  } else {
-    uint32_t w[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      if (dtype == DT_BF16) {
-        const __nv_bfloat162 h = __floats2bfloat162_rn(x[2 * i], x[2 * i + 1]);
-        w[i] = *reinterpret_cast<const uint32_t*>(&h);
-      } else {
-        const __half2 h = __floats2half2_rn(x[2 * i], x[2 * i + 1]);
-        w[i] = *reinterpret_cast<const uint32_t*>(&h);
-      }
-    }
-    *reinterpret_cast<uint4*>(ptr) = make_uint4(w[0], w[1], w[2], w[3]);
-  }
-}
-
 __device__ __forceinline__ int dtype_bytes(int dt) { return dt == DT_F32 ? 4 : 2; }
 
-// Raw bits of one thread's 32 columns of C (16-bit C uses w[0..3], fp32 C all 8).
+// Raw bits of one thread's 32 columns of a 16-bit C, loaded one chunk ahead.
+// (An fp32 C is read where it is used: holding two chunks of it would cost 32
+// more registers than the epilogue has.)
 struct CRegs {
-  uint4 w[8];
+  uint4 w[4];
 };
 
-// Issue the loads of C[row, col0 .. col0+32) (no arithmetic: the values are
-// used one chunk later, so the load latency hides behind that chunk's work).
-__device__ __forceinline__ void load_c_chunk(const Params& p, int32_t row, int32_t col0,
-                                             int32_t batch, CRegs& c) {
+// Address of C[row, col0] of batch `batch`.
+__device__ __forceinline__ const char* c_ptr(const Params& p, int32_t row, int32_t col0,
+                                             int32_t batch) {
   const int64_t out_batch = (p.num_groups > 0) ? 0 : batch;
-  const int es = dtype_bytes(p.c_dtype);
-  const uint4* base = reinterpret_cast<const uint4*>(
-      static_cast<const char*>(p.c) +
-      (out_batch * p.sbc + static_cast<int64_t>(row) * p.ldc + col0) * es);
-  const int per = 8 / (4 / es);  // 16-byte words of 32 columns: 4 (16-bit) or 8 (fp32)
-  const int cols = 16 / es;      // columns per 16-byte word
-#pragma unroll
-  for (int i = 0; i < 8; ++i)
-    if (i < per && col0 + cols * i < p.N) c.w[i] = __ldg(base + i);
+  return static_cast<const char*>(p.c) +
+         (out_batch * p.sbc + static_cast<int64_t>(row) * p.ldc + col0) * dtype_bytes(p.c_dtype);
 }
 
-// Eight values of the prefetched C chunk (group g of 8 columns) as fp32.
-__device__ __forceinline__ void c_values8(const CRegs& c, int dtype, int g, float* out) {
-  if (dtype == DT_F32) {
-    const uint4 a = c.w[2 * g], b = c.w[2 * g + 1];
-    out[0] = __uint_as_float(a.x); out[1] = __uint_as_float(a.y);
-    out[2] = __uint_as_float(a.z); out[3] = __uint_as_float(a.w);
-    out[4] = __uint_as_float(b.x); out[5] = __uint_as_float(b.y);
-    out[6] = __uint_as_float(b.z); out[7] = __uint_as_float(b.w);
+// Issue the loads of a 16-bit C[row, col0 .. col0+32) (no arithmetic: the
+// values are used one chunk later, so the load latency hides behind that
+// chunk's work).
+__device__ __forceinline__ void load_c_chunk(const Params& p, int32_t row, int32_t col0,
+                                             int32_t batch, CRegs& c) {
+  if (p.c_dtype == DT_F32) return;
+  const uint4* base = reinterpret_cast<const uint4*>(c_ptr(p, row, col0, batch));
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    if (col0 + 8 * i < p.N) c.w[i] = __ldg(base + i);
+}
+
+// Eight values of C (group g of 8 columns of the chunk) as fp32: from the
+// prefetched registers (16-bit C), or read now through `crow` (fp32 C; NULL
+// for a row that does not exist).
+__device__ __forceinline__ void c_values8(const CRegs& c, const Params& p, const char* crow,
+                                          int32_t col0, int g, float* out) {
+  if (p.c_dtype == DT_F32) {
+    float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a;
+    if (crow != nullptr && col0 + 8 * g < p.N) {
+      a = __ldg(reinterpret_cast<const float4*>(crow) + 2 * g);
+      b = __ldg(reinterpret_cast<const float4*>(crow) + 2 * g + 1);
+    }
+    out[0] = a.x; out[1] = a.y; out[2] = a.z; out[3] = a.w;
+    out[4] = b.x; out[5] = b.y; out[6] = b.z; out[7] = b.w;
   } else {
     const uint32_t w[4] = {c.w[g].x, c.w[g].y, c.w[g].z, c.w[g].w};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       float2 f;
-      if (dtype == DT_BF16) f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[i]));
-      else f = __half22float2(*reinterpret_cast<const __half2*>(&w[i]));
+      if (p.c_dtype == DT_BF16)
+        f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[i]));
+      else
+        f = __half22float2(*reinterpret_cast<const __half2*>(&w[i]));
       out[2 * i] = f.x;
       out[2 * i + 1] = f.y;
     }
   }
 }
 
-// Backward epilogue for one thread's 32 columns: x (the pre-activation) comes
+// Pack 8 fp32 values into one 16-byte word of the output dtype (RNE); fp32
+// takes two words.
+__device__ __forceinline__ uint32_t pack2(int dtype, float a, float b) {
+  if (dtype == DT_BF16) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<const uint32_t*>(&h);
+  }
+  const __half2 h = __floats2half2_rn(a, b);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+// Write a warp's 32 x 32 output chunk (lane = row, x = its 32 columns) to global
+// memory through the warp's shared-memory staging buffer, so that each store
+// instruction writes whole row segments: 16-bit outputs 8 rows x 64 B, fp32
+// 4 rows x 128 B (instead of 32 rows x 16 B).  The 16-byte pieces of a row are
+// XOR-swizzled so that both the row-wise writes and the transposed reads are
+// free of bank conflicts.  `out` points at (row 0, column 0) of the chunk;
+// rows >= rows_valid and columns >= cols_valid are not written.  Warp-collective.
+__device__ __forceinline__ void store_chunk_staged(uint32_t stg, const float (&x)[32], int dtype,
+                                                   char* out, int64_t ld_bytes,
+                                                   int32_t rows_valid, int32_t cols_valid) {
+  const int lane = threadIdx.x & 31;
+  if (dtype == DT_F32) {
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+      ptx::st_shared_v4(stg + lane * 128 + ((q ^ (lane & 7)) << 4),
+                        make_uint4(__float_as_uint(x[4 * q]), __float_as_uint(x[4 * q + 1]),
+                                   __float_as_uint(x[4 * q + 2]), __float_as_uint(x[4 * q + 3])));
+    __syncwarp();
+    const int q = lane & 7;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int r = 4 * j + (lane >> 3);
+      const uint4 v = ptx::ld_shared_v4(stg + r * 128 + ((q ^ (r & 7)) << 4));
+      if (r < rows_valid && 4 * q < cols_valid)
+        *reinterpret_cast<uint4*>(out + r * ld_bytes + 16 * q) = v;
+    }
+  } else {
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      ptx::st_shared_v4(stg + lane * 64 + ((q ^ ((lane >> 1) & 3)) << 4),
+                        make_uint4(pack2(dtype, x[8 * q], x[8 * q + 1]),
+                                   pack2(dtype, x[8 * q + 2], x[8 * q + 3]),
+                                   pack2(dtype, x[8 * q + 4], x[8 * q + 5]),
+                                   pack2(dtype, x[8 * q + 6], x[8 * q + 7])));
+    __syncwarp();
+    const int q = lane & 3;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int r = 8 * j + (lane >> 2);
+      const uint4 v = ptx::ld_shared_v4(stg + r * 64 + ((q ^ ((r >> 1) & 3)) << 4));
+      if (r < rows_valid && 8 * q < cols_valid)
+        *reinterpret_cast<uint4*>(out + r * ld_bytes + 16 * q) = v;
+    }
+  }
+  __syncwarp();  // the buffer is free again
+}
+
+// Where a warp's chunk of an output starts: (row_base, col0) of batch `batch`.
+__device__ __forceinline__ char* out_ptr(void* base, int64_t ld, int64_t sb, int dtype,
+                                         int32_t row_base, int32_t col0, int32_t batch,
+                                         const Params& p) {
+  const int64_t out_batch = (p.num_groups > 0) ? 0 : batch;
+  return static_cast<char*>(base) +
+         (out_batch * sb + static_cast<int64_t>(row_base) * ld + col0) * dtype_bytes(dtype);
+}
+
+// Backward epilogue for one warp's 32 x 32 chunk: x (the pre-activation) comes
 // from C, dout is the accumulator; D = act'(x) * dout, PostAct = act(x).
 __device__ __forceinline__ void epilogue_chunk_dact(const Params& p, const uint32_t (&acc)[32],
-                                                 int32_t row, int32_t col0, int32_t batch,
-                                                 const CRegs& creg) {
-  const int64_t out_batch = (p.num_groups > 0) ? 0 : batch;
-  char* dbase = static_cast<char*>(p.d) +
-                (out_batch * p.sbd + static_cast<int64_t>(row) * p.ldd + col0) *
-                    dtype_bytes(p.d_dtype);
-  char* pbase = p.post == nullptr ? nullptr
-                                  : static_cast<char*>(p.post) +
-                                        (out_batch * p.sbp + static_cast<int64_t>(row) * p.ldp +
-                                         col0) * dtype_bytes(p.p_dtype);
+                                                    int32_t row_base, int32_t rows_valid,
+                                                    int32_t col0, int32_t batch,
+                                                    const CRegs& creg, uint32_t stg) {
+  const int32_t cols_valid = min(32, p.N - col0);
+  const int lane = threadIdx.x & 31;
+  const char* crow = (p.c_dtype == DT_F32 && lane < rows_valid)
+                         ? c_ptr(p, row_base + lane, col0, batch) : nullptr;
+  float x[32], y[32];
 #pragma unroll
-  for (int g = 0; g < 4; ++g) {  // unrolled: acc stays in registers
-    if (col0 + 8 * g >= p.N) continue;
-    float x[8], dx[8];
-    c_values8(creg, p.c_dtype, g, x);
+  for (int g = 0; g < 4; ++g) c_values8(creg, p, crow, col0, g, &x[8 * g]);
 #pragma unroll
-    for (int j = 0; j < 8; ++j) dx[j] = dact_apply(p.act, x[j]) * __uint_as_float(acc[8 * g + j]);
-    store8(dbase + 8 * g * dtype_bytes(p.d_dtype), p.d_dtype, dx);
-    if (pbase != nullptr) {
+  for (int j = 0; j < 32; ++j) y[j] = dact_apply(p.act, x[j]) * __uint_as_float(acc[j]);
+  store_chunk_staged(stg, y, p.d_dtype,
+                     out_ptr(p.d, p.ldd, p.sbd, p.d_dtype, row_base, col0, batch, p),
+                     p.ldd * dtype_bytes(p.d_dtype), rows_valid, cols_valid);
+  if (p.post != nullptr) {
 #pragma unroll
-      for (int j = 0; j < 8; ++j) x[j] = act_apply(p.act, x[j]);
-      store8(pbase + 8 * g * dtype_bytes(p.p_dtype), p.p_dtype, x);
-    }
+    for (int j = 0; j < 32; ++j) y[j] = act_apply(p.act, x[j]);
+    store_chunk_staged(stg, y, p.p_dtype,
+                       out_ptr(p.post, p.ldp, p.sbp, p.p_dtype, row_base, col0, batch, p),
+                       p.ldp * dtype_bytes(p.p_dtype), rows_valid, cols_valid);
   }
 }
 
-// One thread, one output row, 32 consecutive columns starting at col0.
+// One warp's 32 x 32 chunk: rows row_base .. +31 (lane = row), columns col0 .. +31.
 __device__ __forceinline__ void epilogue_chunk(const Params& p, const uint32_t (&acc)[32],
-                                               int32_t row, int32_t col0, int32_t batch,
-                                               float alpha, float beta, const CRegs& creg) {
+                                               int32_t row_base, int32_t rows_valid,
+                                               int32_t col0, int32_t batch, float alpha,
+                                               float beta, const CRegs& creg, uint32_t stg) {
   if (p.dact) {
-    epilogue_chunk_dact(p, acc, row, col0, batch, creg);
+    epilogue_chunk_dact(p, acc, row_base, rows_valid, col0, batch, creg, stg);
     return;
   }
+  const int32_t cols_valid = min(32, p.N - col0);
   float v[32];
 #pragma unroll
   for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(acc[j]) * alpha;
-  const int64_t out_batch = (p.num_groups > 0) ? 0 : batch;
   if (p.c != nullptr) {
+    const int lane = threadIdx.x & 31;
+    const char* crow = (p.c_dtype == DT_F32 && lane < rows_valid)
+                           ? c_ptr(p, row_base + lane, col0, batch) : nullptr;
 #pragma unroll
     for (int g = 0; g < 4; ++g) {
-      if (col0 + 8 * g < p.N) {
-        float cv[8];
-        c_values8(creg, p.c_dtype, g, cv);
+      float cv[8];
+      c_values8(creg, p, crow, col0, g, cv);
 #pragma unroll
-        for (int j = 0; j < 8; ++j) v[8 * g + j] = fmaf(beta, cv[j], v[8 * g + j]);
-      }
+      for (int j = 0; j < 8; ++j) v[8 * g + j] = fmaf(beta, cv[j], v[8 * g + j]);
     }
   }
-  if (p.d != nullptr) {
-    char* dbase = static_cast<char*>(p.d) +
-                  (out_batch * p.sbd + static_cast<int64_t>(row) * p.ldd + col0) *
-                      dtype_bytes(p.d_dtype);
-#pragma unroll
-    for (int g = 0; g < 4; ++g)
-      if (col0 + 8 * g < p.N) store8(dbase + 8 * g * dtype_bytes(p.d_dtype), p.d_dtype, &v[8 * g]);
-  }
+  if (p.d != nullptr)
+    store_chunk_staged(stg, v, p.d_dtype,
+                       out_ptr(p.d, p.ldd, p.sbd, p.d_dtype, row_base, col0, batch, p),
+                       p.ldd * dtype_bytes(p.d_dtype), rows_valid, cols_valid);
   if (p.post != nullptr) {
-    char* pbase = static_cast<char*>(p.post) +
-                  (out_batch * p.sbp + static_cast<int64_t>(row) * p.ldp + col0) *
-                      dtype_bytes(p.p_dtype);
 #pragma unroll
-    for (int g = 0; g < 4; ++g) {
-      if (col0 + 8 * g < p.N) {
-        float a[8];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) a[j] = act_apply(p.act, v[8 * g + j]);
-        store8(pbase + 8 * g * dtype_bytes(p.p_dtype), p.p_dtype, a);
-      }
-    }
+    for (int j = 0; j < 32; ++j) v[j] = act_apply(p.act, v[j]);
+    store_chunk_staged(stg, v, p.p_dtype,
+                       out_ptr(p.post, p.ldp, p.sbp, p.p_dtype, row_base, col0, batch, p),
+                       p.ldp * dtype_bytes(p.p_dtype), rows_valid, cols_valid);
   }
 }
 
@@ -467,7 +504,8 @@ __device__ __forceinline__ void epilogue_chunk(const Params& p, const uint32_t (
 template <int BN, bool GATHER, int CG>
 __device__ __forceinline__ void epilogue_role(const Params& p, const Shared& sh,
                                               uint32_t tmem_base, int32_t num_tiles,
-                                              uint32_t rank, const TileSched& ts) {
+                                              uint32_t rank, const TileSched& ts,
+                                              uint32_t stg) {
   using Cfg = KernelCfg<BN, GATHER, CG>;
   constexpr int kChunks = BN / 32;
   constexpr int kStride = Cfg::kEpiWarps / 4;  // warps per TMEM lane quadrant
@@ -482,10 +520,11 @@ __device__ __forceinline__ void epilogue_role(const Params& p, const Shared& sh,
     const TileCoord tc = tile_coord<BN, Cfg::kTileM>(t, p, sh);
     // a tile with no k-tiles (K == 0, or an empty varlen-K group) keeps a zero accumulator
     const bool has_acc = k_range(p, sh, tc.batch).tiles > 0;
-    const int32_t row = tc.m_row0 + static_cast<int32_t>(rank) * kBM + quad * 32 + lane;
-    const bool row_ok = row < tc.row_limit;
-    const bool has_c = p.c != nullptr && row_ok;
-    CRegs cnext;
+    const int32_t row_base = tc.m_row0 + static_cast<int32_t>(rank) * kBM + quad * 32;
+    const int32_t rows_valid = min(32, tc.row_limit - row_base);  // warp-uniform, may be <= 0
+    const int32_t row = row_base + lane;
+    const bool has_c = p.c != nullptr && lane < rows_valid;
+    CRegs cnext = {};
     if (has_c && tc.n0 + half * 32 < p.N) load_c_chunk(p, row, tc.n0 + half * 32, tc.batch, cnext);
     // all lanes take the same branch: tcgen05.ld below is warp-collective
     const bool ok = wait_phase<CG == 2>(sh.tfull + 8 * acc, acc_phase, p, sh, 3, t);
@@ -511,11 +550,12 @@ __device__ __forceinline__ void epilogue_role(const Params& p, const Shared& sh,
         __syncwarp();
         if (lane == 0) {
           if (CG == 1) ptx::mbar_arrive(sh.tempty + 8 * acc);
-          else ptx::mbar_arrive_cluster(ptx::mapa(sh.tempty + 8 * acc, 0));
+          else ptx::mbar_arrive_remote(ptx::mapa(sh.tempty + 8 * acc, 0));
         }
       }
       const int32_t col0 = tc.n0 + c * 32;
-      if (row_ok && col0 < p.N) epilogue_chunk(p, v, row, col0, tc.batch, alpha, beta, ccur);
+      if (rows_valid > 0 && col0 < p.N)
+        epilogue_chunk(p, v, row_base, rows_valid, col0, tc.batch, alpha, beta, ccur, stg);
     }
     if ((p.flags & FLAG_TILE_COUNTS) && p.tile_counts != nullptr && rank == 0 && warp == 0 &&
         lane == 0)
@@ -548,19 +588,21 @@ __device__ __forceinline__ void mma_role(const Params& p, const Shared& sh, uint
     if (!__all_sync(0xffffffffu, ok)) return;
     ptx::tc_fence_after();
     const uint32_t d_tmem = tmem_base + acc * BN;
-    const int32_t k_tiles =
-        p.k_groups > 0 ? k_range(p, sh, tile_coord<BN, Cfg::kTileM>(t, p, sh).batch).tiles
-                       : p.k_tiles;
-    for (int kt = 0; kt < k_tiles; ++kt) {
+    const KRange kr = p.k_groups > 0
+                          ? k_range(p, sh, tile_coord<BN, Cfg::kTileM>(t, p, sh).batch)
+                          : KRange{0, p.K, p.k_tiles, false};
+    for (int kt = 0; kt < kr.tiles; ++kt) {
       ok = wait_phase<CG == 2>(sh.full + 8 * stage, phase, p, sh, 1, t);
       if (!__all_sync(0xffffffffu, ok)) return;
       ptx::tc_fence_after();
       if (GATHER) ptx::fence_proxy_async_smem();  // cp.async (generic proxy) writes -> MMA reads
       const uint32_t a_addr = a0 + stage * Cfg::kABytes;
       const uint32_t b_addr = b0 + stage * Cfg::kBBytes;
+      const int32_t nk = (kt == kr.tiles - 1) ? ksteps_of(p, kr, kt) : 4;
       if (ptx::elect_one()) {
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {  // 4 MMAs of 32 bytes of K each
+        for (int kk = 0; kk < 4; ++kk) {  // up to 4 MMAs of 32 bytes of K each
+          if (kk >= nk) break;
           const uint64_t adesc = smem_desc(a_addr + kk * a_kstep, a_lbo, 1024u);
           const uint64_t bdesc = smem_desc(b_addr + kk * b_kstep, b_lbo, 1024u);
           const uint32_t accumulate = (kt > 0 || kk > 0) ? 1u : 0u;
@@ -637,6 +679,7 @@ __device__ __forceinline__ void tma_producer_role(const Params& p, const Shared&
   // varlen-K: the group whose maps are in use, and the slot they occupy
   int32_t map_group = -1;
   int map_slot = kMapSlots - 1;
+  const uint8_t* map_cur = nullptr;
   const CUtensorMap* mA = tmA;
   const CUtensorMap* mB = tmB;
   for (int i = 0;; ++i) {
@@ -650,15 +693,19 @@ __device__ __forceinline__ void tma_producer_role(const Params& p, const Shared&
     for (int kt = 0; kt < kr.tiles; ++kt) {
       const bool ok = wait_phase<CG == 2>(sh.empty + 8 * stage, phase ^ 1u, p, sh, 0, t);
       if (!__all_sync(0xffffffffu, ok)) return;
-      if (p.k_groups > 0 && kt == 0 && tc.batch != map_group) {
-        // A slot is rewritten kMapSlots (>= stages) group changes after its last
-        // use; every group issues at least one k-tile, and the wait above has
-        // seen the k-tile `stages` back consumed, so no copy still reads it.
-        map_slot = (map_slot + 1 == kMapSlots) ? 0 : map_slot + 1;
-        const uint8_t* m = publish_kmaps(p, tmA, tmB, map_scratch, map_slot, kr.k_end);
-        mA = reinterpret_cast<const CUtensorMap*>(m);
-        mB = reinterpret_cast<const CUtensorMap*>(m + 128);
-        map_group = tc.batch;
+      if (kt == 0) {
+        if (kr.ragged && tc.batch != map_group) {
+          // A slot is rewritten kMapSlots (>= stages) group changes after its last
+          // use; every group issues at least one k-tile, and the wait above has
+          // seen the k-tile `stages` back consumed, so no copy still reads it.
+          map_slot = (map_slot + 1 == kMapSlots) ? 0 : map_slot + 1;
+          map_cur = publish_kmaps(p, tmA, tmB, map_scratch, map_slot, kr.k_end);
+          map_group = tc.batch;
+        }
+        // a ragged group reads through its clipped maps; any other range is cut by
+        // the MMA K-step count, so the launch's maps serve it
+        mA = kr.ragged ? reinterpret_cast<const CUtensorMap*>(map_cur) : tmA;
+        mB = kr.ragged ? reinterpret_cast<const CUtensorMap*>(map_cur + 128) : tmB;
       }
       const uint32_t full = sh.full + 8 * stage;
       const int32_t k0 = kr.k0 + kt * p.bk;
@@ -764,7 +811,8 @@ __global__ void __launch_bounds__(KernelCfg<BN, GATHER, CG>::kThreads, 1)
   const int S = p.stages;
   const uint32_t a0 = base;
   const uint32_t b0 = base + S * Cfg::kABytes;
-  uint8_t* ctrl = base_ptr + S * Cfg::kStageBytes;
+  const uint32_t out_stage = base + S * Cfg::kStageBytes;  // epilogue staging, per warp
+  uint8_t* ctrl = base_ptr + S * Cfg::kStageBytes + Cfg::kEpiWarps * kOutStageBytes;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ctrl + 8 * (2 * S + 5 + 2 * kSchedDepth));
   int32_t* abort_flag = reinterpret_cast<int32_t*>(tmem_slot + 1);
   int32_t* prefix = reinterpret_cast<int32_t*>(ctrl + kCtrlBytes);
@@ -880,7 +928,8 @@ __global__ void __launch_bounds__(KernelCfg<BN, GATHER, CG>::kThreads, 1)
   const int32_t num_tiles = (p.num_groups > 0) ? prefix[p.num_groups] : p.num_tiles;
 
   if (warp < Cfg::kEpiWarps) {
-    epilogue_role<BN, GATHER, CG>(p, sh, tmem_base, num_tiles, rank, ts);
+    epilogue_role<BN, GATHER, CG>(p, sh, tmem_base, num_tiles, rank, ts,
+                                  out_stage + warp * kOutStageBytes);
   } else if (warp == Cfg::kMmaWarp) {
     if (rank == 0) mma_role<BN, GATHER, CG>(p, sh, a0, b0, tmem_base, num_tiles, ts);
   } else if (GATHER) {

@@ -144,7 +144,7 @@ def test_plan_without_gpu(L):
     assert info["cta_group"] == 2 and info["tile_m"] == 256 and info["tile_n"] == 256
     assert info["tile_k"] == 64
     assert info["num_tiles"] == 32 * 32 and info["grid"] == 152
-    assert info["stages"] == 7
+    assert info["stages"] == 6
     cfg1 = binding.make_config(num_ctas=152, cta_group=1)
     info = binding.gge_plan(A, A, D=D, config=cfg1)
     assert info["tile_m"] == 128 and info["num_tiles"] == 64 * 32 and info["stages"] == 4
