@@ -25,13 +25,13 @@ namespace {
 constexpr int kTileM = 128;
 constexpr int kRowBytesHost = 128;
 constexpr int kMaxSmemOptin = 232448;  // 227 KiB per block on sm_100 / sm_103
-constexpr int kCtrlBytesHost = 512;
+constexpr int kCtrlBytesHost = 1024;
 constexpr int kOutStageBytesHost = 4096;  // epilogue staging per epilogue warp (kOutStageBytes)
 constexpr int kMaxGroupsHost = 1024;
 constexpr size_t kWorkspaceBytes = 256;
-constexpr size_t kMapSlotsHost = 8;      // varlen-K tensor-map slots per CTA (kernel kMapSlots)
+constexpr size_t kMapSlotsHost = 16;     // varlen-K tensor-map slots per CTA (kernel kMapSlots)
 constexpr size_t kMapSlotBytesHost = 256;
-constexpr int kMaxStages = 8;            // never more stages than map slots
+constexpr int kMaxStages = 8;            // fewer stages than map slots
 constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;
 constexpr int64_t kMaxExtent = (int64_t(1) << 31) - 1;
 

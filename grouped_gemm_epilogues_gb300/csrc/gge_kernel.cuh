@@ -17,6 +17,8 @@
 //              pages' ping-pong warpgroups).
 //   warp  9    TMA producer: A and B k-tiles into an S-stage shared-memory
 //              ring (128-byte swizzle), one mbarrier pair per stage.
+//   warp 10    varlen-K: writes each ragged group's clipped tensor maps ahead
+//              of the producer (otherwise idle).
 //   warps 9-12 (gather-A form) row gather of A with 16-byte cp.async into the
 //              same swizzled layout, B still by TMA (GemmSm90.load_AB_gather_A).
 //
@@ -52,16 +54,19 @@ constexpr int kRowBytes = 128;     // bytes of K per stage row (one swizzle span
 
 constexpr int kGatherWarps = 4;
 constexpr int kMaxGroups = 1024;   // varlen groups held in shared memory
-constexpr int kCtrlBytes = 512;    // barriers, flags and the tile ring (bytes 0..255),
-                                   // the varlen-K tensor-map scratch (256..511)
+constexpr int kCtrlBytes = 1024;   // barriers, flags and the tile ring (bytes 0..255),
+                                   // the varlen-K tensor-map scratch (256..511) and
+                                   // map-slot barriers (512..767)
 constexpr int kMapScratch = 256;
+constexpr int kMapBars = 512;
 constexpr int kOutStageBytes = 4096;  // epilogue staging per epilogue warp: 32 rows x 128 B
 constexpr int kSchedDepth = 4;     // tile indices in flight between the fetching warp and the rest
-constexpr int kMapSlots = 8;       // varlen-K: tensor-map copies per CTA (>= pipeline stages)
+constexpr int kMapSlots = 16;      // varlen-K: tensor-map copies per CTA (> pipeline stages)
 constexpr int kMapSlotBytes = 256; // one A and one B tensor map
 // barriers for up to 8 stages, the TMEM slot, the abort flag and the tile ring
 static_assert(8 * (2 * 8 + 5 + 2 * kSchedDepth) + 8 + 4 * kSchedDepth <= kMapScratch,
               "control block overlaps the tensor-map scratch");
+static_assert(kMapBars + 16 * kMapSlots <= kCtrlBytes, "map-slot barriers overflow");
 
 template <int BN, bool GATHER, int CG>
 struct KernelCfg {
@@ -75,7 +80,9 @@ struct KernelCfg {
   static constexpr int kEpiWarps = GATHER ? 4 : 8;
   static constexpr int kMmaWarp = kEpiWarps;
   static constexpr int kLoadWarp = kEpiWarps + 1;
-  static constexpr int kWarps = GATHER ? kLoadWarp + kGatherWarps : kLoadWarp + 1;
+  // TMA forms: one more warp writes the varlen-K tensor maps ahead of the producer
+  static constexpr int kMapWarp = kLoadWarp + 1;
+  static constexpr int kWarps = GATHER ? kLoadWarp + kGatherWarps : kLoadWarp + 2;
   static constexpr int kThreads = kWarps * 32;
   // two accumulator buffers of BN columns; the allocation is the next power of two
   static constexpr int kTmemCols = (2 * BN <= 128) ? 128 : (2 * BN <= 256) ? 256 : 512;
@@ -106,6 +113,7 @@ struct TileCoord {
 
 struct Shared {
   uint32_t full, empty, tfull, tempty;  // barrier array bases (shared addresses)
+  uint32_t map_full, map_empty;         // varlen-K map-slot barriers (kMapSlots each)
   volatile int32_t* abort;
   const int32_t* prefix;  // varlen-M: tile prefix [G+1]; varlen-K: group K ends [G]
   const int32_t* cu;      // varlen-M: cu_seqlens copy [G+1]; varlen-K: group K starts [G]
@@ -639,6 +647,11 @@ __device__ __forceinline__ void tma_load(uint32_t dst, const CUtensorMap* m, uin
   else ptx::tma_load_3d_pair(dst, m, bar, x, y, z);
 }
 
+// This CTA's tensor-map slot `slot` in the workspace.
+__device__ __forceinline__ uint8_t* kmap_slot(const Params& p, int slot) {
+  return p.kmaps + (static_cast<int64_t>(blockIdx.x) * kMapSlots + slot) * kMapSlotBytes;
+}
+
 // Varlen-K: write a copy of the A and B tensor maps whose K extent ends at the
 // group's last column into this CTA's map slot `slot` (the pages'
 // update_tensormap_shape), so that the group's last k-tile reads zeros past
@@ -647,7 +660,7 @@ __device__ __forceinline__ const uint8_t* publish_kmaps(const Params& p, const C
                                                         const CUtensorMap* tmB, uint32_t scratch,
                                                         int slot, int32_t k_end) {
   const int lane = threadIdx.x & 31;
-  uint8_t* dst = p.kmaps + (static_cast<int64_t>(blockIdx.x) * kMapSlots + slot) * kMapSlotBytes;
+  uint8_t* dst = kmap_slot(p, slot);
   ptx::st_shared_u32(scratch + 4 * lane, reinterpret_cast<const uint32_t*>(tmA)[lane]);
   ptx::st_shared_u32(scratch + 128 + 4 * lane, reinterpret_cast<const uint32_t*>(tmB)[lane]);
   __syncwarp();
@@ -678,8 +691,9 @@ __device__ __forceinline__ void tma_producer_role(const Params& p, const Shared&
   uint32_t phase = 0;
   // varlen-K: the group whose maps are in use, and the slot they occupy
   int32_t map_group = -1;
-  int map_slot = kMapSlots - 1;
+  uint32_t maps_used = 0;
   const uint8_t* map_cur = nullptr;
+  const bool map_helper = !ts.dyn;  // the map warp walks the static schedule only
   const CUtensorMap* mA = tmA;
   const CUtensorMap* mB = tmB;
   for (int i = 0;; ++i) {
@@ -695,11 +709,26 @@ __device__ __forceinline__ void tma_producer_role(const Params& p, const Shared&
       if (!__all_sync(0xffffffffu, ok)) return;
       if (kt == 0) {
         if (kr.ragged && tc.batch != map_group) {
-          // A slot is rewritten kMapSlots (>= stages) group changes after its last
-          // use; every group issues at least one k-tile, and the wait above has
-          // seen the k-tile `stages` back consumed, so no copy still reads it.
-          map_slot = (map_slot + 1 == kMapSlots) ? 0 : map_slot + 1;
-          map_cur = publish_kmaps(p, tmA, tmB, map_scratch, map_slot, kr.k_end);
+          // The w-th ragged group reads slot w % kMapSlots.  A slot is rewritten only
+          // after the group `stages` later has passed the wait above: every ragged
+          // group issues at least one k-tile, and that wait has seen the k-tile
+          // `stages` back consumed, so no copy still reads the old maps.
+          const int slot = static_cast<int>(maps_used % kMapSlots);
+          if (map_helper) {
+            // the map warp wrote this slot ahead of time
+            const uint32_t par = (maps_used / kMapSlots) & 1u;
+            if (!__all_sync(0xffffffffu, wait_phase(sh.map_full + 8 * slot, par, p, sh, 10, t)))
+              return;
+            map_cur = kmap_slot(p, slot);
+            ptx::tmap_acquire(map_cur);
+            ptx::tmap_acquire(map_cur + 128);
+            if (maps_used >= static_cast<uint32_t>(p.stages) && ptx::elect_one())
+              ptx::mbar_arrive(sh.map_empty + 8 * ((maps_used - p.stages) % kMapSlots));
+            __syncwarp();
+          } else {
+            map_cur = publish_kmaps(p, tmA, tmB, map_scratch, slot, kr.k_end);
+          }
+          ++maps_used;
           map_group = tc.batch;
         }
         // a ragged group reads through its clipped maps; any other range is cut by
@@ -735,6 +764,39 @@ __device__ __forceinline__ void tma_producer_role(const Params& p, const Shared&
       __syncwarp();
       if (++stage == p.stages) { stage = 0; phase ^= 1u; }
     }
+  }
+}
+
+// Varlen-K with the static schedule: walk this CTA's tiles ahead of the
+// producer and write the clipped tensor maps of each ragged group into the
+// next slot, so that the fences of the rewrite stay off the producer's path.
+// It may run kMapSlots - stages groups ahead; the producer hands each slot back.
+template <int BN, int CG>
+__device__ __forceinline__ void map_warp_role(const Params& p, const Shared& sh,
+                                              const CUtensorMap* tmA, const CUtensorMap* tmB,
+                                              uint32_t scratch, int32_t num_tiles,
+                                              const TileSched& ts) {
+  using Cfg = KernelCfg<BN, false, CG>;
+  if (p.k_groups == 0 || ts.dyn) return;
+  int32_t last = -1;
+  uint32_t n = 0;
+  for (int i = 0;; ++i) {
+    const int32_t t = ts.unit + i * ts.units;
+    if (t >= num_tiles) break;
+    const TileCoord tc = tile_coord<BN, Cfg::kTileM>(t, p, sh);
+    const KRange kr = k_range(p, sh, tc.batch);
+    if (!kr.ragged || tc.batch == last) continue;
+    const int slot = static_cast<int>(n % kMapSlots);
+    if (n >= static_cast<uint32_t>(kMapSlots)) {
+      const uint32_t par = ((n / kMapSlots) - 1u) & 1u;
+      if (!__all_sync(0xffffffffu, wait_phase(sh.map_empty + 8 * slot, par, p, sh, 9, t))) return;
+    }
+    publish_kmaps(p, tmA, tmB, scratch, slot, kr.k_end);
+    __syncwarp();
+    if (ptx::elect_one()) ptx::mbar_arrive(sh.map_full + 8 * slot);
+    __syncwarp();
+    last = tc.batch;
+    ++n;
   }
 }
 
@@ -823,6 +885,8 @@ __global__ void __launch_bounds__(KernelCfg<BN, GATHER, CG>::kThreads, 1)
   sh.empty = sh.full + 8 * S;
   sh.tfull = sh.empty + 8 * S;
   sh.tempty = sh.tfull + 16;
+  sh.map_full = ptx::smem_addr(ctrl + kMapBars);
+  sh.map_empty = sh.map_full + 8 * kMapSlots;
   const uint32_t drain_bar = sh.tempty + 16;  // MMAs in flight have finished
   TileSched ts;
   ts.unit = static_cast<int32_t>(blockIdx.x) / CG;
@@ -849,6 +913,10 @@ __global__ void __launch_bounds__(KernelCfg<BN, GATHER, CG>::kThreads, 1)
       ptx::mbar_init(sh.tempty + 8 * b, Cfg::kEpiWarps * CG);
     }
     ptx::mbar_init(drain_bar, 1);
+    for (int i = 0; i < kMapSlots; ++i) {
+      ptx::mbar_init(sh.map_full + 8 * i, 1);
+      ptx::mbar_init(sh.map_empty + 8 * i, 1);
+    }
     // ring slot consumers: the MMA warp, every epilogue warp (both CTAs of a pair),
     // the peer's producer (pair) or the other gather warps
     const uint32_t consumers = (CG == 2) ? 2 * Cfg::kEpiWarps + 2
@@ -934,9 +1002,11 @@ __global__ void __launch_bounds__(KernelCfg<BN, GATHER, CG>::kThreads, 1)
     if (rank == 0) mma_role<BN, GATHER, CG>(p, sh, a0, b0, tmem_base, num_tiles, ts);
   } else if (GATHER) {
     gather_producer_role<BN>(p, sh, &tmB, a0, b0, num_tiles, ts);
-  } else {
+  } else if (warp == Cfg::kLoadWarp) {
     tma_producer_role<BN, GATHER, CG>(p, sh, &tmA, &tmB, a0, b0,
                                       ptx::smem_addr(ctrl + kMapScratch), num_tiles, rank, ts);
+  } else {
+    map_warp_role<BN, CG>(p, sh, &tmA, &tmB, ptx::smem_addr(ctrl + kMapScratch), num_tiles, ts);
   }
 
   __syncthreads();

@@ -143,8 +143,8 @@ typedef struct gge_gemm_args {
 size_t gge_workspace_size(const gge_gemm_args* args, int32_t num_groups);
 
 /* Workspace bytes gge_gemm_varlen_k needs for these arguments on the current
- * device: the status words plus 2 KiB of tensor-map copies per CTA of the
- * launch (one CTA per SM at most: about 0.3 MiB on a 152-SM GPU).  Returns 0
+ * device: the status words plus 4 KiB of tensor-map copies per CTA of the
+ * launch (one CTA per SM at most: about 0.6 MiB on a 152-SM GPU).  Returns 0
  * if the arguments are invalid for gge_gemm_varlen_k. */
 size_t gge_workspace_size_varlen_k(const gge_gemm_args* args, int32_t num_groups);
 
