@@ -66,6 +66,8 @@ _SIGNATURES = {
                                   ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
     "gge_gemm_varlen_k": (c_i32, [ctypes.POINTER(GgeGemmArgs), ctypes.c_void_p, c_i32,
                                   ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
+    "gge_gemm_gather_k": (c_i32, [ctypes.POINTER(GgeGemmArgs), ctypes.c_void_p, ctypes.c_void_p,
+                                  c_i32, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
     "gge_gemm_gather_a": (c_i32, [ctypes.POINTER(GgeGemmArgs), ctypes.c_void_p, ctypes.c_void_p,
                                   c_i32, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
     "gge_gemm_dact": (c_i32, [ctypes.POINTER(GgeGemmArgs), ctypes.c_void_p, ctypes.c_size_t,
@@ -263,6 +265,23 @@ def gge_gemm_varlen_k(A, B, cu_seqlens_k, D=None, PostAct=None, act="none", C=No
            "gge_gemm_varlen_k")
 
 
+def gge_gemm_gather_k(A_src, B, a_idx, cu_seqlens_k, D=None, PostAct=None, act="none", C=None,
+                      alpha=1.0, beta=1.0, config=None):
+    """Gather-K: varlen-K GEMM whose A column k is A_src[:, a_idx[k]].  A_src (M, K_src)
+    M-major (e.g. X.t() of a row-major X [K_src, M]), B (N, total_K), a_idx int32
+    (total_K,), cu_seqlens_k int32 (G+1,); C / D / PostAct (G, M, N)."""
+    lib = load()
+    out = D if D is not None else PostAct
+    args = make_args(A_src, B, C=C, D=D, PostAct=PostAct, alpha=alpha, beta=beta, act=act,
+                     config=config)
+    ws = workspace(out.device)
+    G = cu_seqlens_k.numel() - 1
+    _check(lib.gge_gemm_gather_k(ctypes.byref(args), ctypes.c_void_p(a_idx.data_ptr()),
+                                 ctypes.c_void_p(cu_seqlens_k.data_ptr()), G,
+                                 ctypes.c_void_p(ws.data_ptr()), ws.numel(), _stream(out)),
+           "gge_gemm_gather_k")
+
+
 def gge_gemm_gather_a(A_src, B, a_idx, cu_seqlens_m=None, D=None, PostAct=None, act="none",
                       C=None, alpha=1.0, beta=1.0, config=None):
     """Gather-A GEMM: effective A row r = A_src[a_idx[r]]; varlen-M when cu_seqlens_m is given."""
@@ -287,7 +306,7 @@ def gge_read_device_status(device=None):
     return STATUS.get(code, str(code)), detail[0], detail[1]
 
 
-FORM = {"default": 0, "gather_a": 1, "varlen_k": 2}
+FORM = {"default": 0, "gather_a": 1, "varlen_k": 2, "gather_k": 3}
 
 
 def gge_plan(A, B, C=None, D=None, PostAct=None, act="none", num_groups=0, gather=False,

@@ -105,7 +105,7 @@ gge_status check_mn(const gge_tensor* t, int64_t M, int64_t N, int64_t L, bool i
   return GGE_OK;
 }
 
-enum class Form { Plain, Varlen, Gather, GatherVarlen, VarlenK };
+enum class Form { Plain, Varlen, Gather, GatherVarlen, VarlenK, GatherK };
 
 struct Plan {
   Params p;
@@ -301,8 +301,9 @@ gge_status make_plan(const gge_gemm_args* a, Form form, const int32_t* a_idx,
   Params& p = pl.p;
   const gge_config* cfg = a->config;
   const bool varlen = (form == Form::Varlen || form == Form::GatherVarlen);
-  const bool gather = (form == Form::Gather || form == Form::GatherVarlen);
-  const bool vk = (form == Form::VarlenK);
+  const bool gk = (form == Form::GatherK);  // varlen-K with A gathered along K
+  const bool gather = (form == Form::Gather || form == Form::GatherVarlen || gk);
+  const bool vk = (form == Form::VarlenK || gk);
   pl.gather = gather;
 
   if (a->act < GGE_ACT_NONE || a->act > GGE_ACT_RELU_SQ) return GGE_ERR_INVALID_ARG;
@@ -332,7 +333,8 @@ gge_status make_plan(const gge_gemm_args* a, Form form, const int32_t* a_idx,
   // shapes from the output
   const gge_tensor* o = a->D ? a->D : a->PostAct;
   const int64_t M = o->rows, N = o->cols, L = o->batch;
-  const int64_t K = a->A.cols;
+  // gather-K: A is the source X^T [M, K_src]; the contraction runs over B's columns
+  const int64_t K = gk ? a->B.cols : a->A.cols;
   if (M < 0 || N < 0 || K < 0) return GGE_ERR_INVALID_ARG;
   if (a->D) { s = check_mn(a->D, M, N, L, true); if (s != GGE_OK) return s; }
   if (a->PostAct) { s = check_mn(a->PostAct, M, N, L, true); if (s != GGE_OK) return s; }
@@ -343,8 +345,21 @@ gge_status make_plan(const gge_gemm_args* a, Form form, const int32_t* a_idx,
   // K- or N-major (16-bit).  With K == 0 neither is read.
   bool a_mn = false, b_mn = false;
   if (a->B.rows != N || a->B.cols != K) return GGE_ERR_INVALID_ARG;
+  if (gk) {
+    // the source [M, K_src, 1]: M-major 16-bit, read in 16-byte pieces of 8 rows of M
+    if (f8) return GGE_ERR_UNSUPPORTED;
+    if (a->A.rows != M || a->A.batch != 1) return GGE_ERR_INVALID_ARG;
+    if (M % 8 != 0) return GGE_ERR_UNSUPPORTED;
+    if (K > 0 && a->A.cols < 1) return GGE_ERR_INVALID_ARG;
+    if (M > 1 && a->A.stride_row != 1) return GGE_ERR_UNSUPPORTED;
+    if (a->A.cols > 1 && a->A.stride_col < M) return GGE_ERR_INVALID_ARG;
+    if ((a->A.stride_col * es) % 16 != 0) return GGE_ERR_ALIGNMENT;
+    a_mn = true;
+  }
   if (K > 0) {
-    if (K == 1 || a->A.stride_col == 1) {
+    if (gk) {
+      // checked above
+    } else if (K == 1 || a->A.stride_col == 1) {
       if (a->A.rows > 1 && a->A.stride_row < K) return GGE_ERR_INVALID_ARG;
       if ((a->A.stride_row * es) % 16 != 0) return GGE_ERR_ALIGNMENT;
     } else if (a->A.stride_row == 1 && !gather) {
@@ -389,7 +404,7 @@ gge_status make_plan(const gge_gemm_args* a, Form form, const int32_t* a_idx,
   if (gather) {
     if (a_idx == nullptr) return GGE_ERR_INVALID_ARG;
     if (a->A.batch != 1) return GGE_ERR_INVALID_ARG;
-    if ((K * es) % 16 != 0) return GGE_ERR_UNSUPPORTED;  // whole 16-byte chunks along K
+    if (!gk && (K * es) % 16 != 0) return GGE_ERR_UNSUPPORTED;  // whole 16-byte chunks along K
   }
 
   // tile shape: 128 x BN on one CTA, or 256 x BN on a CTA pair
@@ -459,7 +474,8 @@ gge_status make_plan(const gge_gemm_args* a, Form form, const int32_t* a_idx,
     if (vk) {
       p.k_groups = G;
       p.cu_seqlens_k = cu;
-      // a K-major operand's TMA boxes start on 16-byte boundaries of its rows
+      // a K-major operand's TMA boxes (and gather-K's B copies) start on 16-byte
+      // boundaries of its rows; gather-K's A is always M-major
       p.k_align = (a_mn && b_mn) ? 1 : 16 / es;
     }
   } else {
@@ -473,10 +489,17 @@ gge_status make_plan(const gge_gemm_args* a, Form form, const int32_t* a_idx,
   if (gather) {
     p.a_idx = a_idx;
     p.a_src = static_cast<const uint8_t*>(a->A.ptr);
-    p.a_src_ld = a->A.stride_row * es;
-    p.a_src_rows = static_cast<int32_t>(a->A.rows);
-    p.k_bytes = static_cast<int32_t>(K * es);
+    if (gk) {  // index k selects column a_idx[k] of the source: a contiguous M vector
+      p.a_src_ld = a->A.stride_col * es;
+      p.a_src_rows = static_cast<int32_t>(a->A.cols);
+    } else {
+      p.a_src_ld = a->A.stride_row * es;
+      p.a_src_rows = static_cast<int32_t>(a->A.rows);
+      p.k_bytes = static_cast<int32_t>(K * es);
+    }
   }
+  p.b_src = static_cast<const uint8_t*>(a->B.ptr);
+  p.b_ld = (b_mn ? a->B.stride_col : a->B.stride_row) * es;
   // epilogue
   if (a->D) {
     p.d = a->D->ptr; p.ldd = a->D->stride_row; p.sbd = a->D->stride_batch; p.d_dtype = a->D->dtype;
@@ -640,6 +663,13 @@ gge_status gge_gemm_varlen_k(const gge_gemm_args* args, const int32_t* cu_seqlen
                   ws_bytes, stream);
 }
 
+gge_status gge_gemm_gather_k(const gge_gemm_args* args, const int32_t* a_idx,
+                             const int32_t* cu_seqlens_k, int32_t num_groups, void* ws,
+                             size_t ws_bytes, gge_stream_t stream) {
+  return gge::run(args, Form::GatherK, a_idx, cu_seqlens_k, num_groups, true, false, ws, ws_bytes,
+                  stream);
+}
+
 gge_status gge_read_device_status(void* ws, gge_stream_t stream, int32_t* detail) {
   if (ws == nullptr) return GGE_ERR_WORKSPACE;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
@@ -699,14 +729,15 @@ int32_t gge_schedule_map(int32_t tiles_m, int32_t tiles_n, int32_t batches, int3
 gge_status gge_plan(const gge_gemm_args* args, int32_t num_groups, int32_t form,
                     gge_plan_info* out) {
   if (out == nullptr) return GGE_ERR_INVALID_ARG;
-  if (form != GGE_FORM_DEFAULT && form != GGE_FORM_GATHER_A && form != GGE_FORM_VARLEN_K)
+  if (form != GGE_FORM_DEFAULT && form != GGE_FORM_GATHER_A && form != GGE_FORM_VARLEN_K &&
+      form != GGE_FORM_GATHER_K)
     return GGE_ERR_INVALID_ARG;
   gge::Plan pl;
-  const bool gather = form == GGE_FORM_GATHER_A;
-  const Form f = form == GGE_FORM_VARLEN_K
-                     ? Form::VarlenK
-                     : gather ? (num_groups > 0 ? Form::GatherVarlen : Form::Gather)
-                              : (num_groups > 0 ? Form::Varlen : Form::Plain);
+  const bool gather = form == GGE_FORM_GATHER_A || form == GGE_FORM_GATHER_K;
+  const Form f = form == GGE_FORM_VARLEN_K  ? Form::VarlenK
+                 : form == GGE_FORM_GATHER_K ? Form::GatherK
+                 : gather ? (num_groups > 0 ? Form::GatherVarlen : Form::Gather)
+                          : (num_groups > 0 ? Form::Varlen : Form::Plain);
   // a dummy non-null index pointer lets the shape checks run
   static const int32_t dummy = 0;
   const gge_status s = gge::make_plan(args, f, gather ? &dummy : nullptr,

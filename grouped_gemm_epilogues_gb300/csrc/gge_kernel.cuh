@@ -800,6 +800,125 @@ __device__ __forceinline__ void map_warp_role(const Params& p, const Shared& sh,
   }
 }
 
+// B of a one-CTA tile by TMA: one box (K-major) or BN/64 boxes of 64 columns (N-major).
+template <int BN>
+__device__ __forceinline__ void load_b_1cta(const Params& p, const CUtensorMap* tmB, uint32_t dst,
+                                            uint32_t bar, int32_t k0, int32_t n0, int32_t batch) {
+  if (!p.b_mn_major) {
+    ptx::tma_load_3d(dst, tmB, bar, k0, n0, batch);
+  } else {
+#pragma unroll
+    for (int j = 0; j < BN / 64; ++j)
+      ptx::tma_load_3d(dst + j * (64 * kRowBytes), tmB, bar, n0 + 64 * j, k0, batch);
+  }
+}
+
+// B of a one-CTA tile by 16-byte cp.async that reads nothing at or past column
+// k_end (the rest of each copy is zero-filled): a ragged varlen-K group's last
+// k-tile without a clipped tensor map.  Same swizzled layouts as the TMA boxes.
+// 128 threads; gt = this thread's index among them.
+template <int BN>
+__device__ __forceinline__ void copy_b_clipped(const Params& p, uint32_t dst, int32_t kbase,
+                                               int32_t k_end, int32_t n0, int gt) {
+  const int q = gt & 7;  // 16-byte piece of a 128-byte row
+  const int sub = gt >> 3;
+  if (!p.b_mn_major) {
+    // rows n hold 64 K elements; piece q holds K elements kbase + 8q .. +7
+    const int32_t kel = kbase + 8 * q;
+    const int32_t kbytes = max(0, min(16, 2 * (k_end - kel)));
+#pragma unroll
+    for (int i = 0; i < BN / 16; ++i) {
+      const int n = sub + 16 * i;
+      const uint32_t bytes = (n0 + n < p.N) ? static_cast<uint32_t>(kbytes) : 0u;
+      const uint8_t* src =
+          bytes ? p.b_src + static_cast<int64_t>(n0 + n) * p.b_ld + 2 * static_cast<int64_t>(kel)
+                : p.b_src;
+      ptx::cp_async_16(dst + n * kRowBytes + ((q ^ (n & 7)) << 4), src, bytes);
+    }
+  } else {
+    // 64-column chunks of bk K rows; piece q holds columns 8q .. 8q+7 of the chunk
+#pragma unroll
+    for (int j = 0; j < BN / 64; ++j) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int k = sub + 16 * i;
+        const int32_t nel = n0 + 64 * j + 8 * q;
+        const uint32_t bytes = (kbase + k < k_end && nel < p.N) ? 16u : 0u;
+        const uint8_t* src =
+            bytes ? p.b_src + static_cast<int64_t>(kbase + k) * p.b_ld + 2 * static_cast<int64_t>(nel)
+                  : p.b_src;
+        ptx::cp_async_16(dst + j * (64 * kRowBytes) + k * kRowBytes + ((q ^ (k & 7)) << 4), src,
+                         bytes);
+      }
+    }
+  }
+}
+
+// Gather-K (varlen-K with A gathered along K, the pages' gather_k copy): row k
+// of the k-tile's effective A^T is row a_idx[k] of the source X (M contiguous
+// 16-bit elements), staged M-major: 64-element chunks of bk K rows, 128-byte
+// swizzle.  Thread gt copies 16-byte piece gt % 16 of the tile's 256-byte M
+// segment for K rows gt / 16 + 8 i.  B comes by TMA, or for a ragged group by
+// copies that stop at the group's end.  A K row past the group's end, an M
+// element past M, or an index out of range reads zeros (the last is reported).
+template <int BN>
+__device__ __forceinline__ void gather_k_producer_role(const Params& p, const Shared& sh,
+                                                       const CUtensorMap* tmB, uint32_t a0,
+                                                       uint32_t b0, int32_t num_tiles,
+                                                       const TileSched& ts) {
+  using Cfg = KernelCfg<BN, true, 1>;
+  const int gt = threadIdx.x - Cfg::kLoadWarp * 32;  // 0..127
+  const int q = gt & 15;
+  const int ksub = gt >> 4;
+  const uint32_t a_off = static_cast<uint32_t>(q >> 3) * (64 * kRowBytes);  // M chunk
+  int stage = 0;
+  uint32_t phase = 0;
+  for (int i = 0;; ++i) {
+    const int32_t t = (gt < 32) ? sched_fetch<1>(ts, i, p, sh) : sched_next<1>(ts, i, p, sh);
+    if (t >= num_tiles) break;
+    const TileCoord tc = tile_coord<BN, kBM>(t, p, sh);
+    const KRange kr = k_range(p, sh, tc.batch);
+    const int32_t m_el = tc.m_row0 + 8 * q;
+    const bool m_ok = m_el < p.M;  // M is a multiple of 8: whole pieces
+    for (int kt = 0; kt < kr.tiles; ++kt) {
+      if (!wait_phase(sh.empty + 8 * stage, phase ^ 1u, p, sh, 0, t)) return;
+      const uint32_t full = sh.full + 8 * stage;
+      const int32_t kbase = kr.k0 + kt * p.bk;
+      const uint32_t abase = a0 + stage * Cfg::kABytes;
+      const uint32_t bbase = b0 + stage * Cfg::kBBytes;
+      if (!kr.ragged) {
+        if (gt < 32 && ptx::elect_one()) {
+          ptx::mbar_arrive_expect_tx(full, Cfg::kBBytes);
+          load_b_1cta<BN>(p, tmB, bbase, full, kbase, tc.n0, 0);
+        }
+      } else {
+        if (gt < 32 && ptx::elect_one()) ptx::mbar_arrive(full);
+        copy_b_clipped<BN>(p, bbase, kbase, kr.k_end, tc.n0, gt);
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int k = ksub + 8 * j;
+        const int32_t kg = kbase + k;
+        int32_t src = -1;
+        if (m_ok && kg < kr.k_end) {
+          src = __ldg(p.a_idx + kg);
+          if (src < 0 || src >= p.a_src_rows) {
+            record_status(p, DEV_INDEX_RANGE, 4, t);
+            src = -1;
+          }
+        }
+        const uint8_t* sp =
+            src >= 0 ? p.a_src + static_cast<int64_t>(src) * p.a_src_ld + 2 * static_cast<int64_t>(m_el)
+                     : p.a_src;
+        ptx::cp_async_16(abase + a_off + k * kRowBytes + (((q & 7) ^ (k & 7)) << 4), sp,
+                         src >= 0 ? 16u : 0u);
+      }
+      ptx::cp_async_mbar_arrive_noinc(full);
+      if (++stage == p.stages) { stage = 0; phase ^= 1u; }
+    }
+  }
+}
+
 // Four warps: 8 threads per 128-byte A row, 16 rows per pass, 8 passes.
 template <int BN>
 __device__ __forceinline__ void gather_producer_role(const Params& p, const Shared& sh,
@@ -807,6 +926,10 @@ __device__ __forceinline__ void gather_producer_role(const Params& p, const Shar
                                                      uint32_t b0, int32_t num_tiles,
                                                      const TileSched& ts) {
   using Cfg = KernelCfg<BN, true, 1>;
+  if (p.k_groups > 0) {
+    gather_k_producer_role<BN>(p, sh, tmB, a0, b0, num_tiles, ts);
+    return;
+  }
   const int gt = threadIdx.x - Cfg::kLoadWarp * 32;  // 0..127
   const int chunk = gt & 7;
   const int rsub = gt >> 3;
@@ -838,7 +961,7 @@ __device__ __forceinline__ void gather_producer_role(const Params& p, const Shar
       const uint32_t full = sh.full + 8 * stage;
       if (gt < 32 && ptx::elect_one()) {  // one lane of the first gather warp: B by TMA
         ptx::mbar_arrive_expect_tx(full, Cfg::kBBytes);
-        ptx::tma_load_3d(b0 + stage * Cfg::kBBytes, tmB, full, kt * p.bk, tc.n0, tc.b_batch);
+        load_b_1cta<BN>(p, tmB, b0 + stage * Cfg::kBBytes, full, kt * p.bk, tc.n0, tc.b_batch);
       }
       const int32_t kbyte = kt * kRowBytes + chunk * 16;
       const uint32_t kvalid = (kbyte < p.k_bytes) ? 16u : 0u;

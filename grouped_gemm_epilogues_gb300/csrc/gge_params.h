@@ -48,12 +48,14 @@ struct Params {
   const int32_t* cu_seqlens_k;
   int32_t k_align;             // group starts must be multiples of this (K-major operands)
   uint8_t* kmaps;              // workspace: per CTA, kMapSlots pairs of 128-byte A / B tensor maps
+  const uint8_t* b_src;        // B's storage (gather-K copies a ragged group's B rows)
+  int64_t b_ld;                // bytes between B's storage rows
 
-  // gather-A
-  const int32_t* a_idx;   // [L][M] (plain) or [total_M] (varlen)
+  // gather-A (rows along M) and gather-K (rows of X along K)
+  const int32_t* a_idx;   // [L][M] (plain), [total_M] (varlen-M) or [total_K] (gather-K)
   const uint8_t* a_src;   // source matrix base
   int64_t a_src_ld;       // bytes between source rows
-  int32_t a_src_rows;
+  int32_t a_src_rows;     // valid index range
   int32_t k_bytes;        // K * element size (gather K-tail predicate)
 
   // epilogue

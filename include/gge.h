@@ -202,6 +202,21 @@ gge_status gge_gemm_varlen_k(const gge_gemm_args* args, const int32_t* cu_seqlen
                              int32_t num_groups, void* workspace, size_t workspace_bytes,
                              gge_stream_t stream);
 
+/* Gather-K: the varlen-K GEMM above whose A is gathered along K.  args->A is
+ * the SOURCE [M, K_src, 1], M-major (stride_row == 1; the usual storage of
+ * X [K_src, M] row-major), 16-bit, M a multiple of 8; a_idx is DEVICE int32
+ * [total_K] with total_K = columns of B.  Column k of the effective A is
+ * column a_idx[k] of the source; B [N, total_K] is read at column k itself.
+ * Group rules as in gge_gemm_varlen_k (with a K-major B, non-empty groups
+ * start on multiples of 8); an index outside [0, K_src) reads zeros and is
+ * reported as GGE_ERR_INDEX_RANGE.  One CTA per 128 x BN tile; needs only
+ * gge_workspace_size bytes of workspace.  Page: quack/dense_gemm_sm90.py,
+ * GemmSm90 with gather_A and VarlenArguments(mCuSeqlensK)
+ * (copy_utils.gather_k_get_copy_fn). */
+gge_status gge_gemm_gather_k(const gge_gemm_args* args, const int32_t* a_idx,
+                             const int32_t* cu_seqlens_k, int32_t num_groups, void* workspace,
+                             size_t workspace_bytes, gge_stream_t stream);
+
 /* Gather-A GEMM: row r of the effective A is row a_idx[r] of the source
  * matrix args->A ([rows_src, K, 1], K-major, 16-bit).  With cu_seqlens_m
  * (DEVICE int32 [G+1]) it is the varlen-M problem above, a_idx being
@@ -257,9 +272,9 @@ int32_t gge_schedule_map(int32_t tiles_m, int32_t tiles_n, int32_t batches, int3
 
 /* The launch plan the library would use for `args` (tile and pipeline
  * shape).  form: GGE_FORM_DEFAULT (plain, or varlen-M when num_groups > 0),
- * GGE_FORM_GATHER_A or GGE_FORM_VARLEN_K.  Returns GGE_OK or the validation
+ * GGE_FORM_GATHER_A, GGE_FORM_VARLEN_K or GGE_FORM_GATHER_K.  Returns GGE_OK or the validation
  * error of the call. */
-enum { GGE_FORM_DEFAULT = 0, GGE_FORM_GATHER_A = 1, GGE_FORM_VARLEN_K = 2 };
+enum { GGE_FORM_DEFAULT = 0, GGE_FORM_GATHER_A = 1, GGE_FORM_VARLEN_K = 2, GGE_FORM_GATHER_K = 3 };
 typedef struct gge_plan_info {
   int32_t tile_m, tile_n, tile_k, stages;  /* tile_m: rows per (pair) tile */
   int32_t num_tiles;  /* plain and varlen-K problems; -1 for varlen-M (known on

@@ -174,3 +174,109 @@ def test_varlen_k_full_size_sampled():
     got = dec(D[:, rows].cpu())
     check(got, ref["D"], ref["bound"], FMT_NAME[w.d_dtype], "none", "sampled rows")
     assert binding.gge_read_device_status()[0] == "GGE_OK"
+
+
+# ------------------------------------------------------------------ gather-K
+
+def _gather_k_operands(M, N, total_k, k_src, b_major, seed, G, dtype="bf16", with_c=True):
+    gen = torch.Generator().manual_seed(seed)
+
+    def draw(shape, dt):
+        return (torch.rand(shape, generator=gen, dtype=torch.float32) * 2 - 1).to(wl.DT[dt])
+
+    X = draw((k_src, M), dtype)                   # rows of X are the K columns of A_src
+    A_src = X.t()                                 # [M, K_src], M-major
+    B = draw((total_k, N), dtype).t() if b_major == "n" else draw((N, total_k), dtype)
+    idx = torch.randint(0, k_src, (total_k,), generator=gen, dtype=torch.int32)
+    C = draw((G, M, N), "bf16") if with_c else None
+    return A_src, B, idx, C
+
+
+def _run_gather_k(A_src, B, idx, cu, C, G, d_dtype="bf16", p_dtype=None, act="none", alpha=1.0,
+                  beta=0.0, config=None):
+    M, N = A_src.shape[0], B.shape[0]
+    D = torch.full((G, M, N), -3.0, dtype=wl.DT[d_dtype], device=DEV) if d_dtype else None
+    P = torch.full((G, M, N), -3.0, dtype=wl.DT[p_dtype], device=DEV) if p_dtype else None
+    binding.gge_gemm_gather_k(A_src.to(DEV), B.to(DEV), idx.to(DEV),
+                              torch.as_tensor(cu, dtype=torch.int32).to(DEV), D=D, PostAct=P,
+                              act=act, C=None if C is None else C.to(DEV), alpha=alpha, beta=beta,
+                              config=config)
+    torch.cuda.synchronize()
+    return D, P
+
+
+def _oracle_gather_k(A_src, idx, B, cu, C, d_dtype, p_dtype, act, alpha, beta):
+    return og.gemm_gather_k(dec(A_src), idx.numpy(), dec(B), np.asarray(cu),
+                            None if C is None else dec(C), alpha=alpha, beta=beta, act=act,
+                            d_fmt=FMT_NAME[d_dtype],
+                            p_fmt=FMT_NAME[p_dtype] if act != "none" else None)
+
+
+@pytest.mark.parametrize("b_major,cu,tile_n", [
+    ("n", CU_ANY, 256),
+    ("n", CU_ANY, 128),
+    ("k", [0, 48, 48, 160, 176, 400, 736, 736, 944, 989], 256),   # K-major B: starts on 8s
+], ids=["bN-any-256", "bN-any-128", "bK-8s-256"])
+def test_gather_k_parity(b_major, cu, tile_n):
+    G = len(cu) - 1
+    A_src, B, idx, C = _gather_k_operands(328, 264, 1000, 700, b_major, seed=21, G=G)
+    cfg = binding.make_config(tile_n=tile_n)
+    D, P = _run_gather_k(A_src, B, idx, cu, C, G, "bf16", "bf16", "relu", alpha=0.75, beta=0.5,
+                         config=cfg)
+    ref = _oracle_gather_k(A_src, idx, B, cu, C, "bf16", "bf16", "relu", 0.75, 0.5)
+    _check_all(D, P, ref, "bf16", "bf16", "relu")
+    assert binding.gge_read_device_status()[0] == "GGE_OK"
+
+
+def test_gather_k_f16_gelu_f32_out():
+    cu = [0, 64, 200, 201, 520]          # aligned and ragged groups, N-major B
+    A_src, B, idx, _ = _gather_k_operands(256, 384, 520, 300, "n", seed=22, G=4, dtype="f16",
+                                          with_c=False)
+    D, P = _run_gather_k(A_src, B, idx, cu, None, 4, "f32", "f16", "gelu_tanh", alpha=1.25)
+    ref = _oracle_gather_k(A_src, idx, B, cu, None, "f32", "f16", "gelu_tanh", 1.25, 0.0)
+    _check_all(D, P, ref, "f32", "f16", "gelu_tanh")
+
+
+def test_gather_k_many_groups_one_cta_and_dynamic():
+    rng = np.random.default_rng(4)
+    G = 120
+    lens = rng.integers(0, 150, size=G)
+    cu = np.concatenate([[0], np.cumsum(lens)])
+    total = int(cu[-1]) + 3
+    A_src, B, idx, C = _gather_k_operands(128, 256, total, 4096, "n", seed=23, G=G)
+    ref = _oracle_gather_k(A_src, idx, B, cu, C, "bf16", None, "none", 1.0, 1.0)
+    for cfg in (binding.make_config(num_ctas=1), binding.make_config(num_ctas=3, flags=4)):
+        D, _ = _run_gather_k(A_src, B, idx, cu, C, G, "bf16", alpha=1.0, beta=1.0, config=cfg)
+        _check_all(D, None, ref, "bf16", None, "none")
+    assert binding.gge_read_device_status()[0] == "GGE_OK"
+
+
+def test_gather_k_bad_index_reads_zeros():
+    cu = [0, 100, 300]
+    A_src, B, idx, _ = _gather_k_operands(256, 256, 300, 500, "n", seed=24, G=2, with_c=False)
+    idx[[5, 150, 299]] = torch.tensor([500, -1, 10**6], dtype=torch.int32)
+    D, _ = _run_gather_k(A_src, B, idx, cu, None, 2, "bf16")
+    status, where, _ = binding.gge_read_device_status()
+    assert status == "GGE_ERR_INDEX_RANGE" and where == 4
+    # expected: those K columns contribute nothing (a zero column appended to the source)
+    A_pad = torch.cat([A_src, torch.zeros(256, 1, dtype=A_src.dtype)], dim=1)
+    idx_ok = idx.clone()
+    idx_ok[[5, 150, 299]] = 500
+    ref = _oracle_gather_k(A_pad, idx_ok, B, cu, None, "bf16", None, "none", 1.0, 0.0)
+    _check_all(D, None, ref, "bf16", None, "none")
+
+
+def test_gather_a_with_n_major_b():
+    # the row gather (varlen-M) with B N-major, loaded by 64-column boxes
+    gen = torch.Generator().manual_seed(25)
+    src = (torch.rand((900, 256), generator=gen) * 2 - 1).to(torch.bfloat16)
+    B = (torch.rand((3, 256, 384), generator=gen) * 2 - 1).to(torch.bfloat16).transpose(1, 2)
+    cu = torch.tensor([0, 100, 100, 700], dtype=torch.int32)
+    idx = torch.randint(0, 900, (700,), generator=gen, dtype=torch.int32)
+    for tile_n in (128, 256):
+        D = torch.full((700, 384), -3.0, dtype=torch.bfloat16, device=DEV)
+        binding.gge_gemm_gather_a(src.to(DEV), B.to(DEV), idx.to(DEV), cu.to(DEV), D=D,
+                                  config=binding.make_config(tile_n=tile_n))
+        torch.cuda.synchronize()
+        ref = og.gemm_gather_a(dec(src), idx.numpy(), dec(B), cu.numpy(), d_fmt=FMT_NAME["bf16"])
+        check(dec(D.cpu()), ref["D"], ref["bound"], FMT_NAME["bf16"], "none", "gather-A N-major B")
