@@ -274,8 +274,8 @@ def gge_gemm_gather_k(A_src, B, a_idx, cu_seqlens_k, D=None, PostAct=None, act="
     out = D if D is not None else PostAct
     args = make_args(A_src, B, C=C, D=D, PostAct=PostAct, alpha=alpha, beta=beta, act=act,
                      config=config)
-    ws = workspace(out.device)
     G = cu_seqlens_k.numel() - 1
+    ws = workspace(out.device, lib.gge_workspace_size_varlen_k(ctypes.byref(args), G))
     _check(lib.gge_gemm_gather_k(ctypes.byref(args), ctypes.c_void_p(a_idx.data_ptr()),
                                  ctypes.c_void_p(cu_seqlens_k.data_ptr()), G,
                                  ctypes.c_void_p(ws.data_ptr()), ws.numel(), _stream(out)),

@@ -26,6 +26,7 @@ B[n,k,l], C/D/PostAct[m,n,l]):
   B kmajor (L, N, K) contiguous                -> K-major
   B nmajor (L, K, N) contiguous, used as .transpose(1, 2) -> N-major
   C/D/P    (L, M, N) contiguous                -> N-major
+  gather-K: the source X (rows, M) contiguous, used as .t() -> [M, rows] M-major
   varlen-K (weight-gradient form, per group g: D[g] = A[:, K_g] B[:, K_g]^T):
   A mmajor (total_K, M) contiguous, used as .t() -> [M, total_K] M-major
   A kmajor (M, total_K) contiguous                -> K-major
@@ -106,6 +107,12 @@ WORKLOADS = {
         a_major="m", b_major="n", d_dtype="bf16",
         description="varlen-K weight gradient of the varlen-M layer: 64 groups over 32768 "
                     "tokens, D[g] = dY_g^T X_g (1536 x 4096), A M-major, B N-major, bf16"),
+    "gather_k_g64_k32768_wgrad": Workload(
+        "gather_k_g64_k32768_wgrad", 4096, 1536, 32768, k_groups=64, empty_groups=4,
+        gather_rows=65536, a_major="m", b_major="n", d_dtype="bf16",
+        description="gather-K weight gradient of the varlen-gather layer: D[g] = "
+                    "X[idx[K_g]]^T dY[K_g] (4096 x 1536) over 32768 tokens in 64 groups, "
+                    "X 65536 x 4096 gathered by token, bf16"),
     "gemm_act_8192_bf16_gelu": Workload(
         "gemm_act_8192_bf16_gelu", 8192, 8192, 8192, act="gelu_tanh", d_dtype="bf16",
         p_dtype="bf16", description="8192^3 bf16 GEMM + gelu_tanh, writes D and PostAct"),
@@ -155,7 +162,9 @@ def make(w: Workload, device="cpu"):
     gen = torch.Generator().manual_seed(w.seed)
     out = {"workload": w}
     if w.k_groups:
-        if w.a_major == "m":
+        if w.gather_rows:      # the gather source X [rows, M], used as its M-major transpose
+            out["A"] = _draw(gen, (w.gather_rows, w.M), w.dist, 1.0, w.ab_dtype).t()
+        elif w.a_major == "m":
             out["A"] = _draw(gen, (w.K, w.M), w.dist, 1.0, w.ab_dtype).t()
         else:
             out["A"] = _draw(gen, (w.M, w.K), w.dist, 1.0, w.ab_dtype)
@@ -164,6 +173,10 @@ def make(w: Workload, device="cpu"):
         else:
             out["B"] = _draw(gen, (w.N, w.K), w.dist, w.b_scale, w.bdt)
         out["cu_seqlens_k"] = torch.from_numpy(k_group_offsets(w).astype(np.int32))
+        if w.gather_rows:
+            gi = torch.Generator().manual_seed(w.seed + 104729)
+            idx = torch.floor(torch.rand(w.K, generator=gi, dtype=torch.float64) * w.gather_rows)
+            out["a_idx"] = idx.to(torch.int32)
         if w.with_c:
             out["C"] = _draw(gen, (w.k_groups, w.M, w.N), "uniform", 1.0, w.d_dtype or w.p_dtype)
     elif w.groups:

@@ -142,10 +142,11 @@ typedef struct gge_gemm_args {
  * before first use.  It is reusable across calls on the same stream. */
 size_t gge_workspace_size(const gge_gemm_args* args, int32_t num_groups);
 
-/* Workspace bytes gge_gemm_varlen_k needs for these arguments on the current
- * device: the status words plus 4 KiB of tensor-map copies per CTA of the
- * launch (one CTA per SM at most: about 0.6 MiB on a 152-SM GPU).  Returns 0
- * if the arguments are invalid for gge_gemm_varlen_k. */
+/* Workspace bytes gge_gemm_varlen_k and gge_gemm_gather_k need on the current
+ * device: the status words plus 4 KiB of tensor-map copies for each CTA a
+ * launch can have (one per SM: about 0.6 MiB on a 152-SM GPU).  The arguments
+ * are not inspected (they may be NULL); returns 0 if the device cannot be
+ * queried. */
 size_t gge_workspace_size_varlen_k(const gge_gemm_args* args, int32_t num_groups);
 
 /* D = alpha A B^T + beta C (PostAct must be NULL and act NONE).
@@ -209,8 +210,9 @@ gge_status gge_gemm_varlen_k(const gge_gemm_args* args, const int32_t* cu_seqlen
  * column a_idx[k] of the source; B [N, total_K] is read at column k itself.
  * Group rules as in gge_gemm_varlen_k (with a K-major B, non-empty groups
  * start on multiples of 8); an index outside [0, K_src) reads zeros and is
- * reported as GGE_ERR_INDEX_RANGE.  One CTA per 128 x BN tile; needs only
- * gge_workspace_size bytes of workspace.  Page: quack/dense_gemm_sm90.py,
+ * reported as GGE_ERR_INDEX_RANGE.  The rows are fetched with TMA row
+ * gathers; the workspace (256-byte aligned) must hold
+ * gge_workspace_size_varlen_k bytes.  Page: quack/dense_gemm_sm90.py,
  * GemmSm90 with gather_A and VarlenArguments(mCuSeqlensK)
  * (copy_utils.gather_k_get_copy_fn). */
 gge_status gge_gemm_gather_k(const gge_gemm_args* args, const int32_t* a_idx,

@@ -220,7 +220,7 @@ def _oracle_gather_k(A_src, idx, B, cu, C, d_dtype, p_dtype, act, alpha, beta):
 def test_gather_k_parity(b_major, cu, tile_n):
     G = len(cu) - 1
     A_src, B, idx, C = _gather_k_operands(328, 264, 1000, 700, b_major, seed=21, G=G)
-    cfg = binding.make_config(tile_n=tile_n)
+    cfg = binding.make_config(tile_n=tile_n, cta_group=2 if tile_n == 256 else 1)
     D, P = _run_gather_k(A_src, B, idx, cu, C, G, "bf16", "bf16", "relu", alpha=0.75, beta=0.5,
                          config=cfg)
     ref = _oracle_gather_k(A_src, idx, B, cu, C, "bf16", "bf16", "relu", 0.75, 0.5)
@@ -245,7 +245,8 @@ def test_gather_k_many_groups_one_cta_and_dynamic():
     total = int(cu[-1]) + 3
     A_src, B, idx, C = _gather_k_operands(128, 256, total, 4096, "n", seed=23, G=G)
     ref = _oracle_gather_k(A_src, idx, B, cu, C, "bf16", None, "none", 1.0, 1.0)
-    for cfg in (binding.make_config(num_ctas=1), binding.make_config(num_ctas=3, flags=4)):
+    for cfg in (binding.make_config(num_ctas=1, cta_group=1), binding.make_config(num_ctas=2),
+                binding.make_config(num_ctas=4, flags=4)):
         D, _ = _run_gather_k(A_src, B, idx, cu, C, G, "bf16", alpha=1.0, beta=1.0, config=cfg)
         _check_all(D, None, ref, "bf16", None, "none")
     assert binding.gge_read_device_status()[0] == "GGE_OK"
@@ -273,10 +274,25 @@ def test_gather_a_with_n_major_b():
     B = (torch.rand((3, 256, 384), generator=gen) * 2 - 1).to(torch.bfloat16).transpose(1, 2)
     cu = torch.tensor([0, 100, 100, 700], dtype=torch.int32)
     idx = torch.randint(0, 900, (700,), generator=gen, dtype=torch.int32)
-    for tile_n in (128, 256):
+    for tile_n, cg in ((128, 1), (256, 1), (256, 2)):
         D = torch.full((700, 384), -3.0, dtype=torch.bfloat16, device=DEV)
         binding.gge_gemm_gather_a(src.to(DEV), B.to(DEV), idx.to(DEV), cu.to(DEV), D=D,
-                                  config=binding.make_config(tile_n=tile_n))
+                                  config=binding.make_config(tile_n=tile_n, cta_group=cg))
         torch.cuda.synchronize()
         ref = og.gemm_gather_a(dec(src), idx.numpy(), dec(B), cu.numpy(), d_fmt=FMT_NAME["bf16"])
         check(dec(D.cpu()), ref["D"], ref["bound"], FMT_NAME["bf16"], "none", "gather-A N-major B")
+
+
+@pytest.mark.slow
+def test_gather_k_full_size_sampled():
+    w = wl.WORKLOADS["gather_k_g64_k32768_wgrad"]
+    t = wl.make(w)
+    cu = t["cu_seqlens_k"].numpy()
+    D, _ = _run_gather_k(t["A"], t["B"], t["a_idx"], cu, None, w.k_groups, w.d_dtype)
+    rng = np.random.default_rng(3)
+    rows = np.unique(np.concatenate([rng.integers(0, w.M, 4), [0, w.M - 1]]))
+    ref = og.gemm_gather_k(dec(t["A"][rows]), t["a_idx"].numpy(), dec(t["B"]), cu,
+                           d_fmt=FMT_NAME[w.d_dtype])
+    check(dec(D[:, rows].cpu()), ref["D"], ref["bound"], FMT_NAME[w.d_dtype], "none",
+          "sampled rows")
+    assert binding.gge_read_device_status()[0] == "GGE_OK"
