@@ -129,10 +129,10 @@ struct TmapKey {
   void* ptr;
   uint64_t d0, d1, d2, s1, s2;
   uint32_t b0, b1;
-  int es, rank;
+  int es;
   bool operator==(const TmapKey& o) const {
     return ptr == o.ptr && d0 == o.d0 && d1 == o.d1 && d2 == o.d2 && s1 == o.s1 && s2 == o.s2 &&
-           b0 == o.b0 && b1 == o.b1 && es == o.es && rank == o.rank;
+           b0 == o.b0 && b1 == o.b1 && es == o.es;
   }
 };
 
@@ -150,12 +150,9 @@ TmapCache& tmap_cache() {
   return c;
 }
 
-// A 3-D map (rank 3), or with rank 2 a 2-D map over (d0, d1) for row gathers
-// (d2 and s2 unused).
-gge_status encode_tiled(CUtensorMap* m, void* ptr, int es, int rank, uint64_t d0, uint64_t d1,
-                        uint64_t d2, uint64_t s1_bytes, uint64_t s2_bytes, uint32_t b0,
-                        uint32_t b1) {
-  const TmapKey k{ptr, d0, d1, d2, s1_bytes, s2_bytes, b0, b1, es, rank};
+gge_status encode_3d(CUtensorMap* m, void* ptr, int es, uint64_t d0, uint64_t d1, uint64_t d2,
+                     uint64_t s1_bytes, uint64_t s2_bytes, uint32_t b0, uint32_t b1) {
+  const TmapKey k{ptr, d0, d1, d2, s1_bytes, s2_bytes, b0, b1, es};
   TmapCache& c = tmap_cache();
   {
     std::lock_guard<std::mutex> g(c.mu);
@@ -173,8 +170,7 @@ gge_status encode_tiled(CUtensorMap* m, void* ptr, int es, int rank, uint64_t d0
   const cuuint64_t strides[2] = {s1_bytes, s2_bytes};
   const cuuint32_t box[3] = {b0, b1, 1};
   const cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = fn(m, tmap_type(es), static_cast<cuuint32_t>(rank), ptr, dims, strides, box, estr,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE,
+  CUresult r = fn(m, tmap_type(es), 3, ptr, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return GGE_ERR_CUDA;
@@ -186,11 +182,6 @@ gge_status encode_tiled(CUtensorMap* m, void* ptr, int es, int rank, uint64_t d0
   c.map[victim] = *m;
   c.used[victim] = ++c.tick;
   return GGE_OK;
-}
-
-gge_status encode_3d(CUtensorMap* m, void* ptr, int es, uint64_t d0, uint64_t d1, uint64_t d2,
-                     uint64_t s1_bytes, uint64_t s2_bytes, uint32_t b0, uint32_t b1) {
-  return encode_tiled(m, ptr, es, 3, d0, d1, d2, s1_bytes, s2_bytes, b0, b1);
 }
 
 uint64_t batch_stride_bytes(const gge_tensor& t, int es) {
@@ -313,8 +304,7 @@ gge_status make_plan(const gge_gemm_args* a, Form form, const int32_t* a_idx,
   const bool gk = (form == Form::GatherK);  // varlen-K with A gathered along K
   const bool gather = (form == Form::Gather || form == Form::GatherVarlen || gk);
   const bool vk = (form == Form::VarlenK || gk);
-  // every form runs on the TMA kernels: gathers are TMA row gathers (tile::gather4)
-  pl.gather = false;
+  pl.gather = gather;
 
   if (a->act < GGE_ACT_NONE || a->act > GGE_ACT_RELU_SQ) return GGE_ERR_INVALID_ARG;
   if (dact) {
@@ -415,10 +405,12 @@ gge_status make_plan(const gge_gemm_args* a, Form form, const int32_t* a_idx,
     if (a_idx == nullptr) return GGE_ERR_INVALID_ARG;
     if (a->A.batch != 1) return GGE_ERR_INVALID_ARG;
     if (!gk && K > 0 && a->A.rows < 1) return GGE_ERR_INVALID_ARG;  // nothing to gather from
+    if (!gk && (K * es) % 16 != 0) return GGE_ERR_UNSUPPORTED;  // whole 16-byte chunks along K
   }
 
   // tile shape: 128 x BN on one CTA, or 256 x BN on a CTA pair
-  int cg = cfg && cfg->cta_group ? cfg->cta_group : ((N > 128 && M >= 256) ? 2 : 1);
+  int cg = cfg && cfg->cta_group ? cfg->cta_group : ((!gather && N > 128 && M >= 256) ? 2 : 1);
+  if (cg == 2 && gather) return GGE_ERR_UNSUPPORTED;
   if (cg != 1 && cg != 2) return GGE_ERR_UNSUPPORTED;
   int bn = cfg && cfg->tile_n ? cfg->tile_n : 0;
   if (cg == 1) {
@@ -450,7 +442,7 @@ gge_status make_plan(const gge_gemm_args* a, Form form, const int32_t* a_idx,
   const int bk = kRowBytesHost / es;
   const int stage_bytes = (kTileM + bn / cg) * kRowBytesHost;
   const int varlen_bytes = (varlen || vk) ? 2 * 4 * (kMaxGroupsHost + 1) : 0;
-  const int epi_warps = 8;
+  const int epi_warps = gather ? 4 : 8;
   const int fixed = 1024 + kCtrlBytesHost + varlen_bytes + epi_warps * kOutStageBytesHost;
   int stages = (kMaxSmemOptin - fixed) / stage_bytes;
   stages = std::min(stages, kMaxStages);
@@ -534,7 +526,6 @@ gge_status make_plan(const gge_gemm_args* a, Form form, const int32_t* a_idx,
             ((static_cast<uint32_t>(bn) >> 3) << 17) | ((static_cast<uint32_t>(tile_m) >> 4) << 24);
   p.f8 = f8 ? 1 : 0;
   p.a_mn_major = a_mn ? 1 : 0;
-  p.gather_mode = gk ? 2 : (gather ? 1 : 0);
   p.b_mn_major = b_mn ? 1 : 0;
   p.flags = cfg ? cfg->flags : 0;
   p.tile_counts = cfg ? cfg->tile_counts : nullptr;
@@ -556,16 +547,8 @@ gge_status make_plan(const gge_gemm_args* a, Form form, const int32_t* a_idx,
 
   // tensor maps (never read when K == 0)
   if (K > 0) {
-    if (gk) {
-      // rows of X (the source's K columns), M contiguous: gathered four at a time
-      s = encode_tiled(&pl.tmA, a->A.ptr, es, 2, a->A.rows, a->A.cols, 0,
-                       static_cast<uint64_t>(a->A.stride_col) * es, 0, 64, 1);
-      if (s != GGE_OK) return s;
-    } else if (gather) {
-      // rows of the source, K contiguous: gathered four at a time
-      s = encode_tiled(&pl.tmA, a->A.ptr, es, 2, K, a->A.rows, 0,
-                       static_cast<uint64_t>(a->A.stride_row) * es, 0, bk, 1);
-      if (s != GGE_OK) return s;
+    if (gather) {
+      // A rows are copied by the gather warps: no tensor map
     } else if (!a_mn) {
       s = encode_3d(&pl.tmA, a->A.ptr, es, K, a->A.rows, a->A.batch,
                     static_cast<uint64_t>(a->A.stride_row) * es, batch_stride_bytes(a->A, es), bk,

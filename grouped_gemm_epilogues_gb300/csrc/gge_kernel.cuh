@@ -647,37 +647,6 @@ __device__ __forceinline__ void tma_load(uint32_t dst, const CUtensorMap* m, uin
   else ptx::tma_load_3d_pair(dst, m, bar, x, y, z);
 }
 
-template <int CG>
-__device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* m, uint32_t bar,
-                                            int32_t x, const int32_t (&r)[4]) {
-  if (CG == 1) ptx::tma_gather4(dst, m, bar, x, r[0], r[1], r[2], r[3]);
-  else ptx::tma_gather4_pair(dst, m, bar, x, r[0], r[1], r[2], r[3]);
-}
-
-// A source row index checked against the gather source: a valid row, or the
-// first row past the source (the TMA gather reads zeros there) for a row that
-// reads nothing (-1) or an index out of range (recorded).
-__device__ __forceinline__ int32_t gather_row(const Params& p, int32_t s, bool wanted,
-                                              int32_t tile) {
-  if (!wanted) return p.a_src_rows;
-  if (s < 0 || s >= p.a_src_rows) {
-    record_status(p, DEV_INDEX_RANGE, 4, tile);
-    return p.a_src_rows;
-  }
-  return s;
-}
-
-// Gather-K: the source rows of K rows 4 (lane % 16) .. +3 of k-tile kt.
-__device__ __forceinline__ void gather_k_rows(const Params& p, const KRange& kr, int32_t kt,
-                                              int32_t tile, int32_t (&r)[4]) {
-  const int32_t kg0 = kr.k0 + kt * p.bk + 4 * (threadIdx.x & 15);
-  int32_t v[4];
-#pragma unroll
-  for (int j = 0; j < 4; ++j) v[j] = (kg0 + j < kr.k_end) ? __ldg(p.a_idx + kg0 + j) : -1;
-#pragma unroll
-  for (int j = 0; j < 4; ++j) r[j] = gather_row(p, v[j], kg0 + j < kr.k_end, tile);
-}
-
 // This CTA's tensor-map slot `slot` in the workspace.
 __device__ __forceinline__ uint8_t* kmap_slot(const Params& p, int slot) {
   return p.kmaps + (static_cast<int64_t>(blockIdx.x) * kMapSlots + slot) * kMapSlotBytes;
@@ -697,13 +666,8 @@ __device__ __forceinline__ const uint8_t* publish_kmaps(const Params& p, const C
   __syncwarp();
   if (lane == 0) {
     // K is dimension 0 of a K-major map and dimension 1 of an M- / N-major one
-    // (a gathered A keeps the launch's map: its rows are not K columns)
-    if (p.gather_mode != 0) {
-    } else if (p.a_mn_major) {
-      ptx::tmap_set_global_dim<1>(scratch, k_end);
-    } else {
-      ptx::tmap_set_global_dim<0>(scratch, k_end);
-    }
+    if (p.a_mn_major) ptx::tmap_set_global_dim<1>(scratch, k_end);
+    else ptx::tmap_set_global_dim<0>(scratch, k_end);
     if (p.b_mn_major) ptx::tmap_set_global_dim<1>(scratch + 128, k_end);
     else ptx::tmap_set_global_dim<0>(scratch + 128, k_end);
   }
@@ -723,7 +687,6 @@ __device__ __forceinline__ void tma_producer_role(const Params& p, const Shared&
                                                   int32_t num_tiles, uint32_t rank,
                                                   const TileSched& ts) {
   using Cfg = KernelCfg<BN, GATHER, CG>;
-  const int lane = threadIdx.x & 31;
   int stage = 0;
   uint32_t phase = 0;
   // varlen-K: the group whose maps are in use, and the slot they occupy
@@ -741,27 +704,7 @@ __device__ __forceinline__ void tma_producer_role(const Params& p, const Shared&
     const KRange kr = k_range(p, sh, tc.batch);
     const int32_t row0 = tc.m_row0 + static_cast<int32_t>(rank) * kBM;
     const int32_t bn0 = tc.n0 + static_cast<int32_t>(rank) * Cfg::kBRows;
-    // Row gathers: lane l fetches rows 4l .. 4l+3 of this CTA's 128 A rows (along M,
-    // fixed per tile), or K rows 4 (l % 16) .. +3 of each k-tile, for the 64-column
-    // M chunk l / 16 (along K, indices loaded one k-tile ahead).
-    int32_t grow[4], gnext[4];
-    if (p.gather_mode == 1) {
-      const int32_t r0 = row0 + 4 * lane;
-      const int64_t ibase = (p.num_groups > 0) ? 0 : static_cast<int64_t>(tc.batch) * p.M;
-      int32_t v[4];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) v[j] = (r0 + j < tc.row_limit) ? __ldg(p.a_idx + ibase + r0 + j) : -1;
-#pragma unroll
-      for (int j = 0; j < 4; ++j) grow[j] = gather_row(p, v[j], r0 + j < tc.row_limit, t);
-    } else if (p.gather_mode == 2 && kr.tiles > 0) {
-      gather_k_rows(p, kr, 0, t, gnext);
-    }
     for (int kt = 0; kt < kr.tiles; ++kt) {
-      if (p.gather_mode == 2) {
-#pragma unroll
-        for (int j = 0; j < 4; ++j) grow[j] = gnext[j];
-        if (kt + 1 < kr.tiles) gather_k_rows(p, kr, kt + 1, t, gnext);
-      }
       const bool ok = wait_phase<CG == 2>(sh.empty + 8 * stage, phase ^ 1u, p, sh, 0, t);
       if (!__all_sync(0xffffffffu, ok)) return;
       if (kt == 0) {
@@ -789,9 +732,8 @@ __device__ __forceinline__ void tma_producer_role(const Params& p, const Shared&
           map_group = tc.batch;
         }
         // a ragged group reads through its clipped maps; any other range is cut by
-        // the MMA K-step count, so the launch's maps serve it (a gathered A always
-        // uses the launch's map: rows past the group's end are gathered as zeros)
-        mA = (kr.ragged && p.gather_mode == 0) ? reinterpret_cast<const CUtensorMap*>(map_cur) : tmA;
+        // the MMA K-step count, so the launch's maps serve it
+        mA = kr.ragged ? reinterpret_cast<const CUtensorMap*>(map_cur) : tmA;
         mB = kr.ragged ? reinterpret_cast<const CUtensorMap*>(map_cur + 128) : tmB;
       }
       const uint32_t full = sh.full + 8 * stage;
@@ -804,9 +746,7 @@ __device__ __forceinline__ void tma_producer_role(const Params& p, const Shared&
         else if (rank == 0) ptx::mbar_arrive_expect_tx(full, 2 * Cfg::kStageBytes);
         const uint32_t bar = (CG == 1) ? full : ptx::mapa(full, 0);
         // K-major operands: one box of (bk columns, rows); M- / N-major: 64-wide boxes of bk rows
-        if (p.gather_mode != 0) {
-          // gathered below by every lane
-        } else if (!p.a_mn_major) {
+        if (!p.a_mn_major) {
           tma_load<CG>(adst, mA, bar, k0, row0, tc.a_batch);
         } else {
 #pragma unroll
@@ -822,20 +762,6 @@ __device__ __forceinline__ void tma_producer_role(const Params& p, const Shared&
         }
       }
       __syncwarp();
-      if (p.gather_mode != 0) {
-        // after the elected lane armed the barrier: 32 gathers of four rows each, one
-        // lane at a time (a TMA instruction is carried out once per warp, not per lane)
-        const uint32_t bar = (CG == 1) ? full : ptx::mapa(full, 0);
-        const int j = lane >> 4;
-        const uint32_t gdst = (p.gather_mode == 1)
-                                  ? adst + 4 * lane * kRowBytes
-                                  : adst + j * (64 * kRowBytes) + 4 * (lane & 15) * kRowBytes;
-        const int32_t gx = (p.gather_mode == 1) ? k0 : row0 + 64 * j;
-#pragma unroll 1
-        for (int l = 0; l < 32; ++l)
-          if (lane == l) tma_gather4<CG>(gdst, mA, bar, gx, grow);
-        __syncwarp();
-      }
       if (++stage == p.stages) { stage = 0; phase ^= 1u; }
     }
   }

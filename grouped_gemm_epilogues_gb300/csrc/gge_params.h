@@ -76,7 +76,6 @@ struct Params {
   uint32_t idesc;
   int32_t f8;          // operands are 8-bit (kind::f8f6f4)
   int32_t a_mn_major;  // A staged M-major (16-bit operands only)
-  int32_t gather_mode; // A by TMA row gathers: 0 none, 1 rows of A (along M), 2 rows of X (along K)
   int32_t b_mn_major;  // B staged N-major (16-bit operands only)
 
   // control

@@ -332,30 +332,6 @@ __device__ __forceinline__ void mma_commit_pair(uint32_t bar, uint16_t cta_mask)
       : "memory");
 }
 
-// TMA row gather: rows r0..r3 of a 2-D tensor map (box one row high), from
-// column c, into four consecutive box rows at dst (the map's swizzle applies).
-__device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* m, uint32_t bar,
-                                            int32_t c, int32_t r0, int32_t r1, int32_t r2,
-                                            int32_t r3) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(c), "r"(r0), "r"(r1), "r"(r2), "r"(r3)
-      : "memory");
-}
-
-// The same for a CTA pair: completion is signalled on the leader's barrier.
-__device__ __forceinline__ void tma_gather4_pair(uint32_t dst, const CUtensorMap* m,
-                                                 uint32_t cluster_bar, int32_t c, int32_t r0,
-                                                 int32_t r1, int32_t r2, int32_t r3) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile::gather4.mbarrier::"
-      "complete_tx::bytes [%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(m)), "r"(cluster_bar), "r"(c), "r"(r0), "r"(r1), "r"(r2),
-      "r"(r3)
-      : "memory");
-}
-
 // ---- tensor-map edits (per-group K extents)
 
 // Set the global extent of dimension ORD of a tensor map held in shared memory.

@@ -210,9 +210,10 @@ gge_status gge_gemm_varlen_k(const gge_gemm_args* args, const int32_t* cu_seqlen
  * column a_idx[k] of the source; B [N, total_K] is read at column k itself.
  * Group rules as in gge_gemm_varlen_k (with a K-major B, non-empty groups
  * start on multiples of 8); an index outside [0, K_src) reads zeros and is
- * reported as GGE_ERR_INDEX_RANGE.  The rows are fetched with TMA row
- * gathers; the workspace (256-byte aligned) must hold
- * gge_workspace_size_varlen_k bytes.  Page: quack/dense_gemm_sm90.py,
+ * reported as GGE_ERR_INDEX_RANGE.  One CTA per 128 x BN tile; the rows are
+ * copied by four gather warps with 16-byte cp.async (a TMA row gather issues
+ * too slowly for four rows of 128 bytes at a time).  The workspace (256-byte
+ * aligned) must hold gge_workspace_size_varlen_k bytes.  Page: quack/dense_gemm_sm90.py,
  * GemmSm90 with gather_A and VarlenArguments(mCuSeqlensK)
  * (copy_utils.gather_k_get_copy_fn). */
 gge_status gge_gemm_gather_k(const gge_gemm_args* args, const int32_t* a_idx,

@@ -220,7 +220,7 @@ def _oracle_gather_k(A_src, idx, B, cu, C, d_dtype, p_dtype, act, alpha, beta):
 def test_gather_k_parity(b_major, cu, tile_n):
     G = len(cu) - 1
     A_src, B, idx, C = _gather_k_operands(328, 264, 1000, 700, b_major, seed=21, G=G)
-    cfg = binding.make_config(tile_n=tile_n, cta_group=2 if tile_n == 256 else 1)
+    cfg = binding.make_config(tile_n=tile_n)
     D, P = _run_gather_k(A_src, B, idx, cu, C, G, "bf16", "bf16", "relu", alpha=0.75, beta=0.5,
                          config=cfg)
     ref = _oracle_gather_k(A_src, idx, B, cu, C, "bf16", "bf16", "relu", 0.75, 0.5)
@@ -274,7 +274,7 @@ def test_gather_a_with_n_major_b():
     B = (torch.rand((3, 256, 384), generator=gen) * 2 - 1).to(torch.bfloat16).transpose(1, 2)
     cu = torch.tensor([0, 100, 100, 700], dtype=torch.int32)
     idx = torch.randint(0, 900, (700,), generator=gen, dtype=torch.int32)
-    for tile_n, cg in ((128, 1), (256, 1), (256, 2)):
+    for tile_n, cg in ((128, 1), (256, 1)):
         D = torch.full((700, 384), -3.0, dtype=torch.bfloat16, device=DEV)
         binding.gge_gemm_gather_a(src.to(DEV), B.to(DEV), idx.to(DEV), cu.to(DEV), D=D,
                                   config=binding.make_config(tile_n=tile_n, cta_group=cg))
