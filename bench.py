@@ -207,7 +207,11 @@ def _set_bytes(s):
 
 def _step_fn(w, binding):
     def step(s):
-        if w.k_groups:
+        if w.k_groups and w.gather_rows:
+            binding.gge_gemm_gather_k(s["A"], s["B"], s["a_idx"], s["cu_seqlens_k"],
+                                      D=s.get("D"), PostAct=s.get("P"), act=w.act, C=s.get("C"),
+                                      alpha=w.alpha, beta=w.beta)
+        elif w.k_groups:
             binding.gge_gemm_varlen_k(s["A"], s["B"], s["cu_seqlens_k"], D=s.get("D"),
                                       PostAct=s.get("P"), act=w.act, C=s.get("C"),
                                       alpha=w.alpha, beta=w.beta)
@@ -429,8 +433,12 @@ def _oracle_rows(w, base, rows):
     if w.k_groups:
         # output rows m of every group: A's rows against all of B
         C = base["C"][:, rows] if "C" in base else None
-        og.gemm_varlen_k(dec(base["A"][rows]), dec(base["B"]), base["cu_seqlens_k"].numpy(),
-                         None if C is None else dec(C), **kw)
+        if w.gather_rows:
+            og.gemm_gather_k(dec(base["A"][rows]), base["a_idx"].numpy(), dec(base["B"]),
+                             base["cu_seqlens_k"].numpy(), None if C is None else dec(C), **kw)
+        else:
+            og.gemm_varlen_k(dec(base["A"][rows]), dec(base["B"]), base["cu_seqlens_k"].numpy(),
+                             None if C is None else dec(C), **kw)
         cu = base["cu_seqlens_k"].numpy()
         return 2.0 * len(rows) * w.N * float(cu[-1] - cu[0])
     if w.groups:

@@ -26,7 +26,7 @@ constexpr int kTileM = 128;
 constexpr int kRowBytesHost = 128;
 constexpr int kMaxSmemOptin = 232448;  // 227 KiB per block on sm_100 / sm_103
 constexpr int kCtrlBytesHost = 1024;
-constexpr int kOutStageBytesHost = 4096;  // epilogue staging per epilogue warp (kOutStageBytes)
+constexpr int kEpiWarpsHost = 8;          // epilogue warps of the TMA variants (4 with gathers)
 constexpr int kMaxGroupsHost = 1024;
 constexpr size_t kWorkspaceBytes = 256;
 constexpr size_t kMapSlotsHost = 16;     // varlen-K tensor-map slots per CTA (kernel kMapSlots)
@@ -340,6 +340,10 @@ gge_status make_plan(const gge_gemm_args* a, Form form, const int32_t* a_idx,
   if (a->PostAct) { s = check_mn(a->PostAct, M, N, L, true); if (s != GGE_OK) return s; }
   if (a->C) { s = check_mn(a->C, M, N, L, false); if (s != GGE_OK) return s; }
   if (N % 8 != 0) return GGE_ERR_UNSUPPORTED;
+  // epilogue staging per warp: a 32 x 32 chunk of the widest output
+  const int out_es = std::max(a->D ? elem_bytes(a->D->dtype) : 0,
+                              a->PostAct ? elem_bytes(a->PostAct->dtype) : 0);
+  const int out_stage = 32 * 32 * out_es;
 
   // A: [M, K, La] K-major, or M-major (16-bit, TMA-loaded A only); B: [N, K, Lb]
   // K- or N-major (16-bit).  With K == 0 neither is read.
@@ -424,7 +428,7 @@ gge_status make_plan(const gge_gemm_args* a, Form form, const int32_t* a_idx,
         int64_t units = cfg && cfg->num_ctas > 0 ? cfg->num_ctas / 2 : 0;
         if (units <= 0 && encode) {
           // the 256-wide plan: as many stages of (128 + 128) rows as fit, at most kMaxStages
-          const int fixed256 = 1024 + kCtrlBytesHost + 8 * kOutStageBytesHost;
+          const int fixed256 = 1024 + kCtrlBytesHost + kEpiWarpsHost * out_stage;
           const int st256 = (kTileM + 128) * kRowBytesHost;
           const size_t smem256 =
               fixed256 + std::min(kMaxStages, (kMaxSmemOptin - fixed256) / st256) * st256;
@@ -442,8 +446,8 @@ gge_status make_plan(const gge_gemm_args* a, Form form, const int32_t* a_idx,
   const int bk = kRowBytesHost / es;
   const int stage_bytes = (kTileM + bn / cg) * kRowBytesHost;
   const int varlen_bytes = (varlen || vk) ? 2 * 4 * (kMaxGroupsHost + 1) : 0;
-  const int epi_warps = gather ? 4 : 8;
-  const int fixed = 1024 + kCtrlBytesHost + varlen_bytes + epi_warps * kOutStageBytesHost;
+  const int epi_warps = gather ? kEpiWarpsHost / 2 : kEpiWarpsHost;
+  const int fixed = 1024 + kCtrlBytesHost + varlen_bytes + epi_warps * out_stage;
   int stages = (kMaxSmemOptin - fixed) / stage_bytes;
   stages = std::min(stages, kMaxStages);
   if (cfg && cfg->stages > 0) stages = std::min(stages, cfg->stages);
@@ -514,6 +518,7 @@ gge_status make_plan(const gge_gemm_args* a, Form form, const int32_t* a_idx,
   }
   p.act = a->act;
   p.dact = dact ? 1 : 0;
+  p.out_stage_bytes = out_stage;
   p.alpha = a->alpha;
   p.beta = a->beta;
   p.alpha_dev = a->alpha_dev;

@@ -53,13 +53,13 @@ constexpr int kBM = 128;           // tile rows = TMEM lanes
 constexpr int kRowBytes = 128;     // bytes of K per stage row (one swizzle span)
 
 constexpr int kGatherWarps = 4;
+constexpr int kGatherThreads = kGatherWarps * 32;
 constexpr int kMaxGroups = 1024;   // varlen groups held in shared memory
 constexpr int kCtrlBytes = 1024;   // barriers, flags and the tile ring (bytes 0..255),
                                    // the varlen-K tensor-map scratch (256..511) and
                                    // map-slot barriers (512..767)
 constexpr int kMapScratch = 256;
 constexpr int kMapBars = 512;
-constexpr int kOutStageBytes = 4096;  // epilogue staging per epilogue warp: 32 rows x 128 B
 constexpr int kSchedDepth = 4;     // tile indices in flight between the fetching warp and the rest
 constexpr int kMapSlots = 16;      // varlen-K: tensor-map copies per CTA (> pipeline stages)
 constexpr int kMapSlotBytes = 256; // one A and one B tensor map
@@ -75,8 +75,9 @@ struct KernelCfg {
   static constexpr int kABytes = kBM * kRowBytes;
   static constexpr int kBBytes = kBRows * kRowBytes;
   static constexpr int kStageBytes = kABytes + kBBytes;
-  // epilogue warps: two per TMEM lane quadrant (four with the gather producers,
-  // which need the registers), then the MMA warp, then the producer warp(s)
+  // epilogue warps: two per TMEM lane quadrant (one in the gather forms, whose
+  // four copy warps need the registers), then the MMA warp, then the producer
+  // warp(s): one TMA warp and the map warp, or the gather warps
   static constexpr int kEpiWarps = GATHER ? 4 : 8;
   static constexpr int kMmaWarp = kEpiWarps;
   static constexpr int kLoadWarp = kEpiWarps + 1;
@@ -816,10 +817,11 @@ __device__ __forceinline__ void load_b_1cta(const Params& p, const CUtensorMap* 
 // B of a one-CTA tile by 16-byte cp.async that reads nothing at or past column
 // k_end (the rest of each copy is zero-filled): a ragged varlen-K group's last
 // k-tile without a clipped tensor map.  Same swizzled layouts as the TMA boxes.
-// 128 threads; gt = this thread's index among them.
+// kGatherThreads threads; gt = this thread's index among them.
 template <int BN>
 __device__ __forceinline__ void copy_b_clipped(const Params& p, uint32_t dst, int32_t kbase,
                                                int32_t k_end, int32_t n0, int gt) {
+  constexpr int kStep = kGatherThreads / 8;  // rows between a thread's copies
   const int q = gt & 7;  // 16-byte piece of a 128-byte row
   const int sub = gt >> 3;
   if (!p.b_mn_major) {
@@ -827,8 +829,8 @@ __device__ __forceinline__ void copy_b_clipped(const Params& p, uint32_t dst, in
     const int32_t kel = kbase + 8 * q;
     const int32_t kbytes = max(0, min(16, 2 * (k_end - kel)));
 #pragma unroll
-    for (int i = 0; i < BN / 16; ++i) {
-      const int n = sub + 16 * i;
+    for (int i = 0; i < BN / kStep; ++i) {
+      const int n = sub + kStep * i;
       const uint32_t bytes = (n0 + n < p.N) ? static_cast<uint32_t>(kbytes) : 0u;
       const uint8_t* src =
           bytes ? p.b_src + static_cast<int64_t>(n0 + n) * p.b_ld + 2 * static_cast<int64_t>(kel)
@@ -840,8 +842,8 @@ __device__ __forceinline__ void copy_b_clipped(const Params& p, uint32_t dst, in
 #pragma unroll
     for (int j = 0; j < BN / 64; ++j) {
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int k = sub + 16 * i;
+      for (int i = 0; i < 64 / kStep; ++i) {
+        const int k = sub + kStep * i;
         const int32_t nel = n0 + 64 * j + 8 * q;
         const uint32_t bytes = (kbase + k < k_end && nel < p.N) ? 16u : 0u;
         const uint8_t* src =
@@ -854,33 +856,49 @@ __device__ __forceinline__ void copy_b_clipped(const Params& p, uint32_t dst, in
   }
 }
 
-// Source rows of K rows ksub + 8 j (j < 8) of k-tile kt, or -1 where the row
-// reads zeros (past the group's end, past M, or an index out of range, which is
-// recorded).
-__device__ __forceinline__ void gather_k_indices(const Params& p, const KRange& kr, int32_t kt,
-                                                 int ksub, bool m_ok, int32_t tile,
-                                                 int32_t (&src)[8]) {
-  const int32_t kbase = kr.k0 + kt * p.bk;
-#pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    const int32_t kg = kbase + ksub + 8 * j;
-    src[j] = (m_ok && kg < kr.k_end) ? __ldg(p.a_idx + kg) : -1;
+constexpr int32_t kNoRow = INT32_MIN;  // gather-K: a K row that reads zeros
+
+// Gather-K thread layout: lane l of gather warp w copies 16-byte piece l % 16
+// of K rows 2 w + l / 16 + kGKRowStep j (j < kGKWarpRows / 2), so each copy
+// instruction covers two whole 256-byte row segments and the gather warps
+// together fill the k-tile's 8-row swizzle atoms one after another.  Lane
+// l < kGKWarpRows loads the index of the warp's row with j = l / 2 and
+// l / 16 = l % 2 (one coalesced load per warp), kGKDepth k-tiles ahead, and the
+// rows' owners receive it by shuffle.
+constexpr int kGKWarpRows = 64 / kGatherWarps;
+constexpr int kGKRowStep = 2 * kGatherWarps;
+constexpr int kGKDepth = 2;
+static_assert(kGKWarpRows <= 32 && kGKWarpRows % 2 == 0, "gather-K rows per warp");
+
+// K row of j-th copy of a lane with l / 16 == rsub in gather warp w.
+__device__ __forceinline__ int gather_k_row(int w, int rsub, int j) {
+  return 2 * w + rsub + kGKRowStep * j;
+}
+
+// Raw source row of the K row whose index lane `lane` loads, of k-tile kt
+// (kNoRow past the group's end).
+__device__ __forceinline__ int32_t gather_k_load(const Params& p, const KRange& kr, int32_t kt,
+                                                 int w, int lane) {
+  const int l = lane % kGKWarpRows;
+  const int32_t kg = kr.k0 + kt * p.bk + gather_k_row(w, l & 1, l >> 1);
+  return (kt < kr.tiles && kg < kr.k_end) ? __ldg(p.a_idx + kg) : kNoRow;
+}
+
+// A loaded source row, checked: -1 reads zeros (no row, or an index out of
+// range, which is recorded).
+__device__ __forceinline__ int32_t gather_k_check(const Params& p, int32_t raw, int32_t tile) {
+  if (raw == kNoRow) return -1;
+  if (raw < 0 || raw >= p.a_src_rows) {
+    record_status(p, DEV_INDEX_RANGE, 4, tile);
+    return -1;
   }
-#pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    if (src[j] >= p.a_src_rows || src[j] < -1 ||
-        (src[j] == -1 && m_ok && kbase + ksub + 8 * j < kr.k_end)) {
-      record_status(p, DEV_INDEX_RANGE, 4, tile);
-      src[j] = -1;
-    }
-  }
+  return raw;
 }
 
 // Gather-K (varlen-K with A gathered along K, the pages' gather_k copy): row k
 // of the k-tile's effective A^T is row a_idx[k] of the source X (M contiguous
 // 16-bit elements), staged M-major: 64-element chunks of bk K rows, 128-byte
-// swizzle.  Thread gt copies 16-byte piece gt % 16 of the tile's 256-byte M
-// segment for K rows gt / 16 + 8 i; the indices are loaded one k-tile ahead.
+// swizzle (thread layout above).
 // B comes by TMA, except the last k-tile of a ragged group, copied only up to
 // the group's end.  A K row past the group's end, an M element past M, or an
 // index out of range reads zeros (the last is reported).
@@ -890,9 +908,10 @@ __device__ __forceinline__ void gather_k_producer_role(const Params& p, const Sh
                                                        uint32_t b0, int32_t num_tiles,
                                                        const TileSched& ts) {
   using Cfg = KernelCfg<BN, true, 1>;
-  const int gt = threadIdx.x - Cfg::kLoadWarp * 32;  // 0..127
-  const int q = gt & 15;
-  const int ksub = gt >> 4;
+  const int gt = threadIdx.x - Cfg::kLoadWarp * 32;  // 0 .. kGatherThreads-1
+  const int w = gt >> 5, lane = gt & 31;
+  const int q = lane & 15;
+  const int rsub = lane >> 4;
   const uint32_t a_off = static_cast<uint32_t>(q >> 3) * (64 * kRowBytes);  // M chunk
   int stage = 0;
   uint32_t phase = 0;
@@ -903,14 +922,15 @@ __device__ __forceinline__ void gather_k_producer_role(const Params& p, const Sh
     const KRange kr = k_range(p, sh, tc.batch);
     const int32_t m_el = tc.m_row0 + 8 * q;
     const bool m_ok = m_el < p.M;  // M is a multiple of 8: whole pieces
-    // the source rows of this thread's K rows, loaded one k-tile ahead of their copies
-    int32_t nxt[8];
-    gather_k_indices(p, kr, 0, ksub, m_ok, t, nxt);
-    for (int kt = 0; kt < kr.tiles; ++kt) {
-      int32_t cur[8];
+    // this lane's index loads for the next kGKDepth k-tiles, in flight
+    int32_t ring[kGKDepth];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) cur[j] = nxt[j];
-      if (kt + 1 < kr.tiles) gather_k_indices(p, kr, kt + 1, ksub, m_ok, t, nxt);
+    for (int d = 0; d < kGKDepth; ++d) ring[d] = gather_k_load(p, kr, d, w, lane);
+    for (int kt = 0; kt < kr.tiles; ++kt) {
+      const int32_t raw = ring[0];
+#pragma unroll
+      for (int d = 0; d + 1 < kGKDepth; ++d) ring[d] = ring[d + 1];
+      ring[kGKDepth - 1] = gather_k_load(p, kr, kt + kGKDepth, w, lane);
       if (!wait_phase(sh.empty + 8 * stage, phase ^ 1u, p, sh, 0, t)) return;
       const uint32_t full = sh.full + 8 * stage;
       const int32_t kbase = kr.k0 + kt * p.bk;
@@ -928,9 +948,10 @@ __device__ __forceinline__ void gather_k_producer_role(const Params& p, const Sh
         copy_b_clipped<BN>(p, bbase, kbase, kr.k_end, tc.n0, gt);
       }
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const int k = ksub + 8 * j;
-        const int32_t src = cur[j];
+      for (int j = 0; j < kGKWarpRows / 2; ++j) {
+        const int k = gather_k_row(w, rsub, j);
+        const int32_t v = __shfl_sync(0xffffffffu, raw, rsub + 2 * j);
+        const int32_t src = m_ok ? gather_k_check(p, v, t) : -1;
         const uint8_t* sp =
             src >= 0 ? p.a_src + static_cast<int64_t>(src) * p.a_src_ld + 2 * static_cast<int64_t>(m_el)
                      : p.a_src;
@@ -954,22 +975,24 @@ __device__ __forceinline__ void gather_producer_role(const Params& p, const Shar
     gather_k_producer_role<BN>(p, sh, tmB, a0, b0, num_tiles, ts);
     return;
   }
-  const int gt = threadIdx.x - Cfg::kLoadWarp * 32;  // 0..127
+  constexpr int kRows = kBM * 8 / kGatherThreads;  // rows per thread (8 threads a row)
+  const int gt = threadIdx.x - Cfg::kLoadWarp * 32;  // 0 .. kGatherThreads-1
   const int chunk = gt & 7;
   const int rsub = gt >> 3;
+  constexpr int kRowStep = kGatherThreads / 8;
   int stage = 0;
   uint32_t phase = 0;
   for (int i = 0;; ++i) {
-    // the first gather warp fetches the tile stream, the other three read it
+    // the first gather warp fetches the tile stream, the other reads it
     const int32_t t = (gt < 32) ? sched_fetch<1>(ts, i, p, sh) : sched_next<1>(ts, i, p, sh);
     if (t >= num_tiles) break;
     const TileCoord tc = tile_coord<BN, kBM>(t, p, sh);
     // index rows: plain gather reads a_idx[batch][row], varlen reads a_idx[global row]
     const int64_t idx_base = (p.num_groups > 0) ? 0 : static_cast<int64_t>(tc.batch) * p.M;
-    int32_t src[8];
+    int32_t src[kRows];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int32_t r = tc.m_row0 + rsub + 16 * i;
+    for (int i = 0; i < kRows; ++i) {
+      const int32_t r = tc.m_row0 + rsub + kRowStep * i;
       int32_t s = -1;
       if (r < tc.row_limit) {
         s = __ldg(p.a_idx + idx_base + r);
@@ -991,8 +1014,8 @@ __device__ __forceinline__ void gather_producer_role(const Params& p, const Shar
       const uint32_t kvalid = (kbyte < p.k_bytes) ? 16u : 0u;
       const uint32_t abase = a0 + stage * Cfg::kABytes;
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int r = rsub + 16 * i;
+      for (int i = 0; i < kRows; ++i) {
+        const int r = rsub + kRowStep * i;
         const uint32_t dst = abase + r * kRowBytes + ((chunk ^ (r & 7)) << 4);
         // a zero-byte copy still gets an in-bounds source address
         const bool live = src[i] >= 0 && kvalid != 0u;
@@ -1021,7 +1044,7 @@ __global__ void __launch_bounds__(KernelCfg<BN, GATHER, CG>::kThreads, 1)
   const uint32_t a0 = base;
   const uint32_t b0 = base + S * Cfg::kABytes;
   const uint32_t out_stage = base + S * Cfg::kStageBytes;  // epilogue staging, per warp
-  uint8_t* ctrl = base_ptr + S * Cfg::kStageBytes + Cfg::kEpiWarps * kOutStageBytes;
+  uint8_t* ctrl = base_ptr + S * Cfg::kStageBytes + Cfg::kEpiWarps * p.out_stage_bytes;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ctrl + 8 * (2 * S + 5 + 2 * kSchedDepth));
   int32_t* abort_flag = reinterpret_cast<int32_t*>(tmem_slot + 1);
   int32_t* prefix = reinterpret_cast<int32_t*>(ctrl + kCtrlBytes);
@@ -1144,7 +1167,7 @@ __global__ void __launch_bounds__(KernelCfg<BN, GATHER, CG>::kThreads, 1)
 
   if (warp < Cfg::kEpiWarps) {
     epilogue_role<BN, GATHER, CG>(p, sh, tmem_base, num_tiles, rank, ts,
-                                  out_stage + warp * kOutStageBytes);
+                                  out_stage + warp * p.out_stage_bytes);
   } else if (warp == Cfg::kMmaWarp) {
     if (rank == 0) mma_role<BN, GATHER, CG>(p, sh, a0, b0, tmem_base, num_tiles, ts);
   } else if (GATHER) {

@@ -68,6 +68,7 @@ struct Params {
   int32_t d_dtype, p_dtype, c_dtype;
   int32_t act;
   int32_t dact;  // backward epilogue: C is the pre-activation x, D = act'(x) * acc, PostAct = act(x)
+  int32_t out_stage_bytes;  // shared-memory staging per epilogue warp: 32 x 32 outputs (2 or 4 KiB)
   float alpha, beta;
   const float* alpha_dev;
   const float* beta_dev;
