@@ -81,6 +81,13 @@ _SIGNATURES = {
     "gge_schedule_map": (c_i32, [c_i32, c_i32, c_i32, c_i32, c_i32, ctypes.POINTER(c_i32)]),
     "gge_plan": (c_i32, [ctypes.POINTER(GgeGemmArgs), c_i32, c_i32, ctypes.POINTER(GgePlanInfo)]),
     "gge_version": (ctypes.c_char_p, []),
+    "gge_tune_candidates": (c_i32, [ctypes.POINTER(GgeGemmArgs), c_i32, c_i32,
+                                    ctypes.POINTER(GgeConfig), c_i32]),
+    "gge_autotune": (c_i32, [ctypes.POINTER(GgeGemmArgs), c_i32, ctypes.c_void_p, ctypes.c_void_p,
+                             c_i32, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p, c_i32,
+                             ctypes.POINTER(GgeConfig), ctypes.POINTER(ctypes.c_float)]),
+    "gge_tuned_config": (c_i32, [ctypes.POINTER(GgeGemmArgs), c_i32, c_i32,
+                                 ctypes.POINTER(GgeConfig)]),
 }
 
 _lib = None
@@ -319,3 +326,64 @@ def gge_plan(A, B, C=None, D=None, PostAct=None, act="none", num_groups=0, gathe
     code = lib.gge_plan(ctypes.byref(args), num_groups, f, ctypes.byref(info))
     _check(code, "gge_plan")
     return {k: getattr(info, k) for k, _ in GgePlanInfo._fields_}
+
+
+# ------------------------------------------------------------------ autotuning
+
+OP = {"gemm": 0, "dact": 1, "varlen_m": 2, "gather_a": 3, "varlen_k": 4, "gather_k": 5}
+_CFG_KEYS = ("tile_n", "num_ctas", "raster_band", "stages", "flags", "cta_group")
+
+
+def config_dict(c: GgeConfig) -> dict:
+    return {k: getattr(c, k) for k in _CFG_KEYS}
+
+
+def _tune_args(op, A, B, C, D, PostAct, act, alpha, beta, config):
+    if op == "dact":   # the backward epilogue reads the pre-activation from C
+        return make_args(A, B, C=C, D=D, PostAct=PostAct, act=act, config=config)
+    return make_args(A, B, C=C, D=D, PostAct=PostAct, alpha=alpha, beta=beta, act=act,
+                     config=config)
+
+
+def gge_tune_candidates(op, A, B, C=None, D=None, PostAct=None, act="none", num_groups=0,
+                        config=None):
+    """The launch configurations gge_autotune would time for this problem (host only)."""
+    lib = load()
+    args = _tune_args(op, A, B, C, D, PostAct, act, 1.0, 1.0, config)
+    out = (GgeConfig * 32)()
+    n = lib.gge_tune_candidates(ctypes.byref(args), OP[op], num_groups, out, 32)
+    return [config_dict(out[i]) for i in range(min(n, 32))]
+
+
+def gge_autotune(op, A, B, idx=None, cu=None, C=None, D=None, PostAct=None, act="none",
+                 alpha=1.0, beta=1.0, reps=10, config=None):
+    """Time every candidate launch shape of `op` on the current stream and return
+    (best config as a dict, its mean time in ms).  The outputs hold the result."""
+    lib = load()
+    out = D if D is not None else PostAct
+    args = _tune_args(op, A, B, C, D, PostAct, act, alpha, beta, config)
+    G = cu.numel() - 1 if cu is not None else 0
+    need = 256
+    if op in ("varlen_k", "gather_k"):
+        need = lib.gge_workspace_size_varlen_k(ctypes.byref(args), G)
+    ws = workspace(out.device, need)
+    best = GgeConfig()
+    ms = ctypes.c_float()
+    code = lib.gge_autotune(ctypes.byref(args), OP[op],
+                            ctypes.c_void_p(idx.data_ptr()) if idx is not None else None,
+                            ctypes.c_void_p(cu.data_ptr()) if cu is not None else None, G,
+                            ctypes.c_void_p(ws.data_ptr()), ws.numel(), _stream(out), reps,
+                            ctypes.byref(best), ctypes.byref(ms))
+    _check(code, "gge_autotune")
+    return config_dict(best), ms.value
+
+
+def gge_tuned_config(op, A, B, C=None, D=None, PostAct=None, act="none", num_groups=0,
+                     config=None):
+    """The configuration gge_autotune stored for a problem of this key, or None."""
+    lib = load()
+    args = _tune_args(op, A, B, C, D, PostAct, act, 1.0, 1.0, config)
+    c = GgeConfig()
+    if lib.gge_tuned_config(ctypes.byref(args), OP[op], num_groups, ctypes.byref(c)) != 0:
+        return None
+    return config_dict(c)

@@ -618,6 +618,30 @@ gge_status run(const gge_gemm_args* a, Form form, const int32_t* a_idx, const in
 }
 
 }  // namespace
+
+int32_t validate_op(const gge_gemm_args* args, int32_t op, int32_t num_groups) {
+  static const int32_t dummy = 0;
+  Plan pl;
+  const bool act_entry = args != nullptr && args->PostAct != nullptr;
+  switch (op) {
+    case GGE_OP_GEMM:
+      return make_plan(args, Form::Plain, nullptr, nullptr, 0, act_entry, act_entry, false, &pl);
+    case GGE_OP_DACT:
+      return make_plan(args, Form::Plain, nullptr, nullptr, 0, true, false, false, &pl, true);
+    case GGE_OP_VARLEN_M:
+      return make_plan(args, Form::Varlen, nullptr, &dummy, num_groups, true, false, false, &pl);
+    case GGE_OP_GATHER_A:
+      return make_plan(args, num_groups > 0 ? Form::GatherVarlen : Form::Gather, &dummy,
+                       num_groups > 0 ? &dummy : nullptr, num_groups, true, false, false, &pl);
+    case GGE_OP_VARLEN_K:
+      return make_plan(args, Form::VarlenK, nullptr, &dummy, num_groups, true, false, false, &pl);
+    case GGE_OP_GATHER_K:
+      return make_plan(args, Form::GatherK, &dummy, &dummy, num_groups, true, false, false, &pl);
+    default:
+      return GGE_ERR_INVALID_ARG;
+  }
+}
+
 }  // namespace gge
 
 using gge::Form;

@@ -4,6 +4,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include "../../include/gge.h"
 #include "gge_params.h"
 
 namespace gge {
@@ -24,5 +25,9 @@ int kernel_threads();
 // Clusters of CG CTAs (with `smem` bytes each) that can be resident at once.
 template <int BN, bool GATHER, int CG>
 int max_active_units(size_t smem);
+
+// Host-only validation of one call of entry point `op` (GGE_OP_*) as it would
+// be planned, without launching or touching the GPU (gge_api.cu).
+int32_t validate_op(const ::gge_gemm_args* args, int32_t op, int32_t num_groups);
 
 }  // namespace gge

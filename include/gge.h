@@ -97,7 +97,7 @@ typedef struct gge_config {
                              counter in the workspace (needs a workspace)        */
   int32_t cta_group;      /* 0 = auto; 1 = one CTA per 128-row tile; 2 = a CTA pair
                              per 256-row tile (tcgen05 cta_group::2, 256-column
-                             tiles, not with gather-A)                             */
+                             tiles, not with the gather forms)                     */
   int32_t* tile_counts;   /* device int32 per tile (debug coverage), or NULL       */
   uint64_t timeout_ns;    /* 0 = default (2 s) limit for each pipeline wait        */
 } gge_config;
@@ -105,9 +105,9 @@ typedef struct gge_config {
 /*
  * Arguments of one GEMM.
  *   A : [M, K, L]  rows = M, cols = K.  K-major (stride_col == 1) or, for
- *       16-bit operands loaded by TMA (every form but gather-A), M-major
- *       (stride_row == 1).  In the gather form A is the SOURCE matrix
- *       [rows_src, K, 1], K-major.
+ *       16-bit operands loaded by TMA (every form but the gathers), M-major
+ *       (stride_row == 1).  In gather-A, A is the SOURCE matrix
+ *       [rows_src, K, 1], K-major; in gather-K, the M-major source [M, K_src, 1].
  *   B : [N, K, L]  rows = N, cols = K.  K-major (stride_col == 1) or, for
  *       16-bit operands, N-major (stride_row == 1).  8-bit operands must be
  *       K-major (as on the pages).
@@ -137,7 +137,8 @@ typedef struct gge_gemm_args {
 } gge_gemm_args;
 
 /* Bytes of device workspace a call needs (status words and the dynamic
- * scheduler's counters), for every entry point except gge_gemm_varlen_k; the
+ * scheduler's counters), for every entry point except gge_gemm_varlen_k and
+ * gge_gemm_gather_k (see gge_workspace_size_varlen_k); the
  * workspace is caller-owned, at least 16-byte aligned, and must be zeroed once
  * before first use.  It is reusable across calls on the same stream. */
 size_t gge_workspace_size(const gge_gemm_args* args, int32_t num_groups);
@@ -290,6 +291,50 @@ typedef struct gge_plan_info {
 } gge_plan_info;
 gge_status gge_plan(const gge_gemm_args* args, int32_t num_groups, int32_t form,
                     gge_plan_info* out);
+
+/* ---- autotuning ---------------------------------------------------------
+ * Page: quack-kernels 0.2.0 diff, quack/gemm_config.py (GemmConfig and
+ * get_all_configs: a space of tile shapes, cooperative / ping-pong
+ * warpgroups, 1x2 / 2x1 clusters and swap_ab to search by timing).  Here the space is the launch shapes this library
+ * has: one CTA per 128 x 128 or 128 x 256 tile, or a CTA pair per 256 x 256,
+ * 224, 192 or 160 tile (not with the gather forms), times the raster band of
+ * plain problems.  The pages' swap_ab is not in the space: it needs M-major
+ * output stores, which the epilogue does not have. */
+
+/* Which entry point a tuning call times. */
+enum {
+  GGE_OP_GEMM = 0,      /* gge_gemm (PostAct NULL) or gge_gemm_act          */
+  GGE_OP_DACT = 1,      /* gge_gemm_dact                                      */
+  GGE_OP_VARLEN_M = 2,  /* gge_gemm_varlen_m (cu = cu_seqlens_m)              */
+  GGE_OP_GATHER_A = 3,  /* gge_gemm_gather_a (idx = a_idx, cu may be NULL)    */
+  GGE_OP_VARLEN_K = 4,  /* gge_gemm_varlen_k (cu = cu_seqlens_k)              */
+  GGE_OP_GATHER_K = 5   /* gge_gemm_gather_k (idx = a_idx, cu = cu_seqlens_k) */
+};
+
+/* Writes up to `max` candidate configurations for (args, op) into `out`
+ * (host only, no GPU needed: shapes the planner rejects are left out) and
+ * returns how many there are (which may exceed `max`).  Each candidate is
+ * args->config (or the defaults) with tile_n, cta_group and raster_band set. */
+int32_t gge_tune_candidates(const gge_gemm_args* args, int32_t op, int32_t num_groups,
+                            gge_config* out, int32_t max);
+
+/* Times every candidate of (args, op) on `stream` -- `reps` launches each
+ * after one warm-up launch, CUDA events around them -- and writes the fastest
+ * configuration to *best (and its mean time in ms to *best_ms, if not NULL).
+ * Every launch computes the real outputs, so they hold the result on return.
+ * Synchronises `stream`.  The result is also stored in an in-process cache
+ * keyed by the problem's shapes, dtypes, strides pattern, activation and op,
+ * which gge_tuned_config reads.  Errors of a launch are returned as they are;
+ * a candidate rejected by the planner is skipped. */
+gge_status gge_autotune(const gge_gemm_args* args, int32_t op, const int32_t* idx,
+                        const int32_t* cu, int32_t num_groups, void* workspace,
+                        size_t workspace_bytes, gge_stream_t stream, int32_t reps,
+                        gge_config* best, float* best_ms);
+
+/* The configuration gge_autotune found for a problem of the same key, or
+ * GGE_ERR_INVALID_ARG if there is none (no GPU work). */
+gge_status gge_tuned_config(const gge_gemm_args* args, int32_t op, int32_t num_groups,
+                            gge_config* out);
 
 /* Library version string. */
 const char* gge_version(void);

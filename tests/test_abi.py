@@ -196,3 +196,28 @@ def test_m_major_a_plans_for_tma_forms_only(L):
     assert binding.gge_plan(A, B, D=D, config=cfg)["tile_m"] == 256
     with pytest.raises(binding.GgeError):                     # the row gather reads K-major rows
         binding.gge_plan(A, B, D=D, gather=True, config=cfg)
+
+
+def test_tune_candidates_follow_the_planner(L):
+    A = torch.zeros(4096, 4096, dtype=torch.bfloat16)
+    P = torch.zeros(4096, 4096, dtype=torch.bfloat16)
+    c = binding.gge_tune_candidates("gemm", A, A, D=P, PostAct=P, act="gelu_tanh")
+    shapes = {(x["cta_group"], x["tile_n"]) for x in c}
+    assert shapes == {(2, 256), (2, 224), (2, 192), (2, 160), (1, 256), (1, 128)}
+    assert {x["raster_band"] for x in c} == {0, 2, 8} and len(c) == 18
+    # N-major B: the pair keeps 256-wide tiles only
+    Bn = torch.zeros(4096, 4096, dtype=torch.bfloat16).t()
+    c = binding.gge_tune_candidates("gemm", A, Bn, D=P)
+    assert {(x["cta_group"], x["tile_n"]) for x in c} == {(2, 256), (1, 256), (1, 128)}
+    # the gathers run on single-CTA tiles and have no raster band to search
+    src = torch.zeros(1000, 512, dtype=torch.bfloat16)
+    B = torch.zeros(4, 384, 512, dtype=torch.bfloat16)
+    D = torch.zeros(700, 384, dtype=torch.bfloat16)
+    c = binding.gge_tune_candidates("gather_a", src, B, D=D, num_groups=4)
+    assert {(x["cta_group"], x["tile_n"], x["raster_band"]) for x in c} == {(1, 256, 0), (1, 128, 0)}
+    # a caller's flags are kept in every candidate
+    c = binding.gge_tune_candidates("gemm", A, A, D=P, config=binding.make_config(flags=4))
+    assert all(x["flags"] == 4 for x in c)
+    # nothing valid: no candidates
+    assert binding.gge_tune_candidates("gemm", A, A, D=torch.zeros(4096, 4000,
+                                                                   dtype=torch.bfloat16)) == []
