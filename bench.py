@@ -205,30 +205,38 @@ def _set_bytes(s):
     return sum(v.numel() * v.element_size() for v in s.values() if isinstance(v, torch.Tensor))
 
 
-def _step_fn(w, binding):
+def _op_of(w):
+    if w.k_groups:
+        return "gather_k" if w.gather_rows else "varlen_k"
+    if w.groups:
+        return "gather_a" if w.gather_rows else "varlen_m"
+    return "gemm"
+
+
+def _step_fn(w, binding, config=None):
     def step(s):
         if w.k_groups and w.gather_rows:
             binding.gge_gemm_gather_k(s["A"], s["B"], s["a_idx"], s["cu_seqlens_k"],
                                       D=s.get("D"), PostAct=s.get("P"), act=w.act, C=s.get("C"),
-                                      alpha=w.alpha, beta=w.beta)
+                                      alpha=w.alpha, beta=w.beta, config=config)
         elif w.k_groups:
             binding.gge_gemm_varlen_k(s["A"], s["B"], s["cu_seqlens_k"], D=s.get("D"),
                                       PostAct=s.get("P"), act=w.act, C=s.get("C"),
-                                      alpha=w.alpha, beta=w.beta)
+                                      alpha=w.alpha, beta=w.beta, config=config)
         elif w.groups:
             if w.gather_rows:
                 binding.gge_gemm_gather_a(s["A"], s["B"], s["a_idx"], s["cu_seqlens_m"],
                                           D=s.get("D"), PostAct=s.get("P"), act=w.act,
-                                          C=s.get("C"), alpha=w.alpha, beta=w.beta)
+                                          C=s.get("C"), alpha=w.alpha, beta=w.beta, config=config)
             else:
                 binding.gge_gemm_varlen_m(s["A"], s["B"], s["cu_seqlens_m"], D=s.get("D"),
                                           PostAct=s.get("P"), act=w.act, C=s.get("C"),
-                                          alpha=w.alpha, beta=w.beta)
+                                          alpha=w.alpha, beta=w.beta, config=config)
         elif w.act == "none" and "P" not in s:
-            binding.gge_gemm(s["A"], s["B"], s["D"], C=s.get("C"), alpha=w.alpha, beta=w.beta)
+            binding.gge_gemm(s["A"], s["B"], s["D"], C=s.get("C"), alpha=w.alpha, beta=w.beta, config=config)
         else:
             binding.gge_gemm_act(s["A"], s["B"], s["P"], w.act, D=s.get("D"), C=s.get("C"),
-                                 alpha=w.alpha, beta=w.beta)
+                                 alpha=w.alpha, beta=w.beta, config=config)
     return step
 
 
@@ -249,7 +257,16 @@ def run_ours(args, w):
     n_sets = min(n_sets, 8)
     del probe
     _, sets = _device_sets(w, dev, n_sets)
-    step = _step_fn(w, binding)
+    # launch shape: the autotuner's pick for this problem (tuning runs before the
+    # warm-up and is not timed), or the planner's default with --no-tune
+    tuned = None
+    if not args.no_tune:
+        s0 = sets[0]
+        tuned, _ = binding.gge_autotune(_op_of(w), s0["A"], s0["B"], idx=s0.get("a_idx"),
+                                        cu=s0.get("cu_seqlens_k", s0.get("cu_seqlens_m")),
+                                        C=s0.get("C"), D=s0.get("D"), PostAct=s0.get("P"),
+                                        act=w.act, alpha=w.alpha, beta=w.beta, reps=5)
+    step = _step_fn(w, binding, binding.make_config(**tuned) if tuned else None)
     stream = torch.cuda.current_stream(dev)
 
     def barrier():
@@ -352,7 +369,9 @@ def run_ours(args, w):
                           f"{n_sets} rotating input sets of {per_set / 2**20:.2f} MiB "
                           "(whole working set < L2: L2-resident)"),
                    "parallelism": f"replicas{ws_n}" if ws_n > 1 else "single",
-                   "launch": "eager" if args.eager else "cuda_graph"},
+                   "launch": "eager" if args.eager else "cuda_graph",
+                   "launch_shape": (dict(tuned, source="autotuned") if tuned else
+                                    {"source": "planner default"})},
         "roofline": roofline,
         "e2e": e2e,
         "gpu_launches": args.steps,
@@ -532,6 +551,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-tune", action="store_true",
+                    help="use the planner's default launch shape instead of the autotuner's")
     ap.add_argument("--eager", action="store_true",
                     help="launch every timed step from Python instead of CUDA-graph replay")
     args = ap.parse_args()
