@@ -343,7 +343,8 @@ gge_status make_plan(const gge_gemm_args* a, Form form, const int32_t* a_idx,
   // epilogue staging per warp: a 32 x 32 chunk of the widest output
   const int out_es = std::max(a->D ? elem_bytes(a->D->dtype) : 0,
                               a->PostAct ? elem_bytes(a->PostAct->dtype) : 0);
-  const int out_stage = 32 * 32 * out_es;
+  const bool direct = cfg && (cfg->flags & FLAG_DIRECT_STORES);
+  const int out_stage = direct ? 0 : 32 * 32 * out_es;
 
   // A: [M, K, La] K-major, or M-major (16-bit, TMA-loaded A only); B: [N, K, Lb]
   // K- or N-major (16-bit).  With K == 0 neither is read.

@@ -390,8 +390,31 @@ __device__ __forceinline__ uint32_t pack2(int dtype, float a, float b) {
 // rows >= rows_valid and columns >= cols_valid are not written.  Warp-collective.
 __device__ __forceinline__ void store_chunk_staged(uint32_t stg, const float (&x)[32], int dtype,
                                                    char* out, int64_t ld_bytes,
-                                                   int32_t rows_valid, int32_t cols_valid) {
+                                                   int32_t rows_valid, int32_t cols_valid,
+                                                   bool direct) {
   const int lane = threadIdx.x & 31;
+  if (direct) {
+    // no staging buffer: each lane writes its own row (32 rows x 16 B per instruction)
+    if (lane >= rows_valid) return;
+    char* o = out + lane * ld_bytes;
+    if (dtype == DT_F32) {
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        if (4 * q < cols_valid)
+          *reinterpret_cast<uint4*>(o + 16 * q) =
+              make_uint4(__float_as_uint(x[4 * q]), __float_as_uint(x[4 * q + 1]),
+                         __float_as_uint(x[4 * q + 2]), __float_as_uint(x[4 * q + 3]));
+    } else {
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        if (8 * q < cols_valid)
+          *reinterpret_cast<uint4*>(o + 16 * q) =
+              make_uint4(pack2(dtype, x[8 * q], x[8 * q + 1]), pack2(dtype, x[8 * q + 2], x[8 * q + 3]),
+                         pack2(dtype, x[8 * q + 4], x[8 * q + 5]),
+                         pack2(dtype, x[8 * q + 6], x[8 * q + 7]));
+    }
+    return;
+  }
   if (dtype == DT_F32) {
 #pragma unroll
     for (int q = 0; q < 8; ++q)
@@ -454,13 +477,15 @@ __device__ __forceinline__ void epilogue_chunk_dact(const Params& p, const uint3
   for (int j = 0; j < 32; ++j) y[j] = dact_apply(p.act, x[j]) * __uint_as_float(acc[j]);
   store_chunk_staged(stg, y, p.d_dtype,
                      out_ptr(p.d, p.ldd, p.sbd, p.d_dtype, row_base, col0, batch, p),
-                     p.ldd * dtype_bytes(p.d_dtype), rows_valid, cols_valid);
+                     p.ldd * dtype_bytes(p.d_dtype), rows_valid, cols_valid,
+                     p.out_stage_bytes == 0);
   if (p.post != nullptr) {
 #pragma unroll
     for (int j = 0; j < 32; ++j) y[j] = act_apply(p.act, x[j]);
     store_chunk_staged(stg, y, p.p_dtype,
                        out_ptr(p.post, p.ldp, p.sbp, p.p_dtype, row_base, col0, batch, p),
-                       p.ldp * dtype_bytes(p.p_dtype), rows_valid, cols_valid);
+                       p.ldp * dtype_bytes(p.p_dtype), rows_valid, cols_valid,
+                     p.out_stage_bytes == 0);
   }
 }
 
@@ -492,13 +517,15 @@ __device__ __forceinline__ void epilogue_chunk(const Params& p, const uint32_t (
   if (p.d != nullptr)
     store_chunk_staged(stg, v, p.d_dtype,
                        out_ptr(p.d, p.ldd, p.sbd, p.d_dtype, row_base, col0, batch, p),
-                       p.ldd * dtype_bytes(p.d_dtype), rows_valid, cols_valid);
+                       p.ldd * dtype_bytes(p.d_dtype), rows_valid, cols_valid,
+                     p.out_stage_bytes == 0);
   if (p.post != nullptr) {
 #pragma unroll
     for (int j = 0; j < 32; ++j) v[j] = act_apply(p.act, v[j]);
     store_chunk_staged(stg, v, p.p_dtype,
                        out_ptr(p.post, p.ldp, p.sbp, p.p_dtype, row_base, col0, batch, p),
-                       p.ldp * dtype_bytes(p.p_dtype), rows_valid, cols_valid);
+                       p.ldp * dtype_bytes(p.p_dtype), rows_valid, cols_valid,
+                     p.out_stage_bytes == 0);
   }
 }
 

@@ -22,6 +22,7 @@ enum : int32_t {
   FLAG_TILE_COUNTS = 1,        // epilogue counts visits per tile into tile_counts
   FLAG_TEST_DROP_ACC_FULL = 2, // the MMA warp never signals "accumulator full" (timeout test)
   FLAG_DYNAMIC_SCHED = 4,      // tiles claimed from an atomic counter instead of a fixed stride
+  FLAG_DIRECT_STORES = 8,      // epilogue stores straight from registers (no staging buffers)
 };
 
 struct Params {
@@ -68,7 +69,8 @@ struct Params {
   int32_t d_dtype, p_dtype, c_dtype;
   int32_t act;
   int32_t dact;  // backward epilogue: C is the pre-activation x, D = act'(x) * acc, PostAct = act(x)
-  int32_t out_stage_bytes;  // shared-memory staging per epilogue warp: 32 x 32 outputs (2 or 4 KiB)
+  int32_t out_stage_bytes;  // shared-memory staging per epilogue warp: 32 x 32 outputs (2 or
+                            // 4 KiB); 0: each lane stores its own row directly
   float alpha, beta;
   const float* alpha_dev;
   const float* beta_dev;

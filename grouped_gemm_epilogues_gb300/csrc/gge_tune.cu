@@ -5,7 +5,7 @@
 //
 // The candidates are the shapes the kernels have: one CTA per 128 x 128 or
 // 128 x 256 tile, or a CTA pair per 256 x {256, 224, 192, 160} tile, times the
-// raster band of plain problems.  The pages' cooperative / ping-pong choice
+// raster band of plain problems, times staged or direct epilogue stores.  The pages' cooperative / ping-pong choice
 // has no counterpart (the accumulator is double-buffered in TMEM instead), and
 // their cluster shapes correspond to the one-CTA / CTA-pair choice.
 #include <cuda_runtime.h>
@@ -34,21 +34,25 @@ int32_t enumerate(const gge_gemm_args* args, int32_t op, int32_t num_groups, gge
   if (args->config != nullptr) base = *args->config;
   struct Shape { int cg, tile_n; };
   static const Shape kShapes[] = {{2, 256}, {2, 224}, {2, 192}, {2, 160}, {1, 256}, {1, 128}};
-  static const int kBands[] = {0, 2, 8};
-  const int n_bands = plain_op(op) ? 3 : 1;
+  static const int kBands[] = {0, 8};
+  const int n_bands = plain_op(op) ? 2 : 1;
   int32_t n = 0;
   for (const Shape& sh : kShapes) {
     if (sh.cg == 2 && gather_op(op)) continue;
     for (int b = 0; b < n_bands; ++b) {
-      gge_config c = base;
-      c.cta_group = sh.cg;
-      c.tile_n = sh.tile_n;
-      c.raster_band = kBands[b];
-      gge_gemm_args a = *args;
-      a.config = &c;
-      if (gge::validate_op(&a, op, num_groups) != GGE_OK) continue;
-      if (n < max && out != nullptr) out[n] = c;
-      ++n;
+      for (int direct = 0; direct < 2; ++direct) {
+        gge_config c = base;
+        c.cta_group = sh.cg;
+        c.tile_n = sh.tile_n;
+        c.raster_band = kBands[b];
+        c.flags = direct ? (base.flags | gge::FLAG_DIRECT_STORES)
+                         : (base.flags & ~gge::FLAG_DIRECT_STORES);
+        gge_gemm_args a = *args;
+        a.config = &c;
+        if (gge::validate_op(&a, op, num_groups) != GGE_OK) continue;
+        if (n < max && out != nullptr) out[n] = c;
+        ++n;
+      }
     }
   }
   return n;

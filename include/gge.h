@@ -94,7 +94,11 @@ typedef struct gge_config {
                              runs out and the call reports GGE_ERR_TIMEOUT;
                              bit 2: dynamic tile scheduler -- after its first
                              tile each CTA (pair) claims the next one from a
-                             counter in the workspace (needs a workspace)        */
+                             counter in the workspace (needs a workspace);
+                             bit 3: direct epilogue stores -- each lane stores its
+                             own output row instead of staging 32 x 32 chunks in
+                             shared memory (frees 16-32 KiB: one more pipeline
+                             stage on a CTA pair; best when K is long)          */
   int32_t cta_group;      /* 0 = auto; 1 = one CTA per 128-row tile; 2 = a CTA pair
                              per 256-row tile (tcgen05 cta_group::2, 256-column
                              tiles, not with the gather forms)                     */
@@ -298,7 +302,7 @@ gge_status gge_plan(const gge_gemm_args* args, int32_t num_groups, int32_t form,
  * warpgroups, 1x2 / 2x1 clusters and swap_ab to search by timing).  Here the space is the launch shapes this library
  * has: one CTA per 128 x 128 or 128 x 256 tile, or a CTA pair per 256 x 256,
  * 224, 192 or 160 tile (not with the gather forms), times the raster band of
- * plain problems.  The pages' swap_ab is not in the space: it needs M-major
+ * plain problems (auto or 8), times staged or direct epilogue stores.  The pages' swap_ab is not in the space: it needs M-major
  * output stores, which the epilogue does not have. */
 
 /* Which entry point a tuning call times. */

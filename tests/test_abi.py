@@ -204,7 +204,8 @@ def test_tune_candidates_follow_the_planner(L):
     c = binding.gge_tune_candidates("gemm", A, A, D=P, PostAct=P, act="gelu_tanh")
     shapes = {(x["cta_group"], x["tile_n"]) for x in c}
     assert shapes == {(2, 256), (2, 224), (2, 192), (2, 160), (1, 256), (1, 128)}
-    assert {x["raster_band"] for x in c} == {0, 2, 8} and len(c) == 18
+    assert {x["raster_band"] for x in c} == {0, 8} and len(c) == 24
+    assert {x["flags"] for x in c} == {0, 8}          # staged or direct epilogue stores
     # N-major B: the pair keeps 256-wide tiles only
     Bn = torch.zeros(4096, 4096, dtype=torch.bfloat16).t()
     c = binding.gge_tune_candidates("gemm", A, Bn, D=P)
@@ -215,9 +216,9 @@ def test_tune_candidates_follow_the_planner(L):
     D = torch.zeros(700, 384, dtype=torch.bfloat16)
     c = binding.gge_tune_candidates("gather_a", src, B, D=D, num_groups=4)
     assert {(x["cta_group"], x["tile_n"], x["raster_band"]) for x in c} == {(1, 256, 0), (1, 128, 0)}
-    # a caller's flags are kept in every candidate
+    # a caller's other flags are kept in every candidate
     c = binding.gge_tune_candidates("gemm", A, A, D=P, config=binding.make_config(flags=4))
-    assert all(x["flags"] == 4 for x in c)
+    assert {x["flags"] for x in c} == {4, 12}
     # nothing valid: no candidates
     assert binding.gge_tune_candidates("gemm", A, A, D=torch.zeros(4096, 4000,
                                                                    dtype=torch.bfloat16)) == []

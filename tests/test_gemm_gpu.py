@@ -93,12 +93,15 @@ def test_small_parity(case):
     _check_plain(w, t, out)
 
 
-@pytest.mark.parametrize("tile_n,cta_group", [(128, 1), (256, 1), (256, 2)])
-def test_tile_shapes_and_guard_columns(tile_n, cta_group):
+@pytest.mark.parametrize("tile_n,cta_group,flags", [(128, 1, 0), (256, 1, 0), (256, 2, 0),
+                                                    (128, 1, 8), (224, 2, 8)])
+def test_tile_shapes_and_guard_columns(tile_n, cta_group, flags):
+    # flags 8: direct (unstaged) epilogue stores
     w = wl.small("gemm_act_4096_bf16_gelu", 392, 264, 320, 2)
     t = wl.make(w)
     out = _outputs(w, 392, 264, 2, pad=24, fill=7.0)
-    _run_plain(w, t, out, config=binding.make_config(tile_n=tile_n, cta_group=cta_group))
+    _run_plain(w, t, out, config=binding.make_config(tile_n=tile_n, cta_group=cta_group,
+                                                     flags=flags))
     _check_plain(w, t, out)
     for k in ("D_full", "P_full"):
         assert (out[k][:, :, 264:].float() == 7.0).all()
@@ -224,4 +227,14 @@ def test_m_major_a(M, N, K, L, b_major, cg):
     assert t["A"].stride(1) == 1
     out = _outputs(w, M, N, L)
     _run_plain(w, t, out, config=binding.make_config(cta_group=cg))
+    _check_plain(w, t, out)
+
+
+@pytest.mark.parametrize("d_dtype,p_dtype,act", [("f32", "bf16", "silu"), ("f16", "f32", "relu")])
+def test_direct_stores_mixed_output_dtypes(d_dtype, p_dtype, act):
+    w = wl.small("gemm_act_4096_bf16_gelu", 300, 392, 136, 1, d_dtype=d_dtype, p_dtype=p_dtype,
+                 act=act)
+    t = wl.make(w)
+    out = _outputs(w, 300, 392, 1)
+    _run_plain(w, t, out, config=binding.make_config(flags=8))
     _check_plain(w, t, out)
