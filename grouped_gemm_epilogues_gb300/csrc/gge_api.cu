@@ -215,11 +215,11 @@ int variant_threads(int bn, bool gather, int cg) {
   return bn == 128 ? kernel_threads<128, false, 1>() : kernel_threads<256, false, 1>();
 }
 
-int variant_units_uncached(int bn, bool gather, int cg, size_t smem);
+int variant_units_uncached(int bn, bool gather, int cg, size_t smem, int cluster);
 
 // Resident CTAs (pairs) per device for a variant and shared-memory size, cached.
-int variant_units(int bn, bool gather, int cg, size_t smem) {
-  struct Entry { int dev, bn, cg; bool gather; size_t smem; int units; };
+int variant_units(int bn, bool gather, int cg, size_t smem, int cluster) {
+  struct Entry { int dev, bn, cg; bool gather; size_t smem; int cluster, units; };
   static std::mutex mu;
   static Entry cache[64];
   static int n = 0;
@@ -229,29 +229,31 @@ int variant_units(int bn, bool gather, int cg, size_t smem) {
     std::lock_guard<std::mutex> g(mu);
     for (int i = 0; i < n; ++i) {
       const Entry& e = cache[i];
-      if (e.dev == dev && e.bn == bn && e.cg == cg && e.gather == gather && e.smem == smem)
+      if (e.dev == dev && e.bn == bn && e.cg == cg && e.gather == gather && e.smem == smem &&
+          e.cluster == cluster)
         return e.units;
     }
   }
-  const int units = variant_units_uncached(bn, gather, cg, smem);
+  const int units = variant_units_uncached(bn, gather, cg, smem, cluster);
   if (units > 0) {
     std::lock_guard<std::mutex> g(mu);
-    if (n < 64) cache[n++] = Entry{dev, bn, cg, gather, smem, units};
+    if (n < 64) cache[n++] = Entry{dev, bn, cg, gather, smem, cluster, units};
   }
   return units;
 }
 
-int variant_units_uncached(int bn, bool gather, int cg, size_t smem) {
-  if (gather) return bn == 128 ? max_active_units<128, true, 1>(smem) : max_active_units<256, true, 1>(smem);
+int variant_units_uncached(int bn, bool gather, int cg, size_t smem, int cluster) {
+  if (gather)
+    return bn == 128 ? max_active_units<128, true, 1>(smem, 1) : max_active_units<256, true, 1>(smem, 1);
   if (cg == 2) {
     switch (bn) {
-      case 224: return max_active_units<224, false, 2>(smem);
-      case 192: return max_active_units<192, false, 2>(smem);
-      case 160: return max_active_units<160, false, 2>(smem);
-      default: return max_active_units<256, false, 2>(smem);
+      case 224: return max_active_units<224, false, 2>(smem, cluster);
+      case 192: return max_active_units<192, false, 2>(smem, cluster);
+      case 160: return max_active_units<160, false, 2>(smem, cluster);
+      default: return max_active_units<256, false, 2>(smem, cluster);
     }
   }
-  return bn == 128 ? max_active_units<128, false, 1>(smem) : max_active_units<256, false, 1>(smem);
+  return bn == 128 ? max_active_units<128, false, 1>(smem, 1) : max_active_units<256, false, 1>(smem, 1);
 }
 
 cudaError_t variant_launch(const Plan& pl, cudaStream_t st) {
@@ -416,6 +418,10 @@ gge_status make_plan(const gge_gemm_args* a, Form form, const int32_t* a_idx,
   // tile shape: 128 x BN on one CTA, or 256 x BN on a CTA pair
   int cg = cfg && cfg->cta_group ? cfg->cta_group : ((!gather && N > 128 && M >= 256) ? 2 : 1);
   if (cg == 2 && gather) return GGE_ERR_UNSUPPORTED;
+  // two CTA pairs per cluster sharing A by multicast: plain problems on pairs, static schedule
+  const bool mc = cfg && (cfg->flags & FLAG_PAIR_CLUSTER);
+  if (mc && (cg != 2 || varlen || gather || vk || (cfg->flags & (FLAG_DYNAMIC_SCHED | FLAG_TILE_COUNTS))))
+    return GGE_ERR_UNSUPPORTED;
   if (cg != 1 && cg != 2) return GGE_ERR_UNSUPPORTED;
   int bn = cfg && cfg->tile_n ? cfg->tile_n : 0;
   if (cg == 1) {
@@ -433,7 +439,7 @@ gge_status make_plan(const gge_gemm_args* a, Form form, const int32_t* a_idx,
           const int st256 = (kTileM + 128) * kRowBytesHost;
           const size_t smem256 =
               fixed256 + std::min(kMaxStages, (kMaxSmemOptin - fixed256) / st256) * st256;
-          units = variant_units(256, false, 2, smem256);
+          units = variant_units(256, false, 2, smem256, 2);
         }
         if (units > 0) bn = choose_pair_bn((M + 2 * kTileM - 1) / (2 * kTileM), N, L, units);
       }
@@ -471,10 +477,13 @@ gge_status make_plan(const gge_gemm_args* a, Form form, const int32_t* a_idx,
   int band = cfg && cfg->raster_band > 0 ? cfg->raster_band : 16;
   int64_t num_tiles = 0;
   if (!varlen) {
-    num_tiles = tiles_m * tiles_n * L;
+    // with two-pair clusters the schedule walks pairs of adjacent n-tiles
+    const int64_t sched_n = mc ? (tiles_n + 1) / 2 : tiles_n;
+    num_tiles = tiles_m * sched_n * L;
     if (num_tiles > kMaxExtent) return GGE_ERR_UNSUPPORTED;
-    p.sched = PlainSchedule::create(static_cast<int32_t>(tiles_m), static_cast<int32_t>(tiles_n),
+    p.sched = PlainSchedule::create(static_cast<int32_t>(tiles_m), static_cast<int32_t>(sched_n),
                                     static_cast<int32_t>(L), band);
+    p.mc = mc ? 1 : 0;
     band = p.sched.band;
     p.num_tiles = static_cast<int32_t>(num_tiles);
     if (vk) {
@@ -540,13 +549,16 @@ gge_status make_plan(const gge_gemm_args* a, Form form, const int32_t* a_idx,
   // launch shape: a persistent grid of at most one CTA (pair) per resident slot
   pl.shape.smem = static_cast<size_t>(fixed + stages * stage_bytes);
   pl.shape.threads = variant_threads(bn, pl.gather, cg);
-  int units_cap = cfg && cfg->num_ctas > 0 ? std::max(1, cfg->num_ctas / cg) : -1;
+  pl.shape.cluster = mc ? 4 : cg;
+  const int unit_ctas = pl.shape.cluster;
+  int units_cap = cfg && cfg->num_ctas > 0 ? std::max(1, cfg->num_ctas / unit_ctas) : -1;
   if (encode) {
-    const int resident = variant_units(bn, pl.gather, cg, pl.shape.smem);
+    const int resident = variant_units(bn, pl.gather, cg, pl.shape.smem, pl.shape.cluster);
     if (resident <= 0) return GGE_ERR_CUDA;
     units_cap = units_cap > 0 ? std::min(units_cap, resident) : resident;
   }
-  pl.shape.grid = units_cap > 0 ? cg * static_cast<int>(std::min<int64_t>(num_tiles, units_cap)) : -1;
+  pl.shape.grid =
+      units_cap > 0 ? unit_ctas * static_cast<int>(std::min<int64_t>(num_tiles, units_cap)) : -1;
   if (pl.empty || !encode) return GGE_OK;
   if (pl.shape.grid <= 0) pl.empty = true;  // e.g. varlen with no rows
   if (pl.empty) return GGE_OK;
@@ -556,9 +568,10 @@ gge_status make_plan(const gge_gemm_args* a, Form form, const int32_t* a_idx,
     if (gather) {
       // A rows are copied by the gather warps: no tensor map
     } else if (!a_mn) {
+      // two-pair clusters: each CTA loads half of its 128 rows and multicasts them
       s = encode_3d(&pl.tmA, a->A.ptr, es, K, a->A.rows, a->A.batch,
                     static_cast<uint64_t>(a->A.stride_row) * es, batch_stride_bytes(a->A, es), bk,
-                    kTileM);
+                    mc ? kTileM / 2 : kTileM);
       if (s != GGE_OK) return s;
     } else {
       s = encode_3d(&pl.tmA, a->A.ptr, es, a->A.rows, K, a->A.batch,

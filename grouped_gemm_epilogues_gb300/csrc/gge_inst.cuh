@@ -39,9 +39,9 @@ cudaError_t launch_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const Pa
   cfg.stream = stream;
   cfg.attrs = nullptr;
   cfg.numAttrs = 0;
-  if (CG > 1) {
+  if (shape.cluster > 1) {
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = CG;
+    attr[0].val.clusterDim.x = shape.cluster;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
@@ -56,10 +56,10 @@ int kernel_threads() {
 }
 
 template <int BN, bool GATHER, int CG>
-int max_active_units(size_t smem) {
+int max_active_units(size_t smem, int cluster) {
   auto kern = gemm_kernel<BN, GATHER, CG>;
   if (set_smem_limit<BN, GATHER, CG>(smem) != cudaSuccess) return -1;
-  if (CG == 1) {
+  if (cluster <= 1) {
     int per_sm = 0, dev = 0, sms = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, KernelCfg<BN, GATHER, CG>::kThreads,
                                                       smem) != cudaSuccess)
@@ -70,11 +70,11 @@ int max_active_units(size_t smem) {
   }
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = CG;
+  attr[0].val.clusterDim.x = cluster;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(CG * 256, 1, 1);
+  cfg.gridDim = dim3(cluster * 64, 1, 1);
   cfg.blockDim = dim3(KernelCfg<BN, GATHER, CG>::kThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.attrs = attr;
@@ -89,6 +89,6 @@ int max_active_units(size_t smem) {
                                                    const Params&, const LaunchShape&,      \
                                                    cudaStream_t);                          \
   template int kernel_threads<BN, GATHER, CG>();                                           \
-  template int max_active_units<BN, GATHER, CG>(size_t);
+  template int max_active_units<BN, GATHER, CG>(size_t, int);
 
 }  // namespace gge

@@ -115,6 +115,10 @@ struct TileCoord {
 struct Shared {
   uint32_t full, empty, tfull, tempty;  // barrier array bases (shared addresses)
   uint32_t map_full, map_empty;         // varlen-K map-slot barriers (kMapSlots each)
+  uint32_t pair;                        // this CTA's pair in a two-pair cluster (else 0)
+  uint32_t lead;                        // cluster rank of this pair's leader CTA
+  uint16_t pair_mask;                   // cluster ranks of this pair
+  uint16_t all_mask;                    // cluster ranks of every pair of the cluster
   volatile int32_t* abort;
   const int32_t* prefix;  // varlen-M: tile prefix [G+1]; varlen-K: group K ends [G]
   const int32_t* cu;      // varlen-M: cu_seqlens copy [G+1]; varlen-K: group K starts [G]
@@ -142,7 +146,8 @@ __device__ __forceinline__ TileCoord tile_coord(int32_t t, const Params& p, cons
     p.sched.map(t, l, mb, nb);
     tc.m_row0 = mb * TILE_M;
     tc.row_limit = p.M;
-    tc.n0 = nb * BN;
+    // two-pair clusters: the schedule walks n-tile pairs, pair q takes the q-th
+    tc.n0 = (p.mc ? 2 * nb + static_cast<int32_t>(sh.pair) : nb) * BN;
     tc.batch = l;
     // varlen-K operands are single [rows, total_K] matrices
     tc.a_batch = p.k_groups > 0 ? 0 : l;
@@ -586,7 +591,7 @@ __device__ __forceinline__ void epilogue_role(const Params& p, const Shared& sh,
         __syncwarp();
         if (lane == 0) {
           if (CG == 1) ptx::mbar_arrive(sh.tempty + 8 * acc);
-          else ptx::mbar_arrive_remote(ptx::mapa(sh.tempty + 8 * acc, 0));
+          else ptx::mbar_arrive_remote(ptx::mapa(sh.tempty + 8 * acc, sh.lead));
         }
       }
       const int32_t col0 = tc.n0 + c * 32;
@@ -652,14 +657,14 @@ __device__ __forceinline__ void mma_role(const Params& p, const Shared& sh, uint
         }
         // frees the stage (in both CTAs of a pair) once these MMAs finish
         if (CG == 1) ptx::mma_commit(sh.empty + 8 * stage);
-        else ptx::mma_commit_pair(sh.empty + 8 * stage, 0x3);
+        else ptx::mma_commit_pair(sh.empty + 8 * stage, sh.all_mask);
       }
       __syncwarp();
       if (++stage == p.stages) { stage = 0; phase ^= 1u; }
     }
     if (!(p.flags & FLAG_TEST_DROP_ACC_FULL) && ptx::elect_one()) {
       if (CG == 1) ptx::mma_commit(sh.tfull + 8 * acc);
-      else ptx::mma_commit_pair(sh.tfull + 8 * acc, 0x3);
+      else ptx::mma_commit_pair(sh.tfull + 8 * acc, sh.pair_mask);
     }
     __syncwarp();
     acc ^= 1u;
@@ -772,9 +777,17 @@ __device__ __forceinline__ void tma_producer_role(const Params& p, const Shared&
         // both CTAs' bytes of a pair complete on the leader's barrier, which the leader arms
         if (CG == 1) ptx::mbar_arrive_expect_tx(full, Cfg::kStageBytes);
         else if (rank == 0) ptx::mbar_arrive_expect_tx(full, 2 * Cfg::kStageBytes);
-        const uint32_t bar = (CG == 1) ? full : ptx::mapa(full, 0);
+        const uint32_t bar = (CG == 1) ? full : ptx::mapa(full, sh.lead);
         // K-major operands: one box of (bk columns, rows); M- / N-major: 64-wide boxes of bk rows
-        if (!p.a_mn_major) {
+        if (CG == 2 && p.mc) {
+          // this CTA's half of its A rows, multicast to the same rank in the other pair
+          const uint32_t crank = sh.lead + rank;
+          const uint16_t mask = static_cast<uint16_t>((1u << crank) | (1u << (crank ^ 2u)));
+          const uint32_t hdst = adst + sh.pair * (64 * kRowBytes);
+          const int32_t hrow = row0 + 64 * static_cast<int32_t>(sh.pair);
+          if (!p.a_mn_major) ptx::tma_load_3d_pair_mc(hdst, mA, bar, k0, hrow, tc.a_batch, mask);
+          else ptx::tma_load_3d_pair_mc(hdst, mA, bar, hrow, k0, tc.a_batch, mask);
+        } else if (!p.a_mn_major) {
           tma_load<CG>(adst, mA, bar, k0, row0, tc.a_batch);
         } else {
 #pragma unroll
@@ -1086,8 +1099,10 @@ __global__ void __launch_bounds__(KernelCfg<BN, GATHER, CG>::kThreads, 1)
   sh.map_empty = sh.map_full + 8 * kMapSlots;
   const uint32_t drain_bar = sh.tempty + 16;  // MMAs in flight have finished
   TileSched ts;
-  ts.unit = static_cast<int32_t>(blockIdx.x) / CG;
-  ts.units = static_cast<int32_t>(gridDim.x) / CG;
+  // a unit is a CTA, a pair, or a cluster of two pairs
+  const int unit_ctas = (CG == 2 && p.mc) ? 4 : CG;
+  ts.unit = static_cast<int32_t>(blockIdx.x) / unit_ctas;
+  ts.units = static_cast<int32_t>(gridDim.x) / unit_ctas;
   ts.dyn = (p.flags & FLAG_DYNAMIC_SCHED) != 0 && p.status != nullptr;
   ts.counter = p.status + 4;
   ts.full = drain_bar + 8;
@@ -1098,12 +1113,19 @@ __global__ void __launch_bounds__(KernelCfg<BN, GATHER, CG>::kThreads, 1)
   sh.cu = cu_s;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const uint32_t rank = (CG == 2) ? ptx::cluster_ctarank() : 0u;
+  // rank within the pair; a two-pair cluster has pairs {0, 1} and {2, 3}
+  const uint32_t crank = (CG == 2) ? ptx::cluster_ctarank() : 0u;
+  const uint32_t rank = crank & 1u;
+  sh.pair = crank >> 1;
+  sh.lead = crank & ~1u;
+  sh.pair_mask = static_cast<uint16_t>(3u << sh.lead);
+  sh.all_mask = static_cast<uint16_t>((CG == 2 && p.mc) ? 0xF : 0x3);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       ptx::mbar_init(sh.full + 8 * s, GATHER ? 1 + kGatherWarps * 32 : 1);
-      ptx::mbar_init(sh.empty + 8 * s, 1);
+      // a stage is free once every pair that reads the multicast A half has consumed it
+      ptx::mbar_init(sh.empty + 8 * s, (CG == 2 && p.mc) ? 2 : 1);
     }
     for (int b = 0; b < 2; ++b) {
       ptx::mbar_init(sh.tfull + 8 * b, 1);
@@ -1212,7 +1234,7 @@ __global__ void __launch_bounds__(KernelCfg<BN, GATHER, CG>::kThreads, 1)
   if (warp == Cfg::kMmaWarp && rank == 0) {
     if (ptx::elect_one()) {
       if (CG == 1) ptx::mma_commit(drain_bar);
-      else ptx::mma_commit_pair(drain_bar, 0x1);
+      else ptx::mma_commit_pair(drain_bar, static_cast<uint16_t>(1u << sh.lead));
     }
     __syncwarp();
     wait_phase<CG == 2>(drain_bar, 0, p, sh, 6, -1);

@@ -13,6 +13,7 @@ struct LaunchShape {
   int grid;
   int threads;
   size_t smem;
+  int cluster;  // CTAs per cluster: 1, 2 (a CTA pair) or 4 (two pairs)
 };
 
 template <int BN, bool GATHER, int CG>
@@ -22,9 +23,9 @@ cudaError_t launch_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const Pa
 template <int BN, bool GATHER, int CG>
 int kernel_threads();
 
-// Clusters of CG CTAs (with `smem` bytes each) that can be resident at once.
+// Clusters of `cluster` CTAs (with `smem` bytes each) that can be resident at once.
 template <int BN, bool GATHER, int CG>
-int max_active_units(size_t smem);
+int max_active_units(size_t smem, int cluster);
 
 // Host-only validation of one call of entry point `op` (GGE_OP_*) as it would
 // be planned, without launching or touching the GPU (gge_api.cu).

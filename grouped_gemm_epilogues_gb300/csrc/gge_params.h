@@ -23,6 +23,7 @@ enum : int32_t {
   FLAG_TEST_DROP_ACC_FULL = 2, // the MMA warp never signals "accumulator full" (timeout test)
   FLAG_DYNAMIC_SCHED = 4,      // tiles claimed from an atomic counter instead of a fixed stride
   FLAG_DIRECT_STORES = 8,      // epilogue stores straight from registers (no staging buffers)
+  FLAG_PAIR_CLUSTER = 16,      // two CTA pairs per cluster share A by TMA multicast
 };
 
 struct Params {
@@ -80,6 +81,9 @@ struct Params {
   int32_t f8;          // operands are 8-bit (kind::f8f6f4)
   int32_t a_mn_major;  // A staged M-major (16-bit operands only)
   int32_t b_mn_major;  // B staged N-major (16-bit operands only)
+  int32_t mc;          // clusters of two CTA pairs: pair q of a cluster takes n-tile 2 nb + q
+                       // of the scheduled (m, nb), and each CTA loads half of its A rows
+                       // and multicasts them to the CTA of the same rank in the other pair
 
   // control
   int32_t* status;       // workspace: [0] code, [1] where, [2] tile, [3] detail,

@@ -98,7 +98,12 @@ typedef struct gge_config {
                              bit 3: direct epilogue stores -- each lane stores its
                              own output row instead of staging 32 x 32 chunks in
                              shared memory (frees 16-32 KiB: one more pipeline
-                             stage on a CTA pair; best when K is long)          */
+                             stage on a CTA pair; best when K is long);
+                             bit 4: clusters of two CTA pairs on adjacent n-tiles
+                             of a plain problem: each CTA loads half of its A rows
+                             and TMA-multicasts them to the other pair (a quarter
+                             less L2 traffic; needs cta_group 2, the static
+                             schedule, no tile counts)                            */
   int32_t cta_group;      /* 0 = auto; 1 = one CTA per 128-row tile; 2 = a CTA pair
                              per 256-row tile (tcgen05 cta_group::2, 256-column
                              tiles, not with the gather forms)                     */
