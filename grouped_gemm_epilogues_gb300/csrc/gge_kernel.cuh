@@ -8,19 +8,22 @@
 // tensor core instead of Hopper warpgroup MMA:
 //
 //   warps 0-7  epilogue: TMEM -> registers (tcgen05.ld), alpha / beta / C /
-//              activation in fp32, round, store D and PostAct.  Warp w owns
-//              TMEM lanes 32(w%4)..+31 (tile rows) and every other 32-column chunk.
+//              activation in fp32, round, and store D and PostAct through a
+//              per-warp shared-memory transpose (row-contiguous stores).  Warp w
+//              owns TMEM lanes 32(w%4)..+31 (tile rows) and every other
+//              32-column chunk (warps 0-3 and every chunk in the gather forms).
 //   warp  8    TMEM allocator and MMA issuer (one elected lane): tcgen05.mma
 //              128 x BN x 16 (x32 for 8-bit) from shared memory into a
 //              double-buffered fp32 TMEM accumulator, so the epilogue of
 //              tile i overlaps the main loop of tile i+1 (this replaces the
-//              pages' ping-pong warpgroups).
+//              pages' ping-pong warpgroups).  (warp 4 in the gather forms)
 //   warp  9    TMA producer: A and B k-tiles into an S-stage shared-memory
 //              ring (128-byte swizzle), one mbarrier pair per stage.
 //   warp 10    varlen-K: writes each ragged group's clipped tensor maps ahead
 //              of the producer (otherwise idle).
-//   warps 9-12 (gather-A form) row gather of A with 16-byte cp.async into the
-//              same swizzled layout, B still by TMA (GemmSm90.load_AB_gather_A).
+//   warps 5-8  (gather forms) row gathers with 16-byte cp.async into the same
+//              swizzled layouts, B by TMA (GemmSm90.load_AB_gather_A, and the
+//              gather along K of varlen-K).
 //
 // With CG = 2 a cluster of two CTAs (a CTA pair) computes a 256 x BN tile
 // (BN = 256, 224, 192 or 160; narrower tiles even out the last wave):
@@ -28,12 +31,13 @@
 // leader CTA issues tcgen05.mma.cta_group::2 over both CTAs' shared memory,
 // and each CTA's TMEM receives its own 128 accumulator rows.  The pair halves
 // the B bytes each SM stages per FLOP, so a stage is 32 KiB instead of 48 KiB
-// and seven stages fit; this is the Blackwell counterpart of the pages'
-// Hopper clusters with TMA multicast.
+// and six stages fit.  Optionally two pairs form a cluster of four on adjacent
+// n-tiles and share A by TMA multicast (Params::mc).
 //
-// Every CTA (pair) walks the same static persistent schedule (tile t, t + grid, ...);
-// tile coordinates come from FastDivmod (plain) or from a per-group tile
-// prefix sum in shared memory (varlen-M, VarlenMTileScheduler's role).
+// Every CTA (pair) walks the same static persistent schedule (tile t, t + grid, ...),
+// or claims tiles from an atomic counter; tile coordinates come from
+// FastDivmod (plain) or from a per-group tile prefix sum in shared memory
+// (varlen-M, VarlenMTileScheduler's role).
 //
 // Every mbarrier wait is bounded by Params::timeout_ns of %globaltimer; on
 // expiry the kernel records DEV_TIMEOUT in the status words, raises a
