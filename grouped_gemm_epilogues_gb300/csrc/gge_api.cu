@@ -28,6 +28,7 @@ constexpr int kMaxSmemOptin = 232448;  // 227 KiB per block on sm_100 / sm_103
 constexpr int kCtrlBytesHost = 1024;
 constexpr int kEpiWarpsHost = 8;          // epilogue warps of the TMA variants (4 with gathers)
 constexpr int kMaxGroupsHost = 1024;
+constexpr int kIdxChunkHost = 2048;       // gather-K index entries staged in shared memory
 constexpr size_t kWorkspaceBytes = 256;
 constexpr size_t kMapSlotsHost = 16;     // varlen-K tensor-map slots per CTA (kernel kMapSlots)
 constexpr size_t kMapSlotBytesHost = 256;
@@ -452,7 +453,9 @@ gge_status make_plan(const gge_gemm_args* a, Form form, const int32_t* a_idx,
   const int tile_m = kTileM * cg;
   const int bk = kRowBytesHost / es;
   const int stage_bytes = (kTileM + bn / cg) * kRowBytesHost;
-  const int varlen_bytes = (varlen || vk) ? 2 * 4 * (kMaxGroupsHost + 1) : 0;
+  // the varlen group tables, then (gather-K) the staged source-row indices
+  const int varlen_bytes = ((varlen || vk) ? 2 * 4 * (kMaxGroupsHost + 1) : 0) +
+                           (gk ? 16 + 4 * kIdxChunkHost : 0);  // + alignment padding
   const int epi_warps = gather ? kEpiWarpsHost / 2 : kEpiWarpsHost;
   const int fixed = 1024 + kCtrlBytesHost + varlen_bytes + epi_warps * out_stage;
   int stages = (kMaxSmemOptin - fixed) / stage_bytes;

@@ -59,6 +59,9 @@ constexpr int kRowBytes = 128;     // bytes of K per stage row (one swizzle span
 constexpr int kGatherWarps = 4;
 constexpr int kGatherThreads = kGatherWarps * 32;
 constexpr int kMaxGroups = 1024;   // varlen groups held in shared memory
+// gather-K: source-row indices of up to this many K rows (32 k-tiles) are staged
+// in shared memory at a time
+constexpr int kIdxChunk = 2048;
 constexpr int kCtrlBytes = 1024;   // barriers, flags and the tile ring (bytes 0..255),
                                    // the varlen-K tensor-map scratch (256..511) and
                                    // map-slot barriers (512..767)
@@ -126,6 +129,7 @@ struct Shared {
   volatile int32_t* abort;
   const int32_t* prefix;  // varlen-M: tile prefix [G+1]; varlen-K: group K ends [G]
   const int32_t* cu;      // varlen-M: cu_seqlens copy [G+1]; varlen-K: group K starts [G]
+  int32_t* idx;           // gather-K: staged source-row indices [kIdxChunk]
 };
 
 template <int BN, int TILE_M>
@@ -912,28 +916,34 @@ __device__ __forceinline__ void copy_b_clipped(const Params& p, uint32_t dst, in
 }
 
 static_assert(kGatherThreads == 128, "gather-K: 16 threads per K row, 8 rows per thread");
+static_assert(kIdxChunk % kGatherThreads == 0 && (kIdxChunk / 64 & (kIdxChunk / 64 - 1)) == 0,
+              "gather-K index chunks: whole passes of the gather threads, a power of two of k-tiles");
 
-// (A layout with one index load per warp and shuffles measured 22 % slower than
-// these per-thread loads, whose 16 same-address lanes are served together.)
-// Source rows of K rows ksub + 8 j (j < 8) of k-tile kt, or -1 where the row
-// reads zeros (past the group's end, past M, or an index out of range, which is
-// recorded).
-__device__ __forceinline__ void gather_k_indices(const Params& p, const KRange& kr, int32_t kt,
-                                                 int ksub, bool m_ok, int32_t tile,
-                                                 int32_t (&src)[8]) {
-  const int32_t kbase = kr.k0 + kt * p.bk;
+// Stages into this warp's index buffer the source rows of the K rows it copies
+// (rows 2w + r + 8j, r < 2, j < 8, of each k-tile; w = this gather warp) for the
+// kIdxChunk / 64 k-tiles from K row kbase0 on, at entry 16 * k-tile + 8 r + j.
+// Rows at or past k_end get -1 (zeros); an index out of range (or negative) too,
+// and it is recorded.  Loading the indices per k-tile instead left every k-tile
+// waiting for loads queued behind the gather copies (half the producer's time).
+__device__ __forceinline__ void stage_k_indices(const Params& p, int32_t* idxw, int32_t kbase0,
+                                                int32_t k_end, int w, int lane, int32_t tile) {
+  constexpr int kPer = kIdxChunk / kGatherThreads;  // entries per lane
+  int32_t v[kPer];
 #pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    const int32_t kg = kbase + ksub + 8 * j;
-    src[j] = (m_ok && kg < kr.k_end) ? __ldg(p.a_idx + kg) : -1;
+  for (int i = 0; i < kPer; ++i) {
+    const int e = lane + 32 * i;
+    const int32_t kg = kbase0 + (e >> 4) * 64 + 2 * w + ((e >> 3) & 1) + 8 * (e & 7);
+    v[i] = (kg < k_end) ? __ldg(p.a_idx + kg) : -1;
   }
 #pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    if (src[j] >= p.a_src_rows || src[j] < -1 ||
-        (src[j] == -1 && m_ok && kbase + ksub + 8 * j < kr.k_end)) {
+  for (int i = 0; i < kPer; ++i) {
+    const int e = lane + 32 * i;
+    const int32_t kg = kbase0 + (e >> 4) * 64 + 2 * w + ((e >> 3) & 1) + 8 * (e & 7);
+    if (kg < k_end && (v[i] < 0 || v[i] >= p.a_src_rows)) {
       record_status(p, DEV_INDEX_RANGE, 4, tile);
-      src[j] = -1;
+      v[i] = -1;
     }
+    idxw[e] = v[i];
   }
 }
 
@@ -941,7 +951,8 @@ __device__ __forceinline__ void gather_k_indices(const Params& p, const KRange& 
 // of the k-tile's effective A^T is row a_idx[k] of the source X (M contiguous
 // 16-bit elements), staged M-major: 64-element chunks of bk K rows, 128-byte
 // swizzle.  Thread gt copies 16-byte piece gt % 16 of the tile's 256-byte M
-// segment for K rows gt / 16 + 8 i; the indices are loaded one k-tile ahead.
+// segment for K rows gt / 16 + 8 i; the indices come from shared memory,
+// staged kIdxChunk at a time.
 // B comes by TMA, except the last k-tile of a ragged group, copied only up to
 // the group's end.  A K row past the group's end, an M element past M, or an
 // index out of range reads zeros (the last is reported).
@@ -955,6 +966,10 @@ __device__ __forceinline__ void gather_k_producer_role(const Params& p, const Sh
   const int q = gt & 15;
   const int ksub = gt >> 4;
   const uint32_t a_off = static_cast<uint32_t>(q >> 3) * (64 * kRowBytes);  // M chunk
+  const int gw = gt >> 5, lane = gt & 31;
+  int32_t* idxw = sh.idx + gw * (kIdxChunk / kGatherWarps);  // this warp's index buffer
+  // this thread's eight rows of a k-tile: 32 contiguous bytes, 64 bytes per k-tile
+  const uint32_t my_idx = ptx::smem_addr(idxw + (lane >> 4) * 8);
   int stage = 0;
   uint32_t phase = 0;
   for (int i = 0;; ++i) {
@@ -964,15 +979,15 @@ __device__ __forceinline__ void gather_k_producer_role(const Params& p, const Sh
     const KRange kr = k_range(p, sh, tc.batch);
     const int32_t m_el = tc.m_row0 + 8 * q;
     const bool m_ok = m_el < p.M;  // M is a multiple of 8: whole pieces
-    // the source rows of this thread's K rows, loaded one k-tile ahead of their copies
-    int32_t nxt[8];
-    gather_k_indices(p, kr, 0, ksub, m_ok, t, nxt);
+    constexpr int kChunkTiles = kIdxChunk / 64;
     for (int kt = 0; kt < kr.tiles; ++kt) {
-      int32_t cur[8];
-#pragma unroll
-      for (int j = 0; j < 8; ++j) cur[j] = nxt[j];
-      if (kt + 1 < kr.tiles) gather_k_indices(p, kr, kt + 1, ksub, m_ok, t, nxt);
-      if (!wait_phase(sh.empty + 8 * stage, phase ^ 1u, p, sh, 0, t)) return;
+      if ((kt & (kChunkTiles - 1)) == 0) {
+        __syncwarp();  // the warp is done with the previous chunk
+        stage_k_indices(p, idxw, kr.k0 + kt * 64, kr.k_end, gw, lane, t);
+        __syncwarp();
+      }
+      const bool ok = wait_phase(sh.empty + 8 * stage, phase ^ 1u, p, sh, 0, t);
+      if (!__all_sync(0xffffffffu, ok)) return;
       const uint32_t full = sh.full + 8 * stage;
       const int32_t kbase = kr.k0 + kt * p.bk;
       const uint32_t abase = a0 + stage * Cfg::kABytes;
@@ -988,10 +1003,20 @@ __device__ __forceinline__ void gather_k_producer_role(const Params& p, const Sh
         if (gt < 32 && ptx::elect_one()) ptx::mbar_arrive(full);
         copy_b_clipped<BN>(p, bbase, kbase, kr.k_end, tc.n0, gt);
       }
+      // the k-tile's eight source rows in two vector loads, all read before the first
+      // copy (read one by one between the copies, their latencies added up: ~1,200
+      // cycles per k-tile)
+      const uint32_t ia = my_idx + static_cast<uint32_t>(kt & (kChunkTiles - 1)) * 64u;
+      const uint4 lo = ptx::ld_shared_v4(ia), hi = ptx::ld_shared_v4(ia + 16);
+      const int32_t rows[8] = {static_cast<int32_t>(lo.x), static_cast<int32_t>(lo.y),
+                               static_cast<int32_t>(lo.z), static_cast<int32_t>(lo.w),
+                               static_cast<int32_t>(hi.x), static_cast<int32_t>(hi.y),
+                               static_cast<int32_t>(hi.z), static_cast<int32_t>(hi.w)};
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
         const int k = ksub + 8 * j;
-        const int32_t src = cur[j];
+        // K rows past the group's end (and M pieces past M) read zeros
+        const int32_t src = m_ok ? rows[j] : -1;
         const uint8_t* sp =
             src >= 0 ? p.a_src + static_cast<int64_t>(src) * p.a_src_ld + 2 * static_cast<int64_t>(m_el)
                      : p.a_src;
@@ -1089,6 +1114,9 @@ __global__ void __launch_bounds__(KernelCfg<BN, GATHER, CG>::kThreads, 1)
   int32_t* abort_flag = reinterpret_cast<int32_t*>(tmem_slot + 1);
   int32_t* prefix = reinterpret_cast<int32_t*>(ctrl + kCtrlBytes);
   int32_t* cu_s = prefix + (kMaxGroups + 1);
+  // gather-K only (the host sizes it); 16-byte aligned for vector reads (prefix
+  // is 1 KiB aligned)
+  int32_t* idx_s = prefix + ((2 * (kMaxGroups + 1) + 3) & ~3);
 
   Shared sh;
   sh.full = ptx::smem_addr(ctrl);
@@ -1111,6 +1139,7 @@ __global__ void __launch_bounds__(KernelCfg<BN, GATHER, CG>::kThreads, 1)
   sh.abort = abort_flag;
   sh.prefix = prefix;
   sh.cu = cu_s;
+  sh.idx = idx_s;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // rank within the pair; a two-pair cluster has pairs {0, 1} and {2, 3}
