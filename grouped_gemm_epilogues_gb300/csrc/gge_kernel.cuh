@@ -285,44 +285,80 @@ __device__ __forceinline__ int32_t sched_next(const TileSched& ts, int i, const 
 
 // ------------------------------------------------------------- epilogue math
 
-__device__ __forceinline__ float act_apply(int act, float x) {
-  switch (act) {
-    case ACT_RELU:
-      return (x <= 0.f) ? 0.f : x;  // NaN propagates, -0 -> +0
-    case ACT_GELU_TANH: {
-      // 0.5 x (1 + tanh u) written as x / (1 + exp(-2u)): no cancellation in the tail
-      const float u = 0.7978845608028654f * fmaf(0.044715f * x, x * x, x);
-      return __fdividef(x, 1.f + __expf(-2.f * u));
-    }
-    case ACT_SILU:
-      return __fdividef(x, 1.f + __expf(-x));
-    case ACT_RELU_SQ:
-      return (x <= 0.f) ? 0.f : x * x;
-    default:
-      return x;
+// The activation of one value; ACT is fixed at compile time.
+template <int ACT>
+__device__ __forceinline__ float act_one(float x) {
+  if constexpr (ACT == ACT_RELU) {
+    return (x <= 0.f) ? 0.f : x;  // NaN propagates, -0 -> +0
+  } else if constexpr (ACT == ACT_GELU_TANH) {
+    // 0.5 x (1 + tanh u) written as x / (1 + exp(-2u)): no cancellation in the tail
+    const float u = 0.7978845608028654f * fmaf(0.044715f * x, x * x, x);
+    return __fdividef(x, 1.f + __expf(-2.f * u));
+  } else if constexpr (ACT == ACT_SILU) {
+    return __fdividef(x, 1.f + __expf(-x));
+  } else if constexpr (ACT == ACT_RELU_SQ) {
+    return (x <= 0.f) ? 0.f : x * x;
+  } else {
+    return x;
   }
 }
 
 // act'(x) for the backward epilogue.
-__device__ __forceinline__ float dact_apply(int act, float x) {
+template <int ACT>
+__device__ __forceinline__ float dact_one(float x) {
+  if constexpr (ACT == ACT_RELU) {
+    return (x > 0.f) ? 1.f : 0.f;
+  } else if constexpr (ACT == ACT_RELU_SQ) {
+    return (x <= 0.f) ? 0.f : 2.f * x;
+  } else if constexpr (ACT == ACT_GELU_TANH) {
+    // s = sigmoid(2u) = (1 + tanh u) / 2 and 1 - tanh^2 u = 4 s (1 - s)
+    const float u = 0.7978845608028654f * fmaf(0.044715f * x, x * x, x);
+    const float s = __fdividef(1.f, 1.f + __expf(-2.f * u));
+    const float du = 0.7978845608028654f * fmaf(3.f * 0.044715f * x, x, 1.f);
+    return fmaf(2.f * x * s * (1.f - s), du, s);
+  } else if constexpr (ACT == ACT_SILU) {
+    const float s = __fdividef(1.f, 1.f + __expf(-x));
+    return s * fmaf(x, 1.f - s, 1.f);
+  } else {
+    return 1.f;
+  }
+}
+
+// The activation's choice is made once per 32-value chunk, outside the value
+// loop: switched per value, the unrolled loop kept every activation's
+// arithmetic in the instruction stream.
+template <int ACT>
+__device__ __forceinline__ void act_chunk_t(float (&v)[32]) {
+#pragma unroll
+  for (int j = 0; j < 32; ++j) v[j] = act_one<ACT>(v[j]);
+}
+
+__device__ __forceinline__ void act_chunk(int act, float (&v)[32]) {
   switch (act) {
-    case ACT_RELU:
-      return (x > 0.f) ? 1.f : 0.f;
-    case ACT_RELU_SQ:
-      return (x <= 0.f) ? 0.f : 2.f * x;
-    case ACT_GELU_TANH: {
-      // s = sigmoid(2u) = (1 + tanh u) / 2 and 1 - tanh^2 u = 4 s (1 - s)
-      const float u = 0.7978845608028654f * fmaf(0.044715f * x, x * x, x);
-      const float s = __fdividef(1.f, 1.f + __expf(-2.f * u));
-      const float du = 0.7978845608028654f * fmaf(3.f * 0.044715f * x, x, 1.f);
-      return fmaf(2.f * x * s * (1.f - s), du, s);
-    }
-    case ACT_SILU: {
-      const float s = __fdividef(1.f, 1.f + __expf(-x));
-      return s * fmaf(x, 1.f - s, 1.f);
-    }
-    default:
-      return 1.f;
+    case ACT_RELU: act_chunk_t<ACT_RELU>(v); break;
+    case ACT_GELU_TANH: act_chunk_t<ACT_GELU_TANH>(v); break;
+    case ACT_SILU: act_chunk_t<ACT_SILU>(v); break;
+    case ACT_RELU_SQ: act_chunk_t<ACT_RELU_SQ>(v); break;
+    default: break;
+  }
+}
+
+// y = act'(x) * dout over a chunk.
+template <int ACT>
+__device__ __forceinline__ void dact_chunk_t(const float (&x)[32], const uint32_t (&dout)[32],
+                                             float (&y)[32]) {
+#pragma unroll
+  for (int j = 0; j < 32; ++j) y[j] = dact_one<ACT>(x[j]) * __uint_as_float(dout[j]);
+}
+
+__device__ __forceinline__ void dact_chunk(int act, const float (&x)[32],
+                                           const uint32_t (&dout)[32], float (&y)[32]) {
+  switch (act) {
+    case ACT_RELU: dact_chunk_t<ACT_RELU>(x, dout, y); break;
+    case ACT_GELU_TANH: dact_chunk_t<ACT_GELU_TANH>(x, dout, y); break;
+    case ACT_SILU: dact_chunk_t<ACT_SILU>(x, dout, y); break;
+    case ACT_RELU_SQ: dact_chunk_t<ACT_RELU_SQ>(x, dout, y); break;
+    default: dact_chunk_t<ACT_NONE>(x, dout, y); break;
   }
 }
 
@@ -383,15 +419,27 @@ __device__ __forceinline__ void c_values8(const CRegs& c, const Params& p, const
   }
 }
 
-// Pack 8 fp32 values into one 16-byte word of the output dtype (RNE); fp32
-// takes two words.
-__device__ __forceinline__ uint32_t pack2(int dtype, float a, float b) {
-  if (dtype == DT_BF16) {
+// Two fp32 values as one 32-bit word of a 16-bit output type (RNE).
+template <bool BF16>
+__device__ __forceinline__ uint32_t pack2(float a, float b) {
+  if constexpr (BF16) {
     const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
     return *reinterpret_cast<const uint32_t*>(&h);
+  } else {
+    const __half2 h = __floats2half2_rn(a, b);
+    return *reinterpret_cast<const uint32_t*>(&h);
   }
-  const __half2 h = __floats2half2_rn(a, b);
-  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+// A lane's 32 values as 16 words of the 16-bit output type, the type chosen once.
+__device__ __forceinline__ void pack32(int dtype, const float (&x)[32], uint32_t (&w)[16]) {
+  if (dtype == DT_BF16) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) w[i] = pack2<true>(x[2 * i], x[2 * i + 1]);
+  } else {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) w[i] = pack2<false>(x[2 * i], x[2 * i + 1]);
+  }
 }
 
 // Write a warp's 32 x 32 output chunk (lane = row, x = its 32 columns) to global
@@ -418,13 +466,13 @@ __device__ __forceinline__ void store_chunk_staged(uint32_t stg, const float (&x
               make_uint4(__float_as_uint(x[4 * q]), __float_as_uint(x[4 * q + 1]),
                          __float_as_uint(x[4 * q + 2]), __float_as_uint(x[4 * q + 3]));
     } else {
+      uint32_t w[16];
+      pack32(dtype, x, w);
 #pragma unroll
       for (int q = 0; q < 4; ++q)
         if (8 * q < cols_valid)
           *reinterpret_cast<uint4*>(o + 16 * q) =
-              make_uint4(pack2(dtype, x[8 * q], x[8 * q + 1]), pack2(dtype, x[8 * q + 2], x[8 * q + 3]),
-                         pack2(dtype, x[8 * q + 4], x[8 * q + 5]),
-                         pack2(dtype, x[8 * q + 6], x[8 * q + 7]));
+              make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
     }
     return;
   }
@@ -444,13 +492,12 @@ __device__ __forceinline__ void store_chunk_staged(uint32_t stg, const float (&x
         *reinterpret_cast<uint4*>(out + r * ld_bytes + 16 * q) = v;
     }
   } else {
+    uint32_t w[16];
+    pack32(dtype, x, w);
 #pragma unroll
     for (int q = 0; q < 4; ++q)
       ptx::st_shared_v4(stg + lane * 64 + ((q ^ ((lane >> 1) & 3)) << 4),
-                        make_uint4(pack2(dtype, x[8 * q], x[8 * q + 1]),
-                                   pack2(dtype, x[8 * q + 2], x[8 * q + 3]),
-                                   pack2(dtype, x[8 * q + 4], x[8 * q + 5]),
-                                   pack2(dtype, x[8 * q + 6], x[8 * q + 7])));
+                        make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]));
     __syncwarp();
     const int q = lane & 3;
 #pragma unroll
@@ -486,15 +533,15 @@ __device__ __forceinline__ void epilogue_chunk_dact(const Params& p, const uint3
   float x[32], y[32];
 #pragma unroll
   for (int g = 0; g < 4; ++g) c_values8(creg, p, crow, col0, g, &x[8 * g]);
-#pragma unroll
-  for (int j = 0; j < 32; ++j) y[j] = dact_apply(p.act, x[j]) * __uint_as_float(acc[j]);
+  dact_chunk(p.act, x, acc, y);
   store_chunk_staged(stg, y, p.d_dtype,
                      out_ptr(p.d, p.ldd, p.sbd, p.d_dtype, row_base, col0, batch, p),
                      p.ldd * dtype_bytes(p.d_dtype), rows_valid, cols_valid,
                      p.out_stage_bytes == 0);
   if (p.post != nullptr) {
 #pragma unroll
-    for (int j = 0; j < 32; ++j) y[j] = act_apply(p.act, x[j]);
+    for (int j = 0; j < 32; ++j) y[j] = x[j];
+    act_chunk(p.act, y);
     store_chunk_staged(stg, y, p.p_dtype,
                        out_ptr(p.post, p.ldp, p.sbp, p.p_dtype, row_base, col0, batch, p),
                        p.ldp * dtype_bytes(p.p_dtype), rows_valid, cols_valid,
@@ -533,8 +580,7 @@ __device__ __forceinline__ void epilogue_chunk(const Params& p, const uint32_t (
                        p.ldd * dtype_bytes(p.d_dtype), rows_valid, cols_valid,
                      p.out_stage_bytes == 0);
   if (p.post != nullptr) {
-#pragma unroll
-    for (int j = 0; j < 32; ++j) v[j] = act_apply(p.act, v[j]);
+    act_chunk(p.act, v);
     store_chunk_staged(stg, v, p.p_dtype,
                        out_ptr(p.post, p.ldp, p.sbp, p.p_dtype, row_base, col0, batch, p),
                        p.ldp * dtype_bytes(p.p_dtype), rows_valid, cols_valid,
