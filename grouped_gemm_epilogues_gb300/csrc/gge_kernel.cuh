@@ -393,10 +393,11 @@ __device__ __forceinline__ void load_c_chunk(const Params& p, int32_t row, int32
 
 // Eight values of C (group g of 8 columns of the chunk) as fp32: from the
 // prefetched registers (16-bit C), or read now through `crow` (fp32 C; NULL
-// for a row that does not exist).
+// for a row that does not exist).  CDT is C's dtype.
+template <int CDT>
 __device__ __forceinline__ void c_values8(const CRegs& c, const Params& p, const char* crow,
-                                          int32_t col0, int g, float* out) {
-  if (p.c_dtype == DT_F32) {
+                                          int32_t col0, int g, float (&out)[8]) {
+  if constexpr (CDT == DT_F32) {
     float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a;
     if (crow != nullptr && col0 + 8 * g < p.N) {
       a = __ldg(reinterpret_cast<const float4*>(crow) + 2 * g);
@@ -409,7 +410,7 @@ __device__ __forceinline__ void c_values8(const CRegs& c, const Params& p, const
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       float2 f;
-      if (p.c_dtype == DT_BF16)
+      if constexpr (CDT == DT_BF16)
         f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[i]));
       else
         f = __half22float2(*reinterpret_cast<const __half2*>(&w[i]));
@@ -417,6 +418,46 @@ __device__ __forceinline__ void c_values8(const CRegs& c, const Params& p, const
       out[2 * i + 1] = f.y;
     }
   }
+}
+
+// v += beta * C over the chunk (C's dtype chosen once, outside the value loops).
+template <int CDT>
+__device__ __forceinline__ void add_beta_c_t(const CRegs& c, const Params& p, const char* crow,
+                                             int32_t col0, float beta, float (&v)[32]) {
+#pragma unroll
+  for (int g = 0; g < 4; ++g) {
+    float cv[8];
+    c_values8<CDT>(c, p, crow, col0, g, cv);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) v[8 * g + j] = fmaf(beta, cv[j], v[8 * g + j]);
+  }
+}
+
+__device__ __forceinline__ void add_beta_c(const CRegs& c, const Params& p, const char* crow,
+                                           int32_t col0, float beta, float (&v)[32]) {
+  if (p.c_dtype == DT_F32) add_beta_c_t<DT_F32>(c, p, crow, col0, beta, v);
+  else if (p.c_dtype == DT_BF16) add_beta_c_t<DT_BF16>(c, p, crow, col0, beta, v);
+  else add_beta_c_t<DT_F16>(c, p, crow, col0, beta, v);
+}
+
+// All 32 values of C as fp32 (the backward epilogue's pre-activation).
+template <int CDT>
+__device__ __forceinline__ void c_values32_t(const CRegs& c, const Params& p, const char* crow,
+                                             int32_t col0, float (&x)[32]) {
+#pragma unroll
+  for (int g = 0; g < 4; ++g) {
+    float cv[8];
+    c_values8<CDT>(c, p, crow, col0, g, cv);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) x[8 * g + j] = cv[j];
+  }
+}
+
+__device__ __forceinline__ void c_values32(const CRegs& c, const Params& p, const char* crow,
+                                           int32_t col0, float (&x)[32]) {
+  if (p.c_dtype == DT_F32) c_values32_t<DT_F32>(c, p, crow, col0, x);
+  else if (p.c_dtype == DT_BF16) c_values32_t<DT_BF16>(c, p, crow, col0, x);
+  else c_values32_t<DT_F16>(c, p, crow, col0, x);
 }
 
 // Two fp32 values as one 32-bit word of a 16-bit output type (RNE).
@@ -531,8 +572,7 @@ __device__ __forceinline__ void epilogue_chunk_dact(const Params& p, const uint3
   const char* crow = (p.c_dtype == DT_F32 && lane < rows_valid)
                          ? c_ptr(p, row_base + lane, col0, batch) : nullptr;
   float x[32], y[32];
-#pragma unroll
-  for (int g = 0; g < 4; ++g) c_values8(creg, p, crow, col0, g, &x[8 * g]);
+  c_values32(creg, p, crow, col0, x);
   dact_chunk(p.act, x, acc, y);
   store_chunk_staged(stg, y, p.d_dtype,
                      out_ptr(p.d, p.ldd, p.sbd, p.d_dtype, row_base, col0, batch, p),
@@ -566,13 +606,7 @@ __device__ __forceinline__ void epilogue_chunk(const Params& p, const uint32_t (
     const int lane = threadIdx.x & 31;
     const char* crow = (p.c_dtype == DT_F32 && lane < rows_valid)
                            ? c_ptr(p, row_base + lane, col0, batch) : nullptr;
-#pragma unroll
-    for (int g = 0; g < 4; ++g) {
-      float cv[8];
-      c_values8(creg, p, crow, col0, g, cv);
-#pragma unroll
-      for (int j = 0; j < 8; ++j) v[8 * g + j] = fmaf(beta, cv[j], v[8 * g + j]);
-    }
+    add_beta_c(creg, p, crow, col0, beta, v);
   }
   if (p.d != nullptr)
     store_chunk_staged(stg, v, p.d_dtype,
