@@ -31,21 +31,24 @@ cudaError_t launch_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const Pa
   auto kern = gemm_kernel<BN, GATHER, CG>;
   cudaError_t e = set_smem_limit<BN, GATHER, CG>(shape.smem);
   if (e != cudaSuccess) return e;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(shape.grid, 1, 1);
   cfg.blockDim = dim3(shape.threads, 1, 1);
   cfg.dynamicSmemBytes = shape.smem;
   cfg.stream = stream;
-  cfg.attrs = nullptr;
-  cfg.numAttrs = 0;
+  cfg.attrs = attr;
+  // programmatic dependent launch: this grid may start while the previous kernel
+  // in the stream finishes (the kernel waits for it before reading global memory)
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.numAttrs = 1;
   if (shape.cluster > 1) {
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = shape.cluster;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = shape.cluster;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.numAttrs = 2;
   }
   return cudaLaunchKernelEx(&cfg, kern, tmA, tmB, p);
 }

@@ -1182,6 +1182,9 @@ __global__ void __launch_bounds__(KernelCfg<BN, GATHER, CG>::kThreads, 1)
                 const __grid_constant__ Params p) {
   using Cfg = KernelCfg<BN, GATHER, CG>;
   extern __shared__ uint8_t smem_raw[];
+  // the next launch may start its own setup on SMs this grid leaves (it waits
+  // for this grid's completion before touching memory)
+  ptx::griddep_launch_dependents();
   const uint32_t raw = ptx::smem_addr(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;  // swizzle atoms need 1 KiB alignment
   uint8_t* base_ptr = smem_raw + (base - raw);
@@ -1270,6 +1273,9 @@ __global__ void __launch_bounds__(KernelCfg<BN, GATHER, CG>::kThreads, 1)
     }
     ptx::tc_fence_before();
   }
+  // Everything above touched only this CTA's shared memory and TMEM; from here
+  // on global memory that an earlier kernel in the stream may write is read.
+  ptx::griddep_wait();
   // varlen-M: copy cu_seqlens and build the per-group tile prefix (warp 0)
   if (p.num_groups > 0 && warp == 0) {
     const int G = p.num_groups;
