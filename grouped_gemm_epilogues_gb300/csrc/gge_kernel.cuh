@@ -198,17 +198,16 @@ __device__ __forceinline__ void record_status(const Params& p, int32_t code, int
   }
 }
 
-// Slow path of a bounded mbarrier wait: poll until the phase completes, the
+// Slow path of a bounded mbarrier wait: wait until the phase completes, the
 // CTA aborts, or timeout_ns of %globaltimer pass (then record and abort).
 static __device__ __noinline__ bool wait_phase_slow(uint32_t bar, uint32_t parity, uint64_t timeout_ns,
                                              int32_t* status, volatile int32_t* abort,
                                              int32_t where, int32_t tile, bool cluster_scope) {
   const uint64_t t0 = ptx::globaltimer();
   while (true) {
-#pragma unroll 1
-    for (int i = 0; i < 32; ++i)
-      if (cluster_scope ? ptx::mbar_try_wait_cluster(bar, parity) : ptx::mbar_try_wait(bar, parity))
-        return true;
+    // each try sleeps until the phase completes or the suspend hint runs out
+    if (cluster_scope ? ptx::mbar_try_wait_cluster(bar, parity) : ptx::mbar_try_wait(bar, parity))
+      return true;
     if (*abort) return false;
     if (ptx::globaltimer() - t0 > timeout_ns) {
       if (status != nullptr && atomicCAS(status, 0, DEV_TIMEOUT) == 0) {
