@@ -51,7 +51,8 @@ class GgeGemmArgs(ctypes.Structure):
 class GgePlanInfo(ctypes.Structure):
     _fields_ = [("tile_m", c_i32), ("tile_n", c_i32), ("tile_k", c_i32), ("stages", c_i32),
                 ("num_tiles", c_i32), ("grid", c_i32), ("threads", c_i32),
-                ("smem_bytes", c_i32), ("raster_band", c_i32), ("cta_group", c_i32)]
+                ("smem_bytes", c_i32), ("raster_band", c_i32), ("cta_group", c_i32),
+                ("tail_tiles", c_i32), ("tail_splits", c_i32)]
 
 
 # every function include/gge.h declares, with its ctypes signature
@@ -206,7 +207,7 @@ def gge_gemm(A, B, D, C=None, alpha=1.0, beta=1.0, alpha_dev=None, beta_dev=None
     lib = load()
     args = make_args(A, B, C=C, D=D, alpha=alpha, beta=beta, alpha_dev=alpha_dev,
                      beta_dev=beta_dev, config=config)
-    ws = workspace(D.device)
+    ws = workspace(D.device, lib.gge_workspace_size(ctypes.byref(args), 0))
     _check(lib.gge_gemm(ctypes.byref(args), ctypes.c_void_p(ws.data_ptr()), ws.numel(),
                         _stream(D)), "gge_gemm")
 
@@ -217,7 +218,7 @@ def gge_gemm_act(A, B, PostAct, act, D=None, C=None, alpha=1.0, beta=1.0, alpha_
     lib = load()
     args = make_args(A, B, C=C, D=D, PostAct=PostAct, alpha=alpha, beta=beta, act=act,
                      alpha_dev=alpha_dev, beta_dev=beta_dev, config=config)
-    ws = workspace(PostAct.device)
+    ws = workspace(PostAct.device, lib.gge_workspace_size(ctypes.byref(args), 0))
     _check(lib.gge_gemm_act(ctypes.byref(args), ctypes.c_void_p(ws.data_ptr()), ws.numel(),
                             _stream(PostAct)), "gge_gemm_act")
 
@@ -226,7 +227,7 @@ def gge_gemm_dact(A, B, PreAct, D, act, PostAct=None, config=None):
     """Backward activation epilogue: D = act'(PreAct) * (A @ B^T), PostAct = act(PreAct)."""
     lib = load()
     args = make_args(A, B, C=PreAct, D=D, PostAct=PostAct, act=act, config=config)
-    ws = workspace(D.device)
+    ws = workspace(D.device, lib.gge_workspace_size(ctypes.byref(args), 0))
     _check(lib.gge_gemm_dact(ctypes.byref(args), ctypes.c_void_p(ws.data_ptr()), ws.numel(),
                              _stream(D)), "gge_gemm_dact")
 
@@ -363,9 +364,10 @@ def gge_autotune(op, A, B, idx=None, cu=None, C=None, D=None, PostAct=None, act=
     out = D if D is not None else PostAct
     args = _tune_args(op, A, B, C, D, PostAct, act, alpha, beta, config)
     G = cu.numel() - 1 if cu is not None else 0
-    need = 256
     if op in ("varlen_k", "gather_k"):
         need = lib.gge_workspace_size_varlen_k(ctypes.byref(args), G)
+    else:
+        need = lib.gge_workspace_size(ctypes.byref(args), G)
     ws = workspace(out.device, need)
     best = GgeConfig()
     ms = ctypes.c_float()

@@ -118,7 +118,24 @@ struct Plan {
   int64_t M, N, K, L;
   bool empty;  // nothing to compute
   int band;
+  // split last wave (plain problems): whole-tile count and units, so that a call
+  // whose workspace is too small can run unsplit
+  int64_t tiles = 0;
+  int units = 0;
 };
+
+// Workspace layout of a split last wave: status words, then the flags (one per
+// slice >= 1, CTA, epilogue warp and lane), then the partial accumulators (one
+// 128 x BN fp32 block per slice >= 1 and CTA), each region 256-byte aligned.
+size_t tail_flag_bytes(int64_t blocks) {
+  return static_cast<size_t>((blocks * kEpiWarpsHost * 32 * 4 + 255) / 256 * 256);
+}
+size_t tail_workspace(const Plan& pl) {
+  if (pl.p.tail_tiles <= 0) return 0;
+  const int64_t blocks = static_cast<int64_t>(pl.p.tail_tiles) * (pl.p.tail_splits - 1) * pl.cg;
+  return kWorkspaceBytes + tail_flag_bytes(blocks) +
+         static_cast<size_t>(blocks) * kTileM * pl.bn * sizeof(float);
+}
 
 CUtensorMapDataType tmap_type(int es) {
   return es == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_UINT16;
@@ -562,6 +579,22 @@ gge_status make_plan(const gge_gemm_args* a, Form form, const int32_t* a_idx,
   }
   pl.shape.grid =
       units_cap > 0 ? unit_ctas * static_cast<int>(std::min<int64_t>(num_tiles, units_cap)) : -1;
+  // split the last, partly filled wave along K (plain problems, fixed schedule)
+  pl.tiles = num_tiles;
+  pl.units = units_cap;
+  const int32_t flags = cfg ? cfg->flags : 0;
+  if (!varlen && !vk && !gather && !mc && K > 0 && units_cap > 0 &&
+      !(flags & (FLAG_DYNAMIC_SCHED | FLAG_NO_SPLIT))) {
+    const TailSplit ts = plan_tail_split(num_tiles, units_cap, p.k_tiles);
+    if (ts.tail > 0) {
+      p.full_tiles = ts.full;
+      p.tail_tiles = ts.tail;
+      p.tail_splits = ts.splits;
+      const int64_t work = static_cast<int64_t>(ts.full) + static_cast<int64_t>(ts.tail) * ts.splits;
+      p.num_tiles = static_cast<int32_t>(work);
+      pl.shape.grid = unit_ctas * static_cast<int>(std::min<int64_t>(work, units_cap));
+    }
+  }
   if (pl.empty || !encode) return GGE_OK;
   if (pl.shape.grid <= 0) pl.empty = true;  // e.g. varlen with no rows
   if (pl.empty) return GGE_OK;
@@ -629,6 +662,20 @@ gge_status run(const gge_gemm_args* a, Form form, const int32_t* a_idx, const in
     pl.p.kmaps = static_cast<uint8_t*>(ws) + kWorkspaceBytes;
   }
   pl.p.status = static_cast<int32_t*>(ws);
+  if (pl.p.tail_tiles > 0) {
+    if (ws != nullptr && ws_bytes >= tail_workspace(pl) &&
+        (reinterpret_cast<uintptr_t>(ws) & 255u) == 0) {
+      const int64_t blocks = static_cast<int64_t>(pl.p.tail_tiles) * (pl.p.tail_splits - 1) * pl.cg;
+      uint8_t* base = static_cast<uint8_t*>(ws) + kWorkspaceBytes;
+      pl.p.tail_flags = reinterpret_cast<int32_t*>(base);
+      pl.p.partials = reinterpret_cast<float*>(base + tail_flag_bytes(blocks));
+    } else {
+      // not enough workspace for the partial sums: run the last wave unsplit
+      pl.p.tail_tiles = 0;
+      pl.p.num_tiles = static_cast<int32_t>(pl.tiles);
+      pl.shape.grid = pl.shape.cluster * static_cast<int>(std::min<int64_t>(pl.tiles, pl.units));
+    }
+  }
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   const cudaError_t e = variant_launch(pl, st);
   return e == cudaSuccess ? GGE_OK : GGE_ERR_CUDA;
@@ -668,7 +715,17 @@ extern "C" {
 size_t gge_workspace_size(const gge_gemm_args* args, int32_t num_groups) {
   (void)args;
   (void)num_groups;
-  return gge::kWorkspaceBytes;
+  // room for the split last wave of any plain problem: at most one partial block
+  // (128 x 256 fp32) and one warp-flag set per CTA the GPU can hold
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+      sms <= 0) {
+    cudaGetLastError();
+    return gge::kWorkspaceBytes;
+  }
+  return gge::kWorkspaceBytes + gge::tail_flag_bytes(sms) +
+         static_cast<size_t>(sms) * gge::kTileM * 256 * sizeof(float);
 }
 
 gge_status gge_gemm(const gge_gemm_args* args, void* ws, size_t ws_bytes, gge_stream_t stream) {
@@ -799,12 +856,14 @@ gge_status gge_plan(const gge_gemm_args* args, int32_t num_groups, int32_t form,
   out->tile_n = pl.bn;
   out->tile_k = pl.p.bk;
   out->stages = pl.p.stages;
-  out->num_tiles = pl.p.num_groups > 0 ? -1 : pl.p.num_tiles;  // varlen-M: formed on the device
+  out->num_tiles = pl.p.num_groups > 0 ? -1 : static_cast<int32_t>(pl.tiles);  // varlen-M: on the device
   out->grid = pl.shape.grid;
   out->threads = pl.shape.threads;
   out->smem_bytes = static_cast<int32_t>(pl.shape.smem);
   out->raster_band = pl.band;
   out->cta_group = pl.cg;
+  out->tail_tiles = pl.p.tail_tiles;
+  out->tail_splits = pl.p.tail_tiles > 0 ? pl.p.tail_splits : 1;
   return GGE_OK;
 }
 

@@ -150,8 +150,11 @@ __device__ __forceinline__ TileCoord tile_coord(int32_t t, const Params& p, cons
     tc.a_batch = 0;
     tc.b_batch = lo;
   } else {
+    // a split tail item computes a slice of tile full_tiles + (t - full_tiles) % tail_tiles
+    const int32_t tt =
+        (p.tail_tiles > 0 && t >= p.full_tiles) ? p.full_tiles + (t - p.full_tiles) % p.tail_tiles : t;
     int32_t l, mb, nb;
-    p.sched.map(t, l, mb, nb);
+    p.sched.map(tt, l, mb, nb);
     tc.m_row0 = mb * TILE_M;
     tc.row_limit = p.M;
     // two-pair clusters: the schedule walks n-tile pairs, pair q takes the q-th
@@ -175,8 +178,20 @@ struct KRange {
 
 __device__ __forceinline__ int32_t mma_kstep(const Params& p) { return p.f8 ? 32 : 16; }
 
-__device__ __forceinline__ KRange k_range(const Params& p, const Shared& sh, int32_t batch) {
-  if (p.k_groups == 0) return KRange{0, p.K, p.k_tiles, false};
+// K range of work item t (batch / group `batch`): all of K, a varlen-K group's
+// columns, or one K-slice of a split tail tile (k-tiles s k_tiles / S ..
+// (s + 1) k_tiles / S of slice s).
+__device__ __forceinline__ KRange k_range(const Params& p, const Shared& sh, int32_t batch,
+                                          int32_t t) {
+  if (p.k_groups == 0) {
+    if (p.tail_tiles > 0 && t >= p.full_tiles) {
+      const int32_t sl = (t - p.full_tiles) / p.tail_tiles;
+      const int32_t kt0 = sl * p.k_tiles / p.tail_splits;
+      const int32_t kt1 = (sl + 1) * p.k_tiles / p.tail_splits;
+      return KRange{kt0 * p.bk, min(p.K, kt1 * p.bk), kt1 - kt0, false};
+    }
+    return KRange{0, p.K, p.k_tiles, false};
+  }
   const int32_t lo = sh.cu[batch], hi = sh.prefix[batch];
   return KRange{lo, hi, (hi - lo + p.bk - 1) / p.bk, ((hi - lo) & (mma_kstep(p) - 1)) != 0};
 }
@@ -621,6 +636,24 @@ __device__ __forceinline__ void epilogue_chunk(const Params& p, const uint32_t (
   }
 }
 
+// Split last wave: wait (bounded) until another unit's epilogue lane has
+// published its partial row for this launch.
+__device__ __forceinline__ void wait_tail_flag(const int32_t* f, int32_t want, const Params& p,
+                                               const Shared& sh, int32_t tile) {
+  if (ptx::ld_acquire_gpu(f) == want) return;
+  const uint64_t t0 = ptx::globaltimer();
+  while (true) {
+    __nanosleep(128);
+    if (ptx::ld_acquire_gpu(f) == want) return;
+    if (*sh.abort) return;
+    if (ptx::globaltimer() - t0 > p.timeout_ns) {
+      record_status(p, DEV_TIMEOUT, 11, tile);
+      *sh.abort = 1;
+      return;
+    }
+  }
+}
+
 // ------------------------------------------------------------------- roles
 // `unit` / `units`: this CTA's (pair's) index and the number of CTAs (pairs).
 
@@ -641,23 +674,51 @@ __device__ __forceinline__ void epilogue_role(const Params& p, const Shared& sh,
   const int quad = warp & 3, half = warp >> 2;
   const float alpha = p.alpha_dev ? *p.alpha_dev : p.alpha;
   const float beta = p.beta_dev ? *p.beta_dev : p.beta;
+  // split last wave: this launch's flags read epoch + 1 (the epoch advances when
+  // the grid finishes, so flags of earlier launches never match)
+  // (the gather forms never split: compiled out of their instances)
+  const int32_t tail_mark =
+      (!GATHER && p.tail_tiles > 0) ? *reinterpret_cast<volatile int32_t*>(p.status + 6) + 1 : 0;
+  const int32_t n_other = p.tail_splits - 1;  // slices besides the owner's
   uint32_t acc = 0, acc_phase = 0;
   for (int i = 0;; ++i) {
     const int32_t t = sched_next<CG>(ts, i, p, sh);
     if (t >= num_tiles) break;
     const TileCoord tc = tile_coord<BN, Cfg::kTileM>(t, p, sh);
     // a tile with no k-tiles (K == 0, or an empty varlen-K group) keeps a zero accumulator
-    const bool has_acc = k_range(p, sh, tc.batch).tiles > 0;
+    const bool has_acc = k_range(p, sh, tc.batch, t).tiles > 0;
+    // split tail item: slice 0 owns the tile's outputs; slices >= 1 only write their
+    // fp32 accumulator rows to the workspace (this lane's row of each chunk)
+    const bool split = !GATHER && p.tail_tiles > 0 && t >= p.full_tiles;
+    int32_t slice = 0, tail_r = 0;
+    if (split) {
+      slice = (t - p.full_tiles) / p.tail_tiles;
+      tail_r = t - p.full_tiles - slice * p.tail_tiles;
+    }
+    const bool writer = split && slice > 0;
+    // partial row and flag of slice sl (>= 1) for this CTA, warp and lane
+    const int64_t part_base = (static_cast<int64_t>(tail_r) * n_other - 1) * CG + rank;
+    auto part_row = [&](int32_t sl) {
+      return p.partials +
+             ((part_base + static_cast<int64_t>(sl) * CG) * kBM + quad * 32 + lane) * BN;
+    };
+    auto part_flag = [&](int32_t sl) {
+      return p.tail_flags +
+             ((part_base + static_cast<int64_t>(sl) * CG) * Cfg::kEpiWarps + warp) * 32 + lane;
+    };
     const int32_t row_base = tc.m_row0 + static_cast<int32_t>(rank) * kBM + quad * 32;
     const int32_t rows_valid = min(32, tc.row_limit - row_base);  // warp-uniform, may be <= 0
     const int32_t row = row_base + lane;
-    const bool has_c = p.c != nullptr && lane < rows_valid;
+    const bool has_c = !writer && p.c != nullptr && lane < rows_valid;
     CRegs cnext = {};
     if (has_c && tc.n0 + half * 32 < p.N) load_c_chunk(p, row, tc.n0 + half * 32, tc.batch, cnext);
     // all lanes take the same branch: tcgen05.ld below is warp-collective
     const bool ok = wait_phase<CG == 2>(sh.tfull + 8 * acc, acc_phase, p, sh, 3, t);
     if (!__all_sync(0xffffffffu, ok)) break;
     ptx::tc_fence_after();
+    // the owner's lanes wait until the other slices' units have written their rows
+    if (split && !writer)
+      for (int32_t sl = 1; sl <= n_other; ++sl) wait_tail_flag(part_flag(sl), tail_mark, p, sh, t);
     const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + acc * BN;
 #pragma unroll 1
     for (int c = half; c < kChunks; c += kStride) {
@@ -681,13 +742,36 @@ __device__ __forceinline__ void epilogue_role(const Params& p, const Shared& sh,
           else ptx::mbar_arrive_remote(ptx::mapa(sh.tempty + 8 * acc, sh.lead));
         }
       }
+      if (writer) {  // the raw accumulator chunk, 128 bytes of this lane's row
+        float4* dst = reinterpret_cast<float4*>(part_row(slice) + c * 32);
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          dst[q] = make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
+                               __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
+        continue;
+      }
+      if (split) {  // the owner adds the other slices' partial sums, in slice order
+        for (int32_t sl = 1; sl <= n_other; ++sl) {
+          const float4* src = reinterpret_cast<const float4*>(part_row(sl) + c * 32);
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            const float4 a = src[q];
+            v[4 * q] = __float_as_uint(__uint_as_float(v[4 * q]) + a.x);
+            v[4 * q + 1] = __float_as_uint(__uint_as_float(v[4 * q + 1]) + a.y);
+            v[4 * q + 2] = __float_as_uint(__uint_as_float(v[4 * q + 2]) + a.z);
+            v[4 * q + 3] = __float_as_uint(__uint_as_float(v[4 * q + 3]) + a.w);
+          }
+        }
+      }
       const int32_t col0 = tc.n0 + c * 32;
       if (rows_valid > 0 && col0 < p.N)
         epilogue_chunk(p, v, row_base, rows_valid, col0, tc.batch, alpha, beta, ccur, stg);
     }
+    // a writer lane publishes its row once all of its chunks are stored
+    if (writer) ptx::st_release_gpu(part_flag(slice), tail_mark);
     if ((p.flags & FLAG_TILE_COUNTS) && p.tile_counts != nullptr && rank == 0 && warp == 0 &&
-        lane == 0)
-      atomicAdd(p.tile_counts + t, 1);
+        lane == 0 && !writer)
+      atomicAdd(p.tile_counts + (split ? p.full_tiles + tail_r : t), 1);
     acc ^= 1u;
     if (acc == 0) acc_phase ^= 1u;
   }
@@ -719,8 +803,8 @@ __device__ __forceinline__ void mma_loop(const Params& p, const Shared& sh, uint
     if (!__all_sync(0xffffffffu, ok)) return;
     ptx::tc_fence_after();
     const uint32_t d_tmem = tmem_base + acc * BN;
-    const KRange kr = p.k_groups > 0
-                          ? k_range(p, sh, tile_coord<BN, Cfg::kTileM>(t, p, sh).batch)
+    const KRange kr = (p.k_groups > 0 || p.tail_tiles > 0)
+                          ? k_range(p, sh, tile_coord<BN, Cfg::kTileM>(t, p, sh).batch, t)
                           : KRange{0, p.K, p.k_tiles, false};
     for (int kt = 0; kt < kr.tiles; ++kt) {
       ok = wait_phase<CG == 2>(sh.full + 8 * stage, phase, p, sh, 1, t);
@@ -832,7 +916,7 @@ __device__ __forceinline__ void tma_producer_role(const Params& p, const Shared&
     const int32_t t = (rank == 0) ? sched_fetch<CG>(ts, i, p, sh) : sched_next<CG>(ts, i, p, sh);
     if (t >= num_tiles) break;
     const TileCoord tc = tile_coord<BN, Cfg::kTileM>(t, p, sh);
-    const KRange kr = k_range(p, sh, tc.batch);
+    const KRange kr = k_range(p, sh, tc.batch, t);
     const int32_t row0 = tc.m_row0 + static_cast<int32_t>(rank) * kBM;
     const int32_t bn0 = tc.n0 + static_cast<int32_t>(rank) * Cfg::kBRows;
     for (int kt = 0; kt < kr.tiles; ++kt) {
@@ -923,7 +1007,7 @@ __device__ __forceinline__ void map_warp_role(const Params& p, const Shared& sh,
     const int32_t t = ts.unit + i * ts.units;
     if (t >= num_tiles) break;
     const TileCoord tc = tile_coord<BN, Cfg::kTileM>(t, p, sh);
-    const KRange kr = k_range(p, sh, tc.batch);
+    const KRange kr = k_range(p, sh, tc.batch, t);
     if (!kr.ragged || tc.batch == last) continue;
     const int slot = static_cast<int>(n % kMapSlots);
     if (n >= static_cast<uint32_t>(kMapSlots)) {
@@ -1055,7 +1139,7 @@ __device__ __forceinline__ void gather_k_producer_role(const Params& p, const Sh
     const int32_t t = (gt < 32) ? sched_fetch<1>(ts, i, p, sh) : sched_next<1>(ts, i, p, sh);
     if (t >= num_tiles) break;
     const TileCoord tc = tile_coord<BN, kBM>(t, p, sh);
-    const KRange kr = k_range(p, sh, tc.batch);
+    const KRange kr = k_range(p, sh, tc.batch, t);
     const int32_t m_el = tc.m_row0 + 8 * q;
     const bool m_ok = m_el < p.M;  // M is a multiple of 8: whole pieces
     constexpr int kChunkTiles = kIdxChunk / 64;
@@ -1367,6 +1451,16 @@ __global__ void __launch_bounds__(KernelCfg<BN, GATHER, CG>::kThreads, 1)
     if (atomicAdd(p.status + 5, 1) == ts.units - 1) {
       atomicExch(p.status + 4, 0);
       atomicExch(p.status + 5, 0);
+    }
+  }
+  // split last wave: the last unit to finish advances the launch epoch, so that
+  // no later launch takes this one's flags for its own (every unit has read the
+  // epoch by then: it is read before any unit counts itself finished)
+  if (p.tail_tiles > 0 && rank == 0 && threadIdx.x == 0) {
+    __threadfence();
+    if (atomicAdd(p.status + 7, 1) == ts.units - 1) {
+      atomicExch(p.status + 7, 0);
+      atomicAdd(p.status + 6, 1);
     }
   }
   if (warp == Cfg::kMmaWarp) {

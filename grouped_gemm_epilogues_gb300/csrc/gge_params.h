@@ -24,6 +24,7 @@ enum : int32_t {
   FLAG_DYNAMIC_SCHED = 4,      // tiles claimed from an atomic counter instead of a fixed stride
   FLAG_DIRECT_STORES = 8,      // epilogue stores straight from registers (no staging buffers)
   FLAG_PAIR_CLUSTER = 16,      // two CTA pairs per cluster share A by TMA multicast
+  FLAG_NO_SPLIT = 32,          // never split the last wave along K
 };
 
 struct Params {
@@ -35,8 +36,14 @@ struct Params {
   int32_t k_tiles;  // ceil(K / bk)
   int32_t bk;       // K elements per stage row (128 bytes)
   int32_t stages;
-  int32_t num_tiles;  // plain only
+  int32_t num_tiles;  // plain only: work items (tiles, plus the split tail's extra slices)
   PlainSchedule sched;
+  // split last wave (plain problems; see plan_tail_split): items >= full_tiles
+  // are slices; tail_tiles == 0 disables it
+  int32_t full_tiles, tail_tiles, tail_splits;
+  int32_t* tail_flags;  // workspace: per slice >= 1, CTA, epilogue warp and lane: the
+                        // launch epoch + 1 once that lane's partial row is written
+  float* partials;      // workspace: per slice >= 1 and CTA, 128 x BN fp32 accumulators
   FastDivmod tiles_n_div;  // varlen: local tile -> (m-tile, n-tile)
   int32_t tiles_n;
 
@@ -87,7 +94,8 @@ struct Params {
 
   // control
   int32_t* status;       // workspace: [0] code, [1] where, [2] tile, [3] detail,
-                         //            [4] tile claim counter, [5] finished CTAs (pairs)
+                         //            [4] tile claim counter, [5] finished CTAs (pairs),
+                         //            [6] split-tail launch epoch, [7] its finished units
   int32_t* tile_counts;  // debug visit counters
   int32_t flags;
   uint64_t timeout_ns;

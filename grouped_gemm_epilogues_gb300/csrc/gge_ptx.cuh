@@ -16,6 +16,18 @@ __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// Global flags between CTAs of one grid (split last wave): a release store
+// after this thread's partial-row stores, an acquire load before reading them.
+__device__ __forceinline__ void st_release_gpu(int32_t* p, int32_t v) {
+  asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ int32_t ld_acquire_gpu(const int32_t* p) {
+  int32_t v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
 // Programmatic dependent launch.  launch_dependents: the next kernel in the
 // stream (launched with programmatic stream serialization) may be scheduled
 // once every CTA of this grid has issued it or exited.  wait: block until the

@@ -101,4 +101,37 @@ struct PlainSchedule {
   }
 };
 
+// Split of the last, partly filled wave along K.  T tiles run on U units (CTAs
+// or CTA pairs) of a persistent grid: W = T / U full waves, then R = T - W U
+// tiles.  When R <= U / 2 each of those R tiles is cut into S K-slices (S <=
+// U / R, so the slices still form one wave; at most 4; at least 8 k-tiles a
+// slice), which S different units compute; slice 0's unit adds the other
+// slices' fp32 partial accumulators before its epilogue.  Work item v < W U is
+// tile v; item W U + q is slice q / R of tile W U + q % R.  The unit stride of
+// the persistent schedule (unit u takes items u, u + U, ...) is unchanged.
+struct TailSplit {
+  int32_t full;    // W * U: items that are whole tiles
+  int32_t tail;    // R: tiles split (0: no split)
+  int32_t splits;  // S
+};
+
+GGE_HD TailSplit plan_tail_split(int64_t tiles, int32_t units, int32_t k_tiles) {
+  TailSplit s;
+  s.full = static_cast<int32_t>(tiles);
+  s.tail = 0;
+  s.splits = 1;
+  if (units < 2 || tiles <= 0) return s;
+  const int64_t waves = tiles / units;
+  const int64_t r = tiles - waves * units;
+  if (r == 0) return s;
+  int64_t splits = units / r;
+  if (splits > 4) splits = 4;
+  if (splits > k_tiles / 8) splits = k_tiles / 8;
+  if (splits < 2) return s;
+  s.full = static_cast<int32_t>(waves * units);
+  s.tail = static_cast<int32_t>(r);
+  s.splits = static_cast<int32_t>(splits);
+  return s;
+}
+
 }  // namespace gge

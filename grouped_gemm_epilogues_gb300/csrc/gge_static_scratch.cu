@@ -60,13 +60,15 @@ void* scratch_address(gge_status* status) {
 extern "C" gge_status gge_gemm_act_static_scratch(const gge_gemm_args* args,
                                                   gge_stream_t stream) {
   if (args == nullptr) return GGE_ERR_INVALID_ARG;
-  const size_t need = gge_workspace_size(args, 0);
-  if (need > kStaticScratchBytes) return GGE_ERR_WORKSPACE;  // larger than the fixed area
+  // the status words only: with no room for partial sums the last wave is not
+  // split (the fixed area is small)
+  const size_t need = 256;
+  if (need > kStaticScratchBytes) return GGE_ERR_WORKSPACE;
   gge_status status = GGE_OK;
   void* scratch = scratch_address(&status);
   if (scratch == nullptr) return status;
   // the area keeps the previous call's contents: the status words must start at zero
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   if (cudaMemsetAsync(scratch, 0, need, st) != cudaSuccess) return GGE_ERR_CUDA;
-  return gge_gemm_act(args, scratch, kStaticScratchBytes, stream);
+  return gge_gemm_act(args, scratch, need, stream);
 }

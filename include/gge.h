@@ -145,11 +145,18 @@ typedef struct gge_gemm_args {
   const gge_config* config;  /* NULL = defaults */
 } gge_gemm_args;
 
-/* Bytes of device workspace a call needs (status words and the dynamic
- * scheduler's counters), for every entry point except gge_gemm_varlen_k and
- * gge_gemm_gather_k (see gge_workspace_size_varlen_k); the
- * workspace is caller-owned, at least 16-byte aligned, and must be zeroed once
- * before first use.  It is reusable across calls on the same stream. */
+/* Bytes of device workspace that let a call run at full speed, for every
+ * entry point except gge_gemm_varlen_k and gge_gemm_gather_k (see
+ * gge_workspace_size_varlen_k): 256 bytes of status words and scheduler
+ * counters, plus, for plain problems, room to split the last, partly filled
+ * wave of tiles along K (one 128 x 256 fp32 partial block and 1 KiB of flags
+ * per SM, about 20 MiB on a 152-SM GPU; the split needs a 256-byte aligned
+ * workspace).  Any workspace of at least 256 bytes works: with less room the
+ * last wave runs unsplit.  The workspace is caller-owned, at least 16-byte
+ * aligned, must be zeroed once before first use, and is reusable across calls
+ * on the same stream (not by calls running concurrently on other streams).
+ * The arguments are not inspected (they may be NULL); the size depends on the
+ * current device. */
 size_t gge_workspace_size(const gge_gemm_args* args, int32_t num_groups);
 
 /* Workspace bytes gge_gemm_varlen_k and gge_gemm_gather_k need on the current
@@ -247,10 +254,10 @@ gge_status gge_gemm_gather_a(const gge_gemm_args* args, const int32_t* a_idx,
  * memory through its own arena or caching allocator, or a latency-critical path
  * that must not call the allocator).  The pages have no counterpart: it is an
  * addition of this library.
- *   - The scratch (the status words) lives in a fixed 1024-byte __device__ area
- *     inside the library, held on every GPU that loads it until process exit.
- *     A call whose gge_workspace_size exceeds 1024 bytes returns
- *     GGE_ERR_WORKSPACE.
+ *   - The scratch (the 256 bytes of status words) lives in a fixed 1024-byte
+ *     __device__ area inside the library, held on every GPU that loads it until
+ *     process exit.  It has no room for partial sums, so the last wave of tiles
+ *     is never split along K on this path (see gge_workspace_size).
  *   - The first call on a device looks up that area's device address (on the
  *     current device); make that first call before any stream capture.
  *   - Each call clears the status words (an async memset on `stream`), then
@@ -297,6 +304,10 @@ typedef struct gge_plan_info {
   int32_t smem_bytes;
   int32_t raster_band;
   int32_t cta_group;  /* 1 or 2 CTAs per tile */
+  int32_t tail_tiles; /* tiles of the last, partly filled wave that are split along K
+                         (plain problems; 0: none).  Reported only when the unit
+                         count is known here, i.e. config->num_ctas is set. */
+  int32_t tail_splits; /* K-slices per split tile (1: none) */
 } gge_plan_info;
 gge_status gge_plan(const gge_gemm_args* args, int32_t num_groups, int32_t form,
                     gge_plan_info* out);

@@ -161,6 +161,50 @@ def test_plan_without_gpu(L):
     assert info["tile_k"] == 128
 
 
+def test_split_tail_plan(L):
+    """The last, partly filled wave is split along K when it is at most half full:
+    W = T // U full waves, R = T - W U tiles, S = min(U // R, 4, k_tiles // 8) slices."""
+    A = torch.zeros(1536, 1536, dtype=torch.bfloat16)
+    B = torch.zeros(4096, 1536, dtype=torch.bfloat16)
+    D = torch.zeros(1536, 4096, dtype=torch.bfloat16)
+    pair = dict(num_ctas=152, cta_group=2, tile_n=256)
+    info = binding.gge_plan(A, B, D=D, config=binding.make_config(**pair))
+    # 6 x 16 = 96 tiles on 76 pairs: one full wave, 20 tiles left, 3 slices of 8 k-tiles
+    assert info["num_tiles"] == 96 and info["grid"] == 152
+    assert info["tail_tiles"] == 20 and info["tail_splits"] == 3
+    # switched off by the flag, by the dynamic scheduler, and for short K
+    for flags in (32, 4):
+        info = binding.gge_plan(A, B, D=D, config=binding.make_config(flags=flags, **pair))
+        assert info["tail_tiles"] == 0 and info["tail_splits"] == 1
+    As, Bs = A[:, :256], B[:, :256]
+    info = binding.gge_plan(As, Bs, D=D, config=binding.make_config(**pair))
+    assert info["tail_tiles"] == 0                       # 4 k-tiles: nothing to split
+    # a last wave more than half full is not split (4096^2 on 76 pairs, 256-wide: 28 of 76
+    # left -> split in 2; on 100 pairs: 56 of 100 left -> not split)
+    A4 = torch.zeros(4096, 4096, dtype=torch.bfloat16)
+    info = binding.gge_plan(A4, A4, D=A4, config=binding.make_config(**pair))
+    assert info["tail_tiles"] == 28 and info["tail_splits"] == 2 and info["num_tiles"] == 256
+    info = binding.gge_plan(A4, A4, D=A4, config=binding.make_config(num_ctas=200, cta_group=2,
+                                                                     tile_n=256))
+    assert info["tail_tiles"] == 0
+    # fewer tiles than units: the classic split-K of a small output (16 tiles, 4 slices)
+    A1 = torch.zeros(1024, 8192, dtype=torch.bfloat16)
+    D1 = torch.zeros(1024, 1024, dtype=torch.bfloat16)
+    info = binding.gge_plan(A1, A1, D=D1, config=binding.make_config(**pair))
+    assert info["num_tiles"] == 16 and info["tail_tiles"] == 16 and info["tail_splits"] == 4
+    assert info["grid"] == 2 * 64
+    # gather forms never split
+    idx = torch.zeros(1536, dtype=torch.int32)
+    info = binding.gge_plan(A, B, D=D, gather=True, config=binding.make_config(num_ctas=152,
+                                                                              tile_n=256))
+    assert info["tail_tiles"] == 0
+
+
+def test_workspace_size_covers_the_split(L):
+    size = L.gge_workspace_size(None, 0)
+    assert size >= 256  # without a GPU only the status words are reported
+
+
 def test_varlen_k_argument_checks_and_plan(L):
     M, N, total, G = 512, 384, 1000, 4
     A = torch.zeros(total, M, dtype=torch.bfloat16).t()       # M-major A [M, total_K]
