@@ -696,11 +696,14 @@ __device__ __forceinline__ void epilogue_role(const Params& p, const Shared& sh,
       tail_r = t - p.full_tiles - slice * p.tail_tiles;
     }
     const bool writer = split && slice > 0;
-    // partial row and flag of slice sl (>= 1) for this CTA, warp and lane
+    // slice sl's (>= 1) partial block for this CTA is laid out lane-major, so that
+    // each warp store / load moves 512 contiguous bytes: float4 q of this lane's
+    // row in chunk c sits at [quad][c][q][lane].  Its flag: per CTA, warp and lane.
     const int64_t part_base = (static_cast<int64_t>(tail_r) * n_other - 1) * CG + rank;
-    auto part_row = [&](int32_t sl) {
-      return p.partials +
-             ((part_base + static_cast<int64_t>(sl) * CG) * kBM + quad * 32 + lane) * BN;
+    auto part_chunk = [&](int32_t sl, int c) {
+      return reinterpret_cast<float4*>(p.partials +
+                                       (part_base + static_cast<int64_t>(sl) * CG) * kBM * BN) +
+             ((quad * kChunks + c) * 8) * 32 + lane;
     };
     auto part_flag = [&](int32_t sl) {
       return p.tail_flags +
@@ -742,20 +745,20 @@ __device__ __forceinline__ void epilogue_role(const Params& p, const Shared& sh,
           else ptx::mbar_arrive_remote(ptx::mapa(sh.tempty + 8 * acc, sh.lead));
         }
       }
-      if (writer) {  // the raw accumulator chunk, 128 bytes of this lane's row
-        float4* dst = reinterpret_cast<float4*>(part_row(slice) + c * 32);
+      if (writer) {  // the raw accumulator chunk: this lane's 32 values
+        float4* dst = part_chunk(slice, c);
 #pragma unroll
         for (int q = 0; q < 8; ++q)
-          dst[q] = make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
-                               __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
+          dst[q * 32] = make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
+                                    __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
         continue;
       }
       if (split) {  // the owner adds the other slices' partial sums, in slice order
         for (int32_t sl = 1; sl <= n_other; ++sl) {
-          const float4* src = reinterpret_cast<const float4*>(part_row(sl) + c * 32);
+          const float4* src = part_chunk(sl, c);
 #pragma unroll
           for (int q = 0; q < 8; ++q) {
-            const float4 a = src[q];
+            const float4 a = src[q * 32];
             v[4 * q] = __float_as_uint(__uint_as_float(v[4 * q]) + a.x);
             v[4 * q + 1] = __float_as_uint(__uint_as_float(v[4 * q + 1]) + a.y);
             v[4 * q + 2] = __float_as_uint(__uint_as_float(v[4 * q + 2]) + a.z);
