@@ -18,6 +18,10 @@
  *     allocated, freed or synchronised by the library (except
  *     gge_read_device_status, which synchronises the given stream).
  *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default).
+ *     Kernels are launched with programmatic stream serialization: a launch may
+ *     begin its setup (shared memory, TMEM) while the previous kernel in the
+ *     stream is finishing, but reads and writes no global memory before that
+ *     kernel has completed, so stream order holds as for any launch.
  *   - Validation happens on the host before any launch; a rejected call
  *     launches nothing and returns GGE_ERR_INVALID_ARG / GGE_ERR_UNSUPPORTED /
  *     GGE_ERR_ALIGNMENT / GGE_ERR_WORKSPACE.  A failed launch returns
@@ -103,7 +107,15 @@ typedef struct gge_config {
                              of a plain problem: each CTA loads half of its A rows
                              and TMA-multicasts them to the other pair (a quarter
                              less L2 traffic; needs cta_group 2, the static
-                             schedule, no tile counts)                            */
+                             schedule, no tile counts);
+                             bit 5: never split the last wave.  By default a
+                             plain problem whose last wave of tiles is at most
+                             half full cuts those tiles into 2-4 K-slices that
+                             otherwise idle CTAs compute; the tile's first slice
+                             adds the others' fp32 partial sums (kept in the
+                             workspace) before its epilogue.  Not with the
+                             dynamic scheduler, two-pair clusters or the gather
+                             and varlen forms; needs gge_workspace_size bytes.   */
   int32_t cta_group;      /* 0 = auto; 1 = one CTA per 128-row tile; 2 = a CTA pair
                              per 256-row tile (tcgen05 cta_group::2, 256-column
                              tiles, not with the gather forms)                     */
