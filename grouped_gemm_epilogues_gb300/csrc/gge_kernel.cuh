@@ -215,14 +215,27 @@ __device__ __forceinline__ void record_status(const Params& p, int32_t code, int
 
 // Slow path of a bounded mbarrier wait: wait until the phase completes, the
 // CTA aborts, or timeout_ns of %globaltimer pass (then record and abort).
+// `sleep`: probe with the sleeping try_wait (the thread issues nothing until the
+// phase completes) instead of short polls.  Measured: sleeping waits for the
+// epilogue's accumulator (long waits, many warps) are ~0.5 % faster under the
+// power cap; for the copy warps' and MMA warp's short stage waits they cost up
+// to 2.5 % (gather-K), so those poll.
 static __device__ __noinline__ bool wait_phase_slow(uint32_t bar, uint32_t parity, uint64_t timeout_ns,
                                              int32_t* status, volatile int32_t* abort,
-                                             int32_t where, int32_t tile, bool cluster_scope) {
+                                             int32_t where, int32_t tile, bool cluster_scope,
+                                             bool sleep) {
   const uint64_t t0 = ptx::globaltimer();
   while (true) {
-    // each try sleeps until the phase completes or the suspend hint runs out
-    if (cluster_scope ? ptx::mbar_try_wait_cluster(bar, parity) : ptx::mbar_try_wait(bar, parity))
-      return true;
+    if (sleep) {
+      if (cluster_scope ? ptx::mbar_try_wait_cluster_sleep(bar, parity)
+                        : ptx::mbar_try_wait_sleep(bar, parity))
+        return true;
+    } else {
+#pragma unroll 1
+      for (int i = 0; i < 32; ++i)
+        if (cluster_scope ? ptx::mbar_try_wait_cluster(bar, parity) : ptx::mbar_try_wait(bar, parity))
+          return true;
+    }
     if (*abort) return false;
     if (ptx::globaltimer() - t0 > timeout_ns) {
       if (status != nullptr && atomicCAS(status, 0, DEV_TIMEOUT) == 0) {
@@ -237,12 +250,14 @@ static __device__ __noinline__ bool wait_phase_slow(uint32_t bar, uint32_t parit
 
 // Bounded wait on an mbarrier phase.  Returns false on abort or timeout.
 // CLUSTER: acquire at cluster scope (barriers that the peer CTA signals).
-template <bool CLUSTER = false>
+// SLEEP: the slow path sleeps in try_wait instead of polling.
+template <bool CLUSTER = false, bool SLEEP = false>
 __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, const Params& p,
                                            const Shared& sh, int32_t where, int32_t tile) {
   if (CLUSTER ? ptx::mbar_try_wait_cluster(bar, parity) : ptx::mbar_try_wait(bar, parity))
     return true;
-  return wait_phase_slow(bar, parity, p.timeout_ns, p.status, sh.abort, where, tile, CLUSTER);
+  return wait_phase_slow(bar, parity, p.timeout_ns, p.status, sh.abort, where, tile, CLUSTER,
+                         SLEEP);
 }
 
 // ------------------------------------------------------------- tile stream
@@ -716,7 +731,7 @@ __device__ __forceinline__ void epilogue_role(const Params& p, const Shared& sh,
     CRegs cnext = {};
     if (has_c && tc.n0 + half * 32 < p.N) load_c_chunk(p, row, tc.n0 + half * 32, tc.batch, cnext);
     // all lanes take the same branch: tcgen05.ld below is warp-collective
-    const bool ok = wait_phase<CG == 2>(sh.tfull + 8 * acc, acc_phase, p, sh, 3, t);
+    const bool ok = wait_phase<CG == 2, true>(sh.tfull + 8 * acc, acc_phase, p, sh, 3, t);
     if (!__all_sync(0xffffffffu, ok)) break;
     ptx::tc_fence_after();
     // the owner's lanes wait until the other slices' units have written their rows

@@ -87,14 +87,26 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
                : "memory");
 }
 
-// How long (ns) one try_wait may keep the thread suspended before it returns
-// false; the thread wakes as soon as the phase completes.  Suspended waiters
-// issue nothing (measured ~0.5 % faster under the power cap than short polls).
+// One probe: true once the phase with the given parity has completed.
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// How long (ns) a sleeping probe may keep the thread suspended before it
+// returns false; the thread wakes as soon as the phase completes.
 constexpr uint32_t kSuspendHintNs = 1000000;
 
-// One probe: true once the phase with the given parity has completed (the
-// thread may sleep up to kSuspendHintNs waiting for it).
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+// A probe that sleeps until the phase completes (or kSuspendHintNs pass), for
+// long waits whose waiters should issue nothing meanwhile.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
@@ -289,6 +301,19 @@ __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
 
 // try_wait with acquire at cluster scope (for barriers other CTAs arrive on).
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// The sleeping form of mbar_try_wait_cluster (see mbar_try_wait_sleep).
+__device__ __forceinline__ bool mbar_try_wait_cluster_sleep(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
