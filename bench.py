@@ -90,7 +90,8 @@ def kernel_source_hash():
         if not device:
             continue
         with open(os.path.join(csrc, name)) as f:
-            code = "\n".join(line.split("//", 1)[0].rstrip() for line in f)
+            lines = (line.split("//", 1)[0].rstrip() for line in f)
+            code = "\n".join(line for line in lines if line)
         h.update(name.encode() + code.encode())
     return h.hexdigest()[:16]
 

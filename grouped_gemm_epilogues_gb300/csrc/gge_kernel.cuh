@@ -37,12 +37,20 @@
 // Every CTA (pair) walks the same static persistent schedule (tile t, t + grid, ...),
 // or claims tiles from an atomic counter; tile coordinates come from
 // FastDivmod (plain) or from a per-group tile prefix sum in shared memory
-// (varlen-M, VarlenMTileScheduler's role).
+// (varlen-M, VarlenMTileScheduler's role).  On plain problems a last wave that
+// is at most half full is split along K: its tiles' K-slices run on otherwise
+// idle units, which leave fp32 partial sums in the workspace for the slice-0
+// unit's epilogue (plan_tail_split).
 //
-// Every mbarrier wait is bounded by Params::timeout_ns of %globaltimer; on
-// expiry the kernel records DEV_TIMEOUT in the status words, raises a
-// shared abort flag so that every role leaves its loop, lets copies in flight
-// land, frees its TMEM and returns.
+// Launches use programmatic dependent launch: a CTA sets up its shared memory
+// and TMEM, then waits (griddepcontrol.wait) for the previous kernel in the
+// stream before touching global memory, and lets the next launch start as
+// soon as SMs free up.
+//
+// Every mbarrier wait (and the split tail's flag waits) is bounded by
+// Params::timeout_ns of %globaltimer; on expiry the kernel records
+// DEV_TIMEOUT in the status words, raises a shared abort flag so that every
+// role leaves its loop, lets copies in flight land, frees its TMEM and returns.
 #pragma once
 
 #include <cuda_bf16.h>
