@@ -125,8 +125,8 @@ struct Plan {
 };
 
 // Workspace layout of a split last wave: status words, then the flags (one per
-// slice >= 1, CTA, epilogue warp and lane), then the partial accumulators (one
-// 128 x BN fp32 block per slice >= 1 and CTA), each region 256-byte aligned.
+// slice but the last, CTA, epilogue warp and lane), then the partial accumulators
+// (one 128 x BN fp32 block per slice but the last and CTA), each region 256-byte aligned.
 size_t tail_flag_bytes(int64_t blocks) {
   return static_cast<size_t>((blocks * kEpiWarpsHost * 32 * 4 + 255) / 256 * 256);
 }

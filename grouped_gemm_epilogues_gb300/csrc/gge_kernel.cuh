@@ -39,8 +39,8 @@
 // FastDivmod (plain) or from a per-group tile prefix sum in shared memory
 // (varlen-M, VarlenMTileScheduler's role).  On plain problems a last wave that
 // is at most half full is split along K: its tiles' K-slices run on otherwise
-// idle units, which leave fp32 partial sums in the workspace for the slice-0
-// unit's epilogue (plan_tail_split).
+// idle units, which leave fp32 partial sums in the workspace for the epilogue
+// of the unit that runs the tile's last slice (plan_tail_split).
 //
 // Launches use programmatic dependent launch: a CTA sets up its shared memory
 // and TMEM, then waits (griddepcontrol.wait) for the previous kernel in the
@@ -710,19 +710,23 @@ __device__ __forceinline__ void epilogue_role(const Params& p, const Shared& sh,
     const TileCoord tc = tile_coord<BN, Cfg::kTileM>(t, p, sh);
     // a tile with no k-tiles (K == 0, or an empty varlen-K group) keeps a zero accumulator
     const bool has_acc = k_range(p, sh, tc.batch, t).tiles > 0;
-    // split tail item: slice 0 owns the tile's outputs; slices >= 1 only write their
-    // fp32 accumulator rows to the workspace (this lane's row of each chunk)
+    // split tail item: the last slice owns the tile's outputs; the others only
+    // write their fp32 accumulator rows to the workspace.  Slice s of tail tile r
+    // runs on unit s R + r, so the owner waits only on units of lower index,
+    // which the hardware makes resident first: no wait on a unit that cannot
+    // start while other work holds SMs.
     const bool split = !GATHER && p.tail_tiles > 0 && t >= p.full_tiles;
     int32_t slice = 0, tail_r = 0;
     if (split) {
       slice = (t - p.full_tiles) / p.tail_tiles;
       tail_r = t - p.full_tiles - slice * p.tail_tiles;
     }
-    const bool writer = split && slice > 0;
-    // slice sl's (>= 1) partial block for this CTA is laid out lane-major, so that
-    // each warp store / load moves 512 contiguous bytes: float4 q of this lane's
-    // row in chunk c sits at [quad][c][q][lane].  Its flag: per CTA, warp and lane.
-    const int64_t part_base = (static_cast<int64_t>(tail_r) * n_other - 1) * CG + rank;
+    const bool writer = split && slice < n_other;
+    // slice sl's (< S - 1) partial block for this CTA is laid out lane-major, so
+    // that each warp store / load moves 512 contiguous bytes: float4 q of this
+    // lane's row in chunk c sits at [quad][c][q][lane].  Its flag: per CTA, warp
+    // and lane.
+    const int64_t part_base = static_cast<int64_t>(tail_r) * n_other * CG + rank;
     auto part_chunk = [&](int32_t sl, int c) {
       return reinterpret_cast<float4*>(p.partials +
                                        (part_base + static_cast<int64_t>(sl) * CG) * kBM * BN) +
@@ -744,7 +748,7 @@ __device__ __forceinline__ void epilogue_role(const Params& p, const Shared& sh,
     ptx::tc_fence_after();
     // the owner's lanes wait until the other slices' units have written their rows
     if (split && !writer)
-      for (int32_t sl = 1; sl <= n_other; ++sl) wait_tail_flag(part_flag(sl), tail_mark, p, sh, t);
+      for (int32_t sl = 0; sl < n_other; ++sl) wait_tail_flag(part_flag(sl), tail_mark, p, sh, t);
     const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + acc * BN;
 #pragma unroll 1
     for (int c = half; c < kChunks; c += kStride) {
@@ -777,7 +781,7 @@ __device__ __forceinline__ void epilogue_role(const Params& p, const Shared& sh,
         continue;
       }
       if (split) {  // the owner adds the other slices' partial sums, in slice order
-        for (int32_t sl = 1; sl <= n_other; ++sl) {
+        for (int32_t sl = 0; sl < n_other; ++sl) {
           const float4* src = part_chunk(sl, c);
 #pragma unroll
           for (int q = 0; q < 8; ++q) {

@@ -41,9 +41,9 @@ struct Params {
   // split last wave (plain problems; see plan_tail_split): items >= full_tiles
   // are slices; tail_tiles == 0 disables it
   int32_t full_tiles, tail_tiles, tail_splits;
-  int32_t* tail_flags;  // workspace: per slice >= 1, CTA, epilogue warp and lane: the
+  int32_t* tail_flags;  // workspace: per slice but the last, CTA, epilogue warp and lane: the
                         // launch epoch + 1 once that lane's partial row is written
-  float* partials;      // workspace: per slice >= 1 and CTA, 128 x BN fp32 accumulators
+  float* partials;      // workspace: per slice but the last and CTA, 128 x BN fp32 accumulators
   FastDivmod tiles_n_div;  // varlen: local tile -> (m-tile, n-tile)
   int32_t tiles_n;
 

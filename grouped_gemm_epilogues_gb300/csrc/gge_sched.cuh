@@ -105,7 +105,7 @@ struct PlainSchedule {
 // or CTA pairs) of a persistent grid: W = T / U full waves, then R = T - W U
 // tiles.  When R <= U / 2 each of those R tiles is cut into S K-slices (S <=
 // U / R, so the slices still form one wave; at most 4; at least 8 k-tiles a
-// slice), which S different units compute; slice 0's unit adds the other
+// slice), which S different units compute; the last slice's unit adds the other
 // slices' fp32 partial accumulators before its epilogue.  Work item v < W U is
 // tile v; item W U + q is slice q / R of tile W U + q % R.  The unit stride of
 // the persistent schedule (unit u takes items u, u + U, ...) is unchanged.

@@ -1,5 +1,5 @@
 """Split last wave: tiles of the last, partly filled wave are cut into K-slices
-that different CTAs (pairs) compute; slice 0's epilogue adds the others' fp32
+that different CTAs (pairs) compute; the last slice's epilogue adds the others' fp32
 partial sums before alpha, beta * C and the activation.  Every case forces the
 split with a small CTA count (so that it does not depend on the GPU's size),
 checks through gge_plan that it is on, and compares with the oracle."""
