@@ -151,3 +151,11 @@ def test_split_needs_room_else_runs_unsplit():
     torch.cuda.synchronize()
     r = og.gemm(dec(A), dec(B), beta=0.0, act="relu", p_fmt=BF16)
     check(P, r["P"], r["bound"], BF16, "relu", what="static scratch", x=r["v"])
+
+
+def test_workspace_size_has_room_for_the_split():
+    """On a GPU the reported size covers one 128 x 256 fp32 partial block and one
+    warp-flag set per SM after the 256 status bytes."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    size = binding.load().gge_workspace_size(None, 0)
+    assert size >= 256 + sms * (128 * 256 * 4 + 8 * 32 * 4)
