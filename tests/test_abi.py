@@ -200,6 +200,19 @@ def test_split_tail_plan(L):
     assert info["tail_tiles"] == 0
 
 
+def test_skinny_problems_default_to_narrow_tiles(L):
+    """One-CTA tiles default to 128 columns when 256-wide ones would leave CTAs idle."""
+    cfg = binding.make_config(num_ctas=152)
+    B = torch.zeros(8192, 8192, dtype=torch.bfloat16)
+    A1 = torch.zeros(128, 8192, dtype=torch.bfloat16)
+    info = binding.gge_plan(A1, B, D=torch.zeros(128, 8192, dtype=torch.bfloat16), config=cfg)
+    assert info["cta_group"] == 1 and info["tile_n"] == 128      # 32 wide tiles < 152 CTAs
+    A2 = torch.zeros(768, 8192, dtype=torch.bfloat16)               # 6 x 32 = 192 >= 152
+    cfg1 = binding.make_config(num_ctas=152, cta_group=1)
+    info = binding.gge_plan(A2, B, D=torch.zeros(768, 8192, dtype=torch.bfloat16), config=cfg1)
+    assert info["cta_group"] == 1 and info["tile_n"] == 256
+
+
 def test_workspace_size_covers_the_split(L):
     size = L.gge_workspace_size(None, 0)
     assert size >= 256  # without a GPU only the status words are reported
