@@ -104,7 +104,7 @@ struct PlainSchedule {
 // Split of the last, partly filled wave along K.  T tiles run on U units (CTAs
 // or CTA pairs) of a persistent grid: W = T / U full waves, then R = T - W U
 // tiles.  When R <= U / 2 each of those R tiles is cut into S K-slices (S <=
-// U / R, so the slices still form one wave; at most 4; at least 8 k-tiles a
+// U / R, so the slices still form one wave; at most 8; at least 8 k-tiles a
 // slice), which S different units compute; the last slice's unit adds the other
 // slices' fp32 partial accumulators before its epilogue.  Work item v < W U is
 // tile v; item W U + q is slice q / R of tile W U + q % R.  The unit stride of
@@ -125,7 +125,7 @@ GGE_HD TailSplit plan_tail_split(int64_t tiles, int32_t units, int32_t k_tiles) 
   const int64_t r = tiles - waves * units;
   if (r == 0) return s;
   int64_t splits = units / r;
-  if (splits > 4) splits = 4;
+  if (splits > 8) splits = 8;
   if (splits > k_tiles / 8) splits = k_tiles / 8;
   if (splits < 2) return s;
   s.full = static_cast<int32_t>(waves * units);

@@ -110,7 +110,7 @@ typedef struct gge_config {
                              schedule, no tile counts);
                              bit 5: never split the last wave.  By default a
                              plain problem whose last wave of tiles is at most
-                             half full cuts those tiles into 2-4 K-slices that
+                             half full cuts those tiles into 2-8 K-slices that
                              otherwise idle CTAs compute; the tile's last slice
                              adds the others' fp32 partial sums (kept in the
                              workspace) before its epilogue.  Not with the

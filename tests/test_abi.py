@@ -163,7 +163,7 @@ def test_plan_without_gpu(L):
 
 def test_split_tail_plan(L):
     """The last, partly filled wave is split along K when it is at most half full:
-    W = T // U full waves, R = T - W U tiles, S = min(U // R, 4, k_tiles // 8) slices."""
+    W = T // U full waves, R = T - W U tiles, S = min(U // R, 8, k_tiles // 8) slices."""
     A = torch.zeros(1536, 1536, dtype=torch.bfloat16)
     B = torch.zeros(4096, 1536, dtype=torch.bfloat16)
     D = torch.zeros(1536, 4096, dtype=torch.bfloat16)
@@ -193,6 +193,13 @@ def test_split_tail_plan(L):
     info = binding.gge_plan(A1, A1, D=D1, config=binding.make_config(**pair))
     assert info["num_tiles"] == 16 and info["tail_tiles"] == 16 and info["tail_splits"] == 4
     assert info["grid"] == 2 * 64
+    # very skinny, long K: 8 one-CTA tiles of 128 x 128 on 152 CTAs, at most 8 slices
+    A8 = torch.zeros(64, 32768, dtype=torch.bfloat16)
+    B8 = torch.zeros(1024, 32768, dtype=torch.bfloat16)
+    info = binding.gge_plan(A8, B8, D=torch.zeros(64, 1024, dtype=torch.bfloat16),
+                            config=binding.make_config(num_ctas=152))
+    assert info["cta_group"] == 1 and info["tile_n"] == 128
+    assert info["tail_tiles"] == 8 and info["tail_splits"] == 8 and info["grid"] == 64
     # gather forms never split
     idx = torch.zeros(1536, dtype=torch.int32)
     info = binding.gge_plan(A, B, D=D, gather=True, config=binding.make_config(num_ctas=152,
