@@ -798,7 +798,8 @@ __device__ __forceinline__ void epilogue_role(const Params& p, const Shared& sh,
         epilogue_chunk(p, v, row_base, rows_valid, col0, tc.batch, alpha, beta, ccur, stg);
     }
     // a writer lane publishes its row once all of its chunks are stored
-    if (writer) ptx::st_release_gpu(part_flag(slice), tail_mark);
+    if (writer && !(p.flags & FLAG_TEST_DROP_TAIL_FLAG))
+      ptx::st_release_gpu(part_flag(slice), tail_mark);
     if ((p.flags & FLAG_TILE_COUNTS) && p.tile_counts != nullptr && rank == 0 && warp == 0 &&
         lane == 0 && !writer)
       atomicAdd(p.tile_counts + (split ? p.full_tiles + tail_r : t), 1);

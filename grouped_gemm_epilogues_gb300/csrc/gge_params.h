@@ -25,6 +25,8 @@ enum : int32_t {
   FLAG_DIRECT_STORES = 8,      // epilogue stores straight from registers (no staging buffers)
   FLAG_PAIR_CLUSTER = 16,      // two CTA pairs per cluster share A by TMA multicast
   FLAG_NO_SPLIT = 32,          // never split the last wave along K
+  FLAG_TEST_DROP_TAIL_FLAG = 64,  // test hook: split-tail writers never publish, so the
+                                  // owners' bounded waits run out (GGE_ERR_TIMEOUT)
 };
 
 struct Params {

@@ -115,7 +115,11 @@ typedef struct gge_config {
                              adds the others' fp32 partial sums (kept in the
                              workspace) before its epilogue.  Not with the
                              dynamic scheduler, two-pair clusters or the gather
-                             and varlen forms; needs gge_workspace_size bytes.   */
+                             and varlen forms; needs gge_workspace_size bytes;
+                             bit 6: test hook -- the split last wave's partial
+                             sums are never published, so the owning CTAs'
+                             bounded waits run out and the call reports
+                             GGE_ERR_TIMEOUT.                                     */
   int32_t cta_group;      /* 0 = auto; 1 = one CTA per 128-row tile; 2 = a CTA pair
                              per 256-row tile (tcgen05 cta_group::2, 256-column
                              tiles, not with the gather forms)                     */
