@@ -160,6 +160,18 @@ def workspace(device=None, nbytes: int = 256) -> torch.Tensor:
     return ws
 
 
+# gge_config.flags bits (include/gge.h)
+FLAGS = {
+    "tile_counts": 1,          # count tile visits into tile_counts
+    "test_drop_acc_full": 2,   # test hook: the epilogue's accumulator wait runs out
+    "dynamic_sched": 4,        # tiles claimed from a counter in the workspace
+    "direct_stores": 8,        # epilogue stores without shared-memory staging
+    "pair_cluster": 16,        # two CTA pairs share A by TMA multicast
+    "no_split": 32,            # never split the last wave along K
+    "test_drop_tail_flag": 64,  # test hook: the split tail's owners' waits run out
+}
+
+
 def make_config(tile_n=0, num_ctas=0, raster_band=0, stages=0, flags=0, tile_counts=None,
                 timeout_ns=0, cta_group=0):
     return GgeConfig(tile_n, num_ctas, raster_band, stages, flags, cta_group,

@@ -220,6 +220,15 @@ def test_skinny_problems_default_to_narrow_tiles(L):
     assert info["cta_group"] == 1 and info["tile_n"] == 256
 
 
+def test_binding_flag_table_matches_header():
+    """Every bit the header documents for gge_config.flags has a binding name."""
+    with open(os.path.join(os.path.dirname(__file__), "..", "include", "gge.h")) as f:
+        text = f.read()
+    bits = sorted(int(b) for b in re.findall(r"bit (\d+):", text))
+    assert bits == list(range(len(bits)))
+    assert sorted(binding.FLAGS.values()) == [1 << b for b in bits]
+
+
 def test_workspace_size_covers_the_split(L):
     size = L.gge_workspace_size(None, 0)
     assert size >= 256  # without a GPU only the status words are reported
