@@ -713,8 +713,9 @@ __device__ __forceinline__ void epilogue_role(const Params& p, const Shared& sh,
     // split tail item: the last slice owns the tile's outputs; the others only
     // write their fp32 accumulator rows to the workspace.  Slice s of tail tile r
     // runs on unit s R + r, so the owner waits only on units of lower index,
-    // which the hardware makes resident first: no wait on a unit that cannot
-    // start while other work holds SMs.
+    // which are dispatched first (CTAs start in index order in practice; the
+    // wait is bounded in any case), not on one that other work could keep from
+    // starting.
     const bool split = !GATHER && p.tail_tiles > 0 && t >= p.full_tiles;
     int32_t slice = 0, tail_r = 0;
     if (split) {
