@@ -4,7 +4,11 @@
 
 One step is one call of the hot path (one persistent-kernel launch through
 the C ABI) over one batch of seeded synthetic input of the named workload
-(default: 4096^3 bf16 GEMM + C (beta 0.5) + gelu_tanh writing D and PostAct).
+(default: 8192^3 bf16 GEMM + gelu_tanh writing D and PostAct, the shape the
+70 % tensor-peak target is quoted on).  At N = 1 the same run also measures
+the metric's other workloads (``per_config``: 256^3 bf16, 4096^3 bf16 + C +
+GELU, 8192^3 and 16 x 2048^2 x 4096 fp16 ReLU, the varlen gather-A SiLU MoE
+layer, 8192^3 fp8), each autotuned and timed on its own.
 Inputs are resident in HBM; consecutive steps rotate over input sets whose
 total size exceeds the 129 MB L2, so no step reads warm operands.  Device
 time comes from CUDA events on the launching stream around exactly K steps,
@@ -36,7 +40,7 @@ import torch  # noqa: E402
 from grouped_gemm_epilogues_gb300 import workloads as wl  # noqa: E402
 
 METRIC = "TFLOP/s per GEMM shape and % of GB300 dense bf16/fp8 tensor peak (1 GPU)"
-DEFAULT_WORKLOAD = "gemm_act_4096_bf16_gelu"
+DEFAULT_WORKLOAD = "gemm_act_8192_bf16_gelu"
 L2_BYTES = 129 * 1024 * 1024
 NOMINAL_PEAK = {"bf16": 2250.0, "f16": 2250.0, "e4m3": 4500.0, "e5m2": 4500.0}
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
@@ -189,9 +193,9 @@ def _rotate_rows(a, i):
     return r if a.is_contiguous() else r.transpose(-1, -2)
 
 
-def _device_sets(w, dev, n_sets):
+def _device_sets(w, dev, n_sets, base=None):
     sets = []
-    base = wl.make(w)
+    base = wl.make(w) if base is None else base
     for i in range(n_sets):
         s = {}
         for k, v in base.items():
@@ -247,6 +251,143 @@ def _step_fn(w, binding, config=None):
     return step
 
 
+# The other workloads of the metric, measured in the same run (N = 1) next to the
+# headline: (key, workload)
+PER_CONFIG = [("c1", "gemm_256_bf16"), ("c2", "gemm_act_4096_bf16_gelu"),
+              ("c3a", "gemm_8192_f16_relu"), ("c3b", "bgemm_2048x2048x4096x16_f16_relu"),
+              ("c4", "varlen_gather_g64_m32768_silu"), ("c5", "gemm_8192_fp8")]
+
+
+def _prepare(w, dev, binding, tune):
+    """Rotating device input sets (their total above L2 where the problem allows),
+    the launch configuration (autotuned unless tune is False) and the step."""
+    base, probe = _device_sets(w, dev, 1)
+    per_set = _set_bytes(probe[0])
+    n_sets = max(2, int(np.ceil(2.5 * L2_BYTES / per_set)) + 1)
+    n_sets = min(n_sets, 8)
+    del probe
+    _, sets = _device_sets(w, dev, n_sets, base)
+    # launch shape: the autotuner's pick for this problem (tuning runs before the
+    # warm-up and is not timed), or the planner's default
+    tuned = None
+    if tune:
+        s0 = sets[0]
+        tuned, _ = binding.gge_autotune(_op_of(w), s0["A"], s0["B"], idx=s0.get("a_idx"),
+                                        cu=s0.get("cu_seqlens_k", s0.get("cu_seqlens_m")),
+                                        C=s0.get("C"), D=s0.get("D"), PostAct=s0.get("P"),
+                                        act=w.act, alpha=w.alpha, beta=w.beta, reps=5)
+    step = _step_fn(w, binding, binding.make_config(**tuned) if tuned else None)
+    l2 = (f"{n_sets} rotating input sets of {per_set / 2**20:.0f} MiB (> L2)"
+          if n_sets * per_set > L2_BYTES else
+          f"{n_sets} rotating input sets of {per_set / 2**20:.2f} MiB "
+          "(whole working set < L2: L2-resident)")
+    return base, sets, tuned, step, l2
+
+
+def _graph_runner(step, sets, steps):
+    """Exactly `steps` launches replayed from CUDA graphs (a graph of whole passes
+    over the input sets, up to ~64 launches, then one for the remainder), without
+    the per-call host cost of the Python binding in the way of small problems."""
+    n_sets = len(sets)
+    per_graph = n_sets * max(1, min(64 // n_sets, steps // n_sets))
+    full, rem = divmod(steps, per_graph)
+    graphs = []
+    if full:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for i in range(per_graph):
+                step(sets[i % n_sets])
+        graphs += [g] * full
+    if rem:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for i in range(rem):
+                step(sets[i % n_sets])
+        graphs.append(g)
+    torch.cuda.synchronize()
+
+    def run():
+        for g in graphs:
+            g.replay()
+    run()  # warm the graphs once
+    torch.cuda.synchronize()
+    return run
+
+
+def _settle(step, sets, seconds):
+    """Extra untimed work so that clocks settle under load."""
+    t_end = time.time() + seconds
+    i = 0
+    while time.time() < t_end:
+        for _ in range(20):
+            step(sets[i % len(sets)])
+            i += 1
+        torch.cuda.synchronize()
+
+
+def _timed(step, sets, steps, stream, eager, barrier=lambda: None):
+    """Device time (ms) of exactly `steps` steps, CUDA events on the launching
+    stream, bracketed by a barrier and a synchronize on both sides."""
+    runner = None if eager else _graph_runner(step, sets, steps)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    e0.record(stream)
+    if runner is not None:
+        runner()
+    else:
+        for i in range(steps):
+            step(sets[i % len(sets)])
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    return e0.elapsed_time(e1)
+
+
+def _peak_for(w, peaks, src):
+    bf16 = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
+    is8 = w.ab_dtype in ("e4m3", "e5m2")
+    return (bf16 * (2.0 if is8 else 1.0),
+            f"{src} cuBLAS bf16 burst" + (" x2 (fp8/bf16 nominal ratio)" if is8 else ""))
+
+
+def measure_config(args, w, dev, binding, local, peaks, src):
+    """One per-config line: autotuned shape, warm-up, then at least ~0.3 s of
+    timed launches (at least --steps) with the clocks sampled meanwhile."""
+    _, sets, tuned, step, l2 = _prepare(w, dev, binding, not args.no_tune)
+    stream = torch.cuda.current_stream(dev)
+    for i in range(max(args.warmup, len(sets))):
+        step(sets[i % len(sets)])
+    torch.cuda.synchronize()
+    status = binding.gge_read_device_status(dev)
+    if status[0] != "GGE_OK":
+        raise RuntimeError(f"{w.name}: device status after warm-up: {status}")
+    est = _timed(step, sets, len(sets), stream, True) / len(sets)
+    steps = max(args.steps, int(np.ceil(300.0 / max(est, 1e-3))))
+    sampler = ClockSampler(local)
+    sampler.start()
+    _settle(step, sets, 0.2)
+    ms = _timed(step, sets, steps, stream, args.eager)
+    clocks = sampler.stop()
+    status = binding.gge_read_device_status(dev)
+    if status[0] != "GGE_OK":
+        raise RuntimeError(f"{w.name}: device status after the timed region: {status}")
+    ms_per_step = ms / steps
+    tflops = w.flops / (ms_per_step * 1e-3) / 1e12
+    peak, peak_src = _peak_for(w, peaks, src)
+    out = {"workload": w.name, "value": round(tflops, 1), "unit": "TFLOP/s",
+           "ms_per_step": round(ms_per_step, 5), "steps": steps,
+           "frac": round(tflops / peak, 4), "peak": peak, "peak_source": peak_src,
+           "frac_of_nominal_dense_peak": round(tflops / NOMINAL_PEAK[w.ab_dtype], 4),
+           "traffic": profiled_traffic(w.name), "l2": l2, "clocks": clocks,
+           "launch_shape": (dict(tuned, source="autotuned") if tuned else
+                            {"source": "planner default"})}
+    del sets
+    torch.cuda.empty_cache()
+    return out
+
+
 def run_ours(args, w):
     from grouped_gemm_epilogues_gb300 import binding
 
@@ -258,22 +399,8 @@ def run_ours(args, w):
         dist.init_process_group("nccl", device_id=dev)
     binding.load()
 
-    base, probe = _device_sets(w, dev, 1)
-    per_set = _set_bytes(probe[0])
-    n_sets = max(2, int(np.ceil(2.5 * L2_BYTES / per_set)) + 1)
-    n_sets = min(n_sets, 8)
-    del probe
-    _, sets = _device_sets(w, dev, n_sets)
-    # launch shape: the autotuner's pick for this problem (tuning runs before the
-    # warm-up and is not timed), or the planner's default with --no-tune
-    tuned = None
-    if not args.no_tune:
-        s0 = sets[0]
-        tuned, _ = binding.gge_autotune(_op_of(w), s0["A"], s0["B"], idx=s0.get("a_idx"),
-                                        cu=s0.get("cu_seqlens_k", s0.get("cu_seqlens_m")),
-                                        C=s0.get("C"), D=s0.get("D"), PostAct=s0.get("P"),
-                                        act=w.act, alpha=w.alpha, beta=w.beta, reps=5)
-    step = _step_fn(w, binding, binding.make_config(**tuned) if tuned else None)
+    base, sets, tuned, step, l2 = _prepare(w, dev, binding, not args.no_tune)
+    n_sets = len(sets)
     stream = torch.cuda.current_stream(dev)
 
     def barrier():
@@ -290,54 +417,9 @@ def run_ours(args, w):
         raise RuntimeError(f"device status after warm-up: {status}")
 
     sampler.start()
-    # settle clocks under load before the timed region (extra warm-up work)
-    t_end = time.time() + 0.5
-    i = 0
-    while time.time() < t_end:
-        for _ in range(20):
-            step(sets[i % n_sets])
-            i += 1
-        torch.cuda.synchronize()
-    # The timed launches replay from CUDA graphs (one pass over the rotating
-    # input sets, plus the remainder): exactly K kernel launches, without the
-    # per-call host cost of the Python binding in the way of small problems.
-    runner = None
-    if not args.eager:
-        full, rem = divmod(args.steps, n_sets)
-        g_cycle = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g_cycle):
-            for s_ in sets:
-                step(s_)
-        g_rem = None
-        if rem:
-            g_rem = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g_rem):
-                for s_ in sets[:rem]:
-                    step(s_)
-        torch.cuda.synchronize()
-
-        def runner():
-            for _ in range(full):
-                g_cycle.replay()
-            if g_rem is not None:
-                g_rem.replay()
-        runner()  # warm the graphs once
-        torch.cuda.synchronize()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    barrier()
-    torch.cuda.synchronize()
-    e0.record(stream)
-    if runner is not None:
-        runner()
-    else:
-        for i in range(args.steps):
-            step(sets[i % n_sets])
-    e1.record(stream)
-    torch.cuda.synchronize()
-    barrier()
+    _settle(step, sets, 0.5)
+    ms = _timed(step, sets, args.steps, stream, args.eager, barrier)
     clocks = sampler.stop()
-    ms = e0.elapsed_time(e1)
     status = binding.gge_read_device_status(dev)
     if status[0] != "GGE_OK":
         raise RuntimeError(f"device status after the timed region: {status}")
@@ -349,14 +431,12 @@ def run_ours(args, w):
     e2e = run_e2e(args, w, base, dev, step)
 
     peaks, src = measured_peaks()
-    bf16 = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
-    is8 = w.ab_dtype in ("e4m3", "e5m2")
-    peak = bf16 * (2.0 if is8 else 1.0)
+    peak, peak_src = _peak_for(w, peaks, src)
     achieved = flops / (ms_per_step * 1e-3) / 1e12
     roofline = {
         "bound": "tensor", "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
         "frac": round(achieved / peak, 4), "traffic": profiled_traffic(w.name),
-        "peak_source": f"{src} cuBLAS bf16 burst" + (" x2 (fp8/bf16 nominal ratio)" if is8 else ""),
+        "peak_source": peak_src,
         "frac_of_nominal_dense_peak": round(achieved / NOMINAL_PEAK[w.ab_dtype], 4),
     }
     line = {
@@ -371,10 +451,7 @@ def run_ours(args, w):
                       if w.k_groups else {}),
                    "with_c": w.with_c, "alpha": w.alpha, "beta": w.beta,
                    "accumulate": "f32", "out": w.p_dtype or w.d_dtype,
-                   "l2": (f"{n_sets} rotating input sets of {per_set / 2**20:.0f} MiB (> L2)"
-                          if n_sets * per_set > L2_BYTES else
-                          f"{n_sets} rotating input sets of {per_set / 2**20:.2f} MiB "
-                          "(whole working set < L2: L2-resident)"),
+                   "l2": l2,
                    "parallelism": f"replicas{ws_n}" if ws_n > 1 else "single",
                    "launch": "eager" if args.eager else "cuda_graph",
                    "launch_shape": (dict(tuned, source="autotuned") if tuned else
@@ -384,8 +461,14 @@ def run_ours(args, w):
         "gpu_launches": args.steps,
         "clocks": clocks,
     }
+    del sets
+    torch.cuda.empty_cache()
     if rank == 0 and ws_n == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, base, budget_s=args.cpu_seconds)
+    if ws_n == 1 and not args.no_per_config:
+        line["per_config"] = {key: measure_config(args, wl.WORKLOADS[name], dev, binding, local,
+                                                  peaks, src)
+                              for key, name in PER_CONFIG}
     if ws_n > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
@@ -586,6 +669,8 @@ def main():
                     help="use the planner's default launch shape instead of the autotuner's")
     ap.add_argument("--eager", action="store_true",
                     help="launch every timed step from Python instead of CUDA-graph replay")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="skip the per-config lines (the other workloads of the metric)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -52,7 +52,7 @@ class GgePlanInfo(ctypes.Structure):
     _fields_ = [("tile_m", c_i32), ("tile_n", c_i32), ("tile_k", c_i32), ("stages", c_i32),
                 ("num_tiles", c_i32), ("grid", c_i32), ("threads", c_i32),
                 ("smem_bytes", c_i32), ("raster_band", c_i32), ("cta_group", c_i32),
-                ("tail_tiles", c_i32), ("tail_splits", c_i32)]
+                ("raster_along_n", c_i32), ("tail_tiles", c_i32), ("tail_splits", c_i32)]
 
 
 # every function include/gge.h declares, with its ctypes signature
@@ -76,10 +76,12 @@ _SIGNATURES = {
     "gge_gemm_act_static_scratch": (c_i32, [ctypes.POINTER(GgeGemmArgs), ctypes.c_void_p]),
     "gge_read_device_status": (c_i32, [ctypes.c_void_p, ctypes.c_void_p,
                                        ctypes.POINTER(c_i32)]),
+    "gge_read_static_scratch_status": (c_i32, [ctypes.c_void_p, ctypes.POINTER(c_i32)]),
     "gge_status_string": (ctypes.c_char_p, [c_i32]),
     "gge_fastdivmod_params": (None, [c_i32, ctypes.POINTER(c_u32), ctypes.POINTER(c_u32)]),
     "gge_fastdivmod_div": (c_i32, [c_i32, c_i32]),
-    "gge_schedule_map": (c_i32, [c_i32, c_i32, c_i32, c_i32, c_i32, ctypes.POINTER(c_i32)]),
+    "gge_schedule_map": (c_i32, [c_i32, c_i32, c_i32, c_i32, c_i32, c_i32,
+                                 ctypes.POINTER(c_i32)]),
     "gge_plan": (c_i32, [ctypes.POINTER(GgeGemmArgs), c_i32, c_i32, ctypes.POINTER(GgePlanInfo)]),
     "gge_version": (ctypes.c_char_p, []),
     "gge_tune_candidates": (c_i32, [ctypes.POINTER(GgeGemmArgs), c_i32, c_i32,
@@ -166,10 +168,10 @@ FLAGS = {
     "test_drop_acc_full": 2,   # test hook: the epilogue's accumulator wait runs out
     "dynamic_sched": 4,        # tiles claimed from a counter in the workspace
     "direct_stores": 8,        # epilogue stores without shared-memory staging
-    "pair_cluster": 16,        # two CTA pairs share A by TMA multicast
     "no_split": 32,            # never split the last wave along K
-    "test_drop_tail_flag": 64,  # test hook: the split tail's owners' waits run out
+    "raster_n": 128,           # raster bands of n-tiles
 }
+RESERVED_FLAGS = 16 | 64       # a call that sets one of these is rejected
 
 
 def make_config(tile_n=0, num_ctas=0, raster_band=0, stages=0, flags=0, tile_counts=None,
@@ -317,6 +319,17 @@ def gge_gemm_gather_a(A_src, B, a_idx, cu_seqlens_m=None, D=None, PostAct=None, 
            "gge_gemm_gather_a")
 
 
+def gge_read_static_scratch_status(device=None):
+    """Synchronise the current stream and return (status_name, where, tile) that
+    gge_gemm_act_static_scratch calls recorded in the library's area; clears it."""
+    lib = load()
+    dev = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
+    detail = (c_i32 * 2)()
+    stream = ctypes.c_void_p(torch.cuda.current_stream(dev).cuda_stream)
+    code = lib.gge_read_static_scratch_status(stream, detail)
+    return STATUS.get(code, str(code)), detail[0], detail[1]
+
+
 def gge_read_device_status(device=None):
     """Synchronise the current stream and return (status_name, where, tile); clears it."""
     lib = load()
@@ -363,9 +376,9 @@ def gge_tune_candidates(op, A, B, C=None, D=None, PostAct=None, act="none", num_
     """The launch configurations gge_autotune would time for this problem (host only)."""
     lib = load()
     args = _tune_args(op, A, B, C, D, PostAct, act, 1.0, 1.0, config)
-    out = (GgeConfig * 32)()
-    n = lib.gge_tune_candidates(ctypes.byref(args), OP[op], num_groups, out, 32)
-    return [config_dict(out[i]) for i in range(min(n, 32))]
+    out = (GgeConfig * 64)()
+    n = lib.gge_tune_candidates(ctypes.byref(args), OP[op], num_groups, out, 64)
+    return [config_dict(out[i]) for i in range(min(n, 64))]
 
 
 def gge_autotune(op, A, B, idx=None, cu=None, C=None, D=None, PostAct=None, act="none",

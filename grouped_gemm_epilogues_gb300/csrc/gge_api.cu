@@ -30,6 +30,10 @@ constexpr int kEpiWarpsHost = 8;          // epilogue warps of the TMA variants 
 constexpr int kMaxGroupsHost = 1024;
 constexpr int kIdxChunkHost = 2048;       // gather-K index entries staged in shared memory
 constexpr size_t kWorkspaceBytes = 256;
+// the split last wave's tickets (one int32 per tail tile, CTA and epilogue warp)
+// follow the status words in a region of their own: no other call writes there,
+// so a ticket is never mistaken for another call's data
+constexpr size_t kTicketBytes = 16384;
 constexpr size_t kMapSlotsHost = 16;     // varlen-K tensor-map slots per CTA (kernel kMapSlots)
 constexpr size_t kMapSlotBytesHost = 256;
 constexpr int kMaxStages = 8;            // fewer stages than map slots
@@ -124,17 +128,18 @@ struct Plan {
   int units = 0;
 };
 
-// Workspace layout of a split last wave: status words, then the flags (one per
-// slice but the last, CTA, epilogue warp and lane), then the partial accumulators
-// (one 128 x BN fp32 block per slice but the last and CTA), each region 256-byte aligned.
-size_t tail_flag_bytes(int64_t blocks) {
-  return static_cast<size_t>((blocks * kEpiWarpsHost * 32 * 4 + 255) / 256 * 256);
-}
+// Workspace layout: the status words; the split last wave's tickets; then either
+// the split's partial accumulators (one 128 x BN fp32 block per tail tile, slice
+// and CTA) or, for varlen-K and gather-K, the per-CTA tensor-map slots.  Each
+// region starts 256-byte aligned.
+constexpr size_t kTailBase = kWorkspaceBytes + kTicketBytes;
 size_t tail_workspace(const Plan& pl) {
   if (pl.p.tail_tiles <= 0) return 0;
-  const int64_t blocks = static_cast<int64_t>(pl.p.tail_tiles) * (pl.p.tail_splits - 1) * pl.cg;
-  return kWorkspaceBytes + tail_flag_bytes(blocks) +
-         static_cast<size_t>(blocks) * kTileM * pl.bn * sizeof(float);
+  const int64_t blocks = static_cast<int64_t>(pl.p.tail_tiles) * pl.p.tail_splits * pl.cg;
+  return kTailBase + static_cast<size_t>(blocks) * kTileM * pl.bn * sizeof(float);
+}
+bool tickets_fit(const Plan& pl) {
+  return static_cast<size_t>(pl.p.tail_tiles) * pl.cg * kEpiWarpsHost * 4 <= kTicketBytes;
 }
 
 CUtensorMapDataType tmap_type(int es) {
@@ -327,6 +332,7 @@ gge_status make_plan(const gge_gemm_args* a, Form form, const int32_t* a_idx,
   pl.gather = gather;
 
   if (a->act < GGE_ACT_NONE || a->act > GGE_ACT_RELU_SQ) return GGE_ERR_INVALID_ARG;
+  if (cfg && (cfg->flags & FLAG_RESERVED)) return GGE_ERR_UNSUPPORTED;
   if (dact) {
     // backward epilogue: C = pre-activation and D = dx are required, PostAct optional
     if (a->C == nullptr || a->D == nullptr || a->act == GGE_ACT_NONE) return GGE_ERR_INVALID_ARG;
@@ -436,10 +442,6 @@ gge_status make_plan(const gge_gemm_args* a, Form form, const int32_t* a_idx,
   // tile shape: 128 x BN on one CTA, or 256 x BN on a CTA pair
   int cg = cfg && cfg->cta_group ? cfg->cta_group : ((!gather && N > 128 && M >= 256) ? 2 : 1);
   if (cg == 2 && gather) return GGE_ERR_UNSUPPORTED;
-  // two CTA pairs per cluster sharing A by multicast: plain problems on pairs, static schedule
-  const bool mc = cfg && (cfg->flags & FLAG_PAIR_CLUSTER);
-  if (mc && (cg != 2 || varlen || gather || vk || (cfg->flags & (FLAG_DYNAMIC_SCHED | FLAG_TILE_COUNTS))))
-    return GGE_ERR_UNSUPPORTED;
   if (cg != 1 && cg != 2) return GGE_ERR_UNSUPPORTED;
   int bn = cfg && cfg->tile_n ? cfg->tile_n : 0;
   if (cg == 1) {
@@ -504,17 +506,10 @@ gge_status make_plan(const gge_gemm_args* a, Form form, const int32_t* a_idx,
   p.stages = stages;
   p.tiles_n = static_cast<int32_t>(tiles_n);
   p.tiles_n_div = FastDivmod::create(tiles_n > 0 ? static_cast<int32_t>(tiles_n) : 1);
-  int band = cfg && cfg->raster_band > 0 ? cfg->raster_band : 16;
   int64_t num_tiles = 0;
   if (!varlen) {
-    // with two-pair clusters the schedule walks pairs of adjacent n-tiles
-    const int64_t sched_n = mc ? (tiles_n + 1) / 2 : tiles_n;
-    num_tiles = tiles_m * sched_n * L;
+    num_tiles = tiles_m * tiles_n * L;
     if (num_tiles > kMaxExtent) return GGE_ERR_UNSUPPORTED;
-    p.sched = PlainSchedule::create(static_cast<int32_t>(tiles_m), static_cast<int32_t>(sched_n),
-                                    static_cast<int32_t>(L), band);
-    p.mc = mc ? 1 : 0;
-    band = p.sched.band;
     p.num_tiles = static_cast<int32_t>(num_tiles);
     if (vk) {
       p.k_groups = G;
@@ -530,7 +525,6 @@ gge_status make_plan(const gge_gemm_args* a, Form form, const int32_t* a_idx,
     num_tiles = (M / tile_m + G) * tiles_n;
     p.num_tiles = -1;
   }
-  pl.band = band;
   if (gather) {
     p.a_idx = a_idx;
     p.a_src = static_cast<const uint8_t*>(a->A.ptr);
@@ -579,7 +573,7 @@ gge_status make_plan(const gge_gemm_args* a, Form form, const int32_t* a_idx,
   // launch shape: a persistent grid of at most one CTA (pair) per resident slot
   pl.shape.smem = static_cast<size_t>(fixed + stages * stage_bytes);
   pl.shape.threads = variant_threads(bn, pl.gather, cg);
-  pl.shape.cluster = mc ? 4 : cg;
+  pl.shape.cluster = cg;
   const int unit_ctas = pl.shape.cluster;
   int units_cap = cfg && cfg->num_ctas > 0 ? std::max(1, cfg->num_ctas / unit_ctas) : -1;
   if (encode) {
@@ -589,11 +583,22 @@ gge_status make_plan(const gge_gemm_args* a, Form form, const int32_t* a_idx,
   }
   pl.shape.grid =
       units_cap > 0 ? unit_ctas * static_cast<int>(std::min<int64_t>(num_tiles, units_cap)) : -1;
+  if (!varlen) {
+    // raster: bands of m-tiles (or of n-tiles), the band width the caller's or the
+    // one that keeps a wave's operand footprint smallest for the units in use
+    const bool along_n = cfg && (cfg->flags & FLAG_RASTER_N);
+    const int band = cfg && cfg->raster_band > 0
+                         ? cfg->raster_band
+                         : (units_cap > 0 ? auto_band(units_cap, tile_m, bn, along_n) : 8);
+    p.sched = PlainSchedule::create(static_cast<int32_t>(tiles_m), static_cast<int32_t>(tiles_n),
+                                    static_cast<int32_t>(L), band, along_n);
+    pl.band = p.sched.band;
+  }
   // split the last, partly filled wave along K (plain problems, fixed schedule)
   pl.tiles = num_tiles;
   pl.units = units_cap;
   const int32_t flags = cfg ? cfg->flags : 0;
-  if (!varlen && !vk && !gather && !mc && K > 0 && units_cap > 0 &&
+  if (!varlen && !vk && !gather && K > 0 && units_cap > 0 &&
       !(flags & (FLAG_DYNAMIC_SCHED | FLAG_NO_SPLIT))) {
     const TailSplit ts = plan_tail_split(num_tiles, units_cap, p.k_tiles);
     if (ts.tail > 0) {
@@ -614,10 +619,9 @@ gge_status make_plan(const gge_gemm_args* a, Form form, const int32_t* a_idx,
     if (gather) {
       // A rows are copied by the gather warps: no tensor map
     } else if (!a_mn) {
-      // two-pair clusters: each CTA loads half of its 128 rows and multicasts them
       s = encode_3d(&pl.tmA, a->A.ptr, es, K, a->A.rows, a->A.batch,
                     static_cast<uint64_t>(a->A.stride_row) * es, batch_stride_bytes(a->A, es), bk,
-                    mc ? kTileM / 2 : kTileM);
+                    kTileM);
       if (s != GGE_OK) return s;
     } else {
       s = encode_3d(&pl.tmA, a->A.ptr, es, a->A.rows, K, a->A.batch,
@@ -640,8 +644,8 @@ gge_status make_plan(const gge_gemm_args* a, Form form, const int32_t* a_idx,
 }
 
 size_t varlen_k_workspace(const Plan& pl) {
-  return kWorkspaceBytes + static_cast<size_t>(std::max(pl.shape.grid, 0)) * kMapSlotsHost *
-                               kMapSlotBytesHost;
+  return kTailBase + static_cast<size_t>(std::max(pl.shape.grid, 0)) * kMapSlotsHost *
+                         kMapSlotBytesHost;
 }
 
 gge_status check_workspace(void* ws, size_t bytes) {
@@ -665,20 +669,19 @@ gge_status run(const gge_gemm_args* a, Form form, const int32_t* a_idx, const in
   if (s != GGE_OK) return s;
   if (pl.empty) return GGE_OK;
   if (pl.p.k_groups > 0) {
-    // varlen-K and gather-K: per-CTA tensor-map slots follow the status words (the
+    // varlen-K and gather-K: per-CTA tensor-map slots follow the ticket region (the
     // kernel writes the clipped maps of ragged groups there)
     if (ws == nullptr || ws_bytes < varlen_k_workspace(pl)) return GGE_ERR_WORKSPACE;
     if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return GGE_ERR_ALIGNMENT;
-    pl.p.kmaps = static_cast<uint8_t*>(ws) + kWorkspaceBytes;
+    pl.p.kmaps = static_cast<uint8_t*>(ws) + kTailBase;
   }
   pl.p.status = static_cast<int32_t*>(ws);
   if (pl.p.tail_tiles > 0) {
-    if (ws != nullptr && ws_bytes >= tail_workspace(pl) &&
+    if (ws != nullptr && ws_bytes >= tail_workspace(pl) && tickets_fit(pl) &&
         (reinterpret_cast<uintptr_t>(ws) & 255u) == 0) {
-      const int64_t blocks = static_cast<int64_t>(pl.p.tail_tiles) * (pl.p.tail_splits - 1) * pl.cg;
-      uint8_t* base = static_cast<uint8_t*>(ws) + kWorkspaceBytes;
-      pl.p.tail_flags = reinterpret_cast<int32_t*>(base);
-      pl.p.partials = reinterpret_cast<float*>(base + tail_flag_bytes(blocks));
+      uint8_t* base = static_cast<uint8_t*>(ws);
+      pl.p.tail_tickets = reinterpret_cast<int32_t*>(base + kWorkspaceBytes);
+      pl.p.partials = reinterpret_cast<float*>(base + kTailBase);
     } else {
       // not enough workspace for the partial sums: run the last wave unsplit
       pl.p.tail_tiles = 0;
@@ -725,8 +728,8 @@ extern "C" {
 size_t gge_workspace_size(const gge_gemm_args* args, int32_t num_groups) {
   (void)args;
   (void)num_groups;
-  // room for the split last wave of any plain problem: at most one partial block
-  // (128 x 256 fp32) and one warp-flag set per CTA the GPU can hold
+  // room for the split last wave of any plain problem: the tickets and at most
+  // one partial block (128 x 256 fp32) per CTA the GPU can hold
   int dev = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
@@ -734,8 +737,7 @@ size_t gge_workspace_size(const gge_gemm_args* args, int32_t num_groups) {
     cudaGetLastError();
     return gge::kWorkspaceBytes;
   }
-  return gge::kWorkspaceBytes + gge::tail_flag_bytes(sms) +
-         static_cast<size_t>(sms) * gge::kTileM * 256 * sizeof(float);
+  return gge::kTailBase + static_cast<size_t>(sms) * gge::kTileM * 256 * sizeof(float);
 }
 
 gge_status gge_gemm(const gge_gemm_args* args, void* ws, size_t ws_bytes, gge_stream_t stream) {
@@ -771,8 +773,7 @@ size_t gge_workspace_size_varlen_k(const gge_gemm_args* args, int32_t num_groups
   (void)num_groups;
   const int sms = gge::sm_count();
   if (sms <= 0) return 0;
-  return gge::kWorkspaceBytes +
-         static_cast<size_t>(sms) * gge::kMapSlotsHost * gge::kMapSlotBytesHost;
+  return gge::kTailBase + static_cast<size_t>(sms) * gge::kMapSlotsHost * gge::kMapSlotBytesHost;
 }
 
 gge_status gge_gemm_varlen_k(const gge_gemm_args* args, const int32_t* cu_seqlens_k,
@@ -832,8 +833,9 @@ int32_t gge_fastdivmod_div(int32_t divisor, int32_t n) {
 }
 
 int32_t gge_schedule_map(int32_t tiles_m, int32_t tiles_n, int32_t batches, int32_t band,
-                         int32_t count, int32_t* out) {
-  const gge::PlainSchedule s = gge::PlainSchedule::create(tiles_m, tiles_n, batches, band);
+                         int32_t along_n, int32_t count, int32_t* out) {
+  const gge::PlainSchedule s =
+      gge::PlainSchedule::create(tiles_m, tiles_n, batches, band, along_n != 0);
   for (int32_t t = 0; t < count && t < s.num_tiles; ++t) {
     int32_t l, mb, nb;
     s.map(t, l, mb, nb);
@@ -871,6 +873,7 @@ gge_status gge_plan(const gge_gemm_args* args, int32_t num_groups, int32_t form,
   out->threads = pl.shape.threads;
   out->smem_bytes = static_cast<int32_t>(pl.shape.smem);
   out->raster_band = pl.band;
+  out->raster_along_n = pl.p.sched.along_n;
   out->cta_group = pl.cg;
   out->tail_tiles = pl.p.tail_tiles;
   out->tail_splits = pl.p.tail_tiles > 0 ? pl.p.tail_splits : 1;

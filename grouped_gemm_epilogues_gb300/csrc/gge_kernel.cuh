@@ -31,23 +31,23 @@
 // leader CTA issues tcgen05.mma.cta_group::2 over both CTAs' shared memory,
 // and each CTA's TMEM receives its own 128 accumulator rows.  The pair halves
 // the B bytes each SM stages per FLOP, so a stage is 32 KiB instead of 48 KiB
-// and six stages fit.  Optionally two pairs form a cluster of four on adjacent
-// n-tiles and share A by TMA multicast (Params::mc).
+// and six stages fit.
 //
 // Every CTA (pair) walks the same static persistent schedule (tile t, t + grid, ...),
 // or claims tiles from an atomic counter; tile coordinates come from
 // FastDivmod (plain) or from a per-group tile prefix sum in shared memory
 // (varlen-M, VarlenMTileScheduler's role).  On plain problems a last wave that
 // is at most half full is split along K: its tiles' K-slices run on otherwise
-// idle units, which leave fp32 partial sums in the workspace for the epilogue
-// of the unit that runs the tile's last slice (plan_tail_split).
+// idle units, which leave fp32 partial sums in the workspace; whichever unit
+// finishes a tile's slices last adds them up and runs the epilogue
+// (plan_tail_split).  No unit ever waits for another one.
 //
 // Launches use programmatic dependent launch: a CTA sets up its shared memory
 // and TMEM, then waits (griddepcontrol.wait) for the previous kernel in the
 // stream before touching global memory, and lets the next launch start as
 // soon as SMs free up.
 //
-// Every mbarrier wait (and the split tail's flag waits) is bounded by
+// Every mbarrier wait is bounded by
 // Params::timeout_ns of %globaltimer; on expiry the kernel records
 // DEV_TIMEOUT in the status words, raises a shared abort flag so that every
 // role leaves its loop, lets copies in flight land, frees its TMEM and returns.
@@ -130,10 +130,6 @@ struct TileCoord {
 struct Shared {
   uint32_t full, empty, tfull, tempty;  // barrier array bases (shared addresses)
   uint32_t map_full, map_empty;         // varlen-K map-slot barriers (kMapSlots each)
-  uint32_t pair;                        // this CTA's pair in a two-pair cluster (else 0)
-  uint32_t lead;                        // cluster rank of this pair's leader CTA
-  uint16_t pair_mask;                   // cluster ranks of this pair
-  uint16_t all_mask;                    // cluster ranks of every pair of the cluster
   volatile int32_t* abort;
   const int32_t* prefix;  // varlen-M: tile prefix [G+1]; varlen-K: group K ends [G]
   const int32_t* cu;      // varlen-M: cu_seqlens copy [G+1]; varlen-K: group K starts [G]
@@ -165,8 +161,7 @@ __device__ __forceinline__ TileCoord tile_coord(int32_t t, const Params& p, cons
     p.sched.map(tt, l, mb, nb);
     tc.m_row0 = mb * TILE_M;
     tc.row_limit = p.M;
-    // two-pair clusters: the schedule walks n-tile pairs, pair q takes the q-th
-    tc.n0 = (p.mc ? 2 * nb + static_cast<int32_t>(sh.pair) : nb) * BN;
+    tc.n0 = nb * BN;
     tc.batch = l;
     // varlen-K operands are single [rows, total_K] matrices
     tc.a_batch = p.k_groups > 0 ? 0 : l;
@@ -659,26 +654,81 @@ __device__ __forceinline__ void epilogue_chunk(const Params& p, const uint32_t (
   }
 }
 
-// Split last wave: wait (bounded) until another unit's epilogue lane has
-// published its partial row for this launch.
-__device__ __forceinline__ void wait_tail_flag(const int32_t* f, int32_t want, const Params& p,
-                                               const Shared& sh, int32_t tile) {
-  if (ptx::ld_acquire_gpu(f) == want) return;
-  const uint64_t t0 = ptx::globaltimer();
-  while (true) {
-    __nanosleep(128);
-    if (ptx::ld_acquire_gpu(f) == want) return;
-    if (*sh.abort) return;
-    if (ptx::globaltimer() - t0 > p.timeout_ns) {
-      record_status(p, DEV_TIMEOUT, 11, tile);
-      *sh.abort = 1;
-      return;
-    }
-  }
-}
-
 // ------------------------------------------------------------------- roles
 // `unit` / `units`: this CTA's (pair's) index and the number of CTAs (pairs).
+
+// Split last wave, one epilogue warp's share of a tail tile (its 32 rows of the
+// CTA's 128, its 32-column chunks): every slice's unit writes its raw fp32
+// accumulator chunks to the workspace and then takes a ticket; the warp that
+// takes the last ticket adds all slices' chunks in slice order (so the sum
+// does not depend on which unit finished last) and runs the epilogue.  No
+// warp waits for another unit, so the result does not depend on when (or in
+// what order) the units run.  Partial chunk layout: float4 q of a lane's row in
+// chunk c at [quad][c][q][lane], so each warp store / load moves 512
+// contiguous bytes.
+template <int BN, bool GATHER, int CG>
+__device__ __forceinline__ float4* tail_chunk(const Params& p, int32_t tail_r, int32_t slice,
+                                              uint32_t rank, int quad, int c, int lane) {
+  constexpr int kChunks = BN / 32;
+  const int64_t block = (static_cast<int64_t>(tail_r) * p.tail_splits + slice) * CG + rank;
+  return reinterpret_cast<float4*>(p.partials + block * kBM * BN) + ((quad * kChunks + c) * 8) * 32 +
+         lane;
+}
+
+// Writes this lane's 32 accumulator values of chunk c as the slice's partial.
+__device__ __forceinline__ void tail_store(float4* dst, const uint32_t (&v)[32]) {
+#pragma unroll
+  for (int q = 0; q < 8; ++q)
+    dst[q * 32] = make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
+                              __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
+}
+
+// After the warp's partial chunks are written: count this slice in the tile's
+// ticket (per CTA and epilogue warp).  True (in every lane) for the warp whose
+// slice came last, which then owns the tile's outputs; it resets the ticket
+// for the next launch.  The fence before the count publishes every lane's
+// partial stores; the one after it orders the reads of the other slices'.
+__device__ __forceinline__ bool tail_ticket(int32_t* ticket, int32_t splits) {
+  __threadfence();
+  __syncwarp();
+  int32_t last = 0;
+  if ((threadIdx.x & 31) == 0) {
+    last = (atomicAdd(ticket, 1) == splits - 1) ? 1 : 0;
+    if (last) atomicExch(ticket, 0);
+  }
+  last = __shfl_sync(0xffffffffu, last, 0);
+  if (last) __threadfence();
+  return last != 0;
+}
+
+// The sum of every slice's partial of chunk c, in slice order (L2 reads: the
+// other slices were written by other SMs during this launch).
+template <int BN, bool GATHER, int CG>
+__device__ __forceinline__ void tail_sum(const Params& p, int32_t tail_r, uint32_t rank, int quad,
+                                         int c, int lane, uint32_t (&v)[32]) {
+  float4 acc[8];
+  const float4* src = tail_chunk<BN, GATHER, CG>(p, tail_r, 0, rank, quad, c, lane);
+#pragma unroll
+  for (int q = 0; q < 8; ++q) acc[q] = __ldcg(src + q * 32);
+  for (int32_t sl = 1; sl < p.tail_splits; ++sl) {
+    src = tail_chunk<BN, GATHER, CG>(p, tail_r, sl, rank, quad, c, lane);
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const float4 a = __ldcg(src + q * 32);
+      acc[q].x += a.x;
+      acc[q].y += a.y;
+      acc[q].z += a.z;
+      acc[q].w += a.w;
+    }
+  }
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    v[4 * q] = __float_as_uint(acc[q].x);
+    v[4 * q + 1] = __float_as_uint(acc[q].y);
+    v[4 * q + 2] = __float_as_uint(acc[q].z);
+    v[4 * q + 3] = __float_as_uint(acc[q].w);
+  }
+}
 
 // Eight epilogue warps (four in the gather form), two per TMEM lane quadrant
 // (warp w reads lanes 32*(w%4) .. +31); warp w takes the 32-column chunks c
@@ -697,12 +747,6 @@ __device__ __forceinline__ void epilogue_role(const Params& p, const Shared& sh,
   const int quad = warp & 3, half = warp >> 2;
   const float alpha = p.alpha_dev ? *p.alpha_dev : p.alpha;
   const float beta = p.beta_dev ? *p.beta_dev : p.beta;
-  // split last wave: this launch's flags read epoch + 1 (the epoch advances when
-  // the grid finishes, so flags of earlier launches never match)
-  // (the gather forms never split: compiled out of their instances)
-  const int32_t tail_mark =
-      (!GATHER && p.tail_tiles > 0) ? *reinterpret_cast<volatile int32_t*>(p.status + 6) + 1 : 0;
-  const int32_t n_other = p.tail_splits - 1;  // slices besides the owner's
   uint32_t acc = 0, acc_phase = 0;
   for (int i = 0;; ++i) {
     const int32_t t = sched_next<CG>(ts, i, p, sh);
@@ -710,51 +754,29 @@ __device__ __forceinline__ void epilogue_role(const Params& p, const Shared& sh,
     const TileCoord tc = tile_coord<BN, Cfg::kTileM>(t, p, sh);
     // a tile with no k-tiles (K == 0, or an empty varlen-K group) keeps a zero accumulator
     const bool has_acc = k_range(p, sh, tc.batch, t).tiles > 0;
-    // split tail item: the last slice owns the tile's outputs; the others only
-    // write their fp32 accumulator rows to the workspace.  Slice s of tail tile r
-    // runs on unit s R + r, so the owner waits only on units of lower index,
-    // which are dispatched first (CTAs start in index order in practice; the
-    // wait is bounded in any case), not on one that other work could keep from
-    // starting.
+    // split tail item (the gather forms never split: compiled out of their instances)
     const bool split = !GATHER && p.tail_tiles > 0 && t >= p.full_tiles;
     int32_t slice = 0, tail_r = 0;
     if (split) {
       slice = (t - p.full_tiles) / p.tail_tiles;
       tail_r = t - p.full_tiles - slice * p.tail_tiles;
     }
-    const bool writer = split && slice < n_other;
-    // slice sl's (< S - 1) partial block for this CTA is laid out lane-major, so
-    // that each warp store / load moves 512 contiguous bytes: float4 q of this
-    // lane's row in chunk c sits at [quad][c][q][lane].  Its flag: per CTA, warp
-    // and lane.
-    const int64_t part_base = static_cast<int64_t>(tail_r) * n_other * CG + rank;
-    auto part_chunk = [&](int32_t sl, int c) {
-      return reinterpret_cast<float4*>(p.partials +
-                                       (part_base + static_cast<int64_t>(sl) * CG) * kBM * BN) +
-             ((quad * kChunks + c) * 8) * 32 + lane;
-    };
-    auto part_flag = [&](int32_t sl) {
-      return p.tail_flags +
-             ((part_base + static_cast<int64_t>(sl) * CG) * Cfg::kEpiWarps + warp) * 32 + lane;
-    };
     const int32_t row_base = tc.m_row0 + static_cast<int32_t>(rank) * kBM + quad * 32;
     const int32_t rows_valid = min(32, tc.row_limit - row_base);  // warp-uniform, may be <= 0
     const int32_t row = row_base + lane;
-    const bool has_c = !writer && p.c != nullptr && lane < rows_valid;
+    const bool has_c = p.c != nullptr && lane < rows_valid;
     CRegs cnext = {};
-    if (has_c && tc.n0 + half * 32 < p.N) load_c_chunk(p, row, tc.n0 + half * 32, tc.batch, cnext);
+    if (!split && has_c && tc.n0 + half * 32 < p.N)
+      load_c_chunk(p, row, tc.n0 + half * 32, tc.batch, cnext);
     // all lanes take the same branch: tcgen05.ld below is warp-collective
     const bool ok = wait_phase<CG == 2, true>(sh.tfull + 8 * acc, acc_phase, p, sh, 3, t);
     if (!__all_sync(0xffffffffu, ok)) break;
     ptx::tc_fence_after();
-    // the owner's lanes wait until the other slices' units have written their rows
-    if (split && !writer)
-      for (int32_t sl = 0; sl < n_other; ++sl) wait_tail_flag(part_flag(sl), tail_mark, p, sh, t);
     const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + acc * BN;
 #pragma unroll 1
     for (int c = half; c < kChunks; c += kStride) {
       const CRegs ccur = cnext;
-      if (has_c && c + kStride < kChunks && tc.n0 + (c + kStride) * 32 < p.N)
+      if (!split && has_c && c + kStride < kChunks && tc.n0 + (c + kStride) * 32 < p.N)
         load_c_chunk(p, row, tc.n0 + (c + kStride) * 32, tc.batch, cnext);
       uint32_t v[32];
       __syncwarp();  // tcgen05.ld / wait::ld are warp-collective
@@ -770,39 +792,40 @@ __device__ __forceinline__ void epilogue_role(const Params& p, const Shared& sh,
         __syncwarp();
         if (lane == 0) {
           if (CG == 1) ptx::mbar_arrive(sh.tempty + 8 * acc);
-          else ptx::mbar_arrive_remote(ptx::mapa(sh.tempty + 8 * acc, sh.lead));
+          else ptx::mbar_arrive_remote(ptx::mapa(sh.tempty + 8 * acc, 0));
         }
       }
-      if (writer) {  // the raw accumulator chunk: this lane's 32 values
-        float4* dst = part_chunk(slice, c);
-#pragma unroll
-        for (int q = 0; q < 8; ++q)
-          dst[q * 32] = make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
-                                    __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
+      if (split) {  // the slice's raw accumulator chunk: this lane's 32 values
+        tail_store(tail_chunk<BN, GATHER, CG>(p, tail_r, slice, rank, quad, c, lane), v);
         continue;
-      }
-      if (split) {  // the owner adds the other slices' partial sums, in slice order
-        for (int32_t sl = 0; sl < n_other; ++sl) {
-          const float4* src = part_chunk(sl, c);
-#pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            const float4 a = src[q * 32];
-            v[4 * q] = __float_as_uint(__uint_as_float(v[4 * q]) + a.x);
-            v[4 * q + 1] = __float_as_uint(__uint_as_float(v[4 * q + 1]) + a.y);
-            v[4 * q + 2] = __float_as_uint(__uint_as_float(v[4 * q + 2]) + a.z);
-            v[4 * q + 3] = __float_as_uint(__uint_as_float(v[4 * q + 3]) + a.w);
-          }
-        }
       }
       const int32_t col0 = tc.n0 + c * 32;
       if (rows_valid > 0 && col0 < p.N)
         epilogue_chunk(p, v, row_base, rows_valid, col0, tc.batch, alpha, beta, ccur, stg);
     }
-    // a writer lane publishes its row once all of its chunks are stored
-    if (writer && !(p.flags & FLAG_TEST_DROP_TAIL_FLAG))
-      ptx::st_release_gpu(part_flag(slice), tail_mark);
+    bool finished = !split;
+    if (split) {
+      int32_t* ticket =
+          p.tail_tickets + (static_cast<int64_t>(tail_r) * CG + rank) * Cfg::kEpiWarps + warp;
+      if (tail_ticket(ticket, p.tail_splits)) {
+        // this warp's slice came last: add up the tile's slices and run the epilogue
+        finished = true;
+        if (has_c && tc.n0 + half * 32 < p.N) load_c_chunk(p, row, tc.n0 + half * 32, tc.batch, cnext);
+#pragma unroll 1
+        for (int c = half; c < kChunks; c += kStride) {
+          const CRegs ccur = cnext;
+          if (has_c && c + kStride < kChunks && tc.n0 + (c + kStride) * 32 < p.N)
+            load_c_chunk(p, row, tc.n0 + (c + kStride) * 32, tc.batch, cnext);
+          uint32_t v[32];
+          tail_sum<BN, GATHER, CG>(p, tail_r, rank, quad, c, lane, v);
+          const int32_t col0 = tc.n0 + c * 32;
+          if (rows_valid > 0 && col0 < p.N)
+            epilogue_chunk(p, v, row_base, rows_valid, col0, tc.batch, alpha, beta, ccur, stg);
+        }
+      }
+    }
     if ((p.flags & FLAG_TILE_COUNTS) && p.tile_counts != nullptr && rank == 0 && warp == 0 &&
-        lane == 0 && !writer)
+        lane == 0 && finished)
       atomicAdd(p.tile_counts + (split ? p.full_tiles + tail_r : t), 1);
     acc ^= 1u;
     if (acc == 0) acc_phase ^= 1u;
@@ -863,14 +886,14 @@ __device__ __forceinline__ void mma_loop(const Params& p, const Shared& sh, uint
         }
         // frees the stage (in both CTAs of a pair) once these MMAs finish
         if (CG == 1) ptx::mma_commit(sh.empty + 8 * stage);
-        else ptx::mma_commit_pair(sh.empty + 8 * stage, sh.all_mask);
+        else ptx::mma_commit_pair(sh.empty + 8 * stage, 0x3);
       }
       __syncwarp();
       if (++stage == p.stages) { stage = 0; phase ^= 1u; }
     }
     if (!(p.flags & FLAG_TEST_DROP_ACC_FULL) && ptx::elect_one()) {
       if (CG == 1) ptx::mma_commit(sh.tfull + 8 * acc);
-      else ptx::mma_commit_pair(sh.tfull + 8 * acc, sh.pair_mask);
+      else ptx::mma_commit_pair(sh.tfull + 8 * acc, 0x3);
     }
     __syncwarp();
     acc ^= 1u;
@@ -991,17 +1014,9 @@ __device__ __forceinline__ void tma_producer_role(const Params& p, const Shared&
         // both CTAs' bytes of a pair complete on the leader's barrier, which the leader arms
         if (CG == 1) ptx::mbar_arrive_expect_tx(full, Cfg::kStageBytes);
         else if (rank == 0) ptx::mbar_arrive_expect_tx(full, 2 * Cfg::kStageBytes);
-        const uint32_t bar = (CG == 1) ? full : ptx::mapa(full, sh.lead);
+        const uint32_t bar = (CG == 1) ? full : ptx::mapa(full, 0);
         // K-major operands: one box of (bk columns, rows); M- / N-major: 64-wide boxes of bk rows
-        if (CG == 2 && p.mc) {
-          // this CTA's half of its A rows, multicast to the same rank in the other pair
-          const uint32_t crank = sh.lead + rank;
-          const uint16_t mask = static_cast<uint16_t>((1u << crank) | (1u << (crank ^ 2u)));
-          const uint32_t hdst = adst + sh.pair * (64 * kRowBytes);
-          const int32_t hrow = row0 + 64 * static_cast<int32_t>(sh.pair);
-          if (!p.a_mn_major) ptx::tma_load_3d_pair_mc(hdst, mA, bar, k0, hrow, tc.a_batch, mask);
-          else ptx::tma_load_3d_pair_mc(hdst, mA, bar, hrow, k0, tc.a_batch, mask);
-        } else if (!p.a_mn_major) {
+        if (!p.a_mn_major) {
           tma_load<CG>(adst, mA, bar, k0, row0, tc.a_batch);
         } else {
 #pragma unroll
@@ -1325,10 +1340,9 @@ __global__ void __launch_bounds__(KernelCfg<BN, GATHER, CG>::kThreads, 1)
   sh.map_empty = sh.map_full + 8 * kMapSlots;
   const uint32_t drain_bar = sh.tempty + 16;  // MMAs in flight have finished
   TileSched ts;
-  // a unit is a CTA, a pair, or a cluster of two pairs
-  const int unit_ctas = (CG == 2 && p.mc) ? 4 : CG;
-  ts.unit = static_cast<int32_t>(blockIdx.x) / unit_ctas;
-  ts.units = static_cast<int32_t>(gridDim.x) / unit_ctas;
+  // a unit is a CTA or a CTA pair
+  ts.unit = static_cast<int32_t>(blockIdx.x) / CG;
+  ts.units = static_cast<int32_t>(gridDim.x) / CG;
   ts.dyn = (p.flags & FLAG_DYNAMIC_SCHED) != 0 && p.status != nullptr;
   ts.counter = p.status + 4;
   ts.full = drain_bar + 8;
@@ -1340,19 +1354,13 @@ __global__ void __launch_bounds__(KernelCfg<BN, GATHER, CG>::kThreads, 1)
   sh.idx = idx_s;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // rank within the pair; a two-pair cluster has pairs {0, 1} and {2, 3}
-  const uint32_t crank = (CG == 2) ? ptx::cluster_ctarank() : 0u;
-  const uint32_t rank = crank & 1u;
-  sh.pair = crank >> 1;
-  sh.lead = crank & ~1u;
-  sh.pair_mask = static_cast<uint16_t>(3u << sh.lead);
-  sh.all_mask = static_cast<uint16_t>((CG == 2 && p.mc) ? 0xF : 0x3);
+  // rank within the pair (rank 0 leads: it issues the MMAs of the pair)
+  const uint32_t rank = (CG == 2) ? ptx::cluster_ctarank() : 0u;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       ptx::mbar_init(sh.full + 8 * s, GATHER ? 1 + kGatherWarps * 32 : 1);
-      // a stage is free once every pair that reads the multicast A half has consumed it
-      ptx::mbar_init(sh.empty + 8 * s, (CG == 2 && p.mc) ? 2 : 1);
+      ptx::mbar_init(sh.empty + 8 * s, 1);
     }
     for (int b = 0; b < 2; ++b) {
       ptx::mbar_init(sh.tfull + 8 * b, 1);
@@ -1464,7 +1472,7 @@ __global__ void __launch_bounds__(KernelCfg<BN, GATHER, CG>::kThreads, 1)
   if (warp == Cfg::kMmaWarp && rank == 0) {
     if (ptx::elect_one()) {
       if (CG == 1) ptx::mma_commit(drain_bar);
-      else ptx::mma_commit_pair(drain_bar, static_cast<uint16_t>(1u << sh.lead));
+      else ptx::mma_commit_pair(drain_bar, 0x1);
     }
     __syncwarp();
     wait_phase<CG == 2>(drain_bar, 0, p, sh, 6, -1);
@@ -1485,14 +1493,18 @@ __global__ void __launch_bounds__(KernelCfg<BN, GATHER, CG>::kThreads, 1)
       atomicExch(p.status + 5, 0);
     }
   }
-  // split last wave: the last unit to finish advances the launch epoch, so that
-  // no later launch takes this one's flags for its own (every unit has read the
-  // epoch by then: it is read before any unit counts itself finished)
+  // split last wave: every ticket is reset by the warp that takes its last count.
+  // After an abort some may be left counting, so the last unit to finish clears
+  // them whenever a device error is on record (every unit has taken its tickets
+  // before it counts itself finished).
   if (p.tail_tiles > 0 && rank == 0 && threadIdx.x == 0) {
     __threadfence();
     if (atomicAdd(p.status + 7, 1) == ts.units - 1) {
       atomicExch(p.status + 7, 0);
-      atomicAdd(p.status + 6, 1);
+      if (atomicAdd(p.status, 0) != 0) {
+        const int32_t n = p.tail_tiles * CG * Cfg::kEpiWarps;
+        for (int32_t i = 0; i < n; ++i) atomicExch(p.tail_tickets + i, 0);
+      }
     }
   }
   if (warp == Cfg::kMmaWarp) {

@@ -13,7 +13,7 @@ struct LaunchShape {
   int grid;
   int threads;
   size_t smem;
-  int cluster;  // CTAs per cluster: 1, 2 (a CTA pair) or 4 (two pairs)
+  int cluster;  // CTAs per cluster: 1, or 2 (a CTA pair)
 };
 
 template <int BN, bool GATHER, int CG>

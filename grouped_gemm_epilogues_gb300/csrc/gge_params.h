@@ -23,10 +23,9 @@ enum : int32_t {
   FLAG_TEST_DROP_ACC_FULL = 2, // the MMA warp never signals "accumulator full" (timeout test)
   FLAG_DYNAMIC_SCHED = 4,      // tiles claimed from an atomic counter instead of a fixed stride
   FLAG_DIRECT_STORES = 8,      // epilogue stores straight from registers (no staging buffers)
-  FLAG_PAIR_CLUSTER = 16,      // two CTA pairs per cluster share A by TMA multicast
   FLAG_NO_SPLIT = 32,          // never split the last wave along K
-  FLAG_TEST_DROP_TAIL_FLAG = 64,  // test hook: split-tail writers never publish, so the
-                                  // owners' bounded waits run out (GGE_ERR_TIMEOUT)
+  FLAG_RASTER_N = 128,         // raster bands of n-tiles (n varies fastest in a band)
+  FLAG_RESERVED = 16 | 64,     // reserved bits: a call that sets one is rejected
 };
 
 struct Params {
@@ -43,9 +42,9 @@ struct Params {
   // split last wave (plain problems; see plan_tail_split): items >= full_tiles
   // are slices; tail_tiles == 0 disables it
   int32_t full_tiles, tail_tiles, tail_splits;
-  int32_t* tail_flags;  // workspace: per slice but the last, CTA, epilogue warp and lane: the
-                        // launch epoch + 1 once that lane's partial row is written
-  float* partials;      // workspace: per slice but the last and CTA, 128 x BN fp32 accumulators
+  int32_t* tail_tickets;  // workspace: per tail tile, CTA and epilogue warp, the number of
+                          // slices whose partial rows that warp has written (0 between launches)
+  float* partials;        // workspace: per tail tile, slice and CTA, 128 x BN fp32 accumulators
   FastDivmod tiles_n_div;  // varlen: local tile -> (m-tile, n-tile)
   int32_t tiles_n;
 
@@ -90,14 +89,11 @@ struct Params {
   int32_t f8;          // operands are 8-bit (kind::f8f6f4)
   int32_t a_mn_major;  // A staged M-major (16-bit operands only)
   int32_t b_mn_major;  // B staged N-major (16-bit operands only)
-  int32_t mc;          // clusters of two CTA pairs: pair q of a cluster takes n-tile 2 nb + q
-                       // of the scheduled (m, nb), and each CTA loads half of its A rows
-                       // and multicasts them to the CTA of the same rank in the other pair
 
   // control
   int32_t* status;       // workspace: [0] code, [1] where, [2] tile, [3] detail,
                          //            [4] tile claim counter, [5] finished CTAs (pairs),
-                         //            [6] split-tail launch epoch, [7] its finished units
+                         //            [7] finished units of a split launch
   int32_t* tile_counts;  // debug visit counters
   int32_t flags;
   uint64_t timeout_ns;

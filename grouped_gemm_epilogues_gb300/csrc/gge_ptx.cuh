@@ -337,19 +337,6 @@ __device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap
       : "memory");
 }
 
-// The pair load, multicast to the CTAs of `cta_mask` (same shared-memory offset
-// in each); every destination's bytes complete on its own pair leader's barrier.
-__device__ __forceinline__ void tma_load_3d_pair_mc(uint32_t dst, const CUtensorMap* m,
-                                                    uint32_t cluster_bar, int32_t c0, int32_t c1,
-                                                    int32_t c2, uint16_t cta_mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
-      ".multicast::cluster [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(m)), "r"(cluster_bar), "r"(c0), "r"(c1), "r"(c2),
-      "h"(cta_mask)
-      : "memory");
-}
-
 __device__ __forceinline__ void tmem_alloc_pair(uint32_t dst_smem, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
                "r"(ncols)

@@ -10,7 +10,8 @@
 // The plain schedule maps a linear tile index to (batch, m-tile, n-tile):
 // batches outermost, then bands of `band` m-tiles; inside a band the m-tile
 // varies fastest, so CTAs that run at the same time share B tiles and a
-// band's A rows, which keeps the working set of one wave inside L2.
+// band's A rows, which keeps the working set of one wave inside L2.  With
+// `along_n` the roles swap: bands of n-tiles, the n-tile varying fastest.
 // This plays the role of the pages' raster order / max_swizzle_size
 // (quack/dense_gemm_sm90.py, GemmSm90 tile scheduler arguments).
 #pragma once
@@ -63,43 +64,70 @@ struct FastDivmod {
 
 struct PlainSchedule {
   int32_t tiles_m, tiles_n, batches;
-  int32_t band;          // m-tiles per raster band
-  int32_t full_bands;    // tiles_m / band
+  int32_t band;          // tiles of the banded dimension per raster band
+  int32_t along_n;       // 1: bands of n-tiles (n varies fastest); 0: bands of m-tiles
+  int32_t full_bands;    // banded tiles / band
   int32_t num_tiles;     // tiles_m * tiles_n * batches
   FastDivmod per_batch;  // tiles_m * tiles_n
-  FastDivmod band_tiles; // band * tiles_n
+  FastDivmod band_tiles; // band * (tiles of the other dimension)
   FastDivmod band_rows;  // band
-  FastDivmod tail_rows;  // tiles_m % band (1 when the bands divide evenly)
+  FastDivmod tail_rows;  // banded tiles % band (1 when the bands divide evenly)
 
   static inline PlainSchedule create(int32_t tiles_m, int32_t tiles_n, int32_t batches,
-                                     int32_t band) {
+                                     int32_t band, bool along_n = false) {
     PlainSchedule s;
+    const int32_t banded = along_n ? tiles_n : tiles_m;
+    const int32_t other = along_n ? tiles_m : tiles_n;
     if (band < 1) band = 1;
-    if (band > tiles_m) band = tiles_m > 0 ? tiles_m : 1;
+    if (band > banded) band = banded > 0 ? banded : 1;
     s.tiles_m = tiles_m;
     s.tiles_n = tiles_n;
     s.batches = batches;
     s.band = band;
-    s.full_bands = tiles_m / band;
+    s.along_n = along_n ? 1 : 0;
+    s.full_bands = banded / band;
     s.num_tiles = tiles_m * tiles_n * batches;
     s.per_batch = FastDivmod::create(tiles_m * tiles_n > 0 ? tiles_m * tiles_n : 1);
-    s.band_tiles = FastDivmod::create(band * (tiles_n > 0 ? tiles_n : 1));
+    s.band_tiles = FastDivmod::create(band * (other > 0 ? other : 1));
     s.band_rows = FastDivmod::create(band);
-    const int32_t tail = tiles_m % band;
+    const int32_t tail = banded % band;
     s.tail_rows = FastDivmod::create(tail > 0 ? tail : 1);
     return s;
   }
 
   // t in [0, num_tiles)  ->  (batch, m-tile, n-tile)
   GGE_HD void map(int32_t t, int32_t& l, int32_t& mb, int32_t& nb) const {
-    int32_t r, b, w, i;
+    int32_t r, b, w, i, o;
     per_batch.divmod(t, l, r);
     band_tiles.divmod(r, b, w);
     const FastDivmod& rows = (b < full_bands) ? band_rows : tail_rows;
-    rows.divmod(w, nb, i);
-    mb = b * band + i;
+    rows.divmod(w, o, i);
+    if (along_n) {
+      nb = b * band + i;
+      mb = o;
+    } else {
+      mb = b * band + i;
+      nb = o;
+    }
   }
 };
+
+// Raster band width that keeps one wave's operand footprint smallest: a wave
+// of `units` tiles spread over `band` rows of tile_m and units / band columns
+// of tile_n reads band * tile_m + (units / band) * tile_n rows of K, least at
+// band = sqrt(units * tile_n / tile_m) (m-tiles per band; along N the ratio
+// inverts).  At least 1, at most 32.
+inline int32_t auto_band(int32_t units, int32_t tile_m, int32_t tile_n, bool along_n) {
+  if (units < 1 || tile_m < 1 || tile_n < 1) return 8;
+  const double ratio = along_n ? static_cast<double>(tile_m) / tile_n
+                               : static_cast<double>(tile_n) / tile_m;
+  double b = 1.0;
+  while ((b + 1.0) * (b + 1.0) <= units * ratio) b += 1.0;
+  // b = floor(sqrt(units * ratio)); take b + 1 when it is nearer
+  const double x = units * ratio;
+  if ((b + 1.0) * (b + 1.0) - x < x - b * b) b += 1.0;
+  return static_cast<int32_t>(b < 1.0 ? 1.0 : (b > 32.0 ? 32.0 : b));
+}
 
 // Split of the last, partly filled wave along K.  T tiles run on U units (CTAs
 // or CTA pairs) of a persistent grid: W = T / U full waves, then R = T - W U

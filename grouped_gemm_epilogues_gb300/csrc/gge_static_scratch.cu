@@ -27,32 +27,33 @@ constexpr size_t kStaticScratchBytes = 1024;
 
 static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
 
-struct DeviceScratch {
-  std::once_flag once;
-  void* ptr = nullptr;
-  cudaError_t err = cudaSuccess;
-};
+// The array's device address per device, filled in by the first successful
+// lookup on that device.  A failed lookup is not cached: the next call tries
+// again (a call made during stream capture, or after a sticky error, fails
+// without spoiling later calls).
+std::mutex g_scratch_mu;
+void* g_scratch_ptr[64] = {};
 
-DeviceScratch g_device_scratch[64];
-
-// Device address of the scratch array on the current device (set up once).
+// Device address of the scratch array on the current device.
 void* scratch_address(gge_status* status) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+    cudaGetLastError();
     *status = GGE_ERR_CUDA;
     return nullptr;
   }
-  DeviceScratch& d = g_device_scratch[dev];
-  std::call_once(d.once, [&d] {
+  std::lock_guard<std::mutex> g(g_scratch_mu);
+  if (g_scratch_ptr[dev] == nullptr) {
     void* p = nullptr;
-    d.err = cudaGetSymbolAddress(&p, g_static_scratch);
-    d.ptr = p;
-  });
-  if (d.err != cudaSuccess || d.ptr == nullptr) {
-    *status = GGE_ERR_CUDA;
-    return nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_static_scratch);
+    if (e != cudaSuccess || p == nullptr) {
+      cudaGetLastError();  // clear the error so that the caller's next CUDA call is not blamed
+      *status = GGE_ERR_CUDA;
+      return nullptr;
+    }
+    g_scratch_ptr[dev] = p;
   }
-  return d.ptr;
+  return g_scratch_ptr[dev];
 }
 
 }  // namespace
@@ -67,8 +68,22 @@ extern "C" gge_status gge_gemm_act_static_scratch(const gge_gemm_args* args,
   gge_status status = GGE_OK;
   void* scratch = scratch_address(&status);
   if (scratch == nullptr) return status;
-  // the area keeps the previous call's contents: the status words must start at zero
+  // The area keeps the previous call's contents.  The scheduler counters after
+  // the first 16 bytes must start at zero; the error record in those 16 bytes
+  // is kept until gge_read_static_scratch_status reads and clears it, so that an
+  // error is not lost to the next call.  (A __device__ array starts zeroed.)
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  if (cudaMemsetAsync(scratch, 0, need, st) != cudaSuccess) return GGE_ERR_CUDA;
+  if (cudaMemsetAsync(static_cast<unsigned char*>(scratch) + 16, 0, need - 16, st) != cudaSuccess)
+    return GGE_ERR_CUDA;
   return gge_gemm_act(args, scratch, need, stream);
+}
+
+// The device status that calls of gge_gemm_act_static_scratch on the current
+// device recorded in the library's scratch area (the same words
+// gge_read_device_status reads from a caller's workspace).
+extern "C" gge_status gge_read_static_scratch_status(gge_stream_t stream, int32_t* detail) {
+  gge_status status = GGE_OK;
+  void* scratch = scratch_address(&status);
+  if (scratch == nullptr) return status;
+  return gge_read_device_status(scratch, stream, detail);
 }

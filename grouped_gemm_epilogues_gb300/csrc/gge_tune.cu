@@ -5,7 +5,9 @@
 //
 // The candidates are the shapes the kernels have: one CTA per 128 x 128 or
 // 128 x 256 tile, or a CTA pair per 256 x {256, 224, 192, 160} tile, times the
-// raster band of plain problems, times staged or direct epilogue stores.  The pages' cooperative / ping-pong choice
+// raster of plain problems (bands of m-tiles of the automatic width or 8, or
+// bands of n-tiles: the pages' raster_order / max_swizzle_size), times staged
+// or direct epilogue stores.  The pages' cooperative / ping-pong choice
 // has no counterpart (the accumulator is double-buffered in TMEM instead), and
 // their cluster shapes correspond to the one-CTA / CTA-pair choice.
 #include <cuda_runtime.h>
@@ -21,7 +23,7 @@
 
 namespace {
 
-constexpr int kMaxCandidates = 32;
+constexpr int kMaxCandidates = 48;
 
 bool plain_op(int32_t op) { return op == GGE_OP_GEMM || op == GGE_OP_DACT; }
 bool gather_op(int32_t op) { return op == GGE_OP_GATHER_A || op == GGE_OP_GATHER_K; }
@@ -34,19 +36,22 @@ int32_t enumerate(const gge_gemm_args* args, int32_t op, int32_t num_groups, gge
   if (args->config != nullptr) base = *args->config;
   struct Shape { int cg, tile_n; };
   static const Shape kShapes[] = {{2, 256}, {2, 224}, {2, 192}, {2, 160}, {1, 256}, {1, 128}};
-  static const int kBands[] = {0, 8};
-  const int n_bands = plain_op(op) ? 2 : 1;
+  struct Raster { int band; bool along_n; };
+  static const Raster kRasters[] = {{0, false}, {8, false}, {0, true}};
+  const int n_rasters = plain_op(op) ? 3 : 1;
   int32_t n = 0;
   for (const Shape& sh : kShapes) {
     if (sh.cg == 2 && gather_op(op)) continue;
-    for (int b = 0; b < n_bands; ++b) {
+    for (int b = 0; b < n_rasters; ++b) {
       for (int direct = 0; direct < 2; ++direct) {
         gge_config c = base;
         c.cta_group = sh.cg;
         c.tile_n = sh.tile_n;
-        c.raster_band = kBands[b];
-        c.flags = direct ? (base.flags | gge::FLAG_DIRECT_STORES)
-                         : (base.flags & ~gge::FLAG_DIRECT_STORES);
+        c.raster_band = kRasters[b].band;
+        int32_t f = direct ? (base.flags | gge::FLAG_DIRECT_STORES)
+                           : (base.flags & ~gge::FLAG_DIRECT_STORES);
+        if (n_rasters > 1) f = kRasters[b].along_n ? (f | gge::FLAG_RASTER_N) : (f & ~gge::FLAG_RASTER_N);
+        c.flags = f;
         gge_gemm_args a = *args;
         a.config = &c;
         if (gge::validate_op(&a, op, num_groups) != GGE_OK) continue;

@@ -16,7 +16,8 @@
  * Conventions for every entry point:
  *   - All tensor pointers are DEVICE pointers owned by the caller.  Nothing is
  *     allocated, freed or synchronised by the library (except
- *     gge_read_device_status, which synchronises the given stream).
+ *     gge_read_device_status and gge_read_static_scratch_status, which
+ *     synchronise the given stream).
  *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default).
  *     Kernels are launched with programmatic stream serialization: a launch may
  *     begin its setup (shared memory, TMEM) while the previous kernel in the
@@ -90,7 +91,9 @@ typedef struct gge_config {
                              one CTA, 256, 224, 192 or 160 on a CTA pair (the
                              narrower pair tiles need a K-major B)                 */
   int32_t num_ctas;       /* 0 = one persistent CTA per SM                         */
-  int32_t raster_band;    /* 0 = auto; m-tiles per raster band (plain problems)    */
+  int32_t raster_band;    /* 0 = auto; tiles per raster band (plain problems): auto
+                             takes the width that keeps a wave's A and B rows
+                             fewest, sqrt(units * tile_n / tile_m) m-tiles     */
   int32_t stages;         /* 0 = as many as shared memory holds                    */
   int32_t flags;          /* bit 0: count tile visits into tile_counts;
                              bit 1: test hook -- the MMA warp never signals a
@@ -103,23 +106,24 @@ typedef struct gge_config {
                              own output row instead of staging 32 x 32 chunks in
                              shared memory (frees 16-32 KiB: one more pipeline
                              stage on a CTA pair; best when K is long);
-                             bit 4: clusters of two CTA pairs on adjacent n-tiles
-                             of a plain problem: each CTA loads half of its A rows
-                             and TMA-multicasts them to the other pair (a quarter
-                             less L2 traffic; needs cta_group 2, the static
-                             schedule, no tile counts);
+                             bit 4: reserved (a call that sets it returns
+                             GGE_ERR_UNSUPPORTED);
                              bit 5: never split the last wave.  By default a
                              plain problem whose last wave of tiles is at most
                              half full cuts those tiles into 2-8 K-slices that
-                             otherwise idle CTAs compute; the tile's last slice
-                             adds the others' fp32 partial sums (kept in the
-                             workspace) before its epilogue.  Not with the
-                             dynamic scheduler, two-pair clusters or the gather
-                             and varlen forms; needs gge_workspace_size bytes;
-                             bit 6: test hook -- the split last wave's partial
-                             sums are never published, so the owning CTAs'
-                             bounded waits run out and the call reports
-                             GGE_ERR_TIMEOUT.                                     */
+                             otherwise idle CTAs compute.  Each slice leaves its
+                             fp32 partial sums in the workspace; whichever unit
+                             finishes a tile's slices last adds them, in slice
+                             order, and runs the epilogue.  No CTA waits for
+                             another, so the result does not depend on when the
+                             CTAs run.  Not with the dynamic scheduler or the
+                             gather and varlen forms; needs gge_workspace_size
+                             bytes;
+                             bit 6: reserved (a call that sets it returns
+                             GGE_ERR_UNSUPPORTED);
+                             bit 7: raster along N -- plain problems walk bands
+                             of raster_band n-tiles, the n-tile varying fastest
+                             (default: bands of m-tiles, the m-tile fastest).  */
   int32_t cta_group;      /* 0 = auto; 1 = one CTA per 128-row tile; 2 = a CTA pair
                              per 256-row tile (tcgen05 cta_group::2, 256-column
                              tiles, not with the gather forms)                     */
@@ -165,10 +169,12 @@ typedef struct gge_gemm_args {
  * entry point except gge_gemm_varlen_k and gge_gemm_gather_k (see
  * gge_workspace_size_varlen_k): 256 bytes of status words and scheduler
  * counters, plus, for plain problems, room to split the last, partly filled
- * wave of tiles along K (one 128 x 256 fp32 partial block and 1 KiB of flags
- * per SM, about 20 MiB on a 152-SM GPU; the split needs a 256-byte aligned
- * workspace).  Any workspace of at least 256 bytes works: with less room the
- * last wave runs unsplit.  The workspace is caller-owned, at least 16-byte
+ * wave of tiles along K (16 KiB of tickets, then one 128 x 256 fp32 partial
+ * block per SM: about 20 MiB on a 152-SM GPU; the split needs a 256-byte
+ * aligned workspace).  Any workspace of at least 256 bytes works: with less
+ * room the last wave runs unsplit.  Layout: bytes 0-255 status words, then
+ * the tickets, then the partial blocks (or, for varlen-K, the tensor-map
+ * slots), so one workspace serves every entry point in turn.  The workspace is caller-owned, at least 16-byte
  * aligned, must be zeroed once before first use, and is reusable across calls
  * on the same stream (not by calls running concurrently on other streams).
  * The arguments are not inspected (they may be NULL); the size depends on the
@@ -176,10 +182,11 @@ typedef struct gge_gemm_args {
 size_t gge_workspace_size(const gge_gemm_args* args, int32_t num_groups);
 
 /* Workspace bytes gge_gemm_varlen_k and gge_gemm_gather_k need on the current
- * device: the status words plus 4 KiB of tensor-map copies for each CTA a
+ * device: the status words and the ticket region plus 4 KiB of tensor-map copies for each CTA a
  * launch can have (one per SM: about 0.6 MiB on a 152-SM GPU).  The arguments
  * are not inspected (they may be NULL); returns 0 if the device cannot be
- * queried. */
+ * queried.  (The slots start after the 16 KiB ticket region, which these
+ * calls leave untouched.) */
 size_t gge_workspace_size_varlen_k(const gge_gemm_args* args, int32_t num_groups);
 
 /* D = alpha A B^T + beta C (PostAct must be NULL and act NONE).
@@ -275,12 +282,23 @@ gge_status gge_gemm_gather_a(const gge_gemm_args* args, const int32_t* a_idx,
  *     process exit.  It has no room for partial sums, so the last wave of tiles
  *     is never split along K on this path (see gge_workspace_size).
  *   - The first call on a device looks up that area's device address (on the
- *     current device); make that first call before any stream capture.
- *   - Each call clears the status words (an async memset on `stream`), then
- *     launches the same kernel as gge_gemm_act.  Nothing is allocated.
+ *     current device); make that first call before any stream capture.  A
+ *     failed lookup returns GGE_ERR_CUDA and is tried again by the next call.
+ *   - Each call clears the area's scheduler counters (an async memset on
+ *     `stream`), then launches the same kernel as gge_gemm_act.  Nothing is
+ *     allocated.
+ *   - Device errors (a wait past its limit, GGE_ERR_TIMEOUT) are recorded in
+ *     the area and kept until gge_read_static_scratch_status reads them.
  *   - All calls on a device share the one area: calls that overlap on the GPU
  *     (different streams without ordering) race on it. */
 gge_status gge_gemm_act_static_scratch(const gge_gemm_args* args, gge_stream_t stream);
+
+/* gge_read_device_status for the library's own scratch area: synchronises
+ * `stream`, returns the device status that gge_gemm_act_static_scratch calls
+ * on the current device recorded since it was last read (GGE_OK or
+ * GGE_ERR_TIMEOUT), and clears it.  `detail` (may be NULL) receives
+ * [where, tile].  No counterpart on the pages. */
+gge_status gge_read_static_scratch_status(gge_stream_t stream, int32_t* detail);
 
 /* Synchronises `stream`, returns the device status recorded in `workspace`
  * since it was last cleared (GGE_OK, GGE_ERR_TIMEOUT or GGE_ERR_INDEX_RANGE)
@@ -301,10 +319,12 @@ int32_t gge_fastdivmod_div(int32_t divisor, int32_t n);
 
 /* The plain persistent schedule: tile index t -> (batch, m-tile, n-tile) for a
  * grid of tiles_m x tiles_n tiles per batch and `batches` batches, with
- * `band` m-tiles per raster band.  Writes `count` triples into out[3*count]
- * for t = 0 .. count-1.  Returns the number of tiles of the problem. */
+ * `band` m-tiles per raster band (n-tiles when along_n != 0, config flag
+ * bit 7).  Writes `count` triples into out[3*count] for t = 0 .. count-1.
+ * Returns the number of tiles of the problem.  Page: quack/dense_gemm_sm90.py,
+ * the tile scheduler's raster_order and max_swizzle_size. */
 int32_t gge_schedule_map(int32_t tiles_m, int32_t tiles_n, int32_t batches, int32_t band,
-                         int32_t count, int32_t* out);
+                         int32_t along_n, int32_t count, int32_t* out);
 
 /* The launch plan the library would use for `args` (tile and pipeline
  * shape).  form: GGE_FORM_DEFAULT (plain, or varlen-M when num_groups > 0),
@@ -320,6 +340,7 @@ typedef struct gge_plan_info {
   int32_t smem_bytes;
   int32_t raster_band;
   int32_t cta_group;  /* 1 or 2 CTAs per tile */
+  int32_t raster_along_n; /* 1: bands of n-tiles (config flag bit 7) */
   int32_t tail_tiles; /* tiles of the last, partly filled wave that are split along K
                          (plain problems; 0: none).  Reported only when the unit
                          count is known here, i.e. config->num_ctas is set. */
@@ -333,8 +354,9 @@ gge_status gge_plan(const gge_gemm_args* args, int32_t num_groups, int32_t form,
  * get_all_configs: a space of tile shapes, cooperative / ping-pong
  * warpgroups, 1x2 / 2x1 clusters and swap_ab to search by timing).  Here the space is the launch shapes this library
  * has: one CTA per 128 x 128 or 128 x 256 tile, or a CTA pair per 256 x 256,
- * 224, 192 or 160 tile (not with the gather forms), times the raster band of
- * plain problems (auto or 8), times staged or direct epilogue stores.  The pages' swap_ab is not in the space: it needs M-major
+ * 224, 192 or 160 tile (not with the gather forms), times the raster of
+ * plain problems (bands of m-tiles of the automatic width or 8, or bands of
+ * n-tiles: flag bit 7), times staged or direct epilogue stores.  The pages' swap_ab is not in the space: it needs M-major
  * output stores, which the epilogue does not have. */
 
 /* Which entry point a tuning call times. */

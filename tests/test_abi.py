@@ -65,11 +65,42 @@ def test_fastdivmod_host_division(L):
                                             (1, 1, 1, 1), (33, 7, 3, 5)])
 def test_schedule_covers_every_tile_once(L, tm, tn, lb, band):
     n = tm * tn * lb
-    out = (ctypes.c_int32 * (3 * n))()
-    assert L.gge_schedule_map(tm, tn, lb, band, n, out) == n
-    got = [tuple(out[3 * i:3 * i + 3]) for i in range(n)]
-    assert len(set(got)) == n
-    assert set(got) == ot.plain_tiles(tm * 128, tn * 256, lb, 128, 256)
+    for along_n in (0, 1):
+        out = (ctypes.c_int32 * (3 * n))()
+        assert L.gge_schedule_map(tm, tn, lb, band, along_n, n, out) == n
+        got = [tuple(out[3 * i:3 * i + 3]) for i in range(n)]
+        assert len(set(got)) == n
+        assert set(got) == ot.plain_tiles(tm * 128, tn * 256, lb, 128, 256)
+
+
+def test_schedule_raster_order(L):
+    """Bands of m-tiles walk m fastest; bands of n-tiles (flag bit 7) walk n fastest,
+    the band's width at a time."""
+    out = (ctypes.c_int32 * (3 * 12))()
+    L.gge_schedule_map(4, 3, 1, 2, 0, 12, out)
+    got = [tuple(out[3 * i:3 * i + 3]) for i in range(12)]
+    assert got[:6] == [(0, 0, 0), (0, 1, 0), (0, 0, 1), (0, 1, 1), (0, 0, 2), (0, 1, 2)]
+    L.gge_schedule_map(4, 3, 1, 2, 1, 12, out)
+    got = [tuple(out[3 * i:3 * i + 3]) for i in range(12)]
+    assert got[:8] == [(0, 0, 0), (0, 0, 1), (0, 1, 0), (0, 1, 1), (0, 2, 0), (0, 2, 1),
+                       (0, 3, 0), (0, 3, 1)]
+    # the last band of n-tiles is the one column left over
+    assert got[8:] == [(0, 0, 2), (0, 1, 2), (0, 2, 2), (0, 3, 2)]
+
+
+def test_auto_raster_band(L):
+    """The automatic band keeps a wave's operand rows fewest: sqrt(units * tile_n /
+    tile_m) m-tiles (76 pairs of 256 x 256 tiles: 9)."""
+    A = torch.zeros(8192, 8192, dtype=torch.bfloat16)
+    info = binding.gge_plan(A, A, D=A, config=binding.make_config(num_ctas=152, cta_group=2,
+                                                                  tile_n=256))
+    assert info["raster_band"] == 9 and info["raster_along_n"] == 0
+    info = binding.gge_plan(A, A, D=A, config=binding.make_config(num_ctas=152, cta_group=1,
+                                                                  tile_n=256))
+    assert info["raster_band"] == 17                    # 152 x 2
+    info = binding.gge_plan(A, A, D=A, config=binding.make_config(num_ctas=152, cta_group=1,
+                                                                  tile_n=256, flags=128))
+    assert info["raster_band"] == 9 and info["raster_along_n"] == 1   # 152 / 2 = 76
 
 
 def _args(M=256, N=256, K=256, dt=torch.bfloat16, out=torch.bfloat16, **kw):
@@ -226,7 +257,23 @@ def test_binding_flag_table_matches_header():
         text = f.read()
     bits = sorted(int(b) for b in re.findall(r"bit (\d+):", text))
     assert bits == list(range(len(bits)))
-    assert sorted(binding.FLAGS.values()) == [1 << b for b in bits]
+    reserved = sorted(int(b) for b in re.findall(r"bit (\d+): reserved", text))
+    assert sum(1 << b for b in reserved) == binding.RESERVED_FLAGS
+    assert sorted(binding.FLAGS.values()) == [1 << b for b in bits if b not in reserved]
+
+
+@pytest.mark.parametrize("flags", [16, 64, 16 | 8, 64 | 32])
+def test_reserved_flag_bits_are_rejected(L, flags):
+    """Bits 4 and 6 are reserved: planning or calling with one set is
+    GGE_ERR_UNSUPPORTED before anything is launched (no GPU needed)."""
+    A = torch.zeros(512, 512, dtype=torch.bfloat16)
+    D = torch.zeros(512, 512, dtype=torch.bfloat16)
+    cfg = binding.make_config(flags=flags, num_ctas=152)
+    args = binding.make_args(A, A, D=D, config=cfg)
+    info = binding.GgePlanInfo()
+    assert L.gge_plan(ctypes.byref(args), 0, 0, ctypes.byref(info)) == 2
+    assert L.gge_gemm(ctypes.byref(args), None, 0, None) == 2
+    assert binding.gge_tune_candidates("gemm", A, A, D=D, config=cfg) == []
 
 
 def test_workspace_size_covers_the_split(L):
@@ -277,8 +324,9 @@ def test_tune_candidates_follow_the_planner(L):
     c = binding.gge_tune_candidates("gemm", A, A, D=P, PostAct=P, act="gelu_tanh")
     shapes = {(x["cta_group"], x["tile_n"]) for x in c}
     assert shapes == {(2, 256), (2, 224), (2, 192), (2, 160), (1, 256), (1, 128)}
-    assert {x["raster_band"] for x in c} == {0, 8} and len(c) == 24
-    assert {x["flags"] for x in c} == {0, 8}          # staged or direct epilogue stores
+    assert {x["raster_band"] for x in c} == {0, 8} and len(c) == 36
+    # staged or direct epilogue stores, bands of m-tiles or (bit 7) of n-tiles
+    assert {x["flags"] for x in c} == {0, 8, 128, 136}
     # N-major B: the pair keeps 256-wide tiles only
     Bn = torch.zeros(4096, 4096, dtype=torch.bfloat16).t()
     c = binding.gge_tune_candidates("gemm", A, Bn, D=P)
@@ -291,7 +339,7 @@ def test_tune_candidates_follow_the_planner(L):
     assert {(x["cta_group"], x["tile_n"], x["raster_band"]) for x in c} == {(1, 256, 0), (1, 128, 0)}
     # a caller's other flags are kept in every candidate
     c = binding.gge_tune_candidates("gemm", A, A, D=P, config=binding.make_config(flags=4))
-    assert {x["flags"] for x in c} == {4, 12}
+    assert {x["flags"] for x in c} == {4, 12, 132, 140}
     # nothing valid: no candidates
     assert binding.gge_tune_candidates("gemm", A, A, D=torch.zeros(4096, 4000,
                                                                    dtype=torch.bfloat16)) == []

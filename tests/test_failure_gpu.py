@@ -33,35 +33,3 @@ def test_wait_timeout_reported_and_context_survives(cta_group):
     out2 = _outputs(w, 256, 256, 1)
     _run_plain(w, t, out2, config=binding.make_config(cta_group=cta_group, tile_n=256))
     _check_plain(w, t, out2)
-
-
-FLAG_TEST_DROP_TAIL_FLAG = 64
-WHERE_TAIL_FLAG_WAIT = 11
-
-
-@pytest.mark.parametrize("cta_group", [1, 2])
-def test_split_tail_wait_timeout_reported_and_context_survives(cta_group):
-    """The split last wave's owners wait for partial sums that (by the test hook)
-    are never published: their bounded waits run out, the call reports
-    GGE_ERR_TIMEOUT at an owner's work item, and the next call is right."""
-    from oracle import gemm as og
-    from helpers import FMT_NAME, check, dec
-    gen = torch.Generator().manual_seed(21)
-    A = ((torch.rand(512, 1024, generator=gen) * 2 - 1).bfloat16()).to(DEV)
-    B = ((torch.rand(1024, 1024, generator=gen) * 2 - 1).bfloat16()).to(DEV)
-    D = torch.empty(512, 1024, dtype=torch.bfloat16, device=DEV)
-    base = dict(num_ctas=12, cta_group=cta_group, tile_n=256)
-    info = binding.gge_plan(A.cpu(), B.cpu(), D=D.cpu(), config=binding.make_config(**base))
-    assert info["tail_tiles"] > 0 and info["tail_splits"] == 2
-    full = info["num_tiles"] - info["tail_tiles"]
-    hook = binding.make_config(flags=FLAG_TEST_DROP_TAIL_FLAG, timeout_ns=20_000_000, **base)
-    binding.gge_gemm(A, B, D, beta=0.0, config=hook)
-    torch.cuda.synchronize()
-    status, where, item = binding.gge_read_device_status()
-    assert status == "GGE_ERR_TIMEOUT" and where == WHERE_TAIL_FLAG_WAIT and item >= full
-    assert binding.gge_read_device_status()[0] == "GGE_OK"
-    binding.gge_gemm(A, B, D, beta=0.0, config=binding.make_config(**base))
-    torch.cuda.synchronize()
-    assert binding.gge_read_device_status()[0] == "GGE_OK"
-    r = og.gemm(dec(A), dec(B), beta=0.0, d_fmt=FMT_NAME["bf16"])
-    check(D, r["D"], r["bound"], FMT_NAME["bf16"], what="after the timeout")

@@ -184,33 +184,24 @@ def test_cta_group_variants(case, cta_group):
     _check_plain(w, t, out)
 
 
-def _sample_rows(M, BM=128, n=96, seed=0):
-    rng = np.random.default_rng(seed)
-    rows = set(range(0, min(M, BM)))               # the first tile
-    rows |= set(range(max(0, M - 40), M))          # the tail
-    rows |= set(int(x) for x in rng.integers(0, M, n))
-    return np.array(sorted(rows))
-
-
 FULL = ["gemm_256_bf16", "gemm_act_4096_bf16_gelu", "gemm_8192_f16_relu",
         "bgemm_2048x2048x4096x16_f16_relu", "gemm_8192_fp8", "gemm_act_8192_bf16_gelu"]
 
 
 @pytest.mark.slow
 @pytest.mark.parametrize("name", FULL)
-def test_full_size_sampled(name):
+def test_full_size_every_element(name):
+    """The named workloads at full size, in the planner's default launch shape
+    (the split last wave included where the plan has one), every output element
+    against the oracle (computed in blocks of rows)."""
+    from fullsize import full_plain
     w = wl.WORKLOADS[name]
     t = wl.make(w)
     out = _outputs(w, w.M, w.N, w.L)
     _run_plain(w, t, out)
-    rows = None if w.M * w.N * w.K * w.L <= 2 ** 27 else _sample_rows(w.M)
-    _check_plain(w, t, out, rows)
-    # properties over every element: finite, and PostAct consistent with its activation
-    for k in ("D", "P"):
-        if k in out:
-            assert torch.isfinite(out[k].float()).all()
-    if "P" in out and w.act == "relu":
-        assert (out["P"].float() >= 0).all()
+    worst = full_plain(w, t, out)
+    print(f"{name}: worst error / tolerance {worst}")
+    assert worst and max(worst.values()) <= 1.0
 
 
 @pytest.mark.parametrize("M,N,K,L,b_major,cg", [
@@ -238,41 +229,3 @@ def test_direct_stores_mixed_output_dtypes(d_dtype, p_dtype, act):
     out = _outputs(w, 300, 392, 1)
     _run_plain(w, t, out, config=binding.make_config(flags=8))
     _check_plain(w, t, out)
-
-
-@pytest.mark.parametrize("name,M,N,K,L,kw", [
-    ("gemm_act_4096_bf16_gelu", 520, 792, 328, 1, {}),                  # odd n-tile count, tails
-    ("gemm_act_4096_bf16_gelu", 512, 512, 256, 2, {"act": "relu"}),     # batched
-    ("gemm_8192_f16_relu", 384, 1024, 200, 1, {}),                      # N-major B
-    ("gemm_8192_fp8", 512, 768, 512, 1, {}),
-], ids=lambda v: str(v))
-@pytest.mark.parametrize("tile_n", [256, 224])
-def test_two_pair_clusters(name, M, N, K, L, kw, tile_n):
-    # flags 16: clusters of two CTA pairs sharing A by TMA multicast
-    w = wl.small(name, M, N, K, L, **kw)
-    if w.b_major == "n" and tile_n != 256:
-        pytest.skip("N-major B keeps 256-wide pair tiles")
-    t = wl.make(w)
-    out = _outputs(w, M, N, L, pad=8, fill=5.0)
-    _run_plain(w, t, out, config=binding.make_config(flags=16, cta_group=2, tile_n=tile_n))
-    _check_plain(w, t, out)
-    for k in ("D_full", "P_full"):
-        if k in out:
-            assert (out[k][:, :, N:].float() == 5.0).all()
-
-
-def test_two_pair_clusters_m_major_a():
-    w = wl.small("gemm_act_4096_bf16_gelu", 392, 520, 136, 1)
-    t = wl.make(w)
-    t["A"] = t["A"].transpose(1, 2).contiguous().transpose(1, 2)
-    out = _outputs(w, 392, 520, 1)
-    _run_plain(w, t, out, config=binding.make_config(flags=16))
-    _check_plain(w, t, out)
-
-
-def test_two_pair_clusters_rejected_where_unsupported():
-    A = torch.randn(256, 256, device=DEV).bfloat16()
-    D = torch.empty(256, 256, dtype=torch.bfloat16, device=DEV)
-    for cfg in (binding.make_config(flags=16, cta_group=1), binding.make_config(flags=16 | 4)):
-        with pytest.raises(binding.GgeError):
-            binding.gge_gemm(A, A, D, config=cfg)

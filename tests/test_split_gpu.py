@@ -1,8 +1,9 @@
 """Split last wave: tiles of the last, partly filled wave are cut into K-slices
-that different CTAs (pairs) compute; the last slice's epilogue adds the others' fp32
-partial sums before alpha, beta * C and the activation.  Every case forces the
+that different CTAs (pairs) compute; each slice leaves its fp32 partial sums in
+the workspace, and whichever unit finishes a tile's slices last adds them (in
+slice order) before alpha, beta * C and the activation.  Most cases force the
 split with a small CTA count (so that it does not depend on the GPU's size),
-checks through gge_plan that it is on, and compares with the oracle."""
+check through gge_plan that it is on, and compare with the oracle."""
 
 import pytest
 import torch
@@ -117,8 +118,9 @@ def test_split_dact_f16_fp8_and_batched():
 
 
 def test_split_repeated_launches_and_tile_counts():
-    """Back-to-back launches on one workspace (each launch's flags carry its own
-    epoch), with the outputs cleared in between; every tile is finished once."""
+    """Back-to-back launches on one workspace (each tile's tickets are back at zero
+    when its last slice is done), with the outputs cleared in between; every
+    tile is finished once."""
     gen = torch.Generator().manual_seed(9)
     A, B = _rand(gen, 768, 1536), _rand(gen, 1024, 1536)
     D = torch.empty(768, 1024, dtype=torch.bfloat16, device=DEV)
@@ -154,8 +156,63 @@ def test_split_needs_room_else_runs_unsplit():
 
 
 def test_workspace_size_has_room_for_the_split():
-    """On a GPU the reported size covers one 128 x 256 fp32 partial block and one
-    warp-flag set per SM after the 256 status bytes."""
+    """On a GPU the reported size covers the 256 status bytes, the 16 KiB ticket
+    region and one 128 x 256 fp32 partial block per SM."""
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     size = binding.load().gge_workspace_size(None, 0)
-    assert size >= 256 + sms * (128 * 256 * 4 + 8 * 32 * 4)
+    assert size >= 256 + 16384 + sms * 128 * 256 * 4
+
+
+def test_varlen_k_then_split_on_one_workspace():
+    """A varlen-K call writes tensor-map copies into the shared workspace; a split
+    plain call right after it on the same workspace must not take those bytes for
+    tickets or partial sums (the map slots start after the ticket region)."""
+    from grouped_gemm_epilogues_gb300 import workloads as wl
+    gen = torch.Generator().manual_seed(17)
+    wk = wl.small("varlen_k_g64_k32768_wgrad", 256, 256, 3000, k_groups=6, empty_groups=1)
+    tk = wl.make(wk)
+    Dk = torch.empty(6, 256, 256, dtype=torch.bfloat16, device=DEV)
+    A, B = _rand(gen, 512, 1024), _rand(gen, 1024, 1024)
+    D = torch.empty(512, 1024, dtype=torch.bfloat16, device=DEV)
+    cfg = binding.make_config(num_ctas=12, cta_group=2, tile_n=256)
+    _split_on(A, B, D, cfg, 2, 2)
+    r = og.gemm(dec(A), dec(B), beta=0.0, d_fmt=BF16)
+    for _ in range(3):
+        binding.gge_gemm_varlen_k(tk["A"].to(DEV), tk["B"].to(DEV), tk["cu_seqlens_k"].to(DEV),
+                                  D=Dk)
+        D.fill_(float("nan"))
+        binding.gge_gemm(A, B, D, beta=0.0, config=cfg)
+        torch.cuda.synchronize()
+        assert binding.gge_read_device_status()[0] == "GGE_OK"
+        check(D, r["D"], r["bound"], BF16, what="split after varlen-K")
+
+
+def test_split_while_another_stream_holds_the_sms():
+    """The split tail never waits for another CTA, so it is right (and reports no
+    timeout) whatever order its CTAs start in: here a stream of large matmuls on
+    another stream holds most SMs while the split GEMM's CTAs trickle in."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    gen = torch.Generator().manual_seed(23)
+    A, B = _rand(gen, 512, 4096), _rand(gen, 4096, 4096)
+    C = _rand(gen, 512, 4096)
+    D = torch.empty(512, 4096, dtype=torch.bfloat16, device=DEV)
+    P = torch.empty_like(D)
+    cfg = binding.make_config(cta_group=2, tile_n=256)
+    info = binding.gge_plan(A.cpu(), B.cpu(), D=D.cpu(),
+                            config=binding.make_config(cta_group=2, tile_n=256, num_ctas=sms))
+    assert info["tail_tiles"] > 0 and info["tail_splits"] >= 2, info
+    X = torch.randn(8192, 8192, device=DEV, dtype=torch.bfloat16)
+    other = torch.cuda.Stream()
+    r = og.gemm(dec(A), dec(B), dec(C), alpha=1.0, beta=0.5, act="silu", d_fmt=BF16, p_fmt=BF16)
+    for _ in range(3):
+        D.fill_(float("nan"))
+        P.fill_(float("nan"))
+        torch.cuda.synchronize()
+        with torch.cuda.stream(other):
+            for _ in range(8):
+                X = (X @ X) * (1.0 / 128)
+        binding.gge_gemm_act(A, B, P, "silu", D=D, C=C, alpha=1.0, beta=0.5, config=cfg)
+        torch.cuda.synchronize()
+        assert binding.gge_read_device_status()[0] == "GGE_OK"
+        check(D, r["D"], r["bound"], BF16, what="D")
+        check(P, r["P"], r["bound"], BF16, "silu", what="PostAct", x=r["v"])

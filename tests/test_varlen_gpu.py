@@ -166,18 +166,16 @@ def test_gather_index_out_of_range_is_reported():
 
 @pytest.mark.slow
 @pytest.mark.parametrize("gather", [True, False])
-def test_varlen_full_size_sampled(gather):
+def test_varlen_full_size_every_element(gather):
+    """The 64-group workload at full size, every output row of every group
+    against the oracle (group by group, in blocks of rows)."""
+    from fullsize import full_varlen
     w = wl.WORKLOADS["varlen_gather_g64_m32768_silu"]
     if not gather:
         w = wl.small(w.name, w.M, w.N, w.K, gather_rows=0)
     t = wl.make(w)
     out = _run(w, t, gather)
-    rng = np.random.default_rng(1)
-    cu = t["cu_seqlens_m"].numpy()
-    rows = set(int(x) for x in rng.integers(0, w.M, 120))
-    for g in range(len(cu) - 1):   # first and last row of every non-empty group
-        if cu[g + 1] > cu[g]:
-            rows |= {int(cu[g]), int(cu[g + 1]) - 1}
-    rows = np.array(sorted(rows))
-    _check(w, t, out, _oracle(w, t, gather, rows), rows)
     assert binding.gge_read_device_status()[0] == "GGE_OK"
+    worst = full_varlen(w, t, out, gather)
+    print(f"{w.name} gather={gather}: worst error / tolerance {worst}")
+    assert worst and max(worst.values()) <= 1.0
