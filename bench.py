@@ -258,7 +258,7 @@ PER_CONFIG = [("c1", "gemm_256_bf16"), ("c2", "gemm_act_4096_bf16_gelu"),
               ("c4", "varlen_gather_g64_m32768_silu"), ("c5", "gemm_8192_fp8")]
 
 
-def _prepare(w, dev, binding, tune):
+def _prepare(w, dev, binding, tune, fixed=None):
     """Rotating device input sets (their total above L2 where the problem allows),
     the launch configuration (autotuned unless tune is False) and the step."""
     base, probe = _device_sets(w, dev, 1)
@@ -276,6 +276,8 @@ def _prepare(w, dev, binding, tune):
                                         cu=s0.get("cu_seqlens_k", s0.get("cu_seqlens_m")),
                                         C=s0.get("C"), D=s0.get("D"), PostAct=s0.get("P"),
                                         act=w.act, alpha=w.alpha, beta=w.beta, reps=5)
+    if tuned is None and fixed:
+        tuned = dict(fixed)
     step = _step_fn(w, binding, binding.make_config(**tuned) if tuned else None)
     l2 = (f"{n_sets} rotating input sets of {per_set / 2**20:.0f} MiB (> L2)"
           if n_sets * per_set > L2_BYTES else
@@ -352,6 +354,18 @@ def _peak_for(w, peaks, src):
             f"{src} cuBLAS bf16 burst" + (" x2 (fp8/bf16 nominal ratio)" if is8 else ""))
 
 
+def _fixed_shape(args):
+    """A launch shape given on the command line (with --no-tune), or None."""
+    d = {k: v for k, v in (("cta_group", args.cta_group), ("tile_n", args.tile_n)) if v}
+    return d or None
+
+
+def _shape_note(tuned, args):
+    if tuned is None:
+        return {"source": "planner default"}
+    return dict(tuned, source="autotuned" if not args.no_tune else "command line")
+
+
 def measure_config(args, w, dev, binding, local, peaks, src):
     """One per-config line: autotuned shape, warm-up, then at least ~0.3 s of
     timed launches (at least --steps) with the clocks sampled meanwhile."""
@@ -381,8 +395,7 @@ def measure_config(args, w, dev, binding, local, peaks, src):
            "frac": round(tflops / peak, 4), "peak": peak, "peak_source": peak_src,
            "frac_of_nominal_dense_peak": round(tflops / NOMINAL_PEAK[w.ab_dtype], 4),
            "traffic": profiled_traffic(w.name), "l2": l2, "clocks": clocks,
-           "launch_shape": (dict(tuned, source="autotuned") if tuned else
-                            {"source": "planner default"})}
+           "launch_shape": _shape_note(tuned, args)}
     del sets
     torch.cuda.empty_cache()
     return out
@@ -399,7 +412,7 @@ def run_ours(args, w):
         dist.init_process_group("nccl", device_id=dev)
     binding.load()
 
-    base, sets, tuned, step, l2 = _prepare(w, dev, binding, not args.no_tune)
+    base, sets, tuned, step, l2 = _prepare(w, dev, binding, not args.no_tune, _fixed_shape(args))
     n_sets = len(sets)
     stream = torch.cuda.current_stream(dev)
 
@@ -454,8 +467,7 @@ def run_ours(args, w):
                    "l2": l2,
                    "parallelism": f"replicas{ws_n}" if ws_n > 1 else "single",
                    "launch": "eager" if args.eager else "cuda_graph",
-                   "launch_shape": (dict(tuned, source="autotuned") if tuned else
-                                    {"source": "planner default"})},
+                   "launch_shape": _shape_note(tuned, args)},
         "roofline": roofline,
         "e2e": e2e,
         "gpu_launches": args.steps,
@@ -669,6 +681,9 @@ def main():
                     help="use the planner's default launch shape instead of the autotuner's")
     ap.add_argument("--eager", action="store_true",
                     help="launch every timed step from Python instead of CUDA-graph replay")
+    ap.add_argument("--cta-group", type=int, default=0,
+                    help="with --no-tune: CTAs per tile (1, or 2 for a CTA pair)")
+    ap.add_argument("--tile-n", type=int, default=0, help="with --no-tune: tile width")
     ap.add_argument("--no-per-config", action="store_true",
                     help="skip the per-config lines (the other workloads of the metric)")
     args = ap.parse_args()

@@ -226,6 +226,7 @@ uint64_t mn_batch_stride_bytes(const gge_tensor& t, int es) {
 // ---- the kernel variants: (BN, gather, CTAs per tile)
 
 int variant_threads(int bn, bool gather, int cg) {
+  if (gather && cg == 2) return kernel_threads<256, true, 2>();
   if (gather) return bn == 128 ? kernel_threads<128, true, 1>() : kernel_threads<256, true, 1>();
   if (cg == 2) {
     switch (bn) {
@@ -266,6 +267,7 @@ int variant_units(int bn, bool gather, int cg, size_t smem, int cluster) {
 }
 
 int variant_units_uncached(int bn, bool gather, int cg, size_t smem, int cluster) {
+  if (gather && cg == 2) return max_active_units<256, true, 2>(smem, cluster);
   if (gather)
     return bn == 128 ? max_active_units<128, true, 1>(smem, 1) : max_active_units<256, true, 1>(smem, 1);
   if (cg == 2) {
@@ -280,6 +282,7 @@ int variant_units_uncached(int bn, bool gather, int cg, size_t smem, int cluster
 }
 
 cudaError_t variant_launch(const Plan& pl, cudaStream_t st) {
+  if (pl.gather && pl.cg == 2) return launch_gemm<256, true, 2>(pl.tmA, pl.tmB, pl.p, pl.shape, st);
   if (pl.gather)
     return pl.bn == 128 ? launch_gemm<128, true, 1>(pl.tmA, pl.tmB, pl.p, pl.shape, st)
                         : launch_gemm<256, true, 1>(pl.tmA, pl.tmB, pl.p, pl.shape, st);
@@ -441,7 +444,8 @@ gge_status make_plan(const gge_gemm_args* a, Form form, const int32_t* a_idx,
 
   // tile shape: 128 x BN on one CTA, or 256 x BN on a CTA pair
   int cg = cfg && cfg->cta_group ? cfg->cta_group : ((!gather && N > 128 && M >= 256) ? 2 : 1);
-  if (cg == 2 && gather) return GGE_ERR_UNSUPPORTED;
+  // gather-A runs on one CTA or a CTA pair (256 x 256 tiles); gather-K on one CTA
+  if (cg == 2 && gk) return GGE_ERR_UNSUPPORTED;
   if (cg != 1 && cg != 2) return GGE_ERR_UNSUPPORTED;
   int bn = cfg && cfg->tile_n ? cfg->tile_n : 0;
   if (cg == 1) {
@@ -461,7 +465,7 @@ gge_status make_plan(const gge_gemm_args* a, Form form, const int32_t* a_idx,
     if (bn == 0) {
       bn = 256;
       // narrower tiles even out the last wave; N-major B stages 64-column chunks
-      if (!b_mn && !varlen && !vk) {
+      if (!b_mn && !varlen && !vk && !gather) {
         int64_t units = cfg && cfg->num_ctas > 0 ? cfg->num_ctas / 2 : 0;
         if (units <= 0 && encode) {
           // the 256-wide plan: as many stages of (128 + 128) rows as fit, at most kMaxStages
@@ -475,7 +479,7 @@ gge_status make_plan(const gge_gemm_args* a, Form form, const int32_t* a_idx,
       }
     }
     if (bn != 256 && bn != 224 && bn != 192 && bn != 160) return GGE_ERR_UNSUPPORTED;
-    if (b_mn && bn != 256) return GGE_ERR_UNSUPPORTED;
+    if ((b_mn || gather) && bn != 256) return GGE_ERR_UNSUPPORTED;
   }
   pl.bn = bn;
   pl.cg = cg;

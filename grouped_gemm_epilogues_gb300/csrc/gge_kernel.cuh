@@ -105,7 +105,6 @@ struct KernelCfg {
   static_assert(BN % 32 == 0 && BN >= 64 && BN <= 256, "BN: a multiple of 32 in [64, 256]");
   static_assert(kBRows % 8 == 0, "B rows per CTA must fill 8-row swizzle atoms");
   static_assert(CG == 1 || CG == 2, "one CTA or a CTA pair");
-  static_assert(!(GATHER && CG == 2), "the row gather runs on single-CTA tiles");
 };
 
 // Shared-memory matrix descriptor for a K-major (or N-major) operand staged
@@ -1239,16 +1238,45 @@ __device__ __forceinline__ void gather_k_producer_role(const Params& p, const Sh
   }
 }
 
-// Four warps: 8 threads per 128-byte A row, 16 rows per pass, 8 passes.
-template <int BN>
+// This CTA's rows of B for one k-tile by TMA, completing on the stage's barrier
+// (the leader's, for a CTA pair: the leader arms it for both halves).  One lane.
+template <int BN, int CG>
+__device__ __forceinline__ void load_b_stage(const Params& p, const CUtensorMap* tmB, uint32_t dst,
+                                             uint32_t full, uint32_t rank, int32_t k0, int32_t n0,
+                                             int32_t batch) {
+  using Cfg = KernelCfg<BN, true, CG>;
+  if (CG == 1) {
+    ptx::mbar_arrive_expect_tx(full, Cfg::kBBytes);
+    load_b_1cta<BN>(p, tmB, dst, full, k0, n0, batch);
+    return;
+  }
+  if (rank == 0) ptx::mbar_arrive_expect_tx(full, 2 * Cfg::kBBytes);
+  const uint32_t bar = ptx::mapa(full, 0);
+  const int32_t bn0 = n0 + static_cast<int32_t>(rank) * Cfg::kBRows;
+  if (!p.b_mn_major) {
+    ptx::tma_load_3d_pair(dst, tmB, bar, k0, bn0, batch);
+  } else {
+#pragma unroll
+    for (int j = 0; j < Cfg::kBRows / 64; ++j)
+      ptx::tma_load_3d_pair(dst + j * (64 * kRowBytes), tmB, bar, bn0 + 64 * j, k0, batch);
+  }
+}
+
+// Four warps: 8 threads per 128-byte A row, 16 rows per pass, 8 passes.  On a
+// CTA pair each CTA gathers its own 128 rows of the 256-row tile and loads its
+// half of B; the copies land in this CTA's shared memory and arrive on its own
+// stage barrier (the peer's are relayed to the leader by relay_role).
+template <int BN, int CG>
 __device__ __forceinline__ void gather_producer_role(const Params& p, const Shared& sh,
                                                      const CUtensorMap* tmB, uint32_t a0,
                                                      uint32_t b0, int32_t num_tiles,
-                                                     const TileSched& ts) {
-  using Cfg = KernelCfg<BN, true, 1>;
-  if (p.k_groups > 0) {
-    gather_k_producer_role<BN>(p, sh, tmB, a0, b0, num_tiles, ts);
-    return;
+                                                     uint32_t rank, const TileSched& ts) {
+  using Cfg = KernelCfg<BN, true, CG>;
+  if constexpr (CG == 1) {
+    if (p.k_groups > 0) {
+      gather_k_producer_role<BN>(p, sh, tmB, a0, b0, num_tiles, ts);
+      return;
+    }
   }
   constexpr int kRows = kBM * 8 / kGatherThreads;  // rows per thread (8 threads a row)
   const int gt = threadIdx.x - Cfg::kLoadWarp * 32;  // 0 .. kGatherThreads-1
@@ -1258,16 +1286,18 @@ __device__ __forceinline__ void gather_producer_role(const Params& p, const Shar
   int stage = 0;
   uint32_t phase = 0;
   for (int i = 0;; ++i) {
-    // the first gather warp fetches the tile stream, the other reads it
-    const int32_t t = (gt < 32) ? sched_fetch<1>(ts, i, p, sh) : sched_next<1>(ts, i, p, sh);
+    // the first gather warp (of the leader) fetches the tile stream, the others read it
+    const int32_t t = (gt < 32 && rank == 0) ? sched_fetch<CG>(ts, i, p, sh)
+                                             : sched_next<CG>(ts, i, p, sh);
     if (t >= num_tiles) break;
-    const TileCoord tc = tile_coord<BN, kBM>(t, p, sh);
+    const TileCoord tc = tile_coord<BN, Cfg::kTileM>(t, p, sh);
     // index rows: plain gather reads a_idx[batch][row], varlen reads a_idx[global row]
     const int64_t idx_base = (p.num_groups > 0) ? 0 : static_cast<int64_t>(tc.batch) * p.M;
+    const int32_t row0 = tc.m_row0 + static_cast<int32_t>(rank) * kBM;
     int32_t src[kRows];
 #pragma unroll
     for (int i = 0; i < kRows; ++i) {
-      const int32_t r = tc.m_row0 + rsub + kRowStep * i;
+      const int32_t r = row0 + rsub + kRowStep * i;
       int32_t s = -1;
       if (r < tc.row_limit) {
         s = __ldg(p.a_idx + idx_base + r);
@@ -1279,12 +1309,11 @@ __device__ __forceinline__ void gather_producer_role(const Params& p, const Shar
       src[i] = s;
     }
     for (int kt = 0; kt < p.k_tiles; ++kt) {
-      if (!wait_phase(sh.empty + 8 * stage, phase ^ 1u, p, sh, 0, t)) return;
+      if (!wait_phase<CG == 2>(sh.empty + 8 * stage, phase ^ 1u, p, sh, 0, t)) return;
       const uint32_t full = sh.full + 8 * stage;
-      if (gt < 32 && ptx::elect_one()) {  // one lane of the first gather warp: B by TMA
-        ptx::mbar_arrive_expect_tx(full, Cfg::kBBytes);
-        load_b_1cta<BN>(p, tmB, b0 + stage * Cfg::kBBytes, full, kt * p.bk, tc.n0, tc.b_batch);
-      }
+      if (gt < 32 && ptx::elect_one())  // one lane of the first gather warp: B by TMA
+        load_b_stage<BN, CG>(p, tmB, b0 + stage * Cfg::kBBytes, full, rank, kt * p.bk, tc.n0,
+                             tc.b_batch);
       const int32_t kbyte = kt * kRowBytes + chunk * 16;
       const uint32_t kvalid = (kbyte < p.k_bytes) ? 16u : 0u;
       const uint32_t abase = a0 + stage * Cfg::kABytes;
@@ -1299,6 +1328,29 @@ __device__ __forceinline__ void gather_producer_role(const Params& p, const Shar
         ptx::cp_async_16(dst, s, live ? 16u : 0u);
       }
       ptx::cp_async_mbar_arrive_noinc(full);
+      if (++stage == p.stages) { stage = 0; phase ^= 1u; }
+    }
+  }
+}
+
+// CTA pair with gathered A, the peer CTA's idle MMA warp: once the peer's own
+// gather copies of a stage have landed (its local barrier), make them visible
+// to the tensor core's proxy and arrive on the leader's barrier of that stage,
+// whose MMAs read both CTAs' shared memory.  Walks the producers' k-tiles.
+template <int BN>
+__device__ __forceinline__ void relay_role(const Params& p, const Shared& sh, int32_t num_tiles,
+                                           const TileSched& ts) {
+  int stage = 0;
+  uint32_t phase = 0;
+  for (int i = 0;; ++i) {
+    const int32_t t = sched_next<2>(ts, i, p, sh);
+    if (t >= num_tiles) break;
+    for (int kt = 0; kt < p.k_tiles; ++kt) {
+      const bool ok = wait_phase(sh.full + 8 * stage, phase, p, sh, 12, t);
+      if (!__all_sync(0xffffffffu, ok)) return;
+      ptx::fence_proxy_async_smem();
+      if (ptx::elect_one()) ptx::mbar_arrive_cluster(ptx::mapa(sh.full + 8 * stage, 0));
+      __syncwarp();
       if (++stage == p.stages) { stage = 0; phase ^= 1u; }
     }
   }
@@ -1359,7 +1411,11 @@ __global__ void __launch_bounds__(KernelCfg<BN, GATHER, CG>::kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
-      ptx::mbar_init(sh.full + 8 * s, GATHER ? 1 + kGatherWarps * 32 : 1);
+      // gather forms: the copy threads' arrivals, plus the B bytes' arrival (one CTA
+      // or the pair's leader) and the peer's relayed arrival (the pair's leader)
+      ptx::mbar_init(sh.full + 8 * s, !GATHER ? 1
+                                      : (CG == 1 ? 1 + kGatherThreads
+                                                 : (rank == 0 ? 2 + kGatherThreads : kGatherThreads)));
       ptx::mbar_init(sh.empty + 8 * s, 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -1372,9 +1428,12 @@ __global__ void __launch_bounds__(KernelCfg<BN, GATHER, CG>::kThreads, 1)
       ptx::mbar_init(sh.map_empty + 8 * i, 1);
     }
     // ring slot consumers: the MMA warp, every epilogue warp (both CTAs of a pair),
-    // the peer's producer (pair) or the other gather warps
-    const uint32_t consumers = (CG == 2) ? 2 * Cfg::kEpiWarps + 2
-                                         : Cfg::kEpiWarps + 1 + (GATHER ? kGatherWarps - 1 : 0);
+    // the producer warps but the fetching one (both CTAs of a pair) and, for a
+    // gathering pair, the peer's relay warp
+    const uint32_t producers = GATHER ? kGatherWarps : 1;
+    const uint32_t consumers =
+        (CG == 2) ? 2 * Cfg::kEpiWarps + 1 + (2 * producers - 1) + (GATHER ? 1 : 0)
+                  : Cfg::kEpiWarps + 1 + (producers - 1);
     for (int i = 0; i < kSchedDepth; ++i) {
       ptx::mbar_init(ts.full + 8 * i, 1);
       ptx::mbar_init(ts.empty + 8 * i, consumers);
@@ -1457,8 +1516,9 @@ __global__ void __launch_bounds__(KernelCfg<BN, GATHER, CG>::kThreads, 1)
                                   out_stage + warp * p.out_stage_bytes);
   } else if (warp == Cfg::kMmaWarp) {
     if (rank == 0) mma_role<BN, GATHER, CG>(p, sh, a0, b0, tmem_base, num_tiles, ts);
+    else if constexpr (GATHER) relay_role<BN>(p, sh, num_tiles, ts);
   } else if (GATHER) {
-    gather_producer_role<BN>(p, sh, &tmB, a0, b0, num_tiles, ts);
+    gather_producer_role<BN, CG>(p, sh, &tmB, a0, b0, num_tiles, rank, ts);
   } else if (warp == Cfg::kLoadWarp) {
     tma_producer_role<BN, GATHER, CG>(p, sh, &tmA, &tmB, a0, b0,
                                       ptx::smem_addr(ctrl + kMapScratch), num_tiles, rank, ts);

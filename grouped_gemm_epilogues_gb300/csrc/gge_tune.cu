@@ -26,7 +26,11 @@ namespace {
 constexpr int kMaxCandidates = 48;
 
 bool plain_op(int32_t op) { return op == GGE_OP_GEMM || op == GGE_OP_DACT; }
-bool gather_op(int32_t op) { return op == GGE_OP_GATHER_A || op == GGE_OP_GATHER_K; }
+// CTA pairs: every form but gather-K; with gathered A rows, 256-wide tiles only
+bool pair_shape_ok(int32_t op, int tile_n) {
+  if (op == GGE_OP_GATHER_K) return false;
+  return op != GGE_OP_GATHER_A || tile_n == 256;
+}
 
 // All candidates the planner accepts, in a fixed order.
 int32_t enumerate(const gge_gemm_args* args, int32_t op, int32_t num_groups, gge_config* out,
@@ -41,7 +45,7 @@ int32_t enumerate(const gge_gemm_args* args, int32_t op, int32_t num_groups, gge
   const int n_rasters = plain_op(op) ? 3 : 1;
   int32_t n = 0;
   for (const Shape& sh : kShapes) {
-    if (sh.cg == 2 && gather_op(op)) continue;
+    if (sh.cg == 2 && !pair_shape_ok(op, sh.tile_n)) continue;
     for (int b = 0; b < n_rasters; ++b) {
       for (int direct = 0; direct < 2; ++direct) {
         gge_config c = base;

@@ -125,8 +125,8 @@ typedef struct gge_config {
                              of raster_band n-tiles, the n-tile varying fastest
                              (default: bands of m-tiles, the m-tile fastest).  */
   int32_t cta_group;      /* 0 = auto; 1 = one CTA per 128-row tile; 2 = a CTA pair
-                             per 256-row tile (tcgen05 cta_group::2, 256-column
-                             tiles, not with the gather forms)                     */
+                             per 256-row tile (tcgen05 cta_group::2; with gather-A
+                             256-column tiles only; not with gather-K)           */
   int32_t* tile_counts;   /* device int32 per tile (debug coverage), or NULL       */
   uint64_t timeout_ns;    /* 0 = default (2 s) limit for each pipeline wait        */
 } gge_config;

@@ -331,12 +331,13 @@ def test_tune_candidates_follow_the_planner(L):
     Bn = torch.zeros(4096, 4096, dtype=torch.bfloat16).t()
     c = binding.gge_tune_candidates("gemm", A, Bn, D=P)
     assert {(x["cta_group"], x["tile_n"]) for x in c} == {(2, 256), (1, 256), (1, 128)}
-    # the gathers run on single-CTA tiles and have no raster band to search
+    # gather-A runs on one CTA or on 256-wide pair tiles and has no raster band to search
     src = torch.zeros(1000, 512, dtype=torch.bfloat16)
     B = torch.zeros(4, 384, 512, dtype=torch.bfloat16)
     D = torch.zeros(700, 384, dtype=torch.bfloat16)
     c = binding.gge_tune_candidates("gather_a", src, B, D=D, num_groups=4)
-    assert {(x["cta_group"], x["tile_n"], x["raster_band"]) for x in c} == {(1, 256, 0), (1, 128, 0)}
+    assert {(x["cta_group"], x["tile_n"], x["raster_band"]) for x in c} == {
+        (2, 256, 0), (1, 256, 0), (1, 128, 0)}
     # a caller's other flags are kept in every candidate
     c = binding.gge_tune_candidates("gemm", A, A, D=P, config=binding.make_config(flags=4))
     assert {x["flags"] for x in c} == {4, 12, 132, 140}

@@ -35,7 +35,7 @@ def test_dynamic_plain_covers_each_tile_once(cta_group, num_ctas):
     assert ws[4] == 0 and ws[5] == 0
 
 
-@pytest.mark.parametrize("cta_group,gather", [(1, False), (2, False), (1, True)])
+@pytest.mark.parametrize("cta_group,gather", [(1, False), (2, False), (1, True), (2, True)])
 def test_dynamic_varlen_and_gather(cta_group, gather):
     w = wl.small("varlen_gather_g64_m32768_silu", 1500, 520, 136, groups=9, empty_groups=3,
                  gather_rows=4000 if gather else 0)

@@ -22,7 +22,7 @@ def test_autotune_gemm_act():
     D = torch.empty(1, 1024, 768, dtype=torch.bfloat16, device=DEV)
     P = torch.empty_like(D)
     cands = binding.gge_tune_candidates("gemm", A, B, C=C, D=D, PostAct=P, act=w.act)
-    assert len(cands) == 24
+    assert len(cands) == 36
     best, ms = binding.gge_autotune("gemm", A, B, C=C, D=D, PostAct=P, act=w.act, alpha=w.alpha,
                                     beta=w.beta, reps=3)
     assert ms > 0 and best in cands

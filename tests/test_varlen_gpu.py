@@ -97,6 +97,23 @@ def test_varlen_small(case):
     _check(w, t, out, _oracle(w, t, gather))
 
 
+@pytest.mark.parametrize("case", [c for c in VARLEN_SMALL if c[5] > 0] + [
+    (1100, 512, 264, 5, 1, 4000, {"b_major": "n"}),      # N-major B: two 64-column boxes per CTA
+    (640, 264, 200, 3, 0, 900, {"with_c": True, "beta": 0.5, "d_dtype": "bf16"}),
+], ids=lambda c: f"{c[0]}x{c[1]}x{c[2]}-G{c[3]}-g{c[5]}-{c[6]}")
+def test_gather_on_cta_pairs(case):
+    """Gathered A on CTA pairs (256 x 256 tiles): each CTA copies its own 128 rows,
+    the peer's copies are relayed to the leader's stage barrier; group ends fall
+    inside either CTA's half of a tile."""
+    M, N, K, G, empty, gr, kw = case
+    w = wl.small("varlen_gather_g64_m32768_silu", M, N, K, groups=G, empty_groups=empty,
+                 gather_rows=gr, **kw)
+    t = wl.make(w)
+    out = _run(w, t, True, config=binding.make_config(cta_group=2, tile_n=256))
+    _check(w, t, out, _oracle(w, t, True))
+    assert binding.gge_read_device_status()[0] == "GGE_OK"
+
+
 def test_varlen_rows_outside_groups_untouched():
     w = wl.small("varlen_gather_g64_m32768_silu", 600, 256, 64, groups=3, empty_groups=0,
                  gather_rows=0)
@@ -123,17 +140,20 @@ def test_varlen_tile_coverage(cta_group):
     _check(w, t, out, _oracle(w, t, False))
 
 
-def test_gather_identity_equals_varlen():
+@pytest.mark.parametrize("cta_group", [1, 2])
+def test_gather_identity_equals_varlen(cta_group):
     w = wl.small("varlen_gather_g64_m32768_silu", 800, 256, 128, groups=4, empty_groups=1,
                  gather_rows=800)
     t = wl.make(w)
     t["a_idx"] = torch.arange(800, dtype=torch.int32)
-    o_g = _run(w, t, True)
-    o_v = _run(w, t, False)
+    cfg = binding.make_config(cta_group=cta_group, tile_n=256)
+    o_g = _run(w, t, True, config=cfg)
+    o_v = _run(w, t, False, config=cfg)
     assert torch.equal(o_g["P"].view(torch.int16), o_v["P"].view(torch.int16))
 
 
-def test_plain_gather_batched():
+@pytest.mark.parametrize("cta_group", [1, 2])
+def test_plain_gather_batched(cta_group):
     # no cu_seqlens: a_idx is [L][M], B per batch
     L, M, N, K, R = 2, 300, 264, 128, 1000
     g = torch.Generator().manual_seed(3)
@@ -142,7 +162,8 @@ def test_plain_gather_batched():
     idx = torch.floor(torch.rand(L, M, generator=g, dtype=torch.float64) * R).to(torch.int32)
     D = torch.empty(L, M, N, dtype=torch.bfloat16, device=DEV)
     binding.gge_gemm_gather_a(A_src.to(DEV), B.to(DEV), idx.to(DEV), None, D=D, alpha=1.0,
-                              beta=0.0)
+                              beta=0.0, config=binding.make_config(cta_group=cta_group,
+                                                                   tile_n=256))
     torch.cuda.synchronize()
     from oracle import formats
     for l in range(L):
@@ -150,17 +171,20 @@ def test_plain_gather_batched():
         check(D[l].cpu(), ref["D"], ref["bound"], formats.BF16, "none", f"batch {l}")
 
 
-def test_gather_index_out_of_range_is_reported():
+@pytest.mark.parametrize("cta_group", [1, 2])
+def test_gather_index_out_of_range_is_reported(cta_group):
     w = wl.small("varlen_gather_g64_m32768_silu", 256, 256, 64, groups=1, empty_groups=0,
                  gather_rows=500)
     t = wl.make(w)
     t["a_idx"][5] = 500        # one past the end
     t["a_idx"][17] = -1
-    out = _run(w, t, True)
+    t["a_idx"][200] = 1 << 30  # in the second CTA's half of a pair tile
+    out = _run(w, t, True, config=binding.make_config(cta_group=cta_group, tile_n=256))
     status, where, _ = binding.gge_read_device_status()
     assert status == "GGE_ERR_INDEX_RANGE"
     got = dec(out["P"].cpu())
     assert (got[5] == 0).all() and (got[17] == 0).all()   # silu(0) = 0: rows read as zeros
+    assert (got[200] == 0).all()
     assert binding.gge_read_device_status()[0] == "GGE_OK"  # reading clears it
 
 
