@@ -170,6 +170,7 @@ FLAGS = {
     "direct_stores": 8,        # epilogue stores without shared-memory staging
     "no_split": 32,            # never split the last wave along K
     "raster_n": 128,           # raster bands of n-tiles
+    "clc_sched": 256,          # cluster launch control: steal the tiles of unlaunched clusters
 }
 RESERVED_FLAGS = 16 | 64       # a call that sets one of these is rejected
 

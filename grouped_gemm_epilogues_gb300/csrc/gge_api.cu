@@ -336,6 +336,9 @@ gge_status make_plan(const gge_gemm_args* a, Form form, const int32_t* a_idx,
 
   if (a->act < GGE_ACT_NONE || a->act > GGE_ACT_RELU_SQ) return GGE_ERR_INVALID_ARG;
   if (cfg && (cfg->flags & FLAG_RESERVED)) return GGE_ERR_UNSUPPORTED;
+  // one dynamic scheduler at a time: the atomic counter or cluster launch control
+  const bool clc = cfg && (cfg->flags & FLAG_CLC_SCHED);
+  if (clc && (cfg->flags & FLAG_DYNAMIC_SCHED)) return GGE_ERR_INVALID_ARG;
   if (dact) {
     // backward epilogue: C = pre-activation and D = dx are required, PostAct optional
     if (a->C == nullptr || a->D == nullptr || a->act == GGE_ACT_NONE) return GGE_ERR_INVALID_ARG;
@@ -587,6 +590,11 @@ gge_status make_plan(const gge_gemm_args* a, Form form, const int32_t* a_idx,
   }
   pl.shape.grid =
       units_cap > 0 ? unit_ctas * static_cast<int>(std::min<int64_t>(num_tiles, units_cap)) : -1;
+  // cluster launch control: one cluster per tile (those not launched yet are taken over)
+  if (clc) {
+    if (num_tiles * unit_ctas > kMaxExtent) return GGE_ERR_UNSUPPORTED;
+    pl.shape.grid = unit_ctas * static_cast<int>(num_tiles);
+  }
   if (!varlen) {
     // raster: bands of m-tiles (or of n-tiles), the band width the caller's or the
     // one that keeps a wave's operand footprint smallest for the units in use
@@ -603,7 +611,7 @@ gge_status make_plan(const gge_gemm_args* a, Form form, const int32_t* a_idx,
   pl.units = units_cap;
   const int32_t flags = cfg ? cfg->flags : 0;
   if (!varlen && !vk && !gather && K > 0 && units_cap > 0 &&
-      !(flags & (FLAG_DYNAMIC_SCHED | FLAG_NO_SPLIT))) {
+      !(flags & (FLAG_DYNAMIC_SCHED | FLAG_NO_SPLIT | FLAG_CLC_SCHED))) {
     const TailSplit ts = plan_tail_split(num_tiles, units_cap, p.k_tiles);
     if (ts.tail > 0) {
       p.full_tiles = ts.full;

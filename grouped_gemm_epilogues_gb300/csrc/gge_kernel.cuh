@@ -75,13 +75,17 @@ constexpr int kCtrlBytes = 1024;   // barriers, flags and the tile ring (bytes 0
                                    // map-slot barriers (512..767)
 constexpr int kMapScratch = 256;
 constexpr int kMapBars = 512;
+constexpr int kClcBar = 768;       // cluster launch control: its barrier and (at +16) the
+                                   // 16-byte response
+constexpr int kRelayWord = 800;    // gathering pair: the word the peer's relay stores into
 constexpr int kSchedDepth = 4;     // tile indices in flight between the fetching warp and the rest
 constexpr int kMapSlots = 16;      // varlen-K: tensor-map copies per CTA (> pipeline stages)
 constexpr int kMapSlotBytes = 256; // one A and one B tensor map
 // barriers for up to 8 stages, the TMEM slot, the abort flag and the tile ring
 static_assert(8 * (2 * 8 + 5 + 2 * kSchedDepth) + 8 + 4 * kSchedDepth <= kMapScratch,
               "control block overlaps the tensor-map scratch");
-static_assert(kMapBars + 16 * kMapSlots <= kCtrlBytes, "map-slot barriers overflow");
+static_assert(kMapBars + 16 * kMapSlots <= kClcBar, "map-slot barriers overflow");
+static_assert(kClcBar + 32 <= kRelayWord && kRelayWord + 4 <= kCtrlBytes, "control block overflow");
 
 template <int BN, bool GATHER, int CG>
 struct KernelCfg {
@@ -267,19 +271,50 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, const 
 // Dynamic (quack/dense_gemm_sm90.py's tile_count_semaphore): after its first
 // tile, the fetching warp (the producer; the leader's producer for a pair)
 // claims tiles from an atomic counter in the workspace and hands each index to
-// the other warps (and the peer CTA) through a small shared-memory ring.  An
-// index >= num_tiles ends every role's loop.
+// the other warps (and the peer CTA) through a small shared-memory ring.
+// Cluster launch control (the later gemm_sm90.py's use_clc_persistence, which
+// the pages gate on Blackwell): the grid has one cluster per tile; after its
+// own tile, a cluster's fetching warp cancels a cluster that has not been
+// launched yet and takes over its tile, until no cluster is left to cancel.
+// One cancellation request is kept in flight, issued as soon as the previous
+// answer is in, so its latency hides behind the current tile.  An index >=
+// num_tiles ends every role's loop.
 struct TileSched {
   int32_t unit, units;
   int32_t* counter;      // workspace claim counter (dynamic)
   uint32_t full, empty;  // ring barriers (kSchedDepth each)
   uint32_t ring;         // int32 ring[kSchedDepth]
-  bool dyn;
+  bool dyn;              // indices pass through the ring (atomic counter or CLC)
 };
+
+// The fetching warp's lane 0, cluster launch control: the tile of item i.
+// (its barrier and response sit at fixed offsets of the control block)
+__device__ __forceinline__ uint32_t clc_bar_addr(const Shared& sh) {
+  return sh.map_full + (kClcBar - kMapBars);
+}
+
+__device__ __forceinline__ int32_t clc_next(const TileSched& ts, int i, const Params& p,
+                                                const Shared& sh, int32_t num_tiles, int cg) {
+  const uint32_t bar = clc_bar_addr(sh), resp = bar + 16;
+  int32_t t = ts.unit;
+  if (i > 0) {
+    // the answer to the request issued at item i - 1 (request r completes phase r & 1)
+    t = 0x7fffffff;
+    if (wait_phase(bar, static_cast<uint32_t>(i - 1) & 1u, p, sh, 13, i)) {
+      int32_t x = 0;
+      if (ptx::clc_query(resp, x)) t = x / cg;
+    }
+  }
+  if (t < num_tiles) {  // ask for the next one now (none after a refusal: the grid is done)
+    ptx::mbar_arrive_expect_tx(bar, 16);
+    ptx::clc_try_cancel(resp, bar);
+  }
+  return t;
+}
 
 template <int CG>
 __device__ __forceinline__ int32_t sched_fetch(const TileSched& ts, int i, const Params& p,
-                                               const Shared& sh) {
+                                               const Shared& sh, int32_t num_tiles) {
   if (!ts.dyn) return ts.unit + i * ts.units;
   const int slot = i % kSchedDepth;
   const uint32_t ph = static_cast<uint32_t>(i / kSchedDepth) & 1u;
@@ -287,7 +322,8 @@ __device__ __forceinline__ int32_t sched_fetch(const TileSched& ts, int i, const
   if (!__all_sync(0xffffffffu, ok)) return 0x7fffffff;
   int32_t t = 0;
   if ((threadIdx.x & 31) == 0) {
-    t = (i == 0) ? ts.unit : ts.units + atomicAdd(ts.counter, 1);
+    if (p.flags & FLAG_CLC_SCHED) t = clc_next(ts, i, p, sh, num_tiles, CG);
+    else t = (i == 0) ? ts.unit : ts.units + atomicAdd(ts.counter, 1);
     const uint32_t slot_addr = ts.ring + 4 * slot;
     ptx::st_shared_u32(slot_addr, static_cast<uint32_t>(t));
     if (CG == 2) ptx::st_shared_cluster_u32(ptx::mapa(slot_addr, 1), static_cast<uint32_t>(t));
@@ -967,7 +1003,8 @@ __device__ __forceinline__ void tma_producer_role(const Params& p, const Shared&
   const CUtensorMap* mB = tmB;
   for (int i = 0;; ++i) {
     // the producer fetches the tile stream (the peer CTA of a pair reads it)
-    const int32_t t = (rank == 0) ? sched_fetch<CG>(ts, i, p, sh) : sched_next<CG>(ts, i, p, sh);
+    const int32_t t =
+        (rank == 0) ? sched_fetch<CG>(ts, i, p, sh, num_tiles) : sched_next<CG>(ts, i, p, sh);
     if (t >= num_tiles) break;
     const TileCoord tc = tile_coord<BN, Cfg::kTileM>(t, p, sh);
     const KRange kr = k_range(p, sh, tc.batch, t);
@@ -1182,7 +1219,7 @@ __device__ __forceinline__ void gather_k_producer_role(const Params& p, const Sh
   int stage = 0;
   uint32_t phase = 0;
   for (int i = 0;; ++i) {
-    const int32_t t = (gt < 32) ? sched_fetch<1>(ts, i, p, sh) : sched_next<1>(ts, i, p, sh);
+    const int32_t t = (gt < 32) ? sched_fetch<1>(ts, i, p, sh, num_tiles) : sched_next<1>(ts, i, p, sh);
     if (t >= num_tiles) break;
     const TileCoord tc = tile_coord<BN, kBM>(t, p, sh);
     const KRange kr = k_range(p, sh, tc.batch, t);
@@ -1250,7 +1287,8 @@ __device__ __forceinline__ void load_b_stage(const Params& p, const CUtensorMap*
     load_b_1cta<BN>(p, tmB, dst, full, k0, n0, batch);
     return;
   }
-  if (rank == 0) ptx::mbar_arrive_expect_tx(full, 2 * Cfg::kBBytes);
+  // both halves of B, and the 4 bytes the peer's relay stores when its rows are in
+  if (rank == 0) ptx::mbar_arrive_expect_tx(full, 2 * Cfg::kBBytes + 4);
   const uint32_t bar = ptx::mapa(full, 0);
   const int32_t bn0 = n0 + static_cast<int32_t>(rank) * Cfg::kBRows;
   if (!p.b_mn_major) {
@@ -1287,7 +1325,7 @@ __device__ __forceinline__ void gather_producer_role(const Params& p, const Shar
   uint32_t phase = 0;
   for (int i = 0;; ++i) {
     // the first gather warp (of the leader) fetches the tile stream, the others read it
-    const int32_t t = (gt < 32 && rank == 0) ? sched_fetch<CG>(ts, i, p, sh)
+    const int32_t t = (gt < 32 && rank == 0) ? sched_fetch<CG>(ts, i, p, sh, num_tiles)
                                              : sched_next<CG>(ts, i, p, sh);
     if (t >= num_tiles) break;
     const TileCoord tc = tile_coord<BN, Cfg::kTileM>(t, p, sh);
@@ -1335,8 +1373,12 @@ __device__ __forceinline__ void gather_producer_role(const Params& p, const Shar
 
 // CTA pair with gathered A, the peer CTA's idle MMA warp: once the peer's own
 // gather copies of a stage have landed (its local barrier), make them visible
-// to the tensor core's proxy and arrive on the leader's barrier of that stage,
+// to the tensor core's proxy and signal the leader's barrier of that stage,
 // whose MMAs read both CTAs' shared memory.  Walks the producers' k-tiles.
+// The signal is a 4-byte st.async that completes 4 transaction bytes of the
+// leader's barrier: measured, a remote mbarrier arrive with cluster-scope
+// release kept the relay waiting ~1,800 cycles per stage, which throttled the
+// pair to a third of the one-CTA speed.
 template <int BN>
 __device__ __forceinline__ void relay_role(const Params& p, const Shared& sh, int32_t num_tiles,
                                            const TileSched& ts) {
@@ -1349,7 +1391,9 @@ __device__ __forceinline__ void relay_role(const Params& p, const Shared& sh, in
       const bool ok = wait_phase(sh.full + 8 * stage, phase, p, sh, 12, t);
       if (!__all_sync(0xffffffffu, ok)) return;
       ptx::fence_proxy_async_smem();
-      if (ptx::elect_one()) ptx::mbar_arrive_cluster(ptx::mapa(sh.full + 8 * stage, 0));
+      if (ptx::elect_one())
+        ptx::st_async_complete_tx(ptx::mapa(sh.map_full + (kRelayWord - kMapBars), 0), 0u,
+                                  ptx::mapa(sh.full + 8 * stage, 0));
       __syncwarp();
       if (++stage == p.stages) { stage = 0; phase ^= 1u; }
     }
@@ -1395,7 +1439,8 @@ __global__ void __launch_bounds__(KernelCfg<BN, GATHER, CG>::kThreads, 1)
   // a unit is a CTA or a CTA pair
   ts.unit = static_cast<int32_t>(blockIdx.x) / CG;
   ts.units = static_cast<int32_t>(gridDim.x) / CG;
-  ts.dyn = (p.flags & FLAG_DYNAMIC_SCHED) != 0 && p.status != nullptr;
+  const bool clc = (p.flags & FLAG_CLC_SCHED) != 0;
+  ts.dyn = clc || ((p.flags & FLAG_DYNAMIC_SCHED) != 0 && p.status != nullptr);
   ts.counter = p.status + 4;
   ts.full = drain_bar + 8;
   ts.empty = ts.full + 8 * kSchedDepth;
@@ -1412,10 +1457,9 @@ __global__ void __launch_bounds__(KernelCfg<BN, GATHER, CG>::kThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       // gather forms: the copy threads' arrivals, plus the B bytes' arrival (one CTA
-      // or the pair's leader) and the peer's relayed arrival (the pair's leader)
-      ptx::mbar_init(sh.full + 8 * s, !GATHER ? 1
-                                      : (CG == 1 ? 1 + kGatherThreads
-                                                 : (rank == 0 ? 2 + kGatherThreads : kGatherThreads)));
+      // or the pair's leader, which also counts the peer's relayed bytes)
+      ptx::mbar_init(sh.full + 8 * s,
+                     !GATHER ? 1 : ((CG == 1 || rank == 0) ? 1 + kGatherThreads : kGatherThreads));
       ptx::mbar_init(sh.empty + 8 * s, 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -1438,6 +1482,7 @@ __global__ void __launch_bounds__(KernelCfg<BN, GATHER, CG>::kThreads, 1)
       ptx::mbar_init(ts.full + 8 * i, 1);
       ptx::mbar_init(ts.empty + 8 * i, consumers);
     }
+    ptx::mbar_init(clc_bar_addr(sh), 1);
     *abort_flag = 0;
     ptx::fence_barrier_init();
   }
@@ -1546,7 +1591,7 @@ __global__ void __launch_bounds__(KernelCfg<BN, GATHER, CG>::kThreads, 1)
     while (ptx::globaltimer() - t0 < 200000ull) __nanosleep(1000);
   }
   // the last CTA (pair) to finish clears the claim counter for the next call
-  if (ts.dyn && rank == 0 && threadIdx.x == 0) {
+  if (ts.dyn && !clc && rank == 0 && threadIdx.x == 0) {
     __threadfence();
     if (atomicAdd(p.status + 5, 1) == ts.units - 1) {
       atomicExch(p.status + 4, 0);

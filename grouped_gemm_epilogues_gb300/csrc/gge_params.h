@@ -25,6 +25,8 @@ enum : int32_t {
   FLAG_DIRECT_STORES = 8,      // epilogue stores straight from registers (no staging buffers)
   FLAG_NO_SPLIT = 32,          // never split the last wave along K
   FLAG_RASTER_N = 128,         // raster bands of n-tiles (n varies fastest in a band)
+  FLAG_CLC_SCHED = 256,        // one cluster per tile; running clusters take over the tiles
+                               // of clusters not yet launched (cluster launch control)
   FLAG_RESERVED = 16 | 64,     // reserved bits: a call that sets one is rejected
 };
 

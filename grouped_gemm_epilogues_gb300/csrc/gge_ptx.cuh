@@ -385,6 +385,46 @@ __device__ __forceinline__ void mma_commit_pair(uint32_t bar, uint16_t cta_mask)
       : "memory");
 }
 
+// Stores 4 bytes into another CTA's shared memory and completes 4 transaction
+// bytes on that CTA's mbarrier `cluster_bar` (release at cluster scope).  It
+// is asynchronous: unlike a remote mbarrier arrive, the issuing thread does not
+// wait for it.
+__device__ __forceinline__ void st_async_complete_tx(uint32_t cluster_addr, uint32_t v,
+                                                     uint32_t cluster_bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];"
+               ::"r"(cluster_addr), "r"(v), "r"(cluster_bar)
+               : "memory");
+}
+
+// ---- cluster launch control (work stealing from clusters not yet launched)
+
+// Asks the hardware to cancel a cluster of this grid that has not started yet.
+// The 16-byte response lands in this CTA's shared memory at `resp` and
+// completes 16 transaction bytes on the mbarrier `bar` (armed by the caller).
+__device__ __forceinline__ void clc_try_cancel(uint32_t resp, uint32_t bar) {
+  asm volatile(
+      "clusterlaunchcontrol.try_cancel.async.shared::cta.mbarrier::complete_tx::bytes.b128"
+      " [%0], [%1];" ::"r"(resp), "r"(bar)
+      : "memory");
+}
+
+// Decodes a response: true if a cluster was cancelled, and then `cta_x` is the
+// x index of its first CTA (the caller takes over that cluster's work).
+__device__ __forceinline__ bool clc_query(uint32_t resp, int32_t& cta_x) {
+  uint32_t ok, x;
+  asm volatile(
+      "{\n\t.reg .b128 h;\n\t.reg .pred p;\n\t"
+      "ld.shared.b128 h, [%2];\n\t"
+      "clusterlaunchcontrol.query_cancel.is_canceled.pred.b128 p, h;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t"
+      "clusterlaunchcontrol.query_cancel.get_first_ctaid::x.b32.b128 %1, h;\n\t}"
+      : "=r"(ok), "=r"(x)
+      : "r"(resp)
+      : "memory");
+  cta_x = static_cast<int32_t>(x);
+  return ok != 0;
+}
+
 // ---- tensor-map edits (per-group K extents)
 
 // Set the global extent of dimension ORD of a tensor map held in shared memory.

@@ -123,7 +123,13 @@ typedef struct gge_config {
                              GGE_ERR_UNSUPPORTED);
                              bit 7: raster along N -- plain problems walk bands
                              of raster_band n-tiles, the n-tile varying fastest
-                             (default: bands of m-tiles, the m-tile fastest).  */
+                             (default: bands of m-tiles, the m-tile fastest);
+                             bit 8: cluster launch control -- the grid has one
+                             CTA (pair) per tile, and a running one takes over
+                             the tiles of those not launched yet
+                             (clusterlaunchcontrol.try_cancel) instead of a
+                             fixed stride; no workspace needed; not with bit 2;
+                             the last wave is not split.                       */
   int32_t cta_group;      /* 0 = auto; 1 = one CTA per 128-row tile; 2 = a CTA pair
                              per 256-row tile (tcgen05 cta_group::2; with gather-A
                              256-column tiles only; not with gather-K)           */

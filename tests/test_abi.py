@@ -88,6 +88,24 @@ def test_schedule_raster_order(L):
     assert got[8:] == [(0, 0, 2), (0, 1, 2), (0, 2, 2), (0, 3, 2)]
 
 
+def test_clc_plan(L):
+    """Cluster launch control: one CTA (pair) per tile in the grid, no split of the
+    last wave, and not together with the atomic-counter scheduler."""
+    A = torch.zeros(1024, 8192, dtype=torch.bfloat16)
+    B = torch.zeros(1024, 8192, dtype=torch.bfloat16)
+    D = torch.zeros(1024, 1024, dtype=torch.bfloat16)
+    base = dict(num_ctas=152, cta_group=2, tile_n=256)
+    info = binding.gge_plan(A, B, D=D, config=binding.make_config(**base))
+    assert info["tail_tiles"] == 16                     # 16 pair tiles split on 76 pairs
+    info = binding.gge_plan(A, B, D=D, config=binding.make_config(flags=256, **base))
+    assert info["grid"] == 2 * 16 and info["tail_tiles"] == 0 and info["num_tiles"] == 16
+    info = binding.gge_plan(A, B, D=D, config=binding.make_config(flags=256, num_ctas=152,
+                                                                  cta_group=1, tile_n=128))
+    assert info["grid"] == 8 * 8
+    with pytest.raises(binding.GgeError):
+        binding.gge_plan(A, B, D=D, config=binding.make_config(flags=256 | 4, **base))
+
+
 def test_auto_raster_band(L):
     """The automatic band keeps a wave's operand rows fewest: sqrt(units * tile_n /
     tile_m) m-tiles (76 pairs of 256 x 256 tiles: 9)."""

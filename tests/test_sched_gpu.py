@@ -50,3 +50,62 @@ def test_dynamic_varlen_and_gather(cta_group, gather):
     assert (c[:len(expect)] == 1).all() and (c[len(expect):] == 0).all()
     _check(w, t, out, _oracle(w, t, gather))
     assert binding.gge_read_device_status()[0] == "GGE_OK"
+
+
+FLAG_CLC = 256
+
+
+@pytest.mark.parametrize("cta_group", [1, 2])
+def test_clc_plain_covers_each_tile_once(cta_group):
+    """Cluster launch control: one CTA (pair) per tile in the grid; running ones take
+    over the tiles of those not launched yet.  Every tile exactly once, twice in a
+    row, and the outputs match the oracle."""
+    w = wl.small("gemm_act_4096_bf16_gelu", 2000, 1800, 320, 3)
+    t = wl.make(w)
+    tiles = len(ot.plain_tiles(2000, 1800, 3, 128 * cta_group, 256))
+    for call in range(2):
+        out = _outputs(w, 2000, 1800, 3)
+        counts = torch.zeros(tiles + 8, dtype=torch.int32, device=DEV)
+        cfg = binding.make_config(flags=FLAG_TILE_COUNTS | FLAG_CLC, tile_counts=counts,
+                                  cta_group=cta_group, tile_n=256)
+        _run_plain(w, t, out, config=cfg)
+        c = counts.cpu()
+        assert (c[:tiles] == 1).all() and (c[tiles:] == 0).all(), call
+        _check_plain(w, t, out)
+
+
+@pytest.mark.parametrize("cta_group,gather", [(1, False), (2, False), (1, True), (2, True)])
+def test_clc_varlen_and_gather(cta_group, gather):
+    """The varlen grid is sized by an upper bound on the tiles; clusters past the
+    real count (known only on the device) end at once."""
+    w = wl.small("varlen_gather_g64_m32768_silu", 2500, 520, 136, groups=9, empty_groups=3,
+                 gather_rows=4000 if gather else 0)
+    t = wl.make(w)
+    cu = t["cu_seqlens_m"].numpy()
+    expect = ot.varlen_tiles(cu, w.N, 128 * cta_group, 256)
+    counts = torch.zeros(len(expect) + 64, dtype=torch.int32, device=DEV)
+    cfg = binding.make_config(flags=FLAG_TILE_COUNTS | FLAG_CLC, tile_counts=counts,
+                              cta_group=cta_group, tile_n=256)
+    out = _run(w, t, gather, config=cfg)
+    c = counts.cpu().numpy()
+    assert (c[:len(expect)] == 1).all() and (c[len(expect):] == 0).all()
+    _check(w, t, out, _oracle(w, t, gather))
+    assert binding.gge_read_device_status()[0] == "GGE_OK"
+
+
+def test_clc_varlen_k():
+    from oracle import gemm as og
+    from helpers import FMT_NAME, check, dec
+    gen = torch.Generator().manual_seed(31)
+    M, N, total = 328, 264, 1000
+    A = ((torch.rand(total, M, generator=gen) * 2 - 1).bfloat16()).t()
+    B = ((torch.rand(total, N, generator=gen) * 2 - 1).bfloat16()).t()
+    cu = [0, 37, 37, 150, 151, 400, 733, 733, 950, 990]
+    G = len(cu) - 1
+    D = torch.full((G, M, N), -3.0, dtype=torch.bfloat16, device=DEV)
+    binding.gge_gemm_varlen_k(A.to(DEV), B.to(DEV), torch.tensor(cu, dtype=torch.int32).to(DEV),
+                              D=D, config=binding.make_config(flags=FLAG_CLC, cta_group=2))
+    torch.cuda.synchronize()
+    assert binding.gge_read_device_status()[0] == "GGE_OK"
+    r = og.gemm_varlen_k(dec(A), dec(B), np.asarray(cu), None, d_fmt=FMT_NAME["bf16"])
+    check(dec(D.cpu()), r["D"], r["bound"], FMT_NAME["bf16"], "none", "varlen-K with CLC")
