@@ -356,7 +356,9 @@ def _peak_for(w, peaks, src):
 
 def _fixed_shape(args):
     """A launch shape given on the command line (with --no-tune), or None."""
-    d = {k: v for k, v in (("cta_group", args.cta_group), ("tile_n", args.tile_n)) if v}
+    d = json.loads(args.config_json) if args.config_json else {}
+    d.update({k: v for k, v in (("cta_group", args.cta_group), ("tile_n", args.tile_n)) if v})
+    d.pop("source", None)
     return d or None
 
 
@@ -684,6 +686,9 @@ def main():
     ap.add_argument("--cta-group", type=int, default=0,
                     help="with --no-tune: CTAs per tile (1, or 2 for a CTA pair)")
     ap.add_argument("--tile-n", type=int, default=0, help="with --no-tune: tile width")
+    ap.add_argument("--config-json", default="",
+                    help="with --no-tune: a whole launch configuration (gge_config fields as "
+                         "JSON, e.g. a launch_shape this script printed)")
     ap.add_argument("--no-per-config", action="store_true",
                     help="skip the per-config lines (the other workloads of the metric)")
     args = ap.parse_args()

@@ -171,6 +171,8 @@ FLAGS = {
     "no_split": 32,            # never split the last wave along K
     "raster_n": 128,           # raster bands of n-tiles
     "clc_sched": 256,          # cluster launch control: steal the tiles of unlaunched clusters
+    "swap_ab": 512,            # compute D^T = B A^T (outputs stored transposed by the kernel)
+    "k_serpentine": 1024,      # odd waves walk K backwards (L2 reuse across waves)
 }
 RESERVED_FLAGS = 16 | 64       # a call that sets one of these is rejected
 

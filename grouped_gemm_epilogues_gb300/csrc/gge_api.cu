@@ -236,6 +236,7 @@ int variant_threads(int bn, bool gather, int cg) {
       default: return kernel_threads<256, false, 2>();
     }
   }
+  if (bn == 64) return kernel_threads<64, false, 1>();
   return bn == 128 ? kernel_threads<128, false, 1>() : kernel_threads<256, false, 1>();
 }
 
@@ -278,6 +279,7 @@ int variant_units_uncached(int bn, bool gather, int cg, size_t smem, int cluster
       default: return max_active_units<256, false, 2>(smem, cluster);
     }
   }
+  if (bn == 64) return max_active_units<64, false, 1>(smem, 1);
   return bn == 128 ? max_active_units<128, false, 1>(smem, 1) : max_active_units<256, false, 1>(smem, 1);
 }
 
@@ -294,6 +296,12 @@ cudaError_t variant_launch(const Plan& pl, cudaStream_t st) {
       default: return launch_gemm<256, false, 2>(pl.tmA, pl.tmB, pl.p, pl.shape, st);
     }
   }
+  if (pl.p.out_trans) {  // swap_ab: the transposed-output instances (one-CTA tiles)
+    if (pl.bn == 64) return launch_gemm<64, false, 1, true>(pl.tmA, pl.tmB, pl.p, pl.shape, st);
+    return pl.bn == 128 ? launch_gemm<128, false, 1, true>(pl.tmA, pl.tmB, pl.p, pl.shape, st)
+                        : launch_gemm<256, false, 1, true>(pl.tmA, pl.tmB, pl.p, pl.shape, st);
+  }
+  if (pl.bn == 64) return launch_gemm<64, false, 1>(pl.tmA, pl.tmB, pl.p, pl.shape, st);
   return pl.bn == 128 ? launch_gemm<128, false, 1>(pl.tmA, pl.tmB, pl.p, pl.shape, st)
                       : launch_gemm<256, false, 1>(pl.tmA, pl.tmB, pl.p, pl.shape, st);
 }
@@ -328,6 +336,17 @@ gge_status make_plan(const gge_gemm_args* a, Form form, const int32_t* a_idx,
   std::memset(&pl, 0, sizeof(pl));
   Params& p = pl.p;
   const gge_config* cfg = a->config;
+  // swap_ab (the pages' GemmConfig.swap_ab): run D^T = B A^T, i.e. the kernel's A is
+  // the caller's B and its rows are the caller's N; the epilogue stores transposed
+  const bool swap = cfg && (cfg->flags & FLAG_SWAP_AB);
+  gge_gemm_args swapped;
+  if (swap) {
+    if (form != Form::Plain) return GGE_ERR_UNSUPPORTED;
+    swapped = *a;
+    swapped.A = a->B;
+    swapped.B = a->A;
+    a = &swapped;
+  }
   const bool varlen = (form == Form::Varlen || form == Form::GatherVarlen);
   const bool gk = (form == Form::GatherK);  // varlen-K with A gathered along K
   const bool gather = (form == Form::Gather || form == Form::GatherVarlen || gk);
@@ -364,14 +383,17 @@ gge_status make_plan(const gge_gemm_args* a, Form form, const int32_t* a_idx,
 
   // shapes from the output
   const gge_tensor* o = a->D ? a->D : a->PostAct;
-  const int64_t M = o->rows, N = o->cols, L = o->batch;
+  // the kernel's problem: M x N per batch (swapped: the caller's N x M)
+  const int64_t M = swap ? o->cols : o->rows, N = swap ? o->rows : o->cols, L = o->batch;
+  const int64_t out_rows = o->rows, out_cols = o->cols;  // the caller's [M, N]
   // gather-K: A is the source X^T [M, K_src]; the contraction runs over B's columns
   const int64_t K = gk ? a->B.cols : a->A.cols;
   if (M < 0 || N < 0 || K < 0) return GGE_ERR_INVALID_ARG;
-  if (a->D) { s = check_mn(a->D, M, N, L, true); if (s != GGE_OK) return s; }
-  if (a->PostAct) { s = check_mn(a->PostAct, M, N, L, true); if (s != GGE_OK) return s; }
-  if (a->C) { s = check_mn(a->C, M, N, L, false); if (s != GGE_OK) return s; }
-  if (N % 8 != 0) return GGE_ERR_UNSUPPORTED;
+  if (a->D) { s = check_mn(a->D, out_rows, out_cols, L, true); if (s != GGE_OK) return s; }
+  if (a->PostAct) { s = check_mn(a->PostAct, out_rows, out_cols, L, true); if (s != GGE_OK) return s; }
+  if (a->C) { s = check_mn(a->C, out_rows, out_cols, L, false); if (s != GGE_OK) return s; }
+  // the caller's output rows are stored in whole 16-byte pieces
+  if (out_cols % 8 != 0) return GGE_ERR_UNSUPPORTED;
   // epilogue staging per warp: a 32 x 32 chunk of the widest output
   const int out_es = std::max(a->D ? elem_bytes(a->D->dtype) : 0,
                               a->PostAct ? elem_bytes(a->PostAct->dtype) : 0);
@@ -446,14 +468,17 @@ gge_status make_plan(const gge_gemm_args* a, Form form, const int32_t* a_idx,
   }
 
   // tile shape: 128 x BN on one CTA, or 256 x BN on a CTA pair
-  int cg = cfg && cfg->cta_group ? cfg->cta_group : ((!gather && N > 128 && M >= 256) ? 2 : 1);
+  // (swap_ab runs on one-CTA tiles: its kernel N is the caller's small M)
+  int cg = cfg && cfg->cta_group ? cfg->cta_group
+                                 : ((!gather && !swap && N > 128 && M >= 256) ? 2 : 1);
+  if (swap && cg != 1) return GGE_ERR_UNSUPPORTED;
   // gather-A runs on one CTA or a CTA pair (256 x 256 tiles); gather-K on one CTA
   if (cg == 2 && gk) return GGE_ERR_UNSUPPORTED;
   if (cg != 1 && cg != 2) return GGE_ERR_UNSUPPORTED;
   int bn = cfg && cfg->tile_n ? cfg->tile_n : 0;
   if (cg == 1) {
     if (bn == 0) {
-      bn = N <= 128 ? 128 : 256;
+      bn = (N <= 64 && !gather) ? 64 : (N <= 128 ? 128 : 256);
       // fewer 256-wide tiles than CTAs the GPU holds: 128-wide tiles spread the
       // problem over twice as many (measured on skinny problems: 128 x 8192 x 8192
       // 40.8 -> 32.8 us, 64 x 4096 x 8192 26.3 -> 20.7 us)
@@ -463,7 +488,7 @@ gge_status make_plan(const gge_gemm_args* a, Form form, const int32_t* a_idx,
         if (ctas > 0 && tiles256 < ctas) bn = 128;
       }
     }
-    if (bn != 128 && bn != 256) return GGE_ERR_UNSUPPORTED;
+    if (bn != 128 && bn != 256 && !(bn == 64 && !gather)) return GGE_ERR_UNSUPPORTED;
   } else {
     if (bn == 0) {
       bn = 256;
@@ -559,6 +584,7 @@ gge_status make_plan(const gge_gemm_args* a, Form form, const int32_t* a_idx,
   }
   p.act = a->act;
   p.dact = dact ? 1 : 0;
+  p.out_trans = swap ? 1 : 0;
   p.out_stage_bytes = out_stage;
   p.alpha = a->alpha;
   p.beta = a->beta;

@@ -8,9 +8,9 @@
 
 namespace gge {
 
-template <int BN, bool GATHER, int CG>
+template <int BN, bool GATHER, int CG, bool TR = false>
 cudaError_t set_smem_limit(size_t smem) {
-  auto kern = gemm_kernel<BN, GATHER, CG>;
+  auto kern = gemm_kernel<BN, GATHER, CG, TR>;
   // the dynamic shared-memory limit is a per-device function attribute
   static std::atomic<size_t> smem_set[64];
   int dev = 0;
@@ -25,11 +25,11 @@ cudaError_t set_smem_limit(size_t smem) {
   return cudaSuccess;
 }
 
-template <int BN, bool GATHER, int CG>
+template <int BN, bool GATHER, int CG, bool TR>
 cudaError_t launch_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const Params& p,
                         const LaunchShape& shape, cudaStream_t stream) {
-  auto kern = gemm_kernel<BN, GATHER, CG>;
-  cudaError_t e = set_smem_limit<BN, GATHER, CG>(shape.smem);
+  auto kern = gemm_kernel<BN, GATHER, CG, TR>;
+  cudaError_t e = set_smem_limit<BN, GATHER, CG, TR>(shape.smem);
   if (e != cudaSuccess) return e;
   cudaLaunchAttribute attr[2];
   cudaLaunchConfig_t cfg = {};
@@ -88,10 +88,16 @@ int max_active_units(size_t smem, int cluster) {
 }
 
 #define GGE_INSTANTIATE(BN, GATHER, CG)                                                      \
-  template cudaError_t launch_gemm<BN, GATHER, CG>(const CUtensorMap&, const CUtensorMap&, \
-                                                   const Params&, const LaunchShape&,      \
-                                                   cudaStream_t);                          \
+  template cudaError_t launch_gemm<BN, GATHER, CG, false>(const CUtensorMap&,              \
+                                                          const CUtensorMap&, const Params&, \
+                                                          const LaunchShape&, cudaStream_t); \
   template int kernel_threads<BN, GATHER, CG>();                                           \
   template int max_active_units<BN, GATHER, CG>(size_t, int);
+
+// The transposed-output (swap_ab) instance of a one-CTA TMA tile.
+#define GGE_INSTANTIATE_TRANS(BN)                                                             \
+  template cudaError_t launch_gemm<BN, false, 1, true>(const CUtensorMap&, const CUtensorMap&, \
+                                                       const Params&, const LaunchShape&,      \
+                                                       cudaStream_t);
 
 }  // namespace gge

@@ -3,4 +3,5 @@
 
 namespace gge {
 GGE_INSTANTIATE(128, false, 1)
+GGE_INSTANTIATE_TRANS(128)
 }  // namespace gge

@@ -3,4 +3,5 @@
 
 namespace gge {
 GGE_INSTANTIATE(256, false, 1)
+GGE_INSTANTIATE_TRANS(256)
 }  // namespace gge

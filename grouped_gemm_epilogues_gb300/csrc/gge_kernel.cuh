@@ -202,6 +202,14 @@ __device__ __forceinline__ KRange k_range(const Params& p, const Shared& sh, int
   return KRange{lo, hi, (hi - lo + p.bk - 1) / p.bk, ((hi - lo) & (mma_kstep(p) - 1)) != 0};
 }
 
+// Serpentine K (config flag bit 10, plain and varlen-M TMA forms): work items of
+// odd waves (item / units) walk their k-tiles backwards, so that a wave starts
+// on the k-slices of A and B that the previous wave read last and are still
+// in L2.  The direction depends only on the item, so results are reproducible.
+__device__ __forceinline__ bool k_reversed(const Params& p, int32_t t, int32_t units) {
+  return (p.flags & FLAG_K_SERPENTINE) && p.k_groups == 0 && ((t / units) & 1);
+}
+
 // MMA K-steps of k-tile kt (4 per full k-tile; the last one stops at k_end).
 __device__ __forceinline__ int32_t ksteps_of(const Params& p, const KRange& kr, int32_t kt) {
   const int32_t left = kr.k_end - (kr.k0 + kt * p.bk);
@@ -438,33 +446,57 @@ struct CRegs {
   uint4 w[4];
 };
 
-// Address of C[row, col0] of batch `batch`.
+// Address of C[row, col0] of batch `batch`.  TR (swap_ab): the caller's C holds
+// the kernel's element (row, col) at [col][row].
+template <bool TR = false>
 __device__ __forceinline__ const char* c_ptr(const Params& p, int32_t row, int32_t col0,
                                              int32_t batch) {
   const int64_t out_batch = (p.num_groups > 0) ? 0 : batch;
-  return static_cast<const char*>(p.c) +
-         (out_batch * p.sbc + static_cast<int64_t>(row) * p.ldc + col0) * dtype_bytes(p.c_dtype);
+  const int64_t off = TR ? static_cast<int64_t>(col0) * p.ldc + row
+                         : static_cast<int64_t>(row) * p.ldc + col0;
+  return static_cast<const char*>(p.c) + (out_batch * p.sbc + off) * dtype_bytes(p.c_dtype);
 }
 
 // Issue the loads of a 16-bit C[row, col0 .. col0+32) (no arithmetic: the
 // values are used one chunk later, so the load latency hides behind that
-// chunk's work).
+// chunk's work).  TR: the 32 values sit one caller row apart; each load
+// instruction of the warp still reads 32 consecutive elements.
+template <bool TR = false>
 __device__ __forceinline__ void load_c_chunk(const Params& p, int32_t row, int32_t col0,
                                              int32_t batch, CRegs& c) {
   if (p.c_dtype == DT_F32) return;
-  const uint4* base = reinterpret_cast<const uint4*>(c_ptr(p, row, col0, batch));
+  if constexpr (TR) {
+    const uint16_t* base = reinterpret_cast<const uint16_t*>(c_ptr<true>(p, row, col0, batch));
+    uint32_t w[16];
 #pragma unroll
-  for (int i = 0; i < 4; ++i)
-    if (col0 + 8 * i < p.N) c.w[i] = __ldg(base + i);
+    for (int i = 0; i < 16; ++i) {
+      const uint32_t lo = (col0 + 2 * i < p.N) ? __ldg(base + (2 * i) * p.ldc) : 0u;
+      const uint32_t hi = (col0 + 2 * i + 1 < p.N) ? __ldg(base + (2 * i + 1) * p.ldc) : 0u;
+      w[i] = lo | (hi << 16);
+    }
+#pragma unroll
+    for (int g = 0; g < 4; ++g) c.w[g] = make_uint4(w[4 * g], w[4 * g + 1], w[4 * g + 2], w[4 * g + 3]);
+  } else {
+    const uint4* base = reinterpret_cast<const uint4*>(c_ptr(p, row, col0, batch));
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      if (col0 + 8 * i < p.N) c.w[i] = __ldg(base + i);
+  }
 }
 
 // Eight values of C (group g of 8 columns of the chunk) as fp32: from the
 // prefetched registers (16-bit C), or read now through `crow` (fp32 C; NULL
 // for a row that does not exist).  CDT is C's dtype.
-template <int CDT>
+template <int CDT, bool TR>
 __device__ __forceinline__ void c_values8(const CRegs& c, const Params& p, const char* crow,
                                           int32_t col0, int g, float (&out)[8]) {
-  if constexpr (CDT == DT_F32) {
+  if constexpr (CDT == DT_F32 && TR) {
+    // `crow` points at the caller's C[col0][row]: the chunk's columns are rows of C
+    const float* cc = reinterpret_cast<const float*>(crow);
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      out[i] = (cc != nullptr && col0 + 8 * g + i < p.N) ? __ldg(cc + (8 * g + i) * p.ldc) : 0.f;
+  } else if constexpr (CDT == DT_F32) {
     float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a;
     if (crow != nullptr && col0 + 8 * g < p.N) {
       a = __ldg(reinterpret_cast<const float4*>(crow) + 2 * g);
@@ -488,43 +520,45 @@ __device__ __forceinline__ void c_values8(const CRegs& c, const Params& p, const
 }
 
 // v += beta * C over the chunk (C's dtype chosen once, outside the value loops).
-template <int CDT>
+template <int CDT, bool TR>
 __device__ __forceinline__ void add_beta_c_t(const CRegs& c, const Params& p, const char* crow,
                                              int32_t col0, float beta, float (&v)[32]) {
 #pragma unroll
   for (int g = 0; g < 4; ++g) {
     float cv[8];
-    c_values8<CDT>(c, p, crow, col0, g, cv);
+    c_values8<CDT, TR>(c, p, crow, col0, g, cv);
 #pragma unroll
     for (int j = 0; j < 8; ++j) v[8 * g + j] = fmaf(beta, cv[j], v[8 * g + j]);
   }
 }
 
+template <bool TR>
 __device__ __forceinline__ void add_beta_c(const CRegs& c, const Params& p, const char* crow,
                                            int32_t col0, float beta, float (&v)[32]) {
-  if (p.c_dtype == DT_F32) add_beta_c_t<DT_F32>(c, p, crow, col0, beta, v);
-  else if (p.c_dtype == DT_BF16) add_beta_c_t<DT_BF16>(c, p, crow, col0, beta, v);
-  else add_beta_c_t<DT_F16>(c, p, crow, col0, beta, v);
+  if (p.c_dtype == DT_F32) add_beta_c_t<DT_F32, TR>(c, p, crow, col0, beta, v);
+  else if (p.c_dtype == DT_BF16) add_beta_c_t<DT_BF16, TR>(c, p, crow, col0, beta, v);
+  else add_beta_c_t<DT_F16, TR>(c, p, crow, col0, beta, v);
 }
 
 // All 32 values of C as fp32 (the backward epilogue's pre-activation).
-template <int CDT>
+template <int CDT, bool TR>
 __device__ __forceinline__ void c_values32_t(const CRegs& c, const Params& p, const char* crow,
                                              int32_t col0, float (&x)[32]) {
 #pragma unroll
   for (int g = 0; g < 4; ++g) {
     float cv[8];
-    c_values8<CDT>(c, p, crow, col0, g, cv);
+    c_values8<CDT, TR>(c, p, crow, col0, g, cv);
 #pragma unroll
     for (int j = 0; j < 8; ++j) x[8 * g + j] = cv[j];
   }
 }
 
+template <bool TR>
 __device__ __forceinline__ void c_values32(const CRegs& c, const Params& p, const char* crow,
                                            int32_t col0, float (&x)[32]) {
-  if (p.c_dtype == DT_F32) c_values32_t<DT_F32>(c, p, crow, col0, x);
-  else if (p.c_dtype == DT_BF16) c_values32_t<DT_BF16>(c, p, crow, col0, x);
-  else c_values32_t<DT_F16>(c, p, crow, col0, x);
+  if (p.c_dtype == DT_F32) c_values32_t<DT_F32, TR>(c, p, crow, col0, x);
+  else if (p.c_dtype == DT_BF16) c_values32_t<DT_BF16, TR>(c, p, crow, col0, x);
+  else c_values32_t<DT_F16, TR>(c, p, crow, col0, x);
 }
 
 // Two fp32 values as one 32-bit word of a 16-bit output type (RNE).
@@ -619,17 +653,98 @@ __device__ __forceinline__ void store_chunk_staged(uint32_t stg, const float (&x
   __syncwarp();  // the buffer is free again
 }
 
-// Where a warp's chunk of an output starts: (row_base, col0) of batch `batch`.
+// swap_ab: the caller's output holds the kernel's element (row, col) at
+// [col][row], so a warp's chunk is 32 caller rows (the chunk's columns) of 32
+// consecutive elements (its rows).  Each lane writes its 32 values down a
+// column of the warp's staging buffer, then every store instruction writes
+// whole 16-byte pieces of caller rows: 16-bit outputs 8 rows x 64 B, fp32 4 rows
+// x 128 B, as in store_chunk_staged.  `out` points at the caller's [col0][row
+// base]; rows_valid (a multiple of 8: the caller's N is) and cols_valid bound the
+// chunk.  Warp-collective.
+__device__ __forceinline__ void store_chunk_staged_t(uint32_t stg, const float (&x)[32], int dtype,
+                                                     char* out, int64_t ld_bytes,
+                                                     int32_t rows_valid, int32_t cols_valid,
+                                                     bool direct) {
+  const int lane = threadIdx.x & 31;
+  if (direct) {
+    // no staging buffer: each instruction writes one caller row's 32 elements
+    if (lane >= rows_valid) return;
+    if (dtype == DT_F32) {
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        if (j < cols_valid) *reinterpret_cast<float*>(out + j * ld_bytes + 4 * lane) = x[j];
+    } else {
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        if (j < cols_valid) {
+          const uint32_t w = dtype == DT_BF16 ? pack2<true>(x[j], 0.f) : pack2<false>(x[j], 0.f);
+          *reinterpret_cast<uint16_t*>(out + j * ld_bytes + 2 * lane) = static_cast<uint16_t>(w);
+        }
+    }
+    return;
+  }
+  if (dtype == DT_F32) {
+#pragma unroll
+    for (int j = 0; j < 32; ++j) ptx::st_shared_u32(stg + j * 128 + 4 * lane, __float_as_uint(x[j]));
+    __syncwarp();
+#pragma unroll
+    for (int it = 0; it < 8; ++it) {
+      const int pc = lane + 32 * it, j = pc >> 3, q = pc & 7;
+      const uint4 v = ptx::ld_shared_v4(stg + j * 128 + 16 * q);
+      if (j < cols_valid && 4 * q < rows_valid)
+        *reinterpret_cast<uint4*>(out + j * ld_bytes + 16 * q) = v;
+    }
+  } else {
+    if (dtype == DT_BF16) {
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        ptx::st_shared_u16(stg + j * 64 + 2 * lane, static_cast<uint16_t>(pack2<true>(x[j], 0.f)));
+    } else {
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        ptx::st_shared_u16(stg + j * 64 + 2 * lane, static_cast<uint16_t>(pack2<false>(x[j], 0.f)));
+    }
+    __syncwarp();
+#pragma unroll
+    for (int it = 0; it < 4; ++it) {
+      const int pc = lane + 32 * it, j = pc >> 2, q = pc & 3;
+      const uint4 v = ptx::ld_shared_v4(stg + j * 64 + 16 * q);
+      if (j < cols_valid && 8 * q < rows_valid)
+        *reinterpret_cast<uint4*>(out + j * ld_bytes + 16 * q) = v;
+    }
+  }
+  __syncwarp();  // the buffer is free again
+}
+
+// Where a warp's chunk of an output starts: (row_base, col0) of batch `batch`
+// (TR: the caller's [col0][row_base]).
+template <bool TR = false>
 __device__ __forceinline__ char* out_ptr(void* base, int64_t ld, int64_t sb, int dtype,
                                          int32_t row_base, int32_t col0, int32_t batch,
                                          const Params& p) {
   const int64_t out_batch = (p.num_groups > 0) ? 0 : batch;
-  return static_cast<char*>(base) +
-         (out_batch * sb + static_cast<int64_t>(row_base) * ld + col0) * dtype_bytes(dtype);
+  const int64_t off = TR ? static_cast<int64_t>(col0) * ld + row_base
+                         : static_cast<int64_t>(row_base) * ld + col0;
+  return static_cast<char*>(base) + (out_batch * sb + off) * dtype_bytes(dtype);
+}
+
+// One output chunk through the store of the layout (TR: swap_ab's transposed one).
+template <bool TR>
+__device__ __forceinline__ void store_out(const Params& p, uint32_t stg, const float (&x)[32],
+                                          void* base, int64_t ld, int64_t sb, int dtype,
+                                          int32_t row_base, int32_t rows_valid, int32_t col0,
+                                          int32_t cols_valid, int32_t batch) {
+  char* o = out_ptr<TR>(base, ld, sb, dtype, row_base, col0, batch, p);
+  const int64_t ld_bytes = ld * dtype_bytes(dtype);
+  if constexpr (TR)
+    store_chunk_staged_t(stg, x, dtype, o, ld_bytes, rows_valid, cols_valid, p.out_stage_bytes == 0);
+  else
+    store_chunk_staged(stg, x, dtype, o, ld_bytes, rows_valid, cols_valid, p.out_stage_bytes == 0);
 }
 
 // Backward epilogue for one warp's 32 x 32 chunk: x (the pre-activation) comes
 // from C, dout is the accumulator; D = act'(x) * dout, PostAct = act(x).
+template <bool TR>
 __device__ __forceinline__ void epilogue_chunk_dact(const Params& p, const uint32_t (&acc)[32],
                                                     int32_t row_base, int32_t rows_valid,
                                                     int32_t col0, int32_t batch,
@@ -637,32 +752,29 @@ __device__ __forceinline__ void epilogue_chunk_dact(const Params& p, const uint3
   const int32_t cols_valid = min(32, p.N - col0);
   const int lane = threadIdx.x & 31;
   const char* crow = (p.c_dtype == DT_F32 && lane < rows_valid)
-                         ? c_ptr(p, row_base + lane, col0, batch) : nullptr;
+                         ? c_ptr<TR>(p, row_base + lane, col0, batch) : nullptr;
   float x[32], y[32];
-  c_values32(creg, p, crow, col0, x);
+  c_values32<TR>(creg, p, crow, col0, x);
   dact_chunk(p.act, x, acc, y);
-  store_chunk_staged(stg, y, p.d_dtype,
-                     out_ptr(p.d, p.ldd, p.sbd, p.d_dtype, row_base, col0, batch, p),
-                     p.ldd * dtype_bytes(p.d_dtype), rows_valid, cols_valid,
-                     p.out_stage_bytes == 0);
+  store_out<TR>(p, stg, y, p.d, p.ldd, p.sbd, p.d_dtype, row_base, rows_valid, col0, cols_valid,
+                batch);
   if (p.post != nullptr) {
 #pragma unroll
     for (int j = 0; j < 32; ++j) y[j] = x[j];
     act_chunk(p.act, y);
-    store_chunk_staged(stg, y, p.p_dtype,
-                       out_ptr(p.post, p.ldp, p.sbp, p.p_dtype, row_base, col0, batch, p),
-                       p.ldp * dtype_bytes(p.p_dtype), rows_valid, cols_valid,
-                     p.out_stage_bytes == 0);
+    store_out<TR>(p, stg, y, p.post, p.ldp, p.sbp, p.p_dtype, row_base, rows_valid, col0,
+                  cols_valid, batch);
   }
 }
 
 // One warp's 32 x 32 chunk: rows row_base .. +31 (lane = row), columns col0 .. +31.
-__device__ __forceinline__ void epilogue_chunk(const Params& p, const uint32_t (&acc)[32],
-                                               int32_t row_base, int32_t rows_valid,
-                                               int32_t col0, int32_t batch, float alpha,
-                                               float beta, const CRegs& creg, uint32_t stg) {
+template <bool TR>
+__device__ __forceinline__ void epilogue_chunk_t(const Params& p, const uint32_t (&acc)[32],
+                                                 int32_t row_base, int32_t rows_valid,
+                                                 int32_t col0, int32_t batch, float alpha,
+                                                 float beta, const CRegs& creg, uint32_t stg) {
   if (p.dact) {
-    epilogue_chunk_dact(p, acc, row_base, rows_valid, col0, batch, creg, stg);
+    epilogue_chunk_dact<TR>(p, acc, row_base, rows_valid, col0, batch, creg, stg);
     return;
   }
   const int32_t cols_valid = min(32, p.N - col0);
@@ -672,22 +784,20 @@ __device__ __forceinline__ void epilogue_chunk(const Params& p, const uint32_t (
   if (p.c != nullptr) {
     const int lane = threadIdx.x & 31;
     const char* crow = (p.c_dtype == DT_F32 && lane < rows_valid)
-                           ? c_ptr(p, row_base + lane, col0, batch) : nullptr;
-    add_beta_c(creg, p, crow, col0, beta, v);
+                           ? c_ptr<TR>(p, row_base + lane, col0, batch) : nullptr;
+    add_beta_c<TR>(creg, p, crow, col0, beta, v);
   }
   if (p.d != nullptr)
-    store_chunk_staged(stg, v, p.d_dtype,
-                       out_ptr(p.d, p.ldd, p.sbd, p.d_dtype, row_base, col0, batch, p),
-                       p.ldd * dtype_bytes(p.d_dtype), rows_valid, cols_valid,
-                     p.out_stage_bytes == 0);
+    store_out<TR>(p, stg, v, p.d, p.ldd, p.sbd, p.d_dtype, row_base, rows_valid, col0,
+                  cols_valid, batch);
   if (p.post != nullptr) {
     act_chunk(p.act, v);
-    store_chunk_staged(stg, v, p.p_dtype,
-                       out_ptr(p.post, p.ldp, p.sbp, p.p_dtype, row_base, col0, batch, p),
-                       p.ldp * dtype_bytes(p.p_dtype), rows_valid, cols_valid,
-                     p.out_stage_bytes == 0);
+    store_out<TR>(p, stg, v, p.post, p.ldp, p.sbp, p.p_dtype, row_base, rows_valid, col0,
+                  cols_valid, batch);
   }
 }
+
+
 
 // ------------------------------------------------------------------- roles
 // `unit` / `units`: this CTA's (pair's) index and the number of CTAs (pairs).
@@ -769,8 +879,9 @@ __device__ __forceinline__ void tail_sum(const Params& p, int32_t tail_r, uint32
 // (warp w reads lanes 32*(w%4) .. +31); warp w takes the 32-column chunks c
 // with c % 2 == w / 4, so two independent dependency chains per quadrant hide
 // the TMEM-load and memory latencies.  C for the next chunk is loaded one chunk ahead (the
-// first before the accumulator is ready).
-template <int BN, bool GATHER, int CG>
+// first before the accumulator is ready).  TR: swap_ab's transposed output layout
+// (a separate kernel instance, so that the usual one carries none of its code).
+template <int BN, bool GATHER, int CG, bool TR>
 __device__ __forceinline__ void epilogue_role(const Params& p, const Shared& sh,
                                               uint32_t tmem_base, int32_t num_tiles,
                                               uint32_t rank, const TileSched& ts,
@@ -802,7 +913,7 @@ __device__ __forceinline__ void epilogue_role(const Params& p, const Shared& sh,
     const bool has_c = p.c != nullptr && lane < rows_valid;
     CRegs cnext = {};
     if (!split && has_c && tc.n0 + half * 32 < p.N)
-      load_c_chunk(p, row, tc.n0 + half * 32, tc.batch, cnext);
+      load_c_chunk<TR>(p, row, tc.n0 + half * 32, tc.batch, cnext);
     // all lanes take the same branch: tcgen05.ld below is warp-collective
     const bool ok = wait_phase<CG == 2, true>(sh.tfull + 8 * acc, acc_phase, p, sh, 3, t);
     if (!__all_sync(0xffffffffu, ok)) break;
@@ -812,7 +923,7 @@ __device__ __forceinline__ void epilogue_role(const Params& p, const Shared& sh,
     for (int c = half; c < kChunks; c += kStride) {
       const CRegs ccur = cnext;
       if (!split && has_c && c + kStride < kChunks && tc.n0 + (c + kStride) * 32 < p.N)
-        load_c_chunk(p, row, tc.n0 + (c + kStride) * 32, tc.batch, cnext);
+        load_c_chunk<TR>(p, row, tc.n0 + (c + kStride) * 32, tc.batch, cnext);
       uint32_t v[32];
       __syncwarp();  // tcgen05.ld / wait::ld are warp-collective
       if (has_acc) {
@@ -836,7 +947,7 @@ __device__ __forceinline__ void epilogue_role(const Params& p, const Shared& sh,
       }
       const int32_t col0 = tc.n0 + c * 32;
       if (rows_valid > 0 && col0 < p.N)
-        epilogue_chunk(p, v, row_base, rows_valid, col0, tc.batch, alpha, beta, ccur, stg);
+        epilogue_chunk_t<TR>(p, v, row_base, rows_valid, col0, tc.batch, alpha, beta, ccur, stg);
     }
     bool finished = !split;
     if (split) {
@@ -845,17 +956,17 @@ __device__ __forceinline__ void epilogue_role(const Params& p, const Shared& sh,
       if (tail_ticket(ticket, p.tail_splits)) {
         // this warp's slice came last: add up the tile's slices and run the epilogue
         finished = true;
-        if (has_c && tc.n0 + half * 32 < p.N) load_c_chunk(p, row, tc.n0 + half * 32, tc.batch, cnext);
+        if (has_c && tc.n0 + half * 32 < p.N) load_c_chunk<TR>(p, row, tc.n0 + half * 32, tc.batch, cnext);
 #pragma unroll 1
         for (int c = half; c < kChunks; c += kStride) {
           const CRegs ccur = cnext;
           if (has_c && c + kStride < kChunks && tc.n0 + (c + kStride) * 32 < p.N)
-            load_c_chunk(p, row, tc.n0 + (c + kStride) * 32, tc.batch, cnext);
+            load_c_chunk<TR>(p, row, tc.n0 + (c + kStride) * 32, tc.batch, cnext);
           uint32_t v[32];
           tail_sum<BN, GATHER, CG>(p, tail_r, rank, quad, c, lane, v);
           const int32_t col0 = tc.n0 + c * 32;
           if (rows_valid > 0 && col0 < p.N)
-            epilogue_chunk(p, v, row_base, rows_valid, col0, tc.batch, alpha, beta, ccur, stg);
+            epilogue_chunk_t<TR>(p, v, row_base, rows_valid, col0, tc.batch, alpha, beta, ccur, stg);
         }
       }
     }
@@ -896,14 +1007,16 @@ __device__ __forceinline__ void mma_loop(const Params& p, const Shared& sh, uint
     const KRange kr = (p.k_groups > 0 || p.tail_tiles > 0)
                           ? k_range(p, sh, tile_coord<BN, Cfg::kTileM>(t, p, sh).batch, t)
                           : KRange{0, p.K, p.k_tiles, false};
+    const bool rev = !GATHER && k_reversed(p, t, ts.units);
     for (int kt = 0; kt < kr.tiles; ++kt) {
+      const int32_t kte = rev ? kr.tiles - 1 - kt : kt;  // the k-tile this stage holds
       ok = wait_phase<CG == 2>(sh.full + 8 * stage, phase, p, sh, 1, t);
       if (!__all_sync(0xffffffffu, ok)) return;
       ptx::tc_fence_after();
       if (GATHER) ptx::fence_proxy_async_smem();  // cp.async (generic proxy) writes -> MMA reads
       const uint32_t a_addr = a0 + stage * Cfg::kABytes;
       const uint32_t b_addr = b0 + stage * Cfg::kBBytes;
-      const int32_t nk = (kt == kr.tiles - 1) ? ksteps_of(p, kr, kt) : 4;
+      const int32_t nk = (kte == kr.tiles - 1) ? ksteps_of(p, kr, kte) : 4;
       if (ptx::elect_one()) {
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {  // up to 4 MMAs of 32 bytes of K each
@@ -1010,6 +1123,7 @@ __device__ __forceinline__ void tma_producer_role(const Params& p, const Shared&
     const KRange kr = k_range(p, sh, tc.batch, t);
     const int32_t row0 = tc.m_row0 + static_cast<int32_t>(rank) * kBM;
     const int32_t bn0 = tc.n0 + static_cast<int32_t>(rank) * Cfg::kBRows;
+    const bool rev = k_reversed(p, t, ts.units);
     for (int kt = 0; kt < kr.tiles; ++kt) {
       const bool ok = wait_phase<CG == 2>(sh.empty + 8 * stage, phase ^ 1u, p, sh, 0, t);
       if (!__all_sync(0xffffffffu, ok)) return;
@@ -1043,7 +1157,7 @@ __device__ __forceinline__ void tma_producer_role(const Params& p, const Shared&
         mB = kr.ragged ? reinterpret_cast<const CUtensorMap*>(map_cur + 128) : tmB;
       }
       const uint32_t full = sh.full + 8 * stage;
-      const int32_t k0 = kr.k0 + kt * p.bk;
+      const int32_t k0 = kr.k0 + (rev ? kr.tiles - 1 - kt : kt) * p.bk;
       const uint32_t adst = a0 + stage * Cfg::kABytes;
       const uint32_t bdst = b0 + stage * Cfg::kBBytes;
       if (ptx::elect_one()) {
@@ -1402,7 +1516,7 @@ __device__ __forceinline__ void relay_role(const Params& p, const Shared& sh, in
 
 // ------------------------------------------------------------------ kernel
 
-template <int BN, bool GATHER, int CG>
+template <int BN, bool GATHER, int CG, bool TR = false>
 __global__ void __launch_bounds__(KernelCfg<BN, GATHER, CG>::kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ Params p) {
@@ -1557,7 +1671,7 @@ __global__ void __launch_bounds__(KernelCfg<BN, GATHER, CG>::kThreads, 1)
   const int32_t num_tiles = (p.num_groups > 0) ? prefix[p.num_groups] : p.num_tiles;
 
   if (warp < Cfg::kEpiWarps) {
-    epilogue_role<BN, GATHER, CG>(p, sh, tmem_base, num_tiles, rank, ts,
+    epilogue_role<BN, GATHER, CG, TR>(p, sh, tmem_base, num_tiles, rank, ts,
                                   out_stage + warp * p.out_stage_bytes);
   } else if (warp == Cfg::kMmaWarp) {
     if (rank == 0) mma_role<BN, GATHER, CG>(p, sh, a0, b0, tmem_base, num_tiles, ts);

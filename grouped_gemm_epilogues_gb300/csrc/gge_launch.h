@@ -16,7 +16,8 @@ struct LaunchShape {
   int cluster;  // CTAs per cluster: 1, or 2 (a CTA pair)
 };
 
-template <int BN, bool GATHER, int CG>
+// TR: the swap_ab instance, whose epilogue stores C / D / PostAct transposed.
+template <int BN, bool GATHER, int CG, bool TR = false>
 cudaError_t launch_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const Params& p,
                         const LaunchShape& shape, cudaStream_t stream);
 

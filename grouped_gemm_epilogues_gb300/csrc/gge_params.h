@@ -27,6 +27,8 @@ enum : int32_t {
   FLAG_RASTER_N = 128,         // raster bands of n-tiles (n varies fastest in a band)
   FLAG_CLC_SCHED = 256,        // one cluster per tile; running clusters take over the tiles
                                // of clusters not yet launched (cluster launch control)
+  FLAG_SWAP_AB = 512,          // compute D^T = B A^T (the kernel's rows are the caller's N)
+  FLAG_K_SERPENTINE = 1024,    // odd waves walk K backwards (L2 reuse across waves)
   FLAG_RESERVED = 16 | 64,     // reserved bits: a call that sets one is rejected
 };
 
@@ -80,6 +82,7 @@ struct Params {
   int32_t d_dtype, p_dtype, c_dtype;
   int32_t act;
   int32_t dact;  // backward epilogue: C is the pre-activation x, D = act'(x) * acc, PostAct = act(x)
+  int32_t out_trans;  // swap_ab: C / D / PostAct hold the kernel's element (row, col) at [col][row]
   int32_t out_stage_bytes;  // shared-memory staging per epilogue warp: 32 x 32 outputs (2 or
                             // 4 KiB); 0: each lane stores its own row directly
   float alpha, beta;

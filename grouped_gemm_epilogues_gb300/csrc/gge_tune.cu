@@ -23,7 +23,7 @@
 
 namespace {
 
-constexpr int kMaxCandidates = 48;
+constexpr int kMaxCandidates = 64;
 
 bool plain_op(int32_t op) { return op == GGE_OP_GEMM || op == GGE_OP_DACT; }
 // CTA pairs: every form but gather-K; with gathered A rows, 256-wide tiles only
@@ -38,29 +38,43 @@ int32_t enumerate(const gge_gemm_args* args, int32_t op, int32_t num_groups, gge
   if (args == nullptr) return 0;
   gge_config base{};
   if (args->config != nullptr) base = *args->config;
+  base.flags &= ~gge::FLAG_SWAP_AB;
+  const gge_tensor* o = args->D ? args->D : args->PostAct;
+  const int64_t out_m = o ? o->rows : 0, out_n = o ? o->cols : 0;
   struct Shape { int cg, tile_n; };
-  static const Shape kShapes[] = {{2, 256}, {2, 224}, {2, 192}, {2, 160}, {1, 256}, {1, 128}};
+  static const Shape kShapes[] = {{2, 256}, {2, 224}, {2, 192}, {2, 160}, {1, 256}, {1, 128},
+                                  {1, 64}};
   struct Raster { int band; bool along_n; };
   static const Raster kRasters[] = {{0, false}, {8, false}, {0, true}};
   const int n_rasters = plain_op(op) ? 3 : 1;
+  // swap_ab (the pages' GemmConfig.swap_ab) is searched for plain problems whose M
+  // is small next to N: the swapped problem's tile width covers the small M
+  const bool try_swap = plain_op(op) && out_m > 0 && out_m <= 256 && out_m < out_n;
   int32_t n = 0;
-  for (const Shape& sh : kShapes) {
-    if (sh.cg == 2 && !pair_shape_ok(op, sh.tile_n)) continue;
-    for (int b = 0; b < n_rasters; ++b) {
-      for (int direct = 0; direct < 2; ++direct) {
-        gge_config c = base;
-        c.cta_group = sh.cg;
-        c.tile_n = sh.tile_n;
-        c.raster_band = kRasters[b].band;
-        int32_t f = direct ? (base.flags | gge::FLAG_DIRECT_STORES)
-                           : (base.flags & ~gge::FLAG_DIRECT_STORES);
-        if (n_rasters > 1) f = kRasters[b].along_n ? (f | gge::FLAG_RASTER_N) : (f & ~gge::FLAG_RASTER_N);
-        c.flags = f;
-        gge_gemm_args a = *args;
-        a.config = &c;
-        if (gge::validate_op(&a, op, num_groups) != GGE_OK) continue;
-        if (n < max && out != nullptr) out[n] = c;
-        ++n;
+  for (int swap = 0; swap < (try_swap ? 2 : 1); ++swap) {
+    const int64_t width = swap ? out_m : out_n;  // the kernel's N
+    for (const Shape& sh : kShapes) {
+      if (sh.cg == 2 && !pair_shape_ok(op, sh.tile_n)) continue;
+      if (sh.tile_n == 64 && width > 128) continue;  // 64-wide tiles only for narrow outputs
+      // swapped candidates: the automatic raster and staged stores only
+      for (int b = 0; b < (swap ? 1 : n_rasters); ++b) {
+        for (int direct = 0; direct < (swap ? 1 : 2); ++direct) {
+          gge_config c = base;
+          c.cta_group = sh.cg;
+          c.tile_n = sh.tile_n;
+          c.raster_band = kRasters[b].band;
+          int32_t f = direct ? (base.flags | gge::FLAG_DIRECT_STORES)
+                             : (base.flags & ~gge::FLAG_DIRECT_STORES);
+          if (n_rasters > 1)
+            f = kRasters[b].along_n ? (f | gge::FLAG_RASTER_N) : (f & ~gge::FLAG_RASTER_N);
+          if (swap) f |= gge::FLAG_SWAP_AB;
+          c.flags = f;
+          gge_gemm_args a = *args;
+          a.config = &c;
+          if (gge::validate_op(&a, op, num_groups) != GGE_OK) continue;
+          if (n < max && out != nullptr) out[n] = c;
+          ++n;
+        }
       }
     }
   }

@@ -87,9 +87,9 @@ typedef struct gge_tensor {
 
 /* Optional tuning / debug knobs; pass NULL for the defaults. */
 typedef struct gge_config {
-  int32_t tile_n;         /* 0 = auto; else output columns per tile: 128 or 256 on
-                             one CTA, 256, 224, 192 or 160 on a CTA pair (the
-                             narrower pair tiles need a K-major B)                 */
+  int32_t tile_n;         /* 0 = auto; else output columns per tile: 64 (TMA forms),
+                             128 or 256 on one CTA, 256, 224, 192 or 160 on a
+                             CTA pair (the narrower pair tiles need a K-major B) */
   int32_t num_ctas;       /* 0 = one persistent CTA per SM                         */
   int32_t raster_band;    /* 0 = auto; tiles per raster band (plain problems): auto
                              takes the width that keeps a wave's A and B rows
@@ -129,7 +129,20 @@ typedef struct gge_config {
                              the tiles of those not launched yet
                              (clusterlaunchcontrol.try_cancel) instead of a
                              fixed stride; no workspace needed; not with bit 2;
-                             the last wave is not split.                       */
+                             the last wave is not split;
+                             bit 9: swap_ab -- compute D^T = B A^T: the kernel's
+                             tiles run over the caller's N (rows) and M
+                             (columns) and the epilogue stores C / D / PostAct
+                             transposed into the caller's N-major [M, N]
+                             layout (plain problems: gge_gemm, gge_gemm_act,
+                             gge_gemm_dact).  For small M, so that M becomes the
+                             tile width (64-wide one-CTA tiles exist for this);
+                             bit 10: serpentine K -- work items of odd waves
+                             (item index / resident units) walk K backwards, so
+                             each wave starts on the k-slices the previous one
+                             read last, still in L2 (plain and varlen-M forms
+                             with TMA-loaded A; reproducible, the direction is
+                             fixed by the plan).                               */
   int32_t cta_group;      /* 0 = auto; 1 = one CTA per 128-row tile; 2 = a CTA pair
                              per 256-row tile (tcgen05 cta_group::2; with gather-A
                              256-column tiles only; not with gather-K)           */

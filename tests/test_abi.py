@@ -106,6 +106,35 @@ def test_clc_plan(L):
         binding.gge_plan(A, B, D=D, config=binding.make_config(flags=256 | 4, **base))
 
 
+def test_swap_ab_plan(L):
+    """swap_ab plans the transposed problem on one-CTA tiles (the caller's small M
+    as the tile width) and refuses the forms it does not cover."""
+    A = torch.zeros(64, 4096, dtype=torch.bfloat16)
+    B = torch.zeros(8192, 4096, dtype=torch.bfloat16)
+    D = torch.zeros(64, 8192, dtype=torch.bfloat16)
+    info = binding.gge_plan(A, B, D=D, config=binding.make_config(flags=512, num_ctas=152))
+    assert (info["tile_m"], info["tile_n"], info["cta_group"]) == (128, 64, 1)
+    assert info["num_tiles"] == 64                      # 8192 / 128 kernel rows, one 64-wide column
+    with pytest.raises(binding.GgeError):               # no CTA pairs under swap_ab
+        binding.gge_plan(A, B, D=D, config=binding.make_config(flags=512, cta_group=2))
+    Bg = torch.zeros(4, 8192, 4096, dtype=torch.bfloat16)
+    with pytest.raises(binding.GgeError):               # plain problems only
+        binding.gge_plan(A, Bg, D=D, num_groups=4, config=binding.make_config(flags=512))
+    # the caller's N must still be a multiple of 8 (whole 16-byte output pieces)
+    with pytest.raises(binding.GgeError):
+        binding.gge_plan(A, torch.zeros(8190, 4096, dtype=torch.bfloat16),
+                         D=torch.zeros(64, 8190, dtype=torch.bfloat16),
+                         config=binding.make_config(flags=512))
+    c = binding.gge_tune_candidates("gemm", A, B, D=D)
+    swapped = [x for x in c if x["flags"] & 512]
+    assert swapped and all(x["cta_group"] == 1 for x in swapped)
+    assert {x["tile_n"] for x in swapped} == {64, 128, 256}
+    # large M: no swapped candidates
+    A2 = torch.zeros(4096, 4096, dtype=torch.bfloat16)
+    assert not [x for x in binding.gge_tune_candidates("gemm", A2, B, D=torch.zeros(
+        4096, 8192, dtype=torch.bfloat16)) if x["flags"] & 512]
+
+
 def test_auto_raster_band(L):
     """The automatic band keeps a wave's operand rows fewest: sqrt(units * tile_n /
     tile_m) m-tiles (76 pairs of 256 x 256 tiles: 9)."""

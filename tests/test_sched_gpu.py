@@ -109,3 +109,27 @@ def test_clc_varlen_k():
     assert binding.gge_read_device_status()[0] == "GGE_OK"
     r = og.gemm_varlen_k(dec(A), dec(B), np.asarray(cu), None, d_fmt=FMT_NAME["bf16"])
     check(dec(D.cpu()), r["D"], r["bound"], FMT_NAME["bf16"], "none", "varlen-K with CLC")
+
+
+FLAG_K_SERPENTINE = 1024
+
+
+@pytest.mark.parametrize("cta_group,num_ctas", [(1, 6), (2, 8)])
+def test_k_serpentine_parity(cta_group, num_ctas):
+    """Serpentine K: odd waves walk K backwards (a partial last k-tile first),
+    several waves on a few CTAs, with and without the split tail; then varlen-M."""
+    w = wl.small("gemm_act_4096_bf16_gelu", 1000, 776, 1000, 2)   # K % 64 != 0
+    t = wl.make(w)
+    for extra in (0, 32):
+        out = _outputs(w, 1000, 776, 2)
+        cfg = binding.make_config(flags=FLAG_K_SERPENTINE | extra, num_ctas=num_ctas,
+                                  cta_group=cta_group, tile_n=256)
+        _run_plain(w, t, out, config=cfg)
+        _check_plain(w, t, out)
+    wv = wl.small("varlen_gather_g64_m32768_silu", 1500, 520, 200, groups=9, empty_groups=3,
+                  gather_rows=0)
+    tv = wl.make(wv)
+    out = _run(wv, tv, False, config=binding.make_config(flags=FLAG_K_SERPENTINE,
+                                                         num_ctas=num_ctas, cta_group=cta_group))
+    _check(wv, tv, out, _oracle(wv, tv, False))
+    assert binding.gge_read_device_status()[0] == "GGE_OK"
