@@ -69,3 +69,23 @@ def full_varlen(w, t, out, gather, block_rows=2048):
                                                 FMT_NAME[w.p_dtype], w.act, what + " PostAct",
                                                 x=ref["v"]))
     return worst
+
+
+def full_varlen_k(w, t, D, gather):
+    """Varlen-K (optionally gather-K) problem, group by group: every element of
+    D[g] against the oracle of that group's K columns.  D: (G, M, N)."""
+    cu = t["cu_seqlens_k"].numpy()
+    got = D.cpu()
+    worst = 0.0
+    for g in range(len(cu) - 1):
+        lo, hi = int(cu[g]), int(cu[g + 1])
+        if gather:   # column k of the effective A is column a_idx[k] of the source [M, K_src]
+            cols = t["a_idx"][lo:hi].long()
+            A = dec(t["A"].t()[cols]).T                   # [M, K_g]
+        else:
+            A = dec(t["A"][:, lo:hi])                     # [M, K_g]
+        B = dec(t["B"][:, lo:hi])                         # [N, K_g]
+        ref = og.gemm(A[None], B[None], None, alpha=w.alpha, d_fmt=FMT_NAME[w.d_dtype])
+        worst = max(worst, check(got[g:g + 1], ref["D"], ref["bound"], FMT_NAME[w.d_dtype],
+                                 "none", f"{w.name} group {g}"))
+    return worst

@@ -203,3 +203,4 @@ def test_varlen_full_size_every_element(gather):
     worst = full_varlen(w, t, out, gather)
     print(f"{w.name} gather={gather}: worst error / tolerance {worst}")
     assert worst and max(worst.values()) <= 1.0
+
