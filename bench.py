@@ -368,10 +368,58 @@ def _shape_note(tuned, args):
     return dict(tuned, source="autotuned" if not args.no_tune else "command line")
 
 
+def algorithmic_bytes(w, base):
+    """Fewest HBM bytes one call must move: every operand read once and every
+    output written once (varlen gather: the gathered rows, the B of each
+    non-empty group and the indices)."""
+    def nbytes(t):
+        return t.numel() * t.element_size()
+    out_el = (w.k_groups or 1) * w.M * w.N if w.k_groups else (w.M * w.N * (1 if w.groups else w.L))
+    out = sum(out_el * wl.DT[d].itemsize for d in (w.d_dtype, w.p_dtype) if d)
+    c = nbytes(base["C"]) if "C" in base else 0
+    if w.groups:
+        cu = base["cu_seqlens_m"].numpy()
+        live = int((np.diff(cu) > 0).sum())
+        b = nbytes(base["B"]) * live // w.groups
+        a = w.M * w.K * base["A"].element_size()
+        idx = nbytes(base["a_idx"]) if "a_idx" in base else 0
+        return a + b + c + out + idx
+    if w.k_groups and w.gather_rows:
+        return w.K * w.M * base["A"].element_size() + nbytes(base["B"]) + c + out
+    return nbytes(base["A"]) + nbytes(base["B"]) + c + out
+
+
+def cublas_comparator(w, dev, steps=50):
+    """torch.matmul (cuBLAS) on the same 16-bit plain problem, the product alone
+    (no epilogue), as a context column; None for the other forms."""
+    if w.groups or w.k_groups or w.ab_dtype not in ("bf16", "f16"):
+        return None
+    dt = wl.DT[w.ab_dtype]
+    n_sets = 3
+    As = [torch.randn(w.L, w.M, w.K, device=dev).to(dt) for _ in range(n_sets)]
+    Bs = [torch.randn(w.L, w.K, w.N, device=dev).to(dt) for _ in range(n_sets)]
+    for i in range(3):
+        torch.matmul(As[i % n_sets], Bs[i % n_sets])
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(steps):
+        torch.matmul(As[i % n_sets], Bs[i % n_sets])
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    del As, Bs
+    torch.cuda.empty_cache()
+    return {"value": round(w.flops / (ms * 1e-3) / 1e12, 1), "unit": "TFLOP/s",
+            "ms_per_step": round(ms, 5), "what": "torch.matmul of the same shape and dtype, "
+            "no epilogue (context only, not on the product path)"}
+
+
 def measure_config(args, w, dev, binding, local, peaks, src):
     """One per-config line: autotuned shape, warm-up, then at least ~0.3 s of
     timed launches (at least --steps) with the clocks sampled meanwhile."""
-    _, sets, tuned, step, l2 = _prepare(w, dev, binding, not args.no_tune)
+    base, sets, tuned, step, l2 = _prepare(w, dev, binding, not args.no_tune)
     stream = torch.cuda.current_stream(dev)
     for i in range(max(args.warmup, len(sets))):
         step(sets[i % len(sets)])
@@ -392,14 +440,20 @@ def measure_config(args, w, dev, binding, local, peaks, src):
     ms_per_step = ms / steps
     tflops = w.flops / (ms_per_step * 1e-3) / 1e12
     peak, peak_src = _peak_for(w, peaks, src)
+    alg = algorithmic_bytes(w, base)
+    hbm = alg / (ms_per_step * 1e-3) / 1e9
+    hbm_peak = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
     out = {"workload": w.name, "value": round(tflops, 1), "unit": "TFLOP/s",
            "ms_per_step": round(ms_per_step, 5), "steps": steps,
            "frac": round(tflops / peak, 4), "peak": peak, "peak_source": peak_src,
            "frac_of_nominal_dense_peak": round(tflops / NOMINAL_PEAK[w.ab_dtype], 4),
+           "hbm": {"algorithmic_bytes": int(alg), "achieved_gbs": round(hbm, 1),
+                   "peak_gbs": hbm_peak, "frac": round(hbm / hbm_peak, 4)},
            "traffic": profiled_traffic(w.name), "l2": l2, "clocks": clocks,
            "launch_shape": _shape_note(tuned, args)}
     del sets
     torch.cuda.empty_cache()
+    out["cublas"] = cublas_comparator(w, dev)
     return out
 
 
@@ -444,6 +498,7 @@ def run_ours(args, w):
 
     # end-to-end through the public API with host buffers
     e2e = run_e2e(args, w, base, dev, step)
+    alg = algorithmic_bytes(w, base)
 
     peaks, src = measured_peaks()
     peak, peak_src = _peak_for(w, peaks, src)
@@ -471,12 +526,16 @@ def run_ours(args, w):
                    "launch": "eager" if args.eager else "cuda_graph",
                    "launch_shape": _shape_note(tuned, args)},
         "roofline": roofline,
+        "hbm": {"algorithmic_bytes": int(alg),
+                "achieved_gbs": round(alg / (ms_per_step * 1e-3) / 1e9, 1)},
         "e2e": e2e,
         "gpu_launches": args.steps,
         "clocks": clocks,
     }
     del sets
     torch.cuda.empty_cache()
+    if ws_n == 1:
+        line["cublas"] = cublas_comparator(w, dev)
     if rank == 0 and ws_n == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, base, budget_s=args.cpu_seconds)
     if ws_n == 1 and not args.no_per_config:
