@@ -389,31 +389,56 @@ def algorithmic_bytes(w, base):
     return nbytes(base["A"]) + nbytes(base["B"]) + c + out
 
 
-def cublas_comparator(w, dev, steps=50):
+def cublas_comparator(w, dev, local, steps):
     """torch.matmul (cuBLAS) on the same 16-bit plain problem, the product alone
-    (no epilogue), as a context column; None for the other forms."""
+    (no epilogue), as a context column, timed like our own runs: rotating input
+    sets larger than L2, 0.5 s of untimed load first, then at least `steps`
+    launches and ~0.3 s, clocks sampled meanwhile.  None for the other forms."""
     if w.groups or w.k_groups or w.ab_dtype not in ("bf16", "f16"):
         return None
     dt = wl.DT[w.ab_dtype]
-    n_sets = 3
+    per_set = 2 * (w.L * w.M * w.K + w.L * w.K * w.N + w.L * w.M * w.N)
+    n_sets = min(8, max(2, int(np.ceil(2.5 * L2_BYTES / per_set)) + 1))
     As = [torch.randn(w.L, w.M, w.K, device=dev).to(dt) for _ in range(n_sets)]
     Bs = [torch.randn(w.L, w.K, w.N, device=dev).to(dt) for _ in range(n_sets)]
+    Ds = [torch.empty(w.L, w.M, w.N, device=dev, dtype=dt) for _ in range(n_sets)]
+
+    def step(i):
+        torch.matmul(As[i % n_sets], Bs[i % n_sets], out=Ds[i % n_sets])
+
     for i in range(3):
-        torch.matmul(As[i % n_sets], Bs[i % n_sets])
+        step(i)
     torch.cuda.synchronize()
+    sampler = ClockSampler(local)
+    sampler.start()
+    t_end, i = time.time() + 0.5, 0
+    while time.time() < t_end:
+        for _ in range(20):
+            step(i)
+            i += 1
+        torch.cuda.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record()
-    for i in range(steps):
-        torch.matmul(As[i % n_sets], Bs[i % n_sets])
+    for j in range(n_sets):
+        step(j)
     e1.record()
     torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1) / steps
-    del As, Bs
+    est = e0.elapsed_time(e1) / n_sets
+    n = max(steps, int(np.ceil(300.0 / max(est, 1e-3))))
+    e0.record()
+    for j in range(n):
+        step(j)
+    e1.record()
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    ms = e0.elapsed_time(e1) / n
+    del As, Bs, Ds
     torch.cuda.empty_cache()
     return {"value": round(w.flops / (ms * 1e-3) / 1e12, 1), "unit": "TFLOP/s",
-            "ms_per_step": round(ms, 5), "what": "torch.matmul of the same shape and dtype, "
-            "no epilogue (context only, not on the product path)"}
+            "ms_per_step": round(ms, 5), "steps": n, "clocks": clocks,
+            "what": "torch.matmul of the same shape and dtype, no epilogue, timed like this "
+                    "line (context only, not on the product path)"}
 
 
 def measure_config(args, w, dev, binding, local, peaks, src):
@@ -453,7 +478,7 @@ def measure_config(args, w, dev, binding, local, peaks, src):
            "launch_shape": _shape_note(tuned, args)}
     del sets
     torch.cuda.empty_cache()
-    out["cublas"] = cublas_comparator(w, dev)
+    out["cublas"] = cublas_comparator(w, dev, local, args.steps)
     return out
 
 
@@ -535,7 +560,7 @@ def run_ours(args, w):
     del sets
     torch.cuda.empty_cache()
     if ws_n == 1:
-        line["cublas"] = cublas_comparator(w, dev)
+        line["cublas"] = cublas_comparator(w, dev, local, args.steps)
     if rank == 0 and ws_n == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, base, budget_s=args.cpu_seconds)
     if ws_n == 1 and not args.no_per_config:

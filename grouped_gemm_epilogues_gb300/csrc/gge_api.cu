@@ -30,7 +30,7 @@ constexpr int kEpiWarpsHost = 8;          // epilogue warps of the TMA variants 
 constexpr int kMaxGroupsHost = 1024;
 constexpr int kIdxChunkHost = 2048;       // gather-K index entries staged in shared memory
 constexpr size_t kWorkspaceBytes = 256;
-// the split last wave's tickets (one int32 per tail tile, CTA and epilogue warp)
+// the split last wave's tickets (one int32 per tail tile, CTA, epilogue warp and chunk)
 // follow the status words in a region of their own: no other call writes there,
 // so a ticket is never mistaken for another call's data
 constexpr size_t kTicketBytes = 16384;
@@ -138,8 +138,10 @@ size_t tail_workspace(const Plan& pl) {
   const int64_t blocks = static_cast<int64_t>(pl.p.tail_tiles) * pl.p.tail_splits * pl.cg;
   return kTailBase + static_cast<size_t>(blocks) * kTileM * pl.bn * sizeof(float);
 }
+constexpr size_t kTicketsPerWarpHost = 4;  // one per epilogue warp and 32-column chunk
 bool tickets_fit(const Plan& pl) {
-  return static_cast<size_t>(pl.p.tail_tiles) * pl.cg * kEpiWarpsHost * 4 <= kTicketBytes;
+  return static_cast<size_t>(pl.p.tail_tiles) * pl.cg * kEpiWarpsHost * kTicketsPerWarpHost * 4 <=
+         kTicketBytes;
 }
 
 CUtensorMapDataType tmap_type(int es) {

@@ -79,6 +79,7 @@ constexpr int kClcBar = 768;       // cluster launch control: its barrier and (a
                                    // 16-byte response
 constexpr int kRelayWord = 800;    // gathering pair: the word the peer's relay stores into
 constexpr int kSchedDepth = 4;     // tile indices in flight between the fetching warp and the rest
+constexpr int kTicketsPerWarp = 4; // split tail: one ticket per epilogue warp and 32-column chunk
 constexpr int kMapSlots = 16;      // varlen-K: tensor-map copies per CTA (> pipeline stages)
 constexpr int kMapSlotBytes = 256; // one A and one B tensor map
 // barriers for up to 8 stages, the TMEM slot, the abort flag and the tile ring
@@ -109,6 +110,8 @@ struct KernelCfg {
   static_assert(BN % 32 == 0 && BN >= 64 && BN <= 256, "BN: a multiple of 32 in [64, 256]");
   static_assert(kBRows % 8 == 0, "B rows per CTA must fill 8-row swizzle atoms");
   static_assert(CG == 1 || CG == 2, "one CTA or a CTA pair");
+  static_assert(GATHER || (BN / 32 + kEpiWarps / 4 - 1) / (kEpiWarps / 4) <= kTicketsPerWarp,
+                "split-tail tickets: one per epilogue warp and chunk (the gather forms never split)");
 };
 
 // Shared-memory matrix descriptor for a K-major (or N-major) operand staged
@@ -803,12 +806,14 @@ __device__ __forceinline__ void epilogue_chunk_t(const Params& p, const uint32_t
 // `unit` / `units`: this CTA's (pair's) index and the number of CTAs (pairs).
 
 // Split last wave, one epilogue warp's share of a tail tile (its 32 rows of the
-// CTA's 128, its 32-column chunks): every slice's unit writes its raw fp32
-// accumulator chunks to the workspace and then takes a ticket; the warp that
-// takes the last ticket adds all slices' chunks in slice order (so the sum
-// does not depend on which unit finished last) and runs the epilogue.  No
-// warp waits for another unit, so the result does not depend on when (or in
-// what order) the units run.  Partial chunk layout: float4 q of a lane's row in
+// CTA's 128, its 32-column chunks): every slice's unit writes each raw fp32
+// accumulator chunk to the workspace and then takes that chunk's ticket; the
+// warp that takes a chunk's last ticket adds all slices' copies of it in slice
+// order (so the sum does not depend on which unit came last) and runs its
+// epilogue.  The slices walk their chunks in rotated orders, so different
+// units come last for different chunks and share the final epilogue.  No warp
+// waits for another unit, so the result does not depend on when (or in what
+// order) the units run.  Partial chunk layout: float4 q of a lane's row in
 // chunk c at [quad][c][q][lane], so each warp store / load moves 512
 // contiguous bytes.
 template <int BN, bool GATHER, int CG>
@@ -828,10 +833,10 @@ __device__ __forceinline__ void tail_store(float4* dst, const uint32_t (&v)[32])
                               __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
 }
 
-// After the warp's partial chunks are written: count this slice in the tile's
-// ticket (per CTA and epilogue warp).  True (in every lane) for the warp whose
-// slice came last, which then owns the tile's outputs; it resets the ticket
-// for the next launch.  The fence before the count publishes every lane's
+// After the warp's partial chunk is written: count this slice in the chunk's
+// ticket (per CTA, epilogue warp and chunk).  True (in every lane) for the warp
+// whose slice came last, which then owns the chunk's outputs; it resets the
+// ticket for the next launch.  The fence before the count publishes every lane's
 // partial stores; the one after it orders the reads of the other slices'.
 __device__ __forceinline__ bool tail_ticket(int32_t* ticket, int32_t splits) {
   __threadfence();
@@ -919,8 +924,21 @@ __device__ __forceinline__ void epilogue_role(const Params& p, const Shared& sh,
     if (!__all_sync(0xffffffffu, ok)) break;
     ptx::tc_fence_after();
     const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + acc * BN;
+    // this warp's chunks are half, half + kStride, ...; a split item's slice s walks
+    // them rotated by s * n / S, so that the S slices of a tile finish different
+    // chunks last and share the tile's final epilogue between their units
+    constexpr int kMine = (kChunks + kStride - 1) / kStride;
+    const int shift = split ? static_cast<int>((slice * kMine) / p.tail_splits) : 0;
+    // the last iteration that reads TMEM (a warp of a quadrant with one chunk fewer
+    // skips one index, which is the last only without rotation)
+    const int last_ci = (kMine - 1 + shift) % kMine;
+    const int last_i = (half + last_ci * kStride >= kChunks) ? kMine - 2 : kMine - 1;
+    bool finished = !split;
 #pragma unroll 1
-    for (int c = half; c < kChunks; c += kStride) {
+    for (int i = 0; i < kMine; ++i) {
+      const int ci = (i + shift < kMine) ? i + shift : i + shift - kMine;
+      const int c = half + ci * kStride;
+      if (c >= kChunks) continue;  // (kChunks odd: the second warp of a quadrant has one fewer)
       const CRegs ccur = cnext;
       if (!split && has_c && c + kStride < kChunks && tc.n0 + (c + kStride) * 32 < p.N)
         load_c_chunk<TR>(p, row, tc.n0 + (c + kStride) * 32, tc.batch, cnext);
@@ -933,7 +951,8 @@ __device__ __forceinline__ void epilogue_role(const Params& p, const Shared& sh,
 #pragma unroll
         for (int j = 0; j < 32; ++j) v[j] = 0u;
       }
-      if (c + kStride >= kChunks) {  // this warp's last chunk: hand its share of the buffer back
+      if (i == last_i) {
+        // this warp's last TMEM read of the tile: hand its share of the buffer back
         ptx::tc_fence_before();
         __syncwarp();
         if (lane == 0) {
@@ -941,34 +960,27 @@ __device__ __forceinline__ void epilogue_role(const Params& p, const Shared& sh,
           else ptx::mbar_arrive_remote(ptx::mapa(sh.tempty + 8 * acc, 0));
         }
       }
-      if (split) {  // the slice's raw accumulator chunk: this lane's 32 values
+      const int32_t col0 = tc.n0 + c * 32;
+      if (split) {
+        // the slice's raw accumulator chunk (this lane's 32 values), then its ticket;
+        // the warp whose slice comes last for this chunk adds all slices and stores it
         tail_store(tail_chunk<BN, GATHER, CG>(p, tail_r, slice, rank, quad, c, lane), v);
+        int32_t* ticket = p.tail_tickets +
+                          ((static_cast<int64_t>(tail_r) * CG + rank) * Cfg::kEpiWarps + warp) *
+                              kTicketsPerWarp + ci;
+        if (tail_ticket(ticket, p.tail_splits)) {
+          if (ci == 0) finished = true;
+          // (a split item prefetches no C: cnext is free for this chunk's C)
+          if (has_c && col0 < p.N) load_c_chunk<TR>(p, row, col0, tc.batch, cnext);
+          tail_sum<BN, GATHER, CG>(p, tail_r, rank, quad, c, lane, v);
+          if (rows_valid > 0 && col0 < p.N)
+            epilogue_chunk_t<TR>(p, v, row_base, rows_valid, col0, tc.batch, alpha, beta, cnext,
+                                 stg);
+        }
         continue;
       }
-      const int32_t col0 = tc.n0 + c * 32;
       if (rows_valid > 0 && col0 < p.N)
         epilogue_chunk_t<TR>(p, v, row_base, rows_valid, col0, tc.batch, alpha, beta, ccur, stg);
-    }
-    bool finished = !split;
-    if (split) {
-      int32_t* ticket =
-          p.tail_tickets + (static_cast<int64_t>(tail_r) * CG + rank) * Cfg::kEpiWarps + warp;
-      if (tail_ticket(ticket, p.tail_splits)) {
-        // this warp's slice came last: add up the tile's slices and run the epilogue
-        finished = true;
-        if (has_c && tc.n0 + half * 32 < p.N) load_c_chunk<TR>(p, row, tc.n0 + half * 32, tc.batch, cnext);
-#pragma unroll 1
-        for (int c = half; c < kChunks; c += kStride) {
-          const CRegs ccur = cnext;
-          if (has_c && c + kStride < kChunks && tc.n0 + (c + kStride) * 32 < p.N)
-            load_c_chunk<TR>(p, row, tc.n0 + (c + kStride) * 32, tc.batch, cnext);
-          uint32_t v[32];
-          tail_sum<BN, GATHER, CG>(p, tail_r, rank, quad, c, lane, v);
-          const int32_t col0 = tc.n0 + c * 32;
-          if (rows_valid > 0 && col0 < p.N)
-            epilogue_chunk_t<TR>(p, v, row_base, rows_valid, col0, tc.batch, alpha, beta, ccur, stg);
-        }
-      }
     }
     if ((p.flags & FLAG_TILE_COUNTS) && p.tile_counts != nullptr && rank == 0 && warp == 0 &&
         lane == 0 && finished)
@@ -1721,7 +1733,7 @@ __global__ void __launch_bounds__(KernelCfg<BN, GATHER, CG>::kThreads, 1)
     if (atomicAdd(p.status + 7, 1) == ts.units - 1) {
       atomicExch(p.status + 7, 0);
       if (atomicAdd(p.status, 0) != 0) {
-        const int32_t n = p.tail_tiles * CG * Cfg::kEpiWarps;
+        const int32_t n = p.tail_tiles * CG * Cfg::kEpiWarps * kTicketsPerWarp;
         for (int32_t i = 0; i < n; ++i) atomicExch(p.tail_tickets + i, 0);
       }
     }

@@ -46,8 +46,8 @@ struct Params {
   // split last wave (plain problems; see plan_tail_split): items >= full_tiles
   // are slices; tail_tiles == 0 disables it
   int32_t full_tiles, tail_tiles, tail_splits;
-  int32_t* tail_tickets;  // workspace: per tail tile, CTA and epilogue warp, the number of
-                          // slices whose partial rows that warp has written (0 between launches)
+  int32_t* tail_tickets;  // workspace: per tail tile, CTA, epilogue warp and chunk, the number
+                          // of slices whose partial chunk that warp has written (0 between launches)
   float* partials;        // workspace: per tail tile, slice and CTA, 128 x BN fp32 accumulators
   FastDivmod tiles_n_div;  // varlen: local tile -> (m-tile, n-tile)
   int32_t tiles_n;
