@@ -160,9 +160,9 @@ __device__ __forceinline__ TileCoord tile_coord(int32_t t, const Params& p, cons
     tc.a_batch = 0;
     tc.b_batch = lo;
   } else {
-    // a split tail item computes a slice of tile full_tiles + (t - full_tiles) % tail_tiles
+    // a split tail item computes a slice of tile full_tiles + (t - full_tiles) / tail_splits
     const int32_t tt =
-        (p.tail_tiles > 0 && t >= p.full_tiles) ? p.full_tiles + (t - p.full_tiles) % p.tail_tiles : t;
+        (p.tail_tiles > 0 && t >= p.full_tiles) ? p.full_tiles + (t - p.full_tiles) / p.tail_splits : t;
     int32_t l, mb, nb;
     p.sched.map(tt, l, mb, nb);
     tc.m_row0 = mb * TILE_M;
@@ -194,7 +194,7 @@ __device__ __forceinline__ KRange k_range(const Params& p, const Shared& sh, int
                                           int32_t t) {
   if (p.k_groups == 0) {
     if (p.tail_tiles > 0 && t >= p.full_tiles) {
-      const int32_t sl = (t - p.full_tiles) / p.tail_tiles;
+      const int32_t sl = (t - p.full_tiles) % p.tail_splits;
       const int32_t kt0 = sl * p.k_tiles / p.tail_splits;
       const int32_t kt1 = (sl + 1) * p.k_tiles / p.tail_splits;
       return KRange{kt0 * p.bk, min(p.K, kt1 * p.bk), kt1 - kt0, false};
@@ -909,8 +909,8 @@ __device__ __forceinline__ void epilogue_role(const Params& p, const Shared& sh,
     const bool split = !GATHER && p.tail_tiles > 0 && t >= p.full_tiles;
     int32_t slice = 0, tail_r = 0;
     if (split) {
-      slice = (t - p.full_tiles) / p.tail_tiles;
-      tail_r = t - p.full_tiles - slice * p.tail_tiles;
+      tail_r = (t - p.full_tiles) / p.tail_splits;
+      slice = t - p.full_tiles - tail_r * p.tail_splits;
     }
     const int32_t row_base = tc.m_row0 + static_cast<int32_t>(rank) * kBM + quad * 32;
     const int32_t rows_valid = min(32, tc.row_limit - row_base);  // warp-uniform, may be <= 0

@@ -216,3 +216,4 @@ def test_split_while_another_stream_holds_the_sms():
         assert binding.gge_read_device_status()[0] == "GGE_OK"
         check(D, r["D"], r["bound"], BF16, what="D")
         check(P, r["P"], r["bound"], BF16, "silu", what="PostAct", x=r["v"])
+
