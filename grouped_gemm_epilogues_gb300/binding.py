@@ -36,7 +36,8 @@ class GgeTensor(ctypes.Structure):
 class GgeConfig(ctypes.Structure):
     _fields_ = [("tile_n", c_i32), ("num_ctas", c_i32), ("raster_band", c_i32),
                 ("stages", c_i32), ("flags", c_i32), ("cta_group", c_i32),
-                ("tile_counts", ctypes.c_void_p), ("timeout_ns", c_u64)]
+                ("tile_counts", ctypes.c_void_p), ("timeout_ns", c_u64),
+                ("batch_idx_permute", ctypes.c_void_p)]
 
 
 class GgeGemmArgs(ctypes.Structure):
@@ -178,10 +179,13 @@ RESERVED_FLAGS = 16 | 64       # a call that sets one of these is rejected
 
 
 def make_config(tile_n=0, num_ctas=0, raster_band=0, stages=0, flags=0, tile_counts=None,
-                timeout_ns=0, cta_group=0):
+                timeout_ns=0, cta_group=0, batch_idx_permute=None):
+    """batch_idx_permute: None or a device int32 tensor [L] (a permutation of 0..L-1)."""
     return GgeConfig(tile_n, num_ctas, raster_band, stages, flags, cta_group,
                      ctypes.c_void_p(tile_counts.data_ptr()) if tile_counts is not None else None,
-                     timeout_ns)
+                     timeout_ns,
+                     ctypes.c_void_p(batch_idx_permute.data_ptr())
+                     if batch_idx_permute is not None else None)
 
 
 def make_args(A, B, C=None, D=None, PostAct=None, alpha=1.0, beta=1.0, act="none",

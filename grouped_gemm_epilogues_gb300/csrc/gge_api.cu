@@ -360,6 +360,10 @@ gge_status make_plan(const gge_gemm_args* a, Form form, const int32_t* a_idx,
   // one dynamic scheduler at a time: the atomic counter or cluster launch control
   const bool clc = cfg && (cfg->flags & FLAG_CLC_SCHED);
   if (clc && (cfg->flags & FLAG_DYNAMIC_SCHED)) return GGE_ERR_INVALID_ARG;
+  // the pages' batch_idx_permute: batched plain problems only (the varlen and
+  // gather forms order their groups by the group table)
+  const int32_t* perm = cfg ? cfg->batch_idx_permute : nullptr;
+  if (perm != nullptr && form != Form::Plain) return GGE_ERR_UNSUPPORTED;
   if (dact) {
     // backward epilogue: C = pre-activation and D = dx are required, PostAct optional
     if (a->C == nullptr || a->D == nullptr || a->act == GGE_ACT_NONE) return GGE_ERR_INVALID_ARG;
@@ -461,6 +465,8 @@ gge_status make_plan(const gge_gemm_args* a, Form form, const int32_t* a_idx,
   } else {
     if (a->B.batch != L) return GGE_ERR_INVALID_ARG;
     if (!gather && (a->A.rows != M || a->A.batch != L)) return GGE_ERR_INVALID_ARG;
+    // the permutation is copied to shared memory (the group tables' space)
+    if (perm != nullptr && L > kMaxGroupsHost) return GGE_ERR_UNSUPPORTED;
   }
   if (gather) {
     if (a_idx == nullptr) return GGE_ERR_INVALID_ARG;
@@ -517,7 +523,10 @@ gge_status make_plan(const gge_gemm_args* a, Form form, const int32_t* a_idx,
   const int bk = kRowBytesHost / es;
   const int stage_bytes = (kTileM + bn / cg) * kRowBytesHost;
   // the varlen group tables, then (gather-K) the staged source-row indices
-  const int varlen_bytes = ((varlen || vk) ? 2 * 4 * (kMaxGroupsHost + 1) : 0) +
+  // (batch_idx_permute: the permutation, then a 1024-bit table of the batches seen
+  // and a flag, where the kernel's group tables would sit)
+  const int varlen_bytes = ((varlen || vk) ? 2 * 4 * (kMaxGroupsHost + 1)
+                                           : (perm ? 4 * (kMaxGroupsHost + 1) + 4 * 33 : 0)) +
                            (gk ? 16 + 4 * kIdxChunkHost : 0);  // + alignment padding
   const int epi_warps = gather ? kEpiWarpsHost / 2 : kEpiWarpsHost;
   const int fixed = 1024 + kCtrlBytesHost + varlen_bytes + epi_warps * out_stage;
@@ -540,6 +549,7 @@ gge_status make_plan(const gge_gemm_args* a, Form form, const int32_t* a_idx,
   p.stages = stages;
   p.tiles_n = static_cast<int32_t>(tiles_n);
   p.tiles_n_div = FastDivmod::create(tiles_n > 0 ? static_cast<int32_t>(tiles_n) : 1);
+  p.batch_perm = perm;
   int64_t num_tiles = 0;
   if (!varlen) {
     num_tiles = tiles_m * tiles_n * L;

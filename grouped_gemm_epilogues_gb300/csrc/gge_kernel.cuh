@@ -137,7 +137,8 @@ struct Shared {
   uint32_t full, empty, tfull, tempty;  // barrier array bases (shared addresses)
   uint32_t map_full, map_empty;         // varlen-K map-slot barriers (kMapSlots each)
   volatile int32_t* abort;
-  const int32_t* prefix;  // varlen-M: tile prefix [G+1]; varlen-K: group K ends [G]
+  const int32_t* prefix;  // varlen-M: tile prefix [G+1]; varlen-K: group K ends [G];
+                          // plain with batch_idx_permute: the permutation [L]
   const int32_t* cu;      // varlen-M: cu_seqlens copy [G+1]; varlen-K: group K starts [G]
   int32_t* idx;           // gather-K: staged source-row indices [kIdxChunk]
 };
@@ -165,6 +166,7 @@ __device__ __forceinline__ TileCoord tile_coord(int32_t t, const Params& p, cons
         (p.tail_tiles > 0 && t >= p.full_tiles) ? p.full_tiles + (t - p.full_tiles) / p.tail_splits : t;
     int32_t l, mb, nb;
     p.sched.map(tt, l, mb, nb);
+    if (p.batch_perm != nullptr) l = sh.prefix[l];  // checked copy of batch_idx_permute
     tc.m_row0 = mb * TILE_M;
     tc.row_limit = p.M;
     tc.n0 = nb * BN;
@@ -1676,11 +1678,50 @@ __global__ void __launch_bounds__(KernelCfg<BN, GATHER, CG>::kThreads, 1)
       prefix[g] = hi;
     }
   }
+  // batch_idx_permute (plain): copy it and check that it lists each batch once.
+  // Every CTA reaches the same verdict, so on a bad table all of them skip the
+  // work together (no tile is computed, no role waits for another).
+  if (p.batch_perm != nullptr && warp == 0) {
+    const int32_t L = p.L;  // <= kMaxGroups (the host checks)
+    uint32_t* seen = reinterpret_cast<uint32_t*>(cu_s);  // 1024 bits, then the verdict
+    seen[lane] = 0u;
+    __syncwarp();
+    constexpr int32_t kNone = 0x7fffffff;
+    int32_t bad_pos = kNone;  // this lane's first entry outside [0, L)
+    for (int32_t l = lane; l < L; l += 32) {
+      const int32_t b = __ldg(p.batch_perm + l);
+      if (b < 0 || b >= L) {
+        if (bad_pos == kNone) bad_pos = l;
+        continue;
+      }
+      prefix[l] = b;
+      atomicOr(seen + (b >> 5), 1u << (b & 31));
+    }
+    __syncwarp();
+    const int32_t first_pos = __reduce_min_sync(0xffffffffu, bad_pos);
+    // L entries in range name every batch iff no batch is named twice
+    int32_t missing_batch = kNone;
+    if (first_pos == kNone && lane < (L + 31) / 32) {
+      const int32_t rem = L - 32 * lane;
+      const uint32_t want = rem >= 32 ? 0xffffffffu : ((1u << rem) - 1u);
+      const uint32_t missing = want & ~seen[lane];
+      if (missing != 0u) missing_batch = 32 * lane + __ffs(static_cast<int>(missing)) - 1;
+    }
+    const int32_t first_missing = __reduce_min_sync(0xffffffffu, missing_batch);
+    const int32_t detail = first_pos != kNone ? first_pos : first_missing;
+    __syncwarp();
+    if (lane == 0) {
+      if (detail != kNone) record_status(p, DEV_INDEX_RANGE, 14, detail);
+      seen[32] = detail != kNone ? 1u : 0u;
+    }
+  }
   __syncthreads();
   if (CG == 2) ptx::cluster_sync();  // the peer's barriers exist before anyone signals them
   ptx::tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  const int32_t num_tiles = (p.num_groups > 0) ? prefix[p.num_groups] : p.num_tiles;
+  const bool perm_bad = p.batch_perm != nullptr && cu_s[32] != 0;
+  const int32_t num_tiles =
+      (p.num_groups > 0) ? prefix[p.num_groups] : (perm_bad ? 0 : p.num_tiles);
 
   if (warp < Cfg::kEpiWarps) {
     epilogue_role<BN, GATHER, CG, TR>(p, sh, tmem_base, num_tiles, rank, ts,

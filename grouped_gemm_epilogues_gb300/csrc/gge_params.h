@@ -51,6 +51,9 @@ struct Params {
   float* partials;        // workspace: per tail tile, slice and CTA, 128 x BN fp32 accumulators
   FastDivmod tiles_n_div;  // varlen: local tile -> (m-tile, n-tile)
   int32_t tiles_n;
+  // plain: the schedule's batch b computes batch batch_perm[b] (the pages'
+  // batch_idx_permute; copied to shared memory and checked at kernel start)
+  const int32_t* batch_perm;
 
   // varlen-M
   int32_t num_groups;  // 0: plain batched problem

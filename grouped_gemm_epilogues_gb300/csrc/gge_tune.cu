@@ -200,7 +200,13 @@ gge_status gge_tuned_config(const gge_gemm_args* args, int32_t op, int32_t num_g
   std::lock_guard<std::mutex> g(g_mu);
   auto it = cache().find(key_of(args, op, num_groups));
   if (it == cache().end()) return GGE_ERR_INVALID_ARG;
-  *out = it->second;
+  // the search's launch shape with this caller's own pointers and limit
+  gge_config c = it->second;
+  const gge_config* mine = args->config;
+  c.tile_counts = mine ? mine->tile_counts : nullptr;
+  c.timeout_ns = mine ? mine->timeout_ns : 0;
+  c.batch_idx_permute = mine ? mine->batch_idx_permute : nullptr;
+  *out = c;
   return GGE_OK;
 }
 

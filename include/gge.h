@@ -148,6 +148,18 @@ typedef struct gge_config {
                              256-column tiles only; not with gather-K)           */
   int32_t* tile_counts;   /* device int32 per tile (debug coverage), or NULL       */
   uint64_t timeout_ns;    /* 0 = default (2 s) limit for each pipeline wait        */
+  const int32_t* batch_idx_permute;
+                          /* NULL, or device int32[L], a permutation of 0..L-1
+                             (the pages' batch_idx_permute; plain problems with
+                             L <= 1024 only, else GGE_ERR_UNSUPPORTED): the
+                             scheduler visits batch batch_idx_permute[b] where it
+                             would visit batch b, so it fixes the order in which
+                             batches run, never the results.  Every CTA checks
+                             it on the device before any work: an entry outside
+                             [0, L) or a batch listed twice records
+                             GGE_ERR_INDEX_RANGE (where 14, tile = the first bad
+                             position, or the first batch not listed) and the
+                             launch computes and writes nothing.               */
 } gge_config;
 
 /*
@@ -409,7 +421,9 @@ gge_status gge_autotune(const gge_gemm_args* args, int32_t op, const int32_t* id
                         gge_config* best, float* best_ms);
 
 /* The configuration gge_autotune found for a problem of the same key, or
- * GGE_ERR_INVALID_ARG if there is none (no GPU work). */
+ * GGE_ERR_INVALID_ARG if there is none (no GPU work).  The launch-shape
+ * fields are the search's; tile_counts, timeout_ns and batch_idx_permute are
+ * taken from args->config (NULL / 0 without one). */
 gge_status gge_tuned_config(const gge_gemm_args* args, int32_t op, int32_t num_groups,
                             gge_config* out);
 

@@ -135,6 +135,30 @@ def test_swap_ab_plan(L):
         4096, 8192, dtype=torch.bfloat16)) if x["flags"] & 512]
 
 
+def test_batch_idx_permute_plan(L):
+    """batch_idx_permute (the pages' scheduler argument) is planned for batched plain
+    problems of at most 1024 batches: its table takes shared memory where the
+    group tables of the varlen forms sit, and those forms refuse it."""
+    perm = torch.arange(4, dtype=torch.int32)
+    A = torch.zeros(4, 256, 512, dtype=torch.bfloat16)
+    D = torch.zeros(4, 256, 256, dtype=torch.bfloat16)
+    base = dict(num_ctas=152, cta_group=1, tile_n=128)
+    plain = binding.gge_plan(A, A, D=D, config=binding.make_config(**base))
+    info = binding.gge_plan(A, A, D=D, config=binding.make_config(batch_idx_permute=perm, **base))
+    assert info["num_tiles"] == plain["num_tiles"] == 4 * 2 * 2
+    assert info["stages"] == plain["stages"]
+    assert info["smem_bytes"] - plain["smem_bytes"] == 4 * 1025 + 4 * 33
+    A2, Bg = torch.zeros(256, 512, dtype=torch.bfloat16), torch.zeros(4, 256, 512, dtype=torch.bfloat16)
+    with pytest.raises(binding.GgeError):  # varlen-M
+        binding.gge_plan(A2, Bg, D=torch.zeros(256, 256, dtype=torch.bfloat16), num_groups=4,
+                         config=binding.make_config(batch_idx_permute=perm))
+    big = torch.zeros(1025, 128, 64, dtype=torch.bfloat16)
+    binding.gge_plan(big, big, D=torch.zeros(1025, 128, 128, dtype=torch.bfloat16))
+    with pytest.raises(binding.GgeError):  # more batches than the shared-memory table holds
+        binding.gge_plan(big, big, D=torch.zeros(1025, 128, 128, dtype=torch.bfloat16),
+                         config=binding.make_config(batch_idx_permute=perm))
+
+
 def test_auto_raster_band(L):
     """The automatic band keeps a wave's operand rows fewest: sqrt(units * tile_n /
     tile_m) m-tiles (76 pairs of 256 x 256 tiles: 9)."""

@@ -133,3 +133,94 @@ def test_k_serpentine_parity(cta_group, num_ctas):
                                                          num_ctas=num_ctas, cta_group=cta_group))
     _check(wv, tv, out, _oracle(wv, tv, False))
     assert binding.gge_read_device_status()[0] == "GGE_OK"
+
+
+# -------------------------------------------------------------- batch_idx_permute
+FLAG_NO_SPLIT, FLAG_SWAP = 32, 512
+
+
+def _bits(x):
+    return x.cpu().contiguous().view(torch.uint8)
+
+
+@pytest.mark.parametrize("cta_group,num_ctas,flags", [
+    (1, 152, 0), (2, 152, 0), (1, 5, FLAG_DYNAMIC), (2, 0, FLAG_CLC), (2, 6, FLAG_NO_SPLIT)])
+def test_batch_idx_permute_changes_order_not_results(cta_group, num_ctas, flags):
+    """The pages' batch_idx_permute: the schedule visits batch perm[b] where it
+    would visit batch b.  Every tile exactly once, and the outputs are bit-identical
+    to the unpermuted call's (each tile's arithmetic is unchanged) and within the
+    oracle's bound, with the static, atomic-counter and CLC schedules."""
+    M, N, K, L = 300, 520, 200, 6
+    w = wl.small("gemm_act_4096_bf16_gelu", M, N, K, L)
+    t = wl.make(w)
+    perm = torch.tensor([3, 0, 5, 1, 4, 2], dtype=torch.int32, device=DEV)
+    tiles = len(ot.plain_tiles(M, N, L, 128 * cta_group, 256))
+    base = dict(cta_group=cta_group, tile_n=256, num_ctas=num_ctas)
+    ref = _outputs(w, M, N, L)
+    _run_plain(w, t, ref, config=binding.make_config(flags=flags, **base))
+    counts = torch.zeros(tiles + 8, dtype=torch.int32, device=DEV)
+    out = _outputs(w, M, N, L)
+    _run_plain(w, t, out, config=binding.make_config(
+        flags=flags | FLAG_TILE_COUNTS, tile_counts=counts, batch_idx_permute=perm, **base))
+    c = counts.cpu()
+    assert (c[:tiles] == 1).all() and (c[tiles:] == 0).all()
+    for k in ("D", "P"):
+        if k in out:
+            assert torch.equal(_bits(out[k]), _bits(ref[k])), k
+    _check_plain(w, t, out)
+
+
+def test_batch_idx_permute_with_split_tail_and_swap_ab():
+    """With a split last wave (the split tiles are those at the end of the
+    permuted order) and with swap_ab (batch l of the transposed problem is the
+    caller's batch l): oracle parity, every tile once."""
+    M, N, K, L = 512, 776, 1024, 3
+    w = wl.small("gemm_act_4096_bf16_gelu", M, N, K, L)
+    t = wl.make(w)
+    perm = torch.tensor([2, 0, 1], dtype=torch.int32, device=DEV)
+    info = binding.gge_plan(t["A"], t["B"], C=t.get("C"), D=torch.empty(L, M, N, dtype=torch.bfloat16),
+                            PostAct=torch.empty(L, M, N, dtype=torch.bfloat16), act=w.act,
+                            config=binding.make_config(num_ctas=14, cta_group=2, tile_n=256,
+                                                       batch_idx_permute=perm))
+    assert info["tail_tiles"] > 0
+    out = _outputs(w, M, N, L)
+    _run_plain(w, t, out, config=binding.make_config(num_ctas=14, cta_group=2, tile_n=256,
+                                                     batch_idx_permute=perm))
+    _check_plain(w, t, out)
+    Ms = 64
+    w2 = wl.small("gemm_act_4096_bf16_gelu", Ms, N, K, L)
+    t2 = wl.make(w2)
+    ref = _outputs(w2, Ms, N, L)
+    _run_plain(w2, t2, ref, config=binding.make_config(flags=FLAG_SWAP))
+    out2 = _outputs(w2, Ms, N, L)
+    _run_plain(w2, t2, out2, config=binding.make_config(flags=FLAG_SWAP, batch_idx_permute=perm))
+    for k in ("D", "P"):
+        if k in out2:
+            assert torch.equal(_bits(out2[k]), _bits(ref[k])), k
+    _check_plain(w2, t2, out2)
+
+
+@pytest.mark.parametrize("cta_group", [1, 2])
+@pytest.mark.parametrize("perm,detail", [([0, 0, 2, 3], 1), ([0, 1, 4, 3], 2),
+                                         ([3, 2, -1, 0], 2), ([1, 2, 3, 3], 0)])
+def test_batch_idx_permute_bad_table_computes_nothing(cta_group, perm, detail):
+    """A table that is not a permutation of 0..L-1 is refused on the device before
+    any work: GGE_ERR_INDEX_RANGE with where 14 and the first bad position (an
+    entry outside [0, L)) or the first batch no entry names; no output is
+    written, and the next call with a good table is unaffected."""
+    M, N, K, L = 260, 264, 72, 4
+    w = wl.small("gemm_act_4096_bf16_gelu", M, N, K, L)
+    t = wl.make(w)
+    A, B, C = t["A"].to(DEV), t["B"].to(DEV), t["C"].to(DEV)
+    out = _outputs(w, M, N, L)
+    cfg = binding.make_config(cta_group=cta_group, tile_n=256,
+                              batch_idx_permute=torch.tensor(perm, dtype=torch.int32, device=DEV))
+    binding.gge_gemm_act(A, B, out["P"], w.act, D=out["D"], C=C, alpha=w.alpha, beta=w.beta,
+                         config=cfg)
+    torch.cuda.synchronize()
+    assert binding.gge_read_device_status() == ("GGE_ERR_INDEX_RANGE", 14, detail)
+    assert torch.isnan(out["D"].float()).all() and torch.isnan(out["P"].float()).all()
+    good = torch.tensor([1, 3, 0, 2], dtype=torch.int32, device=DEV)
+    _run_plain(w, t, out, config=binding.make_config(cta_group=cta_group, tile_n=256,
+                                                     batch_idx_permute=good))
+    _check_plain(w, t, out)
