@@ -204,6 +204,60 @@ def test_full_size_every_element(name):
     assert worst and max(worst.values()) <= 1.0
 
 
+def _bits(x):
+    return x.contiguous().view(torch.uint8).view(x.shape + (x.element_size(),))
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name", FULL)
+def test_full_size_every_tuner_candidate(name):
+    """Whatever launch shape the autotuner (and so bench.py) picks is checked at
+    full size: every candidate of gge_tune_candidates runs the workload, and its
+    outputs must be bit-identical to the default plan's (whose every element
+    test_full_size_every_element checks) or, on the rows where they differ (a
+    different split of the last wave adds partial sums in another order), match
+    the oracle.  At most 96 differing rows per candidate are checked, spread
+    over the differing ones."""
+    w = wl.WORKLOADS[name]
+    t = wl.make(w)
+    td = {k: v.to(DEV) for k, v in t.items() if isinstance(v, torch.Tensor)}
+    ref = _outputs(w, w.M, w.N, w.L)
+    _run_plain(w, td, ref)
+    keys = [k for k in ("D", "P") if k in ref]
+    A, B = dec(t["A"]), dec(t["B"])          # decoded once for every candidate
+    C = dec(t["C"]) if "C" in t else None
+
+    def check_rows(out, rows):
+        r = og.gemm(A[:, rows], B, C[:, rows] if C is not None else None, alpha=w.alpha,
+                    beta=w.beta, act=w.act, d_fmt=FMT_NAME.get(w.d_dtype),
+                    p_fmt=FMT_NAME.get(w.p_dtype))
+        if "D" in out:
+            check(out["D"].cpu()[:, rows], r["D"], r["bound"], FMT_NAME[w.d_dtype], "none", "D")
+        if "P" in out:
+            check(out["P"].cpu()[:, rows], r["P"], r["bound"], FMT_NAME[w.p_dtype], w.act,
+                  "PostAct", x=r["v"])
+
+    check_rows(ref, [0, w.M // 2, w.M - 1])
+    cands = binding.gge_tune_candidates("gemm", td["A"], td["B"], C=td.get("C"), D=ref.get("D"),
+                                        PostAct=ref.get("P"), act=w.act)
+    assert cands
+    differing = 0
+    for c in cands:
+        out = _outputs(w, w.M, w.N, w.L)
+        _run_plain(w, td, out, config=binding.make_config(**c))
+        rows = torch.zeros(w.M, dtype=torch.bool, device=DEV)
+        for k in keys:
+            rows |= (_bits(out[k]) != _bits(ref[k])).flatten(2).any(2).any(0)
+        idx = torch.nonzero(rows).flatten().cpu()
+        if idx.numel() == 0:
+            continue
+        differing += 1
+        if idx.numel() > 96:
+            idx = idx[torch.linspace(0, idx.numel() - 1, 96).long()]
+        check_rows(out, idx.tolist())
+    print(f"{name}: {len(cands)} candidates, {differing} not bit-identical to the default plan")
+
+
 @pytest.mark.parametrize("M,N,K,L,b_major,cg", [
     (384, 264, 200, 1, "k", 2),
     (328, 512, 136, 2, "n", 2),

@@ -190,6 +190,57 @@ def test_gather_index_out_of_range_is_reported(cta_group):
 
 @pytest.mark.slow
 @pytest.mark.parametrize("gather", [True, False])
+def test_varlen_full_size_every_tuner_candidate(gather):
+    """Whatever launch shape the autotuner (and so bench.py) picks for the 64-group
+    workload is checked at full size: each candidate's outputs must be
+    bit-identical to the default plan's (which test_varlen_full_size_every_element
+    checks element by element) or, on up to 48 of the rows where they differ,
+    match the oracle."""
+    w = wl.WORKLOADS["varlen_gather_g64_m32768_silu"]
+    if not gather:
+        w = wl.small(w.name, w.M, w.N, w.K, gather_rows=0)
+    t = wl.make(w)
+    td = {k: v.to(DEV) for k, v in t.items() if isinstance(v, torch.Tensor)}
+    ref = _run(w, td, gather)
+    assert binding.gge_read_device_status()[0] == "GGE_OK"
+    keys = [k for k in ("D", "P") if k in ref]
+    cu = t["cu_seqlens_m"].numpy()
+    cands = binding.gge_tune_candidates("gather_a" if gather else "varlen_m", td["A"], td["B"],
+                                        C=td.get("C"), D=ref.get("D"), PostAct=ref.get("P"),
+                                        act=w.act, num_groups=len(cu) - 1)
+    assert cands
+    kw = dict(alpha=w.alpha, beta=w.beta, act=w.act, d_fmt=FMT_NAME[w.d_dtype],
+              p_fmt=FMT_NAME[w.p_dtype])
+    b_dec = {}
+    differing = 0
+    for c in cands:
+        out = _run(w, td, gather, config=binding.make_config(**c))
+        assert binding.gge_read_device_status()[0] == "GGE_OK"
+        rows = torch.zeros(w.M, dtype=torch.bool, device=DEV)
+        for k in keys:
+            rows |= (out[k].view(torch.int16) != ref[k].view(torch.int16)).any(1)
+        idx = torch.nonzero(rows).flatten().cpu()
+        if idx.numel() == 0:
+            continue
+        differing += 1
+        if idx.numel() > 48:
+            idx = idx[torch.linspace(0, idx.numel() - 1, 48).long()]
+        for r in idx.tolist():   # one-row GEMMs against the row's group
+            g = int(np.searchsorted(cu, r, side="right") - 1)
+            if g not in b_dec:
+                b_dec[g] = dec(t["B"][g])[None]
+            arow = t["A"][int(t["a_idx"][r])] if gather else t["A"][r]
+            Cr = dec(t["C"][r])[None, None] if "C" in t else None
+            one = og.gemm(dec(arow)[None, None], b_dec[g], Cr, **kw)
+            for k in keys:
+                fmt = FMT_NAME[w.d_dtype if k == "D" else w.p_dtype]
+                check(out[k][r].cpu()[None, None], one[k], one["bound"], fmt,
+                      "none" if k == "D" else w.act, f"{k} row {r}", x=one["v"])
+    print(f"{w.name} gather={gather}: {len(cands)} candidates, {differing} not bit-identical")
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("gather", [True, False])
 def test_varlen_full_size_every_element(gather):
     """The 64-group workload at full size, every output row of every group
     against the oracle (group by group, in blocks of rows)."""
