@@ -354,6 +354,15 @@ def _peak_for(w, peaks, src):
             f"{src} cuBLAS bf16 burst" + (" x2 (fp8/bf16 nominal ratio)" if is8 else ""))
 
 
+def _sustained_frac(w, peaks, tflops):
+    """Context beside `frac`: the same number against cuBLAS run back to back for
+    seconds under the power cap (the timed region here follows 0.2-0.5 s of load)."""
+    s = peaks.get("bf16_tflops_sustained")
+    if not s:
+        return None
+    return round(tflops / (s * (2.0 if w.ab_dtype in ("e4m3", "e5m2") else 1.0)), 4)
+
+
 def _fixed_shape(args):
     """A launch shape given on the command line (with --no-tune), or None."""
     d = json.loads(args.config_json) if args.config_json else {}
@@ -472,6 +481,7 @@ def measure_config(args, w, dev, binding, local, peaks, src):
            "ms_per_step": round(ms_per_step, 5), "steps": steps,
            "frac": round(tflops / peak, 4), "peak": peak, "peak_source": peak_src,
            "frac_of_nominal_dense_peak": round(tflops / NOMINAL_PEAK[w.ab_dtype], 4),
+           "frac_of_measured_sustained": _sustained_frac(w, peaks, tflops),
            "hbm": {"algorithmic_bytes": int(alg), "achieved_gbs": round(hbm, 1),
                    "peak_gbs": hbm_peak, "frac": round(hbm / hbm_peak, 4)},
            "traffic": profiled_traffic(w.name), "l2": l2, "clocks": clocks,
@@ -533,6 +543,7 @@ def run_ours(args, w):
         "frac": round(achieved / peak, 4), "traffic": profiled_traffic(w.name),
         "peak_source": peak_src,
         "frac_of_nominal_dense_peak": round(achieved / NOMINAL_PEAK[w.ab_dtype], 4),
+        "frac_of_measured_sustained": _sustained_frac(w, peaks, achieved),
     }
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": "TFLOP/s", "n_gpus": ws_n,
