@@ -49,6 +49,7 @@ EncodeTiledFn encode_fn() {
   static EncodeTiledFn fn = nullptr;
   static std::once_flag once;
   std::call_once(once, [] {
+    RelaxedCaptureMode relaxed;  // the first call may run inside a stream capture
     void* p = nullptr;
     cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
@@ -261,7 +262,11 @@ int variant_units(int bn, bool gather, int cg, size_t smem, int cluster) {
         return e.units;
     }
   }
-  const int units = variant_units_uncached(bn, gather, cg, smem, cluster);
+  int units;
+  {
+    RelaxedCaptureMode relaxed;  // the first query may run inside a stream capture
+    units = variant_units_uncached(bn, gather, cg, smem, cluster);
+  }
   if (units > 0) {
     std::lock_guard<std::mutex> g(mu);
     if (n < 64) cache[n++] = Entry{dev, bn, cg, gather, smem, cluster, units};

@@ -17,6 +17,7 @@ cudaError_t set_smem_limit(size_t smem) {
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64 || smem_set[dev].load() < smem) {
+    RelaxedCaptureMode relaxed;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem));
     if (e != cudaSuccess) return e;

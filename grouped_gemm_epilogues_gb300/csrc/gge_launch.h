@@ -9,6 +9,19 @@
 
 namespace gge {
 
+// Device queries that are not stream work (a function's shared-memory limit,
+// occupancy) are refused while the calling thread captures a stream in the
+// default (global) mode.  For the lifetime of this object the thread is in
+// relaxed mode, which allows them, so a launch shape's first call on a device
+// may itself be captured into a CUDA graph.
+struct RelaxedCaptureMode {
+  cudaStreamCaptureMode saved = cudaStreamCaptureModeRelaxed;
+  RelaxedCaptureMode() { cudaThreadExchangeStreamCaptureMode(&saved); }
+  ~RelaxedCaptureMode() { cudaThreadExchangeStreamCaptureMode(&saved); }
+  RelaxedCaptureMode(const RelaxedCaptureMode&) = delete;
+  RelaxedCaptureMode& operator=(const RelaxedCaptureMode&) = delete;
+};
+
 struct LaunchShape {
   int grid;
   int threads;
