@@ -365,22 +365,32 @@ __device__ __forceinline__ int32_t sched_next(const TileSched& ts, int i, const 
 
 // ------------------------------------------------------------- epilogue math
 
+// exp(-2u) for gelu_tanh's u = sqrt(2/pi) (x + 0.044715 x^3): with exp(y) = 2^(y log2 e)
+// the exponent is x (k0 + k1 x^2), the three constant factors folded into k0 and k1.
+__device__ __forceinline__ float gelu_exp_m2u(float x) {
+  constexpr float k0 = static_cast<float>(-2.0 * 0.7978845608028654 * 1.4426950408889634);
+  constexpr float k1 = static_cast<float>(-2.0 * 0.7978845608028654 * 1.4426950408889634 *
+                                          0.044715);
+  return ptx::ex2_approx(x * fmaf(k1, x * x, k0));
+}
+
+// exp(-x) as 2^(-x log2 e).
+__device__ __forceinline__ float exp_neg(float x) {
+  constexpr float kNegLog2e = static_cast<float>(-1.4426950408889634);
+  return ptx::ex2_approx(x * kNegLog2e);
+}
+
 // The activation of one value; ACT is fixed at compile time.
 template <int ACT>
 __device__ __forceinline__ float act_one(float x) {
   if constexpr (ACT == ACT_RELU) {
     return (x <= 0.f) ? 0.f : x;  // NaN propagates, -0 -> +0
   } else if constexpr (ACT == ACT_GELU_TANH) {
-    // 0.5 x (1 + tanh u) written as x / (1 + exp(-2u)): no cancellation in the tail.
-    // With u = sqrt(2/pi) (x + 0.044715 x^3) and exp(y) = 2^(y log2 e), the exponent
-    // is x (k0 + k1 x^2) with the three constant factors folded into k0 and k1,
-    // so a value costs one base-2 exponential, one reciprocal and five FP32 ops.
-    constexpr float k0 = static_cast<float>(-2.0 * 0.7978845608028654 * 1.4426950408889634);
-    constexpr float k1 = static_cast<float>(-2.0 * 0.7978845608028654 * 1.4426950408889634 *
-                                            0.044715);
-    return __fdividef(x, 1.f + ptx::ex2_approx(x * fmaf(k1, x * x, k0)));
+    // 0.5 x (1 + tanh u) written as x / (1 + exp(-2u)): no cancellation in the tail;
+    // one base-2 exponential, one reciprocal and five FP32 operations a value
+    return x * ptx::rcp_approx(1.f + gelu_exp_m2u(x));
   } else if constexpr (ACT == ACT_SILU) {
-    return __fdividef(x, 1.f + __expf(-x));
+    return x * ptx::rcp_approx(1.f + exp_neg(x));
   } else if constexpr (ACT == ACT_RELU_SQ) {
     return (x <= 0.f) ? 0.f : x * x;
   } else {
@@ -397,12 +407,11 @@ __device__ __forceinline__ float dact_one(float x) {
     return (x <= 0.f) ? 0.f : 2.f * x;
   } else if constexpr (ACT == ACT_GELU_TANH) {
     // s = sigmoid(2u) = (1 + tanh u) / 2 and 1 - tanh^2 u = 4 s (1 - s)
-    const float u = 0.7978845608028654f * fmaf(0.044715f * x, x * x, x);
-    const float s = __fdividef(1.f, 1.f + __expf(-2.f * u));
+    const float s = ptx::rcp_approx(1.f + gelu_exp_m2u(x));
     const float du = 0.7978845608028654f * fmaf(3.f * 0.044715f * x, x, 1.f);
     return fmaf(2.f * x * s * (1.f - s), du, s);
   } else if constexpr (ACT == ACT_SILU) {
-    const float s = __fdividef(1.f, 1.f + __expf(-x));
+    const float s = ptx::rcp_approx(1.f + exp_neg(x));
     return s * fmaf(x, 1.f - s, 1.f);
   } else {
     return 1.f;

@@ -45,6 +45,13 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 
+// 1/x by the SFU's reciprocal (approximate; +-inf -> +-0, +-0 -> +-inf).
+__device__ __forceinline__ float rcp_approx(float x) {
+  float y;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 __device__ __forceinline__ uint64_t globaltimer() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
