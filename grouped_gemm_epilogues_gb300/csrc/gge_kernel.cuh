@@ -937,6 +937,10 @@ __device__ __forceinline__ void epilogue_role(const Params& p, const Shared& sh,
     const int32_t rows_valid = min(32, tc.row_limit - row_base);  // warp-uniform, may be <= 0
     const int32_t row = row_base + lane;
     const bool has_c = p.c != nullptr && lane < rows_valid;
+    // D only (no C, no PostAct, forward, 16-bit D, staged): each chunk goes straight
+    // to the staging store, without the general epilogue's per-chunk decisions
+    const bool lean = !TR && !p.dact && p.c == nullptr && p.post == nullptr &&
+                      p.out_stage_bytes != 0 && p.d_dtype != DT_F32;
     CRegs cnext = {};
     if (!split && has_c && tc.n0 + half * 32 < p.N)
       load_c_chunk<TR>(p, row, tc.n0 + half * 32, tc.batch, cnext);
@@ -1000,8 +1004,24 @@ __device__ __forceinline__ void epilogue_role(const Params& p, const Shared& sh,
         }
         continue;
       }
-      if (rows_valid > 0 && col0 < p.N)
-        epilogue_chunk_t<TR>(p, v, row_base, rows_valid, col0, tc.batch, alpha, beta, ccur, stg);
+      if (rows_valid > 0 && col0 < p.N) {
+        if (lean) {
+          float x[32];
+          if (alpha == 1.f) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) x[j] = __uint_as_float(v[j]);
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) x[j] = __uint_as_float(v[j]) * alpha;
+          }
+          store_chunk_staged(stg, x, p.d_dtype,
+                             out_ptr(p.d, p.ldd, p.sbd, p.d_dtype, row_base, col0, tc.batch, p),
+                             2 * p.ldd, rows_valid, min(32, p.N - col0), false);
+        } else {
+          epilogue_chunk_t<TR>(p, v, row_base, rows_valid, col0, tc.batch, alpha, beta, ccur,
+                               stg);
+        }
+      }
     }
     if ((p.flags & FLAG_TILE_COUNTS) && p.tile_counts != nullptr && rank == 0 && warp == 0 &&
         lane == 0 && finished)
