@@ -163,6 +163,27 @@ def workspace(device=None, nbytes: int = 256) -> torch.Tensor:
     return ws
 
 
+def new_workspace(device=None, nbytes: int = 32 << 20) -> torch.Tensor:
+    """A zeroed workspace of its own, for calls that may run at the same time on
+    different streams: each such stream passes its own (``workspace=``) to the
+    entry points, since by default every call on a device shares the one that
+    ``workspace()`` keeps (its status words, scheduler counters and split tickets)."""
+    dev = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
+    return torch.zeros(max(int(nbytes), 256), dtype=torch.uint8, device=dev)
+
+
+_shared_workspace = workspace
+
+
+def _ws(device, need, given):
+    """The caller's workspace (checked), or the shared per-device one."""
+    if given is None:
+        return _shared_workspace(device, need)
+    if given.dtype != torch.uint8 or given.device != device or not given.is_contiguous():
+        raise ValueError("workspace: a contiguous uint8 tensor on the outputs' device")
+    return given
+
+
 # gge_config.flags bits (include/gge.h)
 FLAGS = {
     "tile_counts": 1,          # count tile visits into tile_counts
@@ -223,32 +244,34 @@ def _check(code, where):
 
 # ------------------------------------------------------------- entry points
 
-def gge_gemm(A, B, D, C=None, alpha=1.0, beta=1.0, alpha_dev=None, beta_dev=None, config=None):
-    """D = alpha * A @ B^T + beta * C.  A (L,M,K)/(M,K), B (L,N,K)/(N,K), D (L,M,N)/(M,N)."""
+def gge_gemm(A, B, D, C=None, alpha=1.0, beta=1.0, alpha_dev=None, beta_dev=None, config=None,
+             workspace=None):
+    """D = alpha * A @ B^T + beta * C.  A (L,M,K)/(M,K), B (L,N,K)/(N,K), D (L,M,N)/(M,N).
+    workspace: optional buffer of the caller's (see new_workspace)."""
     lib = load()
     args = make_args(A, B, C=C, D=D, alpha=alpha, beta=beta, alpha_dev=alpha_dev,
                      beta_dev=beta_dev, config=config)
-    ws = workspace(D.device, lib.gge_workspace_size(ctypes.byref(args), 0))
+    ws = _ws(D.device, lib.gge_workspace_size(ctypes.byref(args), 0), workspace)
     _check(lib.gge_gemm(ctypes.byref(args), ctypes.c_void_p(ws.data_ptr()), ws.numel(),
                         _stream(D)), "gge_gemm")
 
 
 def gge_gemm_act(A, B, PostAct, act, D=None, C=None, alpha=1.0, beta=1.0, alpha_dev=None,
-                 beta_dev=None, config=None):
+                 beta_dev=None, config=None, workspace=None):
     """D (optional) and PostAct = act(alpha * A @ B^T + beta * C)."""
     lib = load()
     args = make_args(A, B, C=C, D=D, PostAct=PostAct, alpha=alpha, beta=beta, act=act,
                      alpha_dev=alpha_dev, beta_dev=beta_dev, config=config)
-    ws = workspace(PostAct.device, lib.gge_workspace_size(ctypes.byref(args), 0))
+    ws = _ws(PostAct.device, lib.gge_workspace_size(ctypes.byref(args), 0), workspace)
     _check(lib.gge_gemm_act(ctypes.byref(args), ctypes.c_void_p(ws.data_ptr()), ws.numel(),
                             _stream(PostAct)), "gge_gemm_act")
 
 
-def gge_gemm_dact(A, B, PreAct, D, act, PostAct=None, config=None):
+def gge_gemm_dact(A, B, PreAct, D, act, PostAct=None, config=None, workspace=None):
     """Backward activation epilogue: D = act'(PreAct) * (A @ B^T), PostAct = act(PreAct)."""
     lib = load()
     args = make_args(A, B, C=PreAct, D=D, PostAct=PostAct, act=act, config=config)
-    ws = workspace(D.device, lib.gge_workspace_size(ctypes.byref(args), 0))
+    ws = _ws(D.device, lib.gge_workspace_size(ctypes.byref(args), 0), workspace)
     _check(lib.gge_gemm_dact(ctypes.byref(args), ctypes.c_void_p(ws.data_ptr()), ws.numel(),
                              _stream(D)), "gge_gemm_dact")
 
@@ -265,13 +288,13 @@ def gge_gemm_act_static_scratch(A, B, PostAct, act, D=None, C=None, alpha=1.0, b
 
 
 def gge_gemm_varlen_m(A, B, cu_seqlens_m, D=None, PostAct=None, act="none", C=None, alpha=1.0,
-                      beta=1.0, config=None):
+                      beta=1.0, config=None, workspace=None):
     """Varlen-M grouped GEMM: A (total_M, K), B (G, N, K), cu_seqlens_m int32 (G+1,) on device."""
     lib = load()
     out = D if D is not None else PostAct
     args = make_args(A, B, C=C, D=D, PostAct=PostAct, alpha=alpha, beta=beta, act=act,
                      config=config)
-    ws = workspace(out.device)
+    ws = _ws(out.device, 256, workspace)
     G = cu_seqlens_m.numel() - 1
     _check(lib.gge_gemm_varlen_m(ctypes.byref(args), ctypes.c_void_p(cu_seqlens_m.data_ptr()), G,
                                  ctypes.c_void_p(ws.data_ptr()), ws.numel(), _stream(out)),
@@ -279,7 +302,7 @@ def gge_gemm_varlen_m(A, B, cu_seqlens_m, D=None, PostAct=None, act="none", C=No
 
 
 def gge_gemm_varlen_k(A, B, cu_seqlens_k, D=None, PostAct=None, act="none", C=None, alpha=1.0,
-                      beta=1.0, config=None):
+                      beta=1.0, config=None, workspace=None):
     """Varlen-K grouped GEMM: A (M, total_K), B (N, total_K), cu_seqlens_k int32 (G+1,) on
     device; C / D / PostAct (G, M, N).  Group g contracts K columns cu[g] .. cu[g+1]-1."""
     lib = load()
@@ -288,14 +311,14 @@ def gge_gemm_varlen_k(A, B, cu_seqlens_k, D=None, PostAct=None, act="none", C=No
                      config=config)
     G = cu_seqlens_k.numel() - 1
     need = lib.gge_workspace_size_varlen_k(ctypes.byref(args), G)
-    ws = workspace(out.device, need)
+    ws = _ws(out.device, need, workspace)
     _check(lib.gge_gemm_varlen_k(ctypes.byref(args), ctypes.c_void_p(cu_seqlens_k.data_ptr()), G,
                                  ctypes.c_void_p(ws.data_ptr()), ws.numel(), _stream(out)),
            "gge_gemm_varlen_k")
 
 
 def gge_gemm_gather_k(A_src, B, a_idx, cu_seqlens_k, D=None, PostAct=None, act="none", C=None,
-                      alpha=1.0, beta=1.0, config=None):
+                      alpha=1.0, beta=1.0, config=None, workspace=None):
     """Gather-K: varlen-K GEMM whose A column k is A_src[:, a_idx[k]].  A_src (M, K_src)
     M-major (e.g. X.t() of a row-major X [K_src, M]), B (N, total_K), a_idx int32
     (total_K,), cu_seqlens_k int32 (G+1,); C / D / PostAct (G, M, N)."""
@@ -304,7 +327,7 @@ def gge_gemm_gather_k(A_src, B, a_idx, cu_seqlens_k, D=None, PostAct=None, act="
     args = make_args(A_src, B, C=C, D=D, PostAct=PostAct, alpha=alpha, beta=beta, act=act,
                      config=config)
     G = cu_seqlens_k.numel() - 1
-    ws = workspace(out.device, lib.gge_workspace_size_varlen_k(ctypes.byref(args), G))
+    ws = _ws(out.device, lib.gge_workspace_size_varlen_k(ctypes.byref(args), G), workspace)
     _check(lib.gge_gemm_gather_k(ctypes.byref(args), ctypes.c_void_p(a_idx.data_ptr()),
                                  ctypes.c_void_p(cu_seqlens_k.data_ptr()), G,
                                  ctypes.c_void_p(ws.data_ptr()), ws.numel(), _stream(out)),
@@ -312,13 +335,13 @@ def gge_gemm_gather_k(A_src, B, a_idx, cu_seqlens_k, D=None, PostAct=None, act="
 
 
 def gge_gemm_gather_a(A_src, B, a_idx, cu_seqlens_m=None, D=None, PostAct=None, act="none",
-                      C=None, alpha=1.0, beta=1.0, config=None):
+                      C=None, alpha=1.0, beta=1.0, config=None, workspace=None):
     """Gather-A GEMM: effective A row r = A_src[a_idx[r]]; varlen-M when cu_seqlens_m is given."""
     lib = load()
     out = D if D is not None else PostAct
     args = make_args(A_src, B, C=C, D=D, PostAct=PostAct, alpha=alpha, beta=beta, act=act,
                      config=config)
-    ws = workspace(out.device)
+    ws = _ws(out.device, 256, workspace)
     G = cu_seqlens_m.numel() - 1 if cu_seqlens_m is not None else 0
     cu = ctypes.c_void_p(cu_seqlens_m.data_ptr()) if cu_seqlens_m is not None else None
     _check(lib.gge_gemm_gather_a(ctypes.byref(args), ctypes.c_void_p(a_idx.data_ptr()), cu, G,
@@ -337,10 +360,11 @@ def gge_read_static_scratch_status(device=None):
     return STATUS.get(code, str(code)), detail[0], detail[1]
 
 
-def gge_read_device_status(device=None):
-    """Synchronise the current stream and return (status_name, where, tile); clears it."""
+def gge_read_device_status(device=None, workspace=None):
+    """Synchronise the current stream and return (status_name, where, tile) recorded in
+    the shared per-device workspace (or in ``workspace``, a caller's); clears it."""
     lib = load()
-    ws = workspace(device)
+    ws = workspace if workspace is not None else _shared_workspace(device)
     detail = (c_i32 * 2)()
     code = lib.gge_read_device_status(ctypes.c_void_p(ws.data_ptr()), _stream(ws), detail)
     return STATUS.get(code, str(code)), detail[0], detail[1]
