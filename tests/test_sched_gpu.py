@@ -224,3 +224,30 @@ def test_batch_idx_permute_bad_table_computes_nothing(cta_group, perm, detail):
     _run_plain(w, t, out, config=binding.make_config(cta_group=cta_group, tile_n=256,
                                                      batch_idx_permute=good))
     _check_plain(w, t, out)
+
+
+def test_batch_idx_permute_at_the_largest_table():
+    """1024 batches (the largest table the shared-memory copy holds): a reversed
+    order gives the unpermuted call's bits and passes the oracle, and a table
+    that names batch 1022 twice reports the one it leaves out, 1023 (the last
+    bit of the last word of the check)."""
+    M, N, K, L = 128, 64, 64, 1024
+    w = wl.small("gemm_act_4096_bf16_gelu", M, N, K, L)
+    t = wl.make(w)
+    ref = _outputs(w, M, N, L)
+    _run_plain(w, t, ref, config=binding.make_config(cta_group=1, tile_n=64))
+    out = _outputs(w, M, N, L)
+    perm = torch.arange(L - 1, -1, -1, dtype=torch.int32, device=DEV)
+    _run_plain(w, t, out, config=binding.make_config(cta_group=1, tile_n=64, batch_idx_permute=perm))
+    for k in ("D", "P"):
+        assert torch.equal(_bits(out[k]), _bits(ref[k])), k
+    _check_plain(w, t, out)
+    bad = torch.arange(L, dtype=torch.int32, device=DEV)
+    bad[L - 1] = L - 2
+    out2 = _outputs(w, M, N, L)
+    binding.gge_gemm_act(t["A"].to(DEV), t["B"].to(DEV), out2["P"], w.act, D=out2["D"],
+                         C=t["C"].to(DEV), alpha=w.alpha, beta=w.beta,
+                         config=binding.make_config(cta_group=1, tile_n=64, batch_idx_permute=bad))
+    torch.cuda.synchronize()
+    assert binding.gge_read_device_status() == ("GGE_ERR_INDEX_RANGE", 14, L - 1)
+    assert torch.isnan(out2["D"].float()).all()
